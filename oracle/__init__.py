@@ -1,0 +1,151 @@
+"""Oracle for the causal long convolution (double precision, CPU).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm are the only callers.  The product
+path never imports this package.
+
+The arithmetic lives in ``fftconv_oracle.c`` (plain C, compiled here with the
+system C compiler into ``oracle/_build/``).  This module only marshals numpy
+arrays through ctypes; the C calls release the GIL, so rows can be spread
+over threads.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fftconv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into a shared library; returns its path."""
+    with _lock:
+        if (not force and os.path.exists(_LIB_PATH)
+                and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            return _LIB_PATH
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        # -ffp-contract=off keeps every product and sum a separately rounded
+        # double operation, exactly as written.
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+        return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i64 = ctypes.c_int64
+        lib.oracle_fft.argtypes = [_dp, _dp, i64, ctypes.c_int]
+        lib.oracle_dft_direct.argtypes = [_dp, _dp, _dp, _dp, i64, ctypes.c_int]
+        lib.oracle_causal_conv.argtypes = [_dp, _dp, _dp, i64]
+        lib.oracle_causal_conv_gated.argtypes = [_dp, _dp, _dp, _dp, _dp, i64]
+        lib.oracle_causal_conv_rows.argtypes = [_dp, _dp, _dp, _dp, _dp, i64, i64, i64, i64]
+        lib.oracle_direct_causal_conv_at.argtypes = [_dp, _dp, i64, i64]
+        lib.oracle_direct_causal_conv_at.restype = ctypes.c_double
+        lib.oracle_direct_causal_conv.argtypes = [_dp, _dp, _dp, i64]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    return a.ctypes.data_as(_dp)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def fft(x: np.ndarray, inverse: bool = False) -> np.ndarray:
+    """DFT (forward sign -1) or inverse DFT (sign +1, scaled 1/n), radix 2."""
+    x = np.asarray(x, dtype=np.complex128)
+    re, im = _f64(x.real).copy(), _f64(x.imag).copy()
+    if _load().oracle_fft(_ptr(re), _ptr(im), re.size, 1 if inverse else -1):
+        raise ValueError("length must be a power of two")
+    return re + 1j * im
+
+
+def dft_direct(x: np.ndarray, inverse: bool = False) -> np.ndarray:
+    """Brute-force O(n^2) DFT, the definition written out."""
+    x = np.asarray(x, dtype=np.complex128)
+    re, im = _f64(x.real), _f64(x.imag)
+    ore, oim = np.empty_like(re), np.empty_like(im)
+    _load().oracle_dft_direct(_ptr(re), _ptr(im), _ptr(ore), _ptr(oim), re.size,
+                              1 if inverse else -1)
+    return ore + 1j * oim
+
+
+def causal_conv(u: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """One row: y[t] = sum_{j<=t} u[j] k[t-j], through the 2N-point DFT."""
+    u, k = _f64(u), _f64(k)
+    y = np.empty_like(u)
+    if _load().oracle_causal_conv(_ptr(u), _ptr(k), _ptr(y), u.size):
+        raise ValueError("N must be a power of two")
+    return y
+
+
+def direct_causal_conv(u: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """One row by the O(N^2) definition."""
+    u, k = _f64(u), _f64(k)
+    y = np.empty_like(u)
+    _load().oracle_direct_causal_conv(_ptr(u), _ptr(k), _ptr(y), u.size)
+    return y
+
+
+def direct_causal_conv_at(u: np.ndarray, k: np.ndarray, t: int) -> float:
+    """One output y[t] by the definition (compensated sum), O(t)."""
+    u, k = _f64(u), _f64(k)
+    return float(_load().oracle_direct_causal_conv_at(_ptr(u), _ptr(k), u.size, int(t)))
+
+
+def causal_conv_batch(u: np.ndarray, k: np.ndarray, w_in: Optional[np.ndarray] = None,
+                      w_out: Optional[np.ndarray] = None, threads: int = 1,
+                      rows: Optional[range] = None) -> np.ndarray:
+    """u: [B, H, N] (or [rows, N] with H = k.shape[0]); k: [H, N].
+
+    Returns y of u's shape (rows outside ``rows`` are left zero).  Gating is
+    applied when both ``w_in`` and ``w_out`` are given.
+    """
+    k = _f64(k)
+    H, N = k.shape
+    u = _f64(u)
+    shape = u.shape
+    u2 = u.reshape(-1, N)
+    gi = _f64(w_in).reshape(-1, N) if w_in is not None else None
+    go = _f64(w_out).reshape(-1, N) if w_out is not None else None
+    y = np.zeros_like(u2)
+    nrows = u2.shape[0]
+    todo = rows if rows is not None else range(nrows)
+    lib = _load()
+
+    def run(r0: int, r1: int):
+        rc = lib.oracle_causal_conv_rows(_ptr(u2), _ptr(gi), _ptr(go), _ptr(k), _ptr(y),
+                                         H, N, r0, r1)
+        if rc:
+            raise ValueError("oracle failed (N must be a power of two)")
+
+    r_list = list(todo)
+    if threads <= 1 or len(r_list) <= 1:
+        for r in r_list:
+            run(r, r + 1)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda r: run(r, r + 1), r_list))
+    return y.reshape(shape)

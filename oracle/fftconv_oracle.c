@@ -1,0 +1,196 @@
+/*
+ * Oracle for the causal long convolution: plain, slow, double precision.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference arm may load this code.  The product
+ * (the CUDA library and its Python binding) never calls it, and it shares no
+ * code, header, table or constant with the product.
+ *
+ * What it computes (FlashFFTConv page, section 3.4 "The FFT Convolution and
+ * Its Hardware Mismatch"):
+ *   - the convolution  (u * k)[i] = sum_j u[j] k[i - j]  over the indices
+ *     where both are defined, restricted to the causal outputs i = 0..N-1;
+ *   - the same result through the convolution theorem
+ *     u * k = F^-1(F u . F k), with u and k zero-padded to length 2N so the
+ *     circular convolution equals the linear one on the kept outputs;
+ *   - the DFT with element (j, k) = exp(-2 pi i j k / n) (section 3.4,
+ *     "The Monarch FFT Decomposition", definition of F_N); the inverse uses
+ *     exp(+2 pi i j k / n) and divides by n;
+ *   - the gated form y = v . ((u . w) * k) (section 3.4, "Gating operation
+ *     fusion"), here with v = w_out and w = w_in of the same shape as u.
+ *
+ * The FFT is the textbook iterative radix-2 Cooley-Tukey transform (bit
+ * reversal, then log2(n) butterfly passes); twiddles come from cos/sin of the
+ * exact angle at every use.  Nothing is blocked, fused or reordered beyond
+ * that definition.
+ *
+ * Pins (tests that run without a GPU): brute-force DFT and direct
+ * convolution on small sizes, the delta / shifted-delta kernels, u = delta,
+ * constant u (prefix sums), linearity, commutativity, Parseval, single-tone
+ * transforms, numpy's FFT as an independent library, and hand-worked
+ * fixtures.  No function here is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_PI 3.14159265358979323846264338327950288
+
+/* 1 if n is a power of two (n >= 1). */
+static int is_pow2(int64_t n) { return n >= 1 && (n & (n - 1)) == 0; }
+
+/*
+ * In-place DFT of length n (a power of two) of the complex vector (re, im).
+ * sign = -1: forward transform X[k] = sum_j x[j] exp(-2 pi i j k / n).
+ * sign = +1: inverse transform x[j] = (1/n) sum_k X[k] exp(+2 pi i j k / n).
+ * Returns 0 on success, -1 if n is not a power of two.
+ */
+int oracle_fft(double *re, double *im, int64_t n, int sign)
+{
+    if (!is_pow2(n) || (sign != 1 && sign != -1)) return -1;
+    /* bit-reversal permutation */
+    for (int64_t i = 1, j = 0; i < n; ++i) {
+        int64_t bit = n >> 1;
+        for (; j & bit; bit >>= 1) j ^= bit;
+        j ^= bit;
+        if (i < j) {
+            double t = re[i]; re[i] = re[j]; re[j] = t;
+            t = im[i]; im[i] = im[j]; im[j] = t;
+        }
+    }
+    /* butterfly passes: combine pairs of length-len/2 transforms; the
+     * twiddle exp(sign 2 pi i j / len) is evaluated once per (len, j) */
+    for (int64_t len = 2; len <= n; len <<= 1) {
+        int64_t half = len >> 1;
+        for (int64_t j = 0; j < half; ++j) {
+            double ang = sign * 2.0 * ORACLE_PI * (double)j / (double)len;
+            double wr = cos(ang), wi = sin(ang);
+            for (int64_t start = 0; start < n; start += len) {
+                int64_t a = start + j, b = a + half;
+                double tr = re[b] * wr - im[b] * wi;
+                double ti = re[b] * wi + im[b] * wr;
+                re[b] = re[a] - tr; im[b] = im[a] - ti;
+                re[a] += tr;        im[a] += ti;
+            }
+        }
+    }
+    if (sign == 1) {
+        for (int64_t i = 0; i < n; ++i) { re[i] /= (double)n; im[i] /= (double)n; }
+    }
+    return 0;
+}
+
+/*
+ * Brute-force DFT, O(n^2), any n >= 1: the definition written out.  Used only
+ * to pin oracle_fft on small sizes.
+ */
+int oracle_dft_direct(const double *re, const double *im, double *out_re,
+                      double *out_im, int64_t n, int sign)
+{
+    if (n < 1 || (sign != 1 && sign != -1)) return -1;
+    for (int64_t k = 0; k < n; ++k) {
+        double sr = 0.0, si = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            /* reduce j*k mod n first so the angle stays exact for large n */
+            int64_t m = (j * k) % n;
+            double ang = sign * 2.0 * ORACLE_PI * (double)m / (double)n;
+            double c = cos(ang), s = sin(ang);
+            sr += re[j] * c - im[j] * s;
+            si += re[j] * s + im[j] * c;
+        }
+        out_re[k] = sign == 1 ? sr / (double)n : sr;
+        out_im[k] = sign == 1 ? si / (double)n : si;
+    }
+    return 0;
+}
+
+/*
+ * Causal convolution of one row through the convolution theorem:
+ * y[t] = sum_{j=0}^{t} u[j] k[t-j], t = 0..N-1, computed as the first N
+ * outputs of IDFT_{2N}(DFT_{2N}(u0) . DFT_{2N}(k0)) where u0, k0 are u, k
+ * zero-padded to 2N.  N must be a power of two.  Returns 0 or -1.
+ */
+int oracle_causal_conv(const double *u, const double *k, double *y, int64_t N)
+{
+    if (!is_pow2(N)) return -1;
+    int64_t L = 2 * N;
+    double *ur = calloc((size_t)L, sizeof(double)), *ui = calloc((size_t)L, sizeof(double));
+    double *kr = calloc((size_t)L, sizeof(double)), *ki = calloc((size_t)L, sizeof(double));
+    if (!ur || !ui || !kr || !ki) { free(ur); free(ui); free(kr); free(ki); return -1; }
+    memcpy(ur, u, (size_t)N * sizeof(double));
+    memcpy(kr, k, (size_t)N * sizeof(double));
+    oracle_fft(ur, ui, L, -1);
+    oracle_fft(kr, ki, L, -1);
+    for (int64_t i = 0; i < L; ++i) {
+        double pr = ur[i] * kr[i] - ui[i] * ki[i];
+        double pi = ur[i] * ki[i] + ui[i] * kr[i];
+        ur[i] = pr; ui[i] = pi;
+    }
+    oracle_fft(ur, ui, L, 1);
+    memcpy(y, ur, (size_t)N * sizeof(double));
+    free(ur); free(ui); free(kr); free(ki);
+    return 0;
+}
+
+/* Gated row: y = w_out . conv(u . w_in, k), all products in double. */
+int oracle_causal_conv_gated(const double *u, const double *w_in, const double *w_out,
+                             const double *k, double *y, int64_t N)
+{
+    double *x = malloc((size_t)N * sizeof(double));
+    if (!x) return -1;
+    for (int64_t i = 0; i < N; ++i) x[i] = u[i] * w_in[i];
+    int rc = oracle_causal_conv(x, k, y, N);
+    if (rc == 0)
+        for (int64_t i = 0; i < N; ++i) y[i] *= w_out[i];
+    free(x);
+    return rc;
+}
+
+/*
+ * Batched rows: u, y are [rows][N] with row r = b*H + h using kernel row
+ * k[h] = k + h*N (k is [H][N]).  w_in / w_out may be NULL (ungated).
+ * Rows [row_begin, row_end) only, so callers can split the work.
+ */
+int oracle_causal_conv_rows(const double *u, const double *w_in, const double *w_out,
+                            const double *k, double *y, int64_t H, int64_t N,
+                            int64_t row_begin, int64_t row_end)
+{
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        int64_t h = r % H;
+        int rc;
+        if (w_in && w_out)
+            rc = oracle_causal_conv_gated(u + r * N, w_in + r * N, w_out + r * N,
+                                          k + h * N, y + r * N, N);
+        else
+            rc = oracle_causal_conv(u + r * N, k + h * N, y + r * N, N);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+/*
+ * Compensated (Neumaier) sum of u[j] k[t-j] for j = 0..t: one causal output
+ * straight from the definition, O(t).  Any N (not only powers of two).
+ */
+double oracle_direct_causal_conv_at(const double *u, const double *k, int64_t N, int64_t t)
+{
+    if (t < 0 || t >= N) return NAN;
+    double s = 0.0, c = 0.0;
+    for (int64_t j = 0; j <= t; ++j) {
+        double v = u[j] * k[t - j];
+        double nt = s + v;
+        if (fabs(s) >= fabs(v)) c += (s - nt) + v;
+        else c += (v - nt) + s;
+        s = nt;
+    }
+    return s + c;
+}
+
+/* Direct O(N^2) causal convolution of one row (all N outputs). */
+int oracle_direct_causal_conv(const double *u, const double *k, double *y, int64_t N)
+{
+    if (N < 1) return -1;
+    for (int64_t t = 0; t < N; ++t) y[t] = oracle_direct_causal_conv_at(u, k, N, t);
+    return 0;
+}
