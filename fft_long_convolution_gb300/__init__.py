@@ -1,0 +1,191 @@
+"""Python binding of the fftconv C ABI (include/fftconv.h).
+
+Argument marshalling only: every step of the convolution runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  If the
+library cannot be loaded, every call raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from .build import LIB_PATH, build as build_library
+
+F16, BF16 = 0, 1
+PATH_FUSED, PATH_MULTIPASS = 0, 1
+STATUS = {0: "OK", 1: "ERR_INVALID", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIGN", 4: "ERR_WORKSPACE",
+          5: "ERR_CUDA", 6: "ERR_ALLOC", 7: "ERR_TIMEOUT"}
+
+EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy", "fftconv_plan_get_info",
+            "fftconv_kf_bytes", "fftconv_workspace_bytes", "fftconv_set_workspace", "fftconv_kernel_fft",
+            "fftconv_forward", "fftconv_forward_gated", "fftconv_device_status", "fftconv_status_string",
+            "fftconv_version"]
+
+
+class FFTConvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("M", ctypes.c_int64), ("order", ctypes.c_int32),
+                ("factors", ctypes.c_int32 * 8), ("path", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("kf_bytes_per_channel", ctypes.c_int64), ("workspace_bytes_per_row", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {"N": self.N, "M": self.M, "order": self.order,
+                "factors": list(self.factors[: self.order]), "path": self.path, "dtype": self.dtype,
+                "kf_bytes_per_channel": self.kf_bytes_per_channel,
+                "workspace_bytes_per_row": self.workspace_bytes_per_row}
+
+
+_lib = None
+
+
+def lib(auto_build: bool = True):
+    """Load (building first if needed) the CUDA library."""
+    global _lib
+    if _lib is None:
+        if auto_build:
+            build_library()
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"fftconv CUDA library not built: {LIB_PATH}")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        L.fftconv_plan_query.argtypes = [i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(PlanInfo)]
+        L.fftconv_plan_create.argtypes = [ctypes.POINTER(vp), i64, ctypes.c_int, ctypes.c_int]
+        L.fftconv_plan_destroy.argtypes = [vp]
+        L.fftconv_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+        L.fftconv_kf_bytes.argtypes = [vp, i64]
+        L.fftconv_kf_bytes.restype = sz
+        L.fftconv_workspace_bytes.argtypes = [vp, i64, i64]
+        L.fftconv_workspace_bytes.restype = sz
+        L.fftconv_set_workspace.argtypes = [vp, vp, sz]
+        L.fftconv_kernel_fft.argtypes = [vp, vp, vp, i64, vp]
+        L.fftconv_forward.argtypes = [vp, vp, vp, vp, i64, i64, vp]
+        L.fftconv_forward_gated.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp]
+        L.fftconv_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+        L.fftconv_status_string.argtypes = [ctypes.c_int]
+        L.fftconv_status_string.restype = ctypes.c_char_p
+        L.fftconv_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise FFTConvError(st, what)
+
+
+def query(N: int, dtype: int, order: int = 0) -> dict:
+    info = PlanInfo()
+    _check(lib().fftconv_plan_query(N, dtype, order, ctypes.byref(info)), "fftconv_plan_query")
+    return info.as_dict()
+
+
+def _dtype_code(torch_dtype) -> int:
+    import torch
+    if torch_dtype == torch.float16:
+        return F16
+    if torch_dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {torch_dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Plan:
+    """A plan for one sequence length N and dtype (torch.float16 / bfloat16)."""
+
+    def __init__(self, N: int, dtype, order: int = 0):
+        self.N = int(N)
+        self.torch_dtype = dtype
+        self.dtype = _dtype_code(dtype)
+        h = ctypes.c_void_p()
+        _check(lib().fftconv_plan_create(ctypes.byref(h), self.N, self.dtype, order), "fftconv_plan_create")
+        self._h = h
+        info = PlanInfo()
+        _check(lib().fftconv_plan_get_info(self._h, ctypes.byref(info)), "fftconv_plan_get_info")
+        self.info = info.as_dict()
+        self._workspace = None
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().fftconv_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def kf_bytes(self, H: int) -> int:
+        return int(lib().fftconv_kf_bytes(self._h, H))
+
+    def workspace_bytes(self, B: int, H: int) -> int:
+        return int(lib().fftconv_workspace_bytes(self._h, B, H))
+
+    def set_workspace(self, buf) -> None:
+        """Attach a caller-owned device buffer (a torch tensor kept alive here)."""
+        self._workspace = buf
+        n = 0 if buf is None else buf.numel() * buf.element_size()
+        _check(lib().fftconv_set_workspace(self._h, _ptr(buf), n), "fftconv_set_workspace")
+
+    def kernel_fft(self, k, k_f=None, stream=None):
+        """k: float32 [H, N] on the GPU -> opaque k_f (uint8 tensor)."""
+        import torch
+        H = k.shape[0]
+        if k.dtype != torch.float32 or not k.is_contiguous() or k.shape[-1] != self.N:
+            raise ValueError("k must be contiguous float32 [H, N]")
+        if k_f is None:
+            k_f = torch.empty(self.kf_bytes(H), dtype=torch.uint8, device=k.device)
+        _check(lib().fftconv_kernel_fft(self._h, _ptr(k), _ptr(k_f), H, _stream(stream)), "fftconv_kernel_fft")
+        return k_f
+
+    def _ensure_workspace(self, B, H, device):
+        import torch
+        need = self.workspace_bytes(B, H)
+        if need and (self._workspace is None or self._workspace.numel() < need):
+            self.set_workspace(torch.empty(need, dtype=torch.uint8, device=device))
+
+    def forward(self, u, k_f, y=None, stream=None):
+        """u: [B, H, N] (plan dtype, GPU) -> y = causal conv with k."""
+        import torch
+        B, H, N = u.shape
+        if y is None:
+            y = torch.empty_like(u)
+        self._ensure_workspace(B, H, u.device)
+        _check(lib().fftconv_forward(self._h, _ptr(u), _ptr(k_f), _ptr(y), B, H, _stream(stream)),
+               "fftconv_forward")
+        return y
+
+    def forward_gated(self, u, w_in, w_out, k_f, y=None, stream=None):
+        """y = w_out * conv(u * w_in, k)."""
+        import torch
+        B, H, N = u.shape
+        if y is None:
+            y = torch.empty_like(u)
+        self._ensure_workspace(B, H, u.device)
+        _check(lib().fftconv_forward_gated(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y),
+                                           B, H, _stream(stream)), "fftconv_forward_gated")
+        return y
+
+    def device_status(self, stream=None) -> int:
+        v = ctypes.c_int()
+        _check(lib().fftconv_device_status(self._h, _stream(stream), ctypes.byref(v)), "fftconv_device_status")
+        return v.value
+
+
+def status_string(code: int) -> str:
+    return lib().fftconv_status_string(code).decode()

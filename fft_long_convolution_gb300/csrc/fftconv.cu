@@ -1,0 +1,539 @@
+// C-ABI implementation: plans, kernel spectrum, forward launches.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/fftconv.h"
+#include "fused.cuh"
+
+using namespace fftconv;
+
+namespace {
+
+constexpr double kPi = 3.14159265358979323846264338327950288;
+
+struct cd {
+    double r, i;
+};
+
+// exp(-2 pi i e / n), with e reduced mod n first so the angle is exact.
+cd W(int64_t n, int64_t e) {
+    e %= n;
+    if (e < 0) e += n;
+    double a = -2.0 * kPi * double(e) / double(n);
+    return {std::cos(a), std::sin(a)};
+}
+
+// Element of the real embedding of a complex weight w: output part ro
+// (0 = real, 1 = imaginary) from input part ri.
+double embed(cd w, int ro, int ri) {
+    if (ro == 0) return ri == 0 ? w.r : -w.i;
+    return ri == 0 ? w.i : w.r;
+}
+
+uint16_t to_bits(double v, int dtype) {
+    float f = static_cast<float>(v);
+    if (dtype == FFTCONV_F16) {
+        __half h = __float2half_rn(f);
+        uint16_t b;
+        std::memcpy(&b, &h, 2);
+        return b;
+    }
+    uint32_t x;
+    std::memcpy(&x, &f, 4);
+    uint32_t bias = 0x7FFFu + ((x >> 16) & 1u);
+    return static_cast<uint16_t>((x + bias) >> 16);
+}
+
+uint32_t pack2(double lo, double hi, int dtype) {
+    return uint32_t(to_bits(lo, dtype)) | (uint32_t(to_bits(hi, dtype)) << 16);
+}
+
+bool is_pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
+
+}  // namespace
+
+struct fftconv_plan_s {
+    fftconv_plan_info_t info;
+    int R1 = 0;
+    void* dev = nullptr;  // one allocation: tables + error word
+    int* dev_err = nullptr;
+    FusedTables tb{};
+    void* workspace = nullptr;
+    size_t workspace_bytes = 0;
+};
+
+// --------------------------------------------------------------- planning
+
+extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype, int order,
+                                               fftconv_plan_info_t* info) {
+    if (!info) return FFTCONV_ERR_INVALID;
+    if (dtype != FFTCONV_F16 && dtype != FFTCONV_BF16) return FFTCONV_ERR_UNSUPPORTED;
+    if (!is_pow2(N) || N < 1024 || N > (int64_t(1) << 21)) return FFTCONV_ERR_UNSUPPORTED;
+    fftconv_plan_info_t q;
+    std::memset(&q, 0, sizeof(q));
+    q.N = N;
+    q.M = N;
+    q.dtype = dtype;
+    if (N <= 16384) {
+        // fused: M = R1 * 16 * 16
+        q.path = FFTCONV_PATH_FUSED;
+        q.order = 3;
+        q.factors[0] = int32_t(N / 256);
+        q.factors[1] = 16;
+        q.factors[2] = 16;
+        q.workspace_bytes_per_row = 0;
+    } else {
+        return FFTCONV_ERR_UNSUPPORTED;  // multi-pass lengths: not built yet
+    }
+    if (order != 0 && order != q.order) return FFTCONV_ERR_UNSUPPORTED;
+    q.kf_bytes_per_channel = q.M * 8;  // two 16-bit complex coefficients per bin
+    *info = q;
+    return FFTCONV_OK;
+}
+
+namespace {
+
+// Host tables of the fused path for M = R1 * 256 (layouts documented in
+// fused.cuh, FusedTables).
+struct HostTables {
+    std::vector<uint32_t> lf, rf, of, oi;
+    std::vector<float> tw, twf, twi;
+};
+
+HostTables build_fused_tables(int R1, int dtype) {
+    HostTables T;
+    const int64_t M = int64_t(R1) * 256;
+    const double s16 = 0.25, sR = 1.0 / std::sqrt(double(R1));
+    auto F16 = [&](int a, int b) { cd w = W(16, int64_t(a) * b); return cd{w.r * s16, w.i * s16}; };
+    T.lf.assign(32 * 16, 0);
+    T.rf.assign(32 * 16, 0);
+    T.tw.assign(32 * 16, 0.f);
+    for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3;
+        // left product (A operand): rows (k, ro) = (8m + (r&7), r>>3), K (n, ri) = (8s + (q>>1), q&1)
+        for (int m = 0; m < 2; ++m)
+            for (int s = 0; s < 2; ++s) {
+                auto el = [&](int r, int q) {
+                    return embed(F16(8 * m + (r & 7), 8 * s + (q >> 1)), r >> 3, q & 1);
+                };
+                uint32_t* o = &T.lf[lane * 16 + (m * 2 + s) * 4];
+                o[0] = pack2(el(g, 2 * t), el(g, 2 * t + 1), dtype);
+                o[1] = pack2(el(g + 8, 2 * t), el(g + 8, 2 * t + 1), dtype);
+                o[2] = pack2(el(g, 2 * t + 8), el(g, 2 * t + 9), dtype);
+                o[3] = pack2(el(g + 8, 2 * t + 8), el(g + 8, 2 * t + 9), dtype);
+            }
+        // right product (B operand): K (n3, ri) = (8s + 2((q&7)>>1) + (q>>3), q&1),
+        // columns (k3, ro) = (4nt + (c>>1), c&1)
+        for (int s = 0; s < 2; ++s)
+            for (int nt = 0; nt < 4; ++nt) {
+                auto el = [&](int q, int c) {
+                    int n3 = 8 * s + 2 * ((q & 7) >> 1) + (q >> 3);
+                    int k3 = 4 * nt + (c >> 1);
+                    return embed(F16(n3, k3), c & 1, q & 1);
+                };
+                const int q4 = s * 2 + (nt >> 1), slot = nt & 1;
+                uint32_t* o = &T.rf[lane * 16 + q4 * 4 + slot * 2];
+                o[0] = pack2(el(2 * t, g), el(2 * t + 1, g), dtype);
+                o[1] = pack2(el(2 * t + 8, g), el(2 * t + 9, g), dtype);
+            }
+        for (int m = 0; m < 2; ++m)
+            for (int c = 0; c < 2; ++c)
+                for (int e = 0; e < 2; ++e) {
+                    cd w = W(256, int64_t(8 * m + g) * (8 * c + 2 * t + e));
+                    float* o = &T.tw[lane * 16 + (m * 2 + c) * 4 + e * 2];
+                    o[0] = float(w.r);
+                    o[1] = float(w.i);
+                }
+    }
+    // outer stages
+    const bool k8f = R1 <= 8, k8i = R1 <= 4;
+    const int KS_F = k8f ? 1 : R1 / 16, MT_F = (R1 + 7) / 8;
+    const int KS_I = k8i ? 1 : R1 / 8, MT_I = (R1 + 15) / 16;
+    auto FR = [&](int a, int b) { cd w = W(R1, int64_t(a) * b); return cd{w.r * sR, w.i * sR}; };
+    T.of.assign(size_t(MT_F) * KS_F * 32 * 4, 0);
+    T.oi.assign(size_t(MT_I) * KS_I * 32 * 4, 0);
+    for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3;
+        for (int m = 0; m < MT_F; ++m)
+            for (int s = 0; s < KS_F; ++s) {
+                auto el = [&](int r, int q) -> double {
+                    int k1 = 8 * m + (r & 7), n1 = 8 * s + (q >> 1);
+                    if (k1 >= R1 || n1 >= R1 / 2) return 0.0;
+                    return embed(FR(k1, n1), r >> 3, q & 1);
+                };
+                uint32_t* o = &T.of[((m * KS_F + s) * 32 + lane) * 4];
+                o[0] = pack2(el(g, 2 * t), el(g, 2 * t + 1), dtype);
+                o[1] = pack2(el(g + 8, 2 * t), el(g + 8, 2 * t + 1), dtype);
+                if (!k8f) {
+                    o[2] = pack2(el(g, 2 * t + 8), el(g, 2 * t + 9), dtype);
+                    o[3] = pack2(el(g + 8, 2 * t + 8), el(g + 8, 2 * t + 9), dtype);
+                }
+            }
+        for (int m = 0; m < MT_I; ++m)
+            for (int s = 0; s < KS_I; ++s) {
+                auto el = [&](int r, int q) -> double {
+                    int n1 = 8 * m + (r & 7), k1 = 8 * s + (q >> 1);
+                    if (n1 >= R1 / 2 || k1 >= R1) return 0.0;
+                    return embed(FR(n1, k1), r >> 3, q & 1);
+                };
+                uint32_t* o = &T.oi[((m * KS_I + s) * 32 + lane) * 4];
+                o[0] = pack2(el(g, 2 * t), el(g, 2 * t + 1), dtype);
+                o[1] = pack2(el(g + 8, 2 * t), el(g + 8, 2 * t + 1), dtype);
+                if (!k8i) {
+                    o[2] = pack2(el(g, 2 * t + 8), el(g, 2 * t + 9), dtype);
+                    o[3] = pack2(el(g + 8, 2 * t + 8), el(g + 8, 2 * t + 9), dtype);
+                }
+            }
+    }
+    // outer twiddles W_M^(o*k1)
+    T.twf.assign(size_t(32) * MT_F * 32 * 4, 0.f);
+    for (int nt = 0; nt < 32; ++nt)
+        for (int m = 0; m < MT_F; ++m)
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3, k1 = 8 * m + g;
+                float* o = &T.twf[((nt * MT_F + m) * 32 + lane) * 4];
+                if (k1 >= R1) continue;
+                for (int e = 0; e < 2; ++e) {
+                    cd w = W(M, int64_t(8 * nt + 2 * t + e) * k1);
+                    o[2 * e] = float(w.r);
+                    o[2 * e + 1] = float(w.i);
+                }
+            }
+    T.twi.assign(size_t(R1) * 4 * 32 * 4, 0.f);
+    for (int k1 = 0; k1 < R1; ++k1)
+        for (int nt = 0; nt < 4; ++nt)
+            for (int lane = 0; lane < 32; ++lane) {
+                const int g = lane >> 2, t = lane & 3;
+                const int o0 = 16 * (4 * nt + t) + g;
+                float* o = &T.twi[((k1 * 4 + nt) * 32 + lane) * 4];
+                for (int e = 0; e < 2; ++e) {
+                    cd w = W(M, int64_t(o0 + 8 * e) * k1);
+                    o[2 * e] = float(w.r);
+                    o[2 * e + 1] = float(w.i);
+                }
+            }
+    return T;
+}
+
+template <typename T>
+size_t append(std::vector<uint8_t>& blob, const std::vector<T>& v) {
+    size_t off = (blob.size() + 255) & ~size_t(255);
+    blob.resize(off + v.size() * sizeof(T));
+    std::memcpy(blob.data() + off, v.data(), v.size() * sizeof(T));
+    return off;
+}
+
+// ---- fused kernel dispatch
+using FusedFn = void (*)(const uint16_t*, const uint16_t*, const uint16_t*, const uint4*, uint16_t*,
+                         int, int, FusedTables, int*);
+
+template <int DT, int R1, bool G>
+cudaError_t launch_fused_t(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
+                           const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+    using C = FusedCfg<R1, G>;
+    auto fn = fused_conv_kernel<DT, R1, G>;
+    static bool attr_set = false;  // per instantiation, set once per process
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(C::SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int64_t rows = B * H;
+    const int64_t grid = (rows + C::RP - 1) / C::RP;
+    fn<<<dim3(unsigned(grid)), dim3(256), C::SMEM_BYTES, st>>>(
+        static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
+        static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
+        int(B), int(H), p->tb, p->dev_err);
+    return cudaGetLastError();
+}
+
+template <int DT, bool G>
+cudaError_t launch_fused_r(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
+                           const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+    switch (p->R1) {
+        case 4: return launch_fused_t<DT, 4, G>(p, u, wi, wo, kf, y, B, H, st);
+        case 8: return launch_fused_t<DT, 8, G>(p, u, wi, wo, kf, y, B, H, st);
+        case 16: return launch_fused_t<DT, 16, G>(p, u, wi, wo, kf, y, B, H, st);
+        case 32: return launch_fused_t<DT, 32, G>(p, u, wi, wo, kf, y, B, H, st);
+        case 64: return launch_fused_t<DT, 64, G>(p, u, wi, wo, kf, y, B, H, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fused(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
+                         const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+    const bool gated = wi != nullptr;
+    if (p->info.dtype == FFTCONV_F16)
+        return gated ? launch_fused_r<0, true>(p, u, wi, wo, kf, y, B, H, st)
+                     : launch_fused_r<0, false>(p, u, wi, wo, kf, y, B, H, st);
+    return gated ? launch_fused_r<1, true>(p, u, wi, wo, kf, y, B, H, st)
+                 : launch_fused_r<1, false>(p, u, wi, wo, kf, y, B, H, st);
+}
+
+}  // namespace
+
+extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype,
+                                                int order) {
+    if (!out) return FFTCONV_ERR_INVALID;
+    *out = nullptr;
+    fftconv_plan_info_t info;
+    fftconv_status_t st = fftconv_plan_query(N, dtype, order, &info);
+    if (st != FFTCONV_OK) return st;
+    fftconv_plan_s* p = new (std::nothrow) fftconv_plan_s();
+    if (!p) return FFTCONV_ERR_ALLOC;
+    p->info = info;
+    p->R1 = info.factors[0];
+    HostTables T = build_fused_tables(p->R1, dtype);
+    std::vector<uint8_t> blob;
+    const size_t o_err = append(blob, std::vector<int>(64, 0));
+    const size_t o_lf = append(blob, T.lf), o_rf = append(blob, T.rf), o_tw = append(blob, T.tw);
+    const size_t o_of = append(blob, T.of), o_oi = append(blob, T.oi);
+    const size_t o_twf = append(blob, T.twf), o_twi = append(blob, T.twi);
+    if (cudaMalloc(&p->dev, blob.size()) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return FFTCONV_ERR_ALLOC;
+    }
+    if (cudaMemcpy(p->dev, blob.data(), blob.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->dev);
+        delete p;
+        return FFTCONV_ERR_CUDA;
+    }
+    uint8_t* d = static_cast<uint8_t*>(p->dev);
+    p->dev_err = reinterpret_cast<int*>(d + o_err);
+    p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);
+    p->tb.rf = reinterpret_cast<const uint4*>(d + o_rf);
+    p->tb.tw = reinterpret_cast<const float4*>(d + o_tw);
+    p->tb.of = reinterpret_cast<const uint4*>(d + o_of);
+    p->tb.oi = reinterpret_cast<const uint4*>(d + o_oi);
+    p->tb.twf = reinterpret_cast<const float4*>(d + o_twf);
+    p->tb.twi = reinterpret_cast<const float4*>(d + o_twi);
+    *out = p;
+    return FFTCONV_OK;
+}
+
+extern "C" fftconv_status_t fftconv_plan_destroy(fftconv_plan_t plan) {
+    if (!plan) return FFTCONV_OK;
+    cudaError_t e = cudaSuccess;
+    if (plan->dev) e = cudaFree(plan->dev);
+    delete plan;
+    return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+}
+
+extern "C" fftconv_status_t fftconv_plan_get_info(fftconv_plan_t plan, fftconv_plan_info_t* info) {
+    if (!plan || !info) return FFTCONV_ERR_INVALID;
+    *info = plan->info;
+    return FFTCONV_OK;
+}
+
+extern "C" size_t fftconv_kf_bytes(fftconv_plan_t plan, int64_t H) {
+    if (!plan || H < 0) return 0;
+    return size_t(H) * size_t(plan->info.kf_bytes_per_channel);
+}
+
+extern "C" size_t fftconv_workspace_bytes(fftconv_plan_t plan, int64_t B, int64_t H) {
+    if (!plan || B < 0 || H < 0) return 0;
+    return size_t(B) * size_t(H) * size_t(plan->info.workspace_bytes_per_row);
+}
+
+extern "C" fftconv_status_t fftconv_set_workspace(fftconv_plan_t plan, void* dev_ptr, size_t bytes) {
+    if (!plan) return FFTCONV_ERR_INVALID;
+    if (dev_ptr && (reinterpret_cast<uintptr_t>(dev_ptr) & 15)) return FFTCONV_ERR_ALIGN;
+    plan->workspace = dev_ptr;
+    plan->workspace_bytes = dev_ptr ? bytes : 0;
+    return FFTCONV_OK;
+}
+
+// --------------------------------------------------------------- kernel spectrum
+
+namespace {
+
+__global__ void kfft_init(const float* __restrict__ k, float2* __restrict__ buf, int64_t H, int64_t N) {
+    const int64_t L = 2 * N;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * L;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = i / L, n = i - h * L;
+        buf[i] = make_float2(n < N ? k[h * N + n] : 0.f, 0.f);
+    }
+}
+
+// One radix-2 Stockham pass (self-sorting, out of place) of a length-L DFT
+// with exponent sign -1, for every channel.
+__global__ void kfft_pass(const float2* __restrict__ x, float2* __restrict__ yv, int64_t H, int64_t L,
+                          int64_t p) {
+    const int64_t half = L / 2;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * half;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = i / half, r = i - h * half;
+        const int64_t j = r / p, kk = r - j * p;
+        double sw, cw;
+        sincospi(-double(kk) / double(p), &sw, &cw);
+        const float2 c0 = x[h * L + kk + j * p], c1 = x[h * L + kk + j * p + half];
+        const float wr = float(cw), wi = float(sw);
+        const float tr = c1.x * wr - c1.y * wi, ti = c1.x * wi + c1.y * wr;
+        yv[h * L + kk + 2 * j * p] = make_float2(c0.x + tr, c0.y + ti);
+        yv[h * L + kk + 2 * j * p + p] = make_float2(c0.x - tr, c0.y - ti);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_dt(float lo, float hi, int dtype) {
+    return dtype == FFTCONV_F16 ? Op<0>::pack(lo, hi) : Op<1>::pack(lo, hi);
+}
+
+// k_f for the fused layout: per (h, k1, q, lane) two bins, each with
+// alpha~ = conj(alpha), beta~ = conj(beta) of the decimation fold.
+__global__ void kfft_finalize_fused(const float2* __restrict__ K, uint4* __restrict__ kf, int64_t H,
+                                    int R1, int dtype) {
+    const int64_t M = int64_t(R1) * 256, L = 2 * M;
+    const int64_t total = H * R1 * 4 * 32;
+    for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+         idx += int64_t(gridDim.x) * blockDim.x) {
+        const int lane = int(idx & 31);
+        const int q = int((idx >> 5) & 3);
+        const int64_t hk = idx >> 7;
+        const int k1 = int(hk % R1);
+        const int64_t h = hk / R1;
+        const int g = lane >> 2, t = lane & 3;
+        uint32_t words[4];
+        for (int sl = 0; sl < 2; ++sl) {
+            const int i = 2 * q + sl, m = i >> 2, nt = i & 3;
+            const int64_t kap = (g + 8 * m) + 16 * (4 * nt + t);
+            const int64_t k = k1 + int64_t(R1) * kap;
+            const float2 A = K[h * L + k], Bm = K[h * L + (M - k)];
+            double st, ct;
+            sincospi(double(k) / double(M), &st, &ct);  // theta = pi k / M
+            const double Pr = 0.5 * (1.0 - st), Pi = 0.5 * ct;
+            const double Qr = 0.5 * (1.0 + st), Qi = -0.5 * ct;
+            const double Ar = A.x, Ai = A.y, Br = Bm.x, Bi = -Bm.y;  // B = conj K[M-k]
+            const double PAr = Pr * Ar - Pi * Ai, PAi = Pr * Ai + Pi * Ar;
+            const double QBr = Qr * Br - Qi * Bi, QBi = Qr * Bi + Qi * Br;
+            const double Sr = PAr + QBr, Si = PAi + QBi, Dr = PAr - QBr, Di = PAi - QBi;
+            // (i/2) W^k D with W^k = (cos, -sin)
+            const double WDr = ct * Dr + st * Di, WDi = ct * Di - st * Dr;
+            const double Xr = -0.5 * WDi, Xi = 0.5 * WDr;
+            const double ar = 0.5 * Sr - Xr, ai = 0.5 * Si - Xi;
+            const double br = 0.5 * Sr + Xr, bi = 0.5 * Si + Xi;
+            words[2 * sl] = pack_dt(float(ar), float(-ai), dtype);
+            words[2 * sl + 1] = pack_dt(float(br), float(-bi), dtype);
+        }
+        kf[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+    }
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int grid_for(int64_t work) {
+    int64_t g = (work + 255) / 256;
+    return int(g < 1 ? 1 : (g > 65535 * 16 ? 65535 * 16 : g));
+}
+
+}  // namespace
+
+extern "C" fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float* k, void* k_f, int64_t H,
+                                               fftconv_stream_t stream) {
+    if (!plan || H < 0) return FFTCONV_ERR_INVALID;
+    if (H == 0) return FFTCONV_OK;
+    if (!k || !k_f) return FFTCONV_ERR_INVALID;
+    if (misaligned(k) || misaligned(k_f)) return FFTCONV_ERR_ALIGN;
+    const int64_t N = plan->info.N, L = 2 * N;
+    if (overlap(k, size_t(H * N) * 4, k_f, fftconv_kf_bytes(plan, H))) return FFTCONV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float2* buf = nullptr;
+    const size_t bytes = size_t(H) * size_t(L) * sizeof(float2);
+    if (cudaMallocAsync(reinterpret_cast<void**>(&buf), 2 * bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return FFTCONV_ERR_ALLOC;
+    }
+    float2* a = buf;
+    float2* b = buf + H * L;
+    kfft_init<<<grid_for(H * L), 256, 0, st>>>(k, a, H, N);
+    for (int64_t p = 1; p < L; p *= 2) {
+        kfft_pass<<<grid_for(H * L / 2), 256, 0, st>>>(a, b, H, L, p);
+        float2* tmp = a;
+        a = b;
+        b = tmp;
+    }
+    kfft_finalize_fused<<<grid_for(H * plan->R1 * 128), 256, 0, st>>>(
+        a, static_cast<uint4*>(k_f), H, plan->R1, plan->info.dtype);
+    cudaError_t e = cudaGetLastError();
+    cudaFreeAsync(buf, st);
+    return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+}
+
+// --------------------------------------------------------------- forward
+
+static fftconv_status_t forward_impl(fftconv_plan_t plan, const void* u, const void* w_in,
+                                     const void* w_out, const void* k_f, void* y, int64_t B, int64_t H,
+                                     fftconv_stream_t stream, bool gated) {
+    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (B == 0 || H == 0) return FFTCONV_OK;
+    if (!u || !k_f || !y || (gated && (!w_in || !w_out))) return FFTCONV_ERR_INVALID;
+    if (misaligned(u) || misaligned(k_f) || misaligned(y) || (gated && (misaligned(w_in) || misaligned(w_out))))
+        return FFTCONV_ERR_ALIGN;
+    if (B * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    const size_t nb = size_t(B) * size_t(H) * size_t(plan->info.N) * 2;
+    const size_t kb = fftconv_kf_bytes(plan, H);
+    if (overlap(y, nb, u, nb) || overlap(y, nb, k_f, kb) ||
+        (gated && (overlap(y, nb, w_in, nb) || overlap(y, nb, w_out, nb))))
+        return FFTCONV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_fused(plan, u, gated ? w_in : nullptr, gated ? w_out : nullptr, k_f, y, B, H, st);
+    if (e != cudaSuccess) return FFTCONV_ERR_CUDA;
+    return FFTCONV_OK;
+}
+
+extern "C" fftconv_status_t fftconv_forward(fftconv_plan_t plan, const void* u, const void* k_f, void* y,
+                                            int64_t B, int64_t H, fftconv_stream_t stream) {
+    return forward_impl(plan, u, nullptr, nullptr, k_f, y, B, H, stream, false);
+}
+
+extern "C" fftconv_status_t fftconv_forward_gated(fftconv_plan_t plan, const void* u, const void* w_in,
+                                                  const void* w_out, const void* k_f, void* y, int64_t B,
+                                                  int64_t H, fftconv_stream_t stream) {
+    return forward_impl(plan, u, w_in, w_out, k_f, y, B, H, stream, true);
+}
+
+extern "C" fftconv_status_t fftconv_device_status(fftconv_plan_t plan, fftconv_stream_t stream, int* out) {
+    if (!plan || !out) return FFTCONV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, plan->dev_err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemsetAsync(plan->dev_err, 0, sizeof(int), st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return FFTCONV_ERR_CUDA;
+    }
+    *out = v;
+    return FFTCONV_OK;
+}
+
+extern "C" const char* fftconv_status_string(fftconv_status_t s) {
+    switch (s) {
+        case FFTCONV_OK: return "ok";
+        case FFTCONV_ERR_INVALID: return "invalid argument";
+        case FFTCONV_ERR_UNSUPPORTED: return "unsupported length, order or dtype";
+        case FFTCONV_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case FFTCONV_ERR_WORKSPACE: return "workspace missing or too small";
+        case FFTCONV_ERR_CUDA: return "CUDA runtime error";
+        case FFTCONV_ERR_ALLOC: return "device allocation failed";
+        case FFTCONV_ERR_TIMEOUT: return "bounded on-device wait gave up";
+    }
+    return "unknown status";
+}
+
+extern "C" const char* fftconv_version(void) { return "0.1.0"; }

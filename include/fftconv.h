@@ -1,0 +1,177 @@
+/*
+ * fftconv — causal long convolution on one NVIDIA GB300 (sm_103a).
+ *
+ *   y[b,h,t] = sum_{j=0}^{t} u[b,h,j] * k[h,t-j],   t = 0..N-1
+ *            = irfft(rfft(u[b,h,:], 2N) * rfft(k[h,:], 2N))[:N]
+ *
+ * (FlashFFTConv page, section 3.4 "The FFT Convolution and Its Hardware
+ * Mismatch": the convolution, the convolution theorem and the zero-padding to
+ * 2N for causal convolutions.)  The transform is computed as an order-p
+ * Monarch decomposition (section 3.4 "The Monarch FFT Decomposition",
+ * "Higher-order decompositions"): the length-N complex transform left after
+ * the one-stage decimation in time (section 3.4 "The real-valued FFT
+ * optimization") is factored into dense 16-, 32- and 64-point DFT
+ * contractions on the tensor cores, with twiddle scaling and permutations
+ * between them.  The kernel spectrum k_f is precomputed once per filter
+ * (section 3.2, "Input and Kernel Preparation") and reused across the batch.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   never frees them.  Each must be 16-byte aligned.
+ * - u, y, w_in, w_out: contiguous [B][H][N] in the plan dtype (IEEE binary16
+ *   for FFTCONV_F16, bfloat16 for FFTCONV_BF16).  k: contiguous float32
+ *   [H][N].  k_f: opaque, fftconv_kf_bytes(plan, H) bytes, only valid for a
+ *   plan with the same (N, dtype, order).
+ * - y must not overlap any input (checked by address range).
+ * - Work is enqueued on `stream` (cudaStream_t; NULL = legacy default stream)
+ *   and the call returns without waiting.  Validation errors launch nothing.
+ *   Asynchronous faults surface at the caller's next synchronisation.
+ * - Results are bitwise deterministic for a given plan, inputs and GPU (no
+ *   atomics in any reduction).
+ * - B*H == 0 is valid and launches nothing.
+ * - A plan is immutable after creation apart from its workspace; one plan may
+ *   be used from several streams at once unless it needs a workspace
+ *   (multi-pass lengths), in which case calls sharing it must be serialised.
+ */
+#ifndef FFTCONV_H
+#define FFTCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fftconv_plan_s *fftconv_plan_t;
+typedef void *fftconv_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    FFTCONV_F16 = 0,  /* IEEE binary16 storage, fp16 tensor-core operands   */
+    FFTCONV_BF16 = 1  /* bfloat16 storage, bf16 tensor-core operands        */
+} fftconv_dtype_t;
+
+typedef enum {
+    FFTCONV_OK = 0,
+    FFTCONV_ERR_INVALID = 1,     /* bad argument: NULL, overlap, negative size */
+    FFTCONV_ERR_UNSUPPORTED = 2, /* length / order / dtype not supported       */
+    FFTCONV_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned           */
+    FFTCONV_ERR_WORKSPACE = 4,   /* multi-pass length without a big-enough workspace */
+    FFTCONV_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed       */
+    FFTCONV_ERR_ALLOC = 6,       /* device allocation failed                   */
+    FFTCONV_ERR_TIMEOUT = 7      /* a bounded on-device wait gave up           */
+} fftconv_status_t;
+
+/* Which path a plan runs. */
+typedef enum {
+    FFTCONV_PATH_FUSED = 0,     /* one kernel, a whole row resident on chip        */
+    FFTCONV_PATH_MULTIPASS = 1  /* outer stage through HBM, inner stages fused     */
+} fftconv_path_t;
+
+/* Host-side description of a plan (see fftconv_plan_query). */
+typedef struct {
+    int64_t N;            /* sequence length (real samples per row)              */
+    int64_t M;            /* complex transform length after decimation, = N      */
+    int32_t order;        /* p: number of Monarch factors                        */
+    int32_t factors[8];   /* M = factors[0] * ... * factors[order-1], outer first */
+    int32_t path;         /* fftconv_path_t                                      */
+    int32_t dtype;        /* fftconv_dtype_t                                     */
+    int64_t kf_bytes_per_channel; /* bytes of k_f per channel h                 */
+    int64_t workspace_bytes_per_row; /* multi-pass workspace per (b,h) row; 0 if fused */
+} fftconv_plan_info_t;
+
+/*
+ * Describe the plan that fftconv_plan_create would build, without touching
+ * the GPU.  N must be a power of two with 2^10 <= N <= 2^21.  order = 0 picks
+ * the factorization; a nonzero order is honoured or rejected.
+ * Returns OK, INVALID (info NULL) or UNSUPPORTED.
+ */
+fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype, int order,
+                                    fftconv_plan_info_t *info);
+
+/*
+ * Build a plan: choose the factorization (as fftconv_plan_query), build the
+ * DFT-factor and twiddle tables in double precision, round them to the plan
+ * dtype (twiddles stay float32), and upload them to the current device.
+ * *out receives the plan; the plan owns its device tables until
+ * fftconv_plan_destroy.  Returns OK, INVALID, UNSUPPORTED, ALLOC or CUDA.
+ */
+fftconv_status_t fftconv_plan_create(fftconv_plan_t *out, int64_t N, fftconv_dtype_t dtype,
+                                     int order);
+
+/* Release a plan and its device tables (not the caller's buffers).  NULL is OK. */
+fftconv_status_t fftconv_plan_destroy(fftconv_plan_t plan);
+
+/* Copy the plan's description into *info. */
+fftconv_status_t fftconv_plan_get_info(fftconv_plan_t plan, fftconv_plan_info_t *info);
+
+/* Size in bytes of the k_f buffer for H channels (0 if plan is NULL). */
+size_t fftconv_kf_bytes(fftconv_plan_t plan, int64_t H);
+
+/*
+ * Size in bytes of the device workspace a forward call over B*H rows needs:
+ * 0 on the fused path; B*H*N*4 bytes (the 16-bit complex intermediate of
+ * the outer stage) on the multi-pass path (section 3.4, "Kernel Fusion and
+ * Recomputation Strategies": the outer layers spill to HBM).
+ */
+size_t fftconv_workspace_bytes(fftconv_plan_t plan, int64_t B, int64_t H);
+
+/*
+ * Attach a caller-owned device workspace (16-byte aligned) to the plan.
+ * Passing NULL / 0 detaches it.  The plan does not free it.
+ */
+fftconv_status_t fftconv_set_workspace(fftconv_plan_t plan, void *dev_ptr, size_t bytes);
+
+/*
+ * Kernel spectrum: k_f[h] = the plan's encoding of rfft(k[h,:], 2N)
+ * (section 3.2: the FFT of the filter, precomputed and reused across the
+ * batch).  k is float32 [H][N] on the device; k_f is fftconv_kf_bytes(plan,H)
+ * bytes on the device.  The encoding folds the decimation-in-time split and
+ * merge (section 3.4, "The real-valued FFT optimization") into two complex
+ * coefficients per frequency bin, stored in the plan dtype in the order the
+ * forward kernel reads them.  The spectrum itself is computed in float32.
+ * Allocates and frees stream-ordered temporary device memory (about
+ * 16*H*N bytes).  Returns OK, INVALID, ALIGN, ALLOC or CUDA.
+ */
+fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float *k, void *k_f, int64_t H,
+                                    fftconv_stream_t stream);
+
+/*
+ * Forward causal convolution of B*H rows: y[b,h,:] = (u[b,h,:] * k[h,:])[0:N].
+ * u, y: [B][H][N] plan dtype; k_f from fftconv_kernel_fft.  Arithmetic:
+ * tensor-core contractions with 16-bit operands and float32 accumulation;
+ * twiddle, decimation and gating products in float32; y rounded to the plan
+ * dtype (nearest even).  Returns OK, INVALID, ALIGN, WORKSPACE or CUDA.
+ */
+fftconv_status_t fftconv_forward(fftconv_plan_t plan, const void *u, const void *k_f, void *y,
+                                 int64_t B, int64_t H, fftconv_stream_t stream);
+
+/*
+ * Gated forward: y = w_out . ((u . w_in) * k) (section 3.4, "Gating
+ * operation fusion": both gates applied inside the convolution kernel).
+ * w_in, w_out: [B][H][N] plan dtype.  u . w_in is rounded to the plan dtype
+ * before the first contraction; the output gate is applied in float32 before
+ * the final rounding.  Same returns as fftconv_forward.
+ */
+fftconv_status_t fftconv_forward_gated(fftconv_plan_t plan, const void *u, const void *w_in,
+                                       const void *w_out, const void *k_f, void *y, int64_t B,
+                                       int64_t H, fftconv_stream_t stream);
+
+/*
+ * Read and clear the plan's device error word (waits for `stream`).
+ * *out = 0 if no bounded on-device wait has given up since the last call,
+ * else FFTCONV_ERR_TIMEOUT.  Returns OK, INVALID or CUDA.
+ */
+fftconv_status_t fftconv_device_status(fftconv_plan_t plan, fftconv_stream_t stream, int *out);
+
+/* Static English text for a status code (never NULL). */
+const char *fftconv_status_string(fftconv_status_t s);
+
+/* Library version, e.g. "0.1.0". */
+const char *fftconv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FFTCONV_H */
