@@ -1,0 +1,373 @@
+#!/usr/bin/env python3
+"""Benchmark: causal long-convolution throughput (B*H*N outputs/s) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step is one pass of the whole hot path (kernel spectrum precomputed,
+then the fused forward over every (b,h) row) on the workload's synthetic
+inputs, which are resident in HBM before timing starts.  Prints one JSON
+line on rank 0.  Under torchrun every rank runs its own copy of the
+workload (rows are independent: no collective on the data path) and the
+value is the sum over ranks divided by the slowest rank's time.
+
+--impl reference runs the oracle (double-precision CPU FFT convolution) on
+the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = ("long-conv B·H·N outputs/sec on 1 GB300; achieved fraction of "
+          "HBM/tensor roofline")
+DEFAULT_WORKLOAD = "hyena-gated-4k"
+L2_BYTES = 129 * 1000 * 1000
+
+
+def canonical_c(N: int) -> int:
+    """Canonical Monarch contraction count per complex point (fwd + inv):
+    min over factorizations M = prod M_i, M_i in {16, 32, 64}, of
+    sum_{i>=2} M_i + M_1/2 (the padded outer stage does half the work)."""
+    best = None
+    facs = (16, 32, 64)
+
+    def rec(rem, acc, first):
+        nonlocal best
+        if rem == 1:
+            if first is not None:
+                c = first // 2 + acc
+                best = c if best is None else min(best, c)
+            return
+        for f in facs:
+            if rem % f == 0:
+                if first is None:
+                    rec(rem // f, acc, f)
+                else:
+                    rec(rem // f, acc + f, first)
+
+    rec(N, 0, None)
+    return best
+
+
+def algorithmic(w: W.Workload) -> dict:
+    """Compulsory bytes and canonical Monarch FLOPs of one pass."""
+    s = 2
+    per_row = 2 * w.N * s + (2 * w.N * s if w.gated else 0)
+    bytes_ = w.rows * per_row + w.H * (w.N + 1) * 4
+    flops = 16 * w.N * canonical_c(w.N) * w.rows
+    return {"bytes": bytes_, "flops": flops}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fft_long_convolution_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """SM clocks and clock-event (throttle) reasons polled through NVML
+    (read-only queries, libnvidia-ml via ctypes) while the timed region runs."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str):
+        import ctypes
+        import threading
+        self.samples = []
+        self.reason_bits = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._nv, self._h, self._get_reasons = nv, h, get_reasons
+        except Exception:
+            return
+
+        def poll():
+            clk = ctypes.c_uint()
+            rs = ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                if self._nv.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+                    self.samples.append(clk.value)
+                if self._get_reasons(self._h, ctypes.byref(rs)) == 0:
+                    self.reason_bits |= rs.value
+                time.sleep(0.002)
+
+        self._thread = threading.Thread(target=poll, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        if self._thread is None:
+            return None
+        self._stop.set()
+        self._thread.join(timeout=2)
+        reasons = sorted(v for b, v in self.REASONS.items() if self.reason_bits & b)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml"}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 12.0):
+    """The oracle on the host cores over a bounded sample of rows."""
+    import oracle
+    cores = os.cpu_count() or 1
+    rows = min(w.rows, max(cores, 1))
+    # the first `rows` rows (b = 0, h = 0..rows-1) of the workload
+    sl = {n: (r.f64.reshape(-1, w.N)[:rows] if n != "k" else r.f64) for n, r in ins.items()}
+
+    def run():
+        oracle.causal_conv_batch(sl["u"], sl["k"], sl.get("w_in"), sl.get("w_out"), threads=cores)
+
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    reps = max(1, min(int(budget_s / max(dt, 1e-3)), 50))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        run()
+    dt = time.perf_counter() - t0
+    done = rows * reps
+    return {"value": done * w.N / dt, "unit": "outputs/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} rows x {reps} repeats of {w.name} (N={w.N}) in {dt:.1f} s"}
+
+
+def run_reference(args, w: W.Workload):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    small = W.scaled(w, B=1, H=min(w.H, (os.cpu_count() or 1)))
+    ins = W.make_inputs(small, seed=0)
+    cores = os.cpu_count() or 1
+    fn = lambda: oracle.causal_conv_batch(  # noqa: E731
+        ins["u"].f64, ins["k"].f64, ins["w_in"].f64 if w.gated else None,
+        ins["w_out"].f64 if w.gated else None, threads=cores)
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    dt = time.perf_counter() - t0
+    outs = small.rows * small.N * args.steps
+    v = outs / dt
+    sample = f"{small.rows} rows of {w.name} (N={w.N}) per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "outputs/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": v, "unit": "outputs/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "outputs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def config_of(w: W.Workload) -> dict:
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "gated": w.gated, "dtype": w.dtype,
+            "u": w.u_kind, "k": w.k_kind,
+            "l2": "no flush: inputs+outputs exceed L2" if algorithmic(w)["bytes"] > L2_BYTES
+            else "L2 flushed between steps"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import fft_long_convolution_gb300 as F
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    F.build_library()
+
+    ins = W.make_inputs(w, seed=rank)
+    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+
+    def dev_t(r):
+        if r.dtype == "fp32":
+            return torch.from_numpy(r.bits).to(dev)
+        return torch.from_numpy(r.bits.view(np.int16)).view(tdt).to(dev)
+
+    plan = F.Plan(w.N, tdt)
+    k = dev_t(ins["k"])
+    kf = plan.kernel_fft(k)
+    u = dev_t(ins["u"])
+    wi = dev_t(ins["w_in"]) if w.gated else None
+    wo = dev_t(ins["w_out"]) if w.gated else None
+    y = torch.empty_like(u)
+    stream = torch.cuda.current_stream()
+    alg = algorithmic(w)
+    flush = None if alg["bytes"] > L2_BYTES else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        if w.gated:
+            plan.forward_gated(u, wi, wo, kf, y=y, stream=stream)
+        else:
+            plan.forward(u, kf, y=y, stream=stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    barrier()
+    clocks = ClockSampler(torch.cuda.get_device_properties(dev).pci_bus_id if hasattr(torch.cuda.get_device_properties(dev), "pci_bus_id") else "")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = t_start.elapsed_time(t_end)
+    step_ms = sum(kernel_ms) / len(kernel_ms) if flush is not None else total_ms / args.steps
+    assert plan.device_status() == 0
+    t = torch.tensor([step_ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    step_ms_max = float(t.item())
+    value = world * w.outputs / (step_ms_max * 1e-3)
+
+    # end to end through the public API with host buffers (pinned)
+    hu = torch.from_numpy(ins["u"].bits.view(np.int16)).view(tdt).pin_memory()
+    hwi = torch.from_numpy(ins["w_in"].bits.view(np.int16)).view(tdt).pin_memory() if w.gated else None
+    hwo = torch.from_numpy(ins["w_out"].bits.view(np.int16)).view(tdt).pin_memory() if w.gated else None
+    hy = torch.empty_like(hu).pin_memory()
+    h2d = hu.numel() * 2 * (3 if w.gated else 1)
+    d2h = hy.numel() * 2
+
+    def e2e_step():
+        u.copy_(hu, non_blocking=True)
+        if w.gated:
+            wi.copy_(hwi, non_blocking=True)
+            wo.copy_(hwo, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    te = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = world * w.outputs / (float(te.item()) * 1e-3)
+
+    if rank == 0:
+        peaks = measured_peaks()
+        kern_s = (sum(kernel_ms) / len(kernel_ms)) * 1e-3
+        achieved = alg["bytes"] / kern_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(w.name),
+                "peak_source": peaks["source"] + " hbm_gbs (copy)",
+                "algorithmic_bytes_per_launch": alg["bytes"],
+                "tensor_frac": alg["flops"] / kern_s / 1e12 / peaks["bf16_tflops"],
+                "kernel": "fused_conv_kernel"}
+        out = {
+            "metric": METRIC, "value": value, "unit": "outputs/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": step_ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": {"fp16": "f16", "bf16": "bf16"}[w.dtype],
+            "data": "synthetic (seeded SplitMix64 / Box-Muller, see workloads/)",
+            "config": config_of(w), "roofline": roof, "gpu_launches": args.steps,
+            "e2e": {"value": e2e_value, "unit": "outputs/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            import oracle
+            oracle.build()
+            out["cpu_baseline"] = cpu_baseline(w, ins)
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

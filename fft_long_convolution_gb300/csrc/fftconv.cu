@@ -65,6 +65,7 @@ struct fftconv_plan_s {
     void* dev = nullptr;  // one allocation: tables + error word
     int* dev_err = nullptr;
     FusedTables tb{};
+    int num_sms = 0;
     void* workspace = nullptr;
     size_t workspace_bytes = 0;
 };
@@ -231,27 +232,29 @@ size_t append(std::vector<uint8_t>& blob, const std::vector<T>& v) {
 }
 
 // ---- fused kernel dispatch
-using FusedFn = void (*)(const uint16_t*, const uint16_t*, const uint16_t*, const uint4*, uint16_t*,
-                         int, int, FusedTables, int*);
-
 template <int DT, int R1, bool G>
 cudaError_t launch_fused_t(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
                            const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
     using C = FusedCfg<R1, G>;
     auto fn = fused_conv_kernel<DT, R1, G>;
-    static bool attr_set = false;  // per instantiation, set once per process
-    if (!attr_set) {
+    static int blocks_per_sm = 0;  // per instantiation, set once per process
+    if (blocks_per_sm == 0) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(C::SMEM_BYTES));
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, 256, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        blocks_per_sm = nb > 0 ? nb : 1;
     }
-    const int64_t rows = B * H;
-    const int64_t grid = (rows + C::RP - 1) / C::RP;
-    fn<<<dim3(unsigned(grid)), dim3(256), C::SMEM_BYTES, st>>>(
-        static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
-        static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
-        int(B), int(H), p->tb, p->dev_err);
+    if (C::TSMEM && p->tb.outer_bytes > C::TAB_BYTES) return cudaErrorInvalidValue;
+    const int64_t groups = (B * H + C::RP - 1) / C::RP;
+    int64_t grid = int64_t(p->num_sms) * blocks_per_sm;
+    if (grid > groups) grid = groups;
+    FusedArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
+                   static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
+                   int(B), int(H), p->tb, p->dev_err};
+    fn<<<dim3(unsigned(grid)), dim3(256), C::SMEM_BYTES, st>>>(args);
     return cudaGetLastError();
 }
 
@@ -297,6 +300,8 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     const size_t o_lf = append(blob, T.lf), o_rf = append(blob, T.rf), o_tw = append(blob, T.tw);
     const size_t o_of = append(blob, T.of), o_oi = append(blob, T.oi);
     const size_t o_twf = append(blob, T.twf), o_twi = append(blob, T.twi);
+    const size_t outer_end = o_twi + T.twi.size() * sizeof(float);
+    blob.resize((blob.size() + 255) & ~size_t(255));
     if (cudaMalloc(&p->dev, blob.size()) != cudaSuccess) {
         cudaGetLastError();
         delete p;
@@ -308,15 +313,24 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
         delete p;
         return FFTCONV_ERR_CUDA;
     }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->dev);
+        delete p;
+        return FFTCONV_ERR_CUDA;
+    }
     uint8_t* d = static_cast<uint8_t*>(p->dev);
     p->dev_err = reinterpret_cast<int*>(d + o_err);
     p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);
     p->tb.rf = reinterpret_cast<const uint4*>(d + o_rf);
     p->tb.tw = reinterpret_cast<const float4*>(d + o_tw);
-    p->tb.of = reinterpret_cast<const uint4*>(d + o_of);
-    p->tb.oi = reinterpret_cast<const uint4*>(d + o_oi);
-    p->tb.twf = reinterpret_cast<const float4*>(d + o_twf);
-    p->tb.twi = reinterpret_cast<const float4*>(d + o_twi);
+    p->tb.outer = d + o_of;
+    p->tb.outer_bytes = uint32_t(((outer_end - o_of) + 15) & ~size_t(15));
+    p->tb.off_oi = uint32_t(o_oi - o_of);
+    p->tb.off_twf = uint32_t(o_twf - o_of);
+    p->tb.off_twi = uint32_t(o_twi - o_of);
     *out = p;
     return FFTCONV_OK;
 }

@@ -45,14 +45,19 @@
 namespace fftconv {
 
 // Device tables of a fused plan (built on the host in double precision).
+// The four "outer" tables are one contiguous block so a CTA can copy them to
+// shared memory with a single bulk copy.
 struct FusedTables {
-    const uint4* lf;   // [lane][4]  left-product A fragments of F16/4: (m,s) -> uint4
-    const uint4* rf;   // [lane][4]  right-product B fragments of F16/4: (s,nt) pairs
-    const float4* tw;  // [lane][4]  W_256^(k2*n3) for (m,c,e)
-    const uint4* of;   // outer forward A fragments
-    const uint4* oi;   // outer inverse A fragments
-    const float4* twf; // [nt][m][lane]  W_M^(o*k1) in outer-output order
-    const float4* twi; // [k1][nt][lane] W_M^(o*k1) in inner-output order
+    const uint4* lf;       // [lane][4]  left-product A fragments of F16/4: (m,s) -> uint4
+    const uint4* rf;       // [lane][4]  right-product B fragments of F16/4: (s,nt) pairs
+    const float4* tw;      // [lane][4]  W_256^(k2*n3) for (m,c,e)
+    const uint8_t* outer;  // block: of | oi | twf | twi
+    uint32_t outer_bytes;  // multiple of 16
+    uint32_t off_oi, off_twf, off_twi;  // byte offsets inside the block (of at 0)
+    // of : [m][s][lane] uint4   outer forward A fragments of F_R1/sqrt(R1)
+    // oi : [m][s][lane] uint4   outer inverse A fragments
+    // twf: [nt][m][lane] float4 W_M^(o*k1) in outer-output order
+    // twi: [k1][nt][lane] float4 W_M^(o*k1) in inner-output order
 };
 
 template <int R1, bool GATED>
@@ -61,7 +66,7 @@ struct FusedCfg {
     static constexpr int N = M;                   // real samples per row
     static constexpr int RP = R1 >= 16 ? 1 : 16 / R1;  // rows per CTA
     static constexpr int HALF = R1 / 2;           // nonzero outer inputs
-    static constexpr int UNITS = RP * (R1 / 2);   // sub-problem pairs per CTA
+    static constexpr int UNITS = RP * (R1 / 2);   // sub-problem pairs per row group
     static constexpr int NTILES = RP * 32;        // 8-vector tiles of the outer stage
     static constexpr int NWARPS = 8;
     static constexpr int SEG = 264;               // staged segment: 256 words + 8 pad
@@ -71,16 +76,29 @@ struct FusedCfg {
     static constexpr bool K8I = R1 <= 4;          // inverse outer uses K = 8
     static constexpr int KS_I = K8I ? 1 : R1 / 8;
     static constexpr int MT_I = (R1 + 15) / 16;
-    static constexpr int STAGE_WORDS = HALF * SEG;
-    static constexpr int SCRATCH_WORDS = NWARPS * 256 * 2;
-    static constexpr int STAGE_ALL = RP * STAGE_WORDS * (GATED ? 2 : 1);
-    static constexpr int UNION_WORDS = STAGE_ALL > SCRATCH_WORDS ? STAGE_ALL : SCRATCH_WORDS;
-    static constexpr size_t SMEM_BYTES = size_t(RP) * M * 4 + size_t(UNION_WORDS) * 4 + 16;
+    static constexpr bool TSMEM = R1 <= 16;       // outer tables resident in shared memory
+    static constexpr int NSPEC = RP > 1 ? NWARPS : 1;  // warps that own a self-paired sub-problem 0
+    // shared-memory layout (bytes)
+    static constexpr size_t TAB_BYTES = TSMEM ? (size_t(MT_F) * KS_F * 512 + size_t(MT_I) * KS_I * 512 +
+                                                 size_t(MT_F) * 16384 + size_t(R1) * 2048 + 4 * 256)
+                                              : 0;
+    static constexpr size_t ROW_BYTES = size_t(RP) * M * 4;
+    static constexpr size_t SEG_BYTES = size_t(RP) * HALF * SEG * 4;
+    static constexpr size_t IN_BYTES = SEG_BYTES * (GATED ? 2 : 1);
+    static constexpr size_t WO_BYTES = GATED ? SEG_BYTES : 0;
+    static constexpr size_t SCR_BYTES = size_t(NSPEC) * 256 * 8;
+    static constexpr size_t OFF_ROW = TAB_BYTES;
+    static constexpr size_t OFF_IN = OFF_ROW + ROW_BYTES;
+    static constexpr size_t OFF_WO = OFF_IN + IN_BYTES;
+    static constexpr size_t OFF_SCR = OFF_WO + WO_BYTES;
+    static constexpr size_t OFF_BAR = OFF_SCR + SCR_BYTES;
+    static constexpr size_t SMEM_BYTES = OFF_BAR + 32;
 };
 
 // Row-buffer swizzle (complex-word index): XOR bits 3-4 with bits of the
 // sub-problem index and bit 5, which keeps all four access patterns of the
-// kernel free of bank conflicts.
+// kernel free of bank conflicts.  The kernel applies it through hoisted,
+// per-thread bases (the XOR term is constant along each access sequence).
 __device__ __forceinline__ int swz(int p) {
     return p ^ ((((p >> 8) & 3) ^ ((p >> 5) & 1)) << 3);
 }
@@ -117,14 +135,18 @@ struct Inner {
     // Forward 256-point sub-transform of sub-problem k1 of the row buffer:
     // z[m*4+nt] = Z[k2 = g+8m][k3 = 4nt+t].
     __device__ __forceinline__ void forward(const uint32_t* rb, int k1, int g, int t, cpx (&z)[8]) const {
+        // position 256*k1 + 16*(8s + 4j + t) + 8c + g, swizzled
+        const int X = ((k1 & 3) ^ ((t >> 1) & 1)) << 3;
+        const uint32_t* b0 = rb + 256 * k1 + (((16 * t) ^ X) + g);
+        const uint32_t* b1 = rb + 256 * k1 + (((16 * t + 8) ^ X) + g);
         uint32_t b[2][2][2];  // [s][c][reg]
         #pragma unroll
-        for (int s = 0; s < 2; ++s)
-            #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                b[s][c][0] = rb[swz(256 * k1 + 16 * (8 * s + t) + 8 * c + g)];
-                b[s][c][1] = rb[swz(256 * k1 + 16 * (8 * s + 4 + t) + 8 * c + g)];
-            }
+        for (int s = 0; s < 2; ++s) {
+            b[s][0][0] = b0[128 * s];
+            b[s][0][1] = b0[128 * s + 64];
+            b[s][1][0] = b1[128 * s];
+            b[s][1][1] = b1[128 * s + 64];
+        }
         float d[2][2][4];
         #pragma unroll
         for (int m = 0; m < 2; ++m)
@@ -183,222 +205,314 @@ struct Inner {
     }
 };
 
+// One bin of the decimation-in-time fold with the kernel spectrum:
+// returns alpha~ conj(z) + beta~ zp, alpha~ and beta~ packed 16-bit complex.
+template <int DT>
+__device__ __forceinline__ cpx dit_fold(uint32_t alpha, uint32_t beta, cpx z, cpx zp) {
+    const cpx al = Op<DT>::unpack(alpha), be = Op<DT>::unpack(beta);
+    return {al.r * z.r + al.i * z.i + be.r * zp.r - be.i * zp.i,
+            al.i * z.r - al.r * z.i + be.r * zp.i + be.i * zp.r};
+}
+
+struct FusedArgs {
+    const uint16_t* u;
+    const uint16_t* w_in;
+    const uint16_t* w_out;
+    const uint4* kf;
+    uint16_t* y;
+    int B, H;
+    FusedTables tb;
+    int* err;
+};
+
+// Persistent fused kernel: each CTA walks a contiguous range of row groups
+// taken channel-major (row index h*B + b), so consecutive rows share k_f[h].
+// The next group's input is fetched by the TMA engine while the current
+// group runs its inner stages; w_out (gated) is fetched during the same
+// window into its own buffer.
 template <int DT, int R1, bool GATED>
-__global__ void __launch_bounds__(256, 2)
-fused_conv_kernel(const uint16_t* __restrict__ u, const uint16_t* __restrict__ w_in,
-                  const uint16_t* __restrict__ w_out, const uint4* __restrict__ kf,
-                  uint16_t* __restrict__ y, int B, int H, FusedTables tb, int* __restrict__ err) {
+__global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
     using C = FusedCfg<R1, GATED>;
     using O = Op<DT>;
-    constexpr int M = C::M, N = C::N, RP = C::RP, HALF = C::HALF;
+    constexpr int M = C::M, N = C::N, RP = C::RP, HALF = C::HALF, SEG = C::SEG;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint32_t* rowbuf = reinterpret_cast<uint32_t*>(smem);              // [RP][M]
-    uint32_t* stage_u = rowbuf + RP * M;                               // [RP][HALF][SEG]
-    uint32_t* stage_w = stage_u + RP * C::STAGE_WORDS;                 // gated only
-    cpx* scratch = reinterpret_cast<cpx*>(stage_u);                    // aliases staging
-    uint64_t* bar = reinterpret_cast<uint64_t*>(stage_u + C::UNION_WORDS);
+    uint32_t* rowbuf = reinterpret_cast<uint32_t*>(smem + C::OFF_ROW);   // [RP][M]
+    uint32_t* stage_u = reinterpret_cast<uint32_t*>(smem + C::OFF_IN);   // [RP][HALF][SEG]
+    uint32_t* stage_w = stage_u + RP * HALF * SEG;                       // gated: w_in
+    uint32_t* wobuf = reinterpret_cast<uint32_t*>(smem + C::OFF_WO);     // gated: w_out
+    cpx* scratch = reinterpret_cast<cpx*>(smem + C::OFF_SCR);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);     // tab, in, wo
     __shared__ int s_fail;
+
+    const FusedTables& tb = a.tb;
+    const uint4* of_t = reinterpret_cast<const uint4*>(C::TSMEM ? smem : tb.outer);
+    const uint4* oi_t = reinterpret_cast<const uint4*>((C::TSMEM ? smem : tb.outer) + tb.off_oi);
+    const float4* twf_t = reinterpret_cast<const float4*>((C::TSMEM ? smem : tb.outer) + tb.off_twf);
+    const float4* twi_t = reinterpret_cast<const float4*>((C::TSMEM ? smem : tb.outer) + tb.off_twi);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const long rows = long(B) * H;
-    const long row0 = long(blockIdx.x) * RP;  // rows are taken channel-major: idx = h*B + b
+    const long rows = long(a.B) * a.H;
+    const long G = (rows + RP - 1) / RP;
+    const long g0 = long(blockIdx.x) * G / gridDim.x, g1 = long(blockIdx.x + 1) * G / gridDim.x;
+    if (g0 >= g1) return;
 
-    auto row_of = [&](int j) -> long {
-        long idx = row0 + j;
-        long h = idx / B, b = idx - h * B;
-        return b * H + h;
+    auto row_of = [&](long idx) -> long {  // channel-major index -> row b*H + h
+        const long h = idx / a.B, b = idx - h * a.B;
+        return b * a.H + h;
+    };
+    auto issue_in = [&](long grp) {  // thread 0: u (+ w_in) of a row group
+        uint32_t bytes = 0;
+        for (int j = 0; j < RP; ++j)
+            if (grp * RP + j < rows) bytes += HALF * 1024u * (GATED ? 2u : 1u);
+        mbar_expect_tx(&bars[1], bytes);
+        for (int j = 0; j < RP; ++j) {
+            if (grp * RP + j >= rows) break;
+            const long base = row_of(grp * RP + j) * N;
+            for (int n1 = 0; n1 < HALF; ++n1) {
+                bulk_g2s(stage_u + (j * HALF + n1) * SEG, a.u + base + 512 * n1, 1024, &bars[1]);
+                if (GATED) bulk_g2s(stage_w + (j * HALF + n1) * SEG, a.w_in + base + 512 * n1, 1024, &bars[1]);
+            }
+        }
+    };
+    auto issue_wo = [&](long grp) {  // thread 0: w_out of a row group
+        uint32_t bytes = 0;
+        for (int j = 0; j < RP; ++j)
+            if (grp * RP + j < rows) bytes += HALF * 1024u;
+        mbar_expect_tx(&bars[2], bytes);
+        for (int j = 0; j < RP; ++j) {
+            if (grp * RP + j >= rows) break;
+            const long base = row_of(grp * RP + j) * N;
+            for (int n1 = 0; n1 < HALF; ++n1)
+                bulk_g2s(wobuf + (j * HALF + n1) * SEG, a.w_out + base + 512 * n1, 1024, &bars[2]);
+        }
+    };
+    // bounded wait by thread 0, broadcast of the outcome; false = give up
+    auto wait_all = [&](int b, uint32_t parity) -> bool {
+        if (threadIdx.x == 0 && !mbar_wait_bounded(&bars[b], parity, kWaitLimit)) {
+            s_fail = 1;
+            atomicExch(a.err, 7);
+        }
+        __syncthreads();
+        if (s_fail) return false;
+        mbar_wait_bounded(&bars[b], parity, 4);  // completed phase: orders the copied bytes
+        return true;
     };
 
     if (threadIdx.x == 0) {
         s_fail = 0;
-        mbar_init(bar, 1);
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
         fence_mbar_init();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t bytes = 0;
-        for (int j = 0; j < RP; ++j)
-            if (row0 + j < rows) bytes += HALF * 1024u * (GATED ? 2u : 1u);
-        mbar_expect_tx(bar, bytes);
-        for (int j = 0; j < RP; ++j) {
-            if (row0 + j >= rows) break;
-            const long base = row_of(j) * N;
-            for (int n1 = 0; n1 < HALF; ++n1) {
-                bulk_g2s(stage_u + (j * HALF + n1) * C::SEG, u + base + 512 * n1, 1024, bar);
-                if (GATED)
-                    bulk_g2s(stage_w + (j * HALF + n1) * C::SEG, w_in + base + 512 * n1, 1024, bar);
-            }
+        if (C::TSMEM) {
+            mbar_expect_tx(&bars[0], tb.outer_bytes);
+            bulk_g2s(smem, tb.outer, tb.outer_bytes, &bars[0]);
         }
+        issue_in(g0);
     }
-
     Inner<DT> in;
     in.load(tb, lane);
-
-    if (threadIdx.x == 0) {
-        if (!mbar_wait_bounded(bar, 0, kWaitLimit)) {
-            s_fail = 1;
-            atomicExch(err, 7);
-            mbar_wait_bounded(bar, 0, kWaitLimit);  // let copies in flight land
-        }
+    if (C::TSMEM && !wait_all(0, 0)) {
+        if (threadIdx.x == 0) mbar_wait_bounded(&bars[1], 0, kWaitLimit);
+        return;
     }
-    __syncthreads();
-    if (s_fail) return;
-    mbar_wait_bounded(bar, 0, 4);  // phase already complete: orders the copied bytes
 
-    // ---------------- outer forward stage: k1 outputs of 8 vectors per tile
-    for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
-        const int j = ntg >> 5, nt = ntg & 31;
-        if (row0 + j >= rows) continue;
-        const uint32_t* su = stage_u + j * C::STAGE_WORDS;
-        const uint32_t* sw = stage_w + j * C::STAGE_WORDS;
-        uint32_t bf[C::KS_F][2];
-        #pragma unroll
-        for (int s = 0; s < C::KS_F; ++s) {
-            const int na = 8 * s + t, nb = 8 * s + 4 + t;
-            uint32_t va = 0, vb = 0;
-            if (na < HALF) {
-                va = su[na * C::SEG + 8 * nt + g];
-                if (GATED) va = O::mul2(va, sw[na * C::SEG + 8 * nt + g]);
-            }
-            if (!C::K8F && nb < HALF) {
-                vb = su[nb * C::SEG + 8 * nt + g];
-                if (GATED) vb = O::mul2(vb, sw[nb * C::SEG + 8 * nt + g]);
-            }
-            bf[s][0] = va;
-            bf[s][1] = vb;
+    // per-thread address bases (see swz): warp w owns n-tiles w + 8i
+    const int xs = (warp >> 2) & 1;
+    const int st_base = 256 * g + ((8 * warp + 2 * t) ^ (((g & 3) ^ xs) << 3));   // + 2048m + 64i
+    const int oi_base = 256 * t + ((8 * warp + g) ^ (((t & 3) ^ xs) << 3));       // + 256(8s+4j) + 64i
+
+    uint32_t it = 0;
+    for (long grp = g0; grp < g1; ++grp, ++it) {
+        const uint32_t par = it & 1;
+        if (!wait_all(1, par)) {
+            if (threadIdx.x == 0 && GATED) mbar_wait_bounded(&bars[2], par ^ 1, kWaitLimit);
+            return;
         }
-        uint32_t* rb = rowbuf + j * M;
-        #pragma unroll
-        for (int m = 0; m < C::MT_F; ++m) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (C::K8F) {
-                uint4 a = tb.of[m * 32 + lane];
-                O::mma8(acc, a.x, a.y, bf[0][0]);
-            } else {
-                #pragma unroll
-                for (int s = 0; s < C::KS_F; ++s) {
-                    uint4 a = tb.of[(m * C::KS_F + s) * 32 + lane];
-                    const uint32_t af[4] = {a.x, a.y, a.z, a.w};
-                    O::mma16(acc, af, bf[s][0], bf[s][1]);
+        const long rbase = grp * RP;
+
+        // ---------------- outer forward stage: k1 outputs of 8 vectors per tile
+        #pragma unroll 1
+        for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
+            const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
+            if (rbase + j >= rows) continue;
+            const uint32_t* su = stage_u + j * HALF * SEG + t * SEG + 8 * nt + g;
+            const uint32_t* sw = stage_w + j * HALF * SEG + t * SEG + 8 * nt + g;
+            uint32_t bf[C::KS_F][2];
+            #pragma unroll
+            for (int s = 0; s < C::KS_F; ++s) {
+                const int na = 8 * s + t, nb = 8 * s + 4 + t;
+                uint32_t va = 0, vb = 0;
+                if (na < HALF) {
+                    va = su[8 * s * SEG];
+                    if (GATED) va = O::mul2(va, sw[8 * s * SEG]);
+                }
+                if (!C::K8F && nb < HALF) {
+                    vb = su[(8 * s + 4) * SEG];
+                    if (GATED) vb = O::mul2(vb, sw[(8 * s + 4) * SEG]);
+                }
+                bf[s][0] = va;
+                bf[s][1] = vb;
+            }
+            uint32_t* rb = rowbuf + j * M + st_base + 64 * i4;
+            #pragma unroll
+            for (int m = 0; m < C::MT_F; ++m) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (C::K8F) {
+                    const uint4 af = of_t[m * 32 + lane];
+                    O::mma8(acc, af.x, af.y, bf[0][0]);
+                } else {
+                    #pragma unroll
+                    for (int s = 0; s < C::KS_F; ++s) {
+                        const uint4 af = of_t[(m * C::KS_F + s) * 32 + lane];
+                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                    }
+                }
+                if (8 * m + g < R1) {
+                    const float4 w = twf_t[(nt * C::MT_F + m) * 32 + lane];
+                    const cpx v0 = cmul({acc[0], acc[2]}, {w.x, w.y});
+                    const cpx v1 = cmul({acc[1], acc[3]}, {w.z, w.w});
+                    *reinterpret_cast<uint2*>(rb + 2048 * m) = make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
                 }
             }
-            if (8 * m + g < R1) {
-                const float4 w = tb.twf[(nt * C::MT_F + m) * 32 + lane];
-                const cpx v0 = cmul({acc[0], acc[2]}, {w.x, w.y});
-                const cpx v1 = cmul({acc[1], acc[3]}, {w.z, w.w});
-                const int p = 256 * (8 * m + g) + 8 * nt + 2 * t;
-                *reinterpret_cast<uint2*>(rb + swz(p)) = make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {  // staging is free again: fetch ahead
+            if (GATED) issue_wo(grp);
+            if (grp + 1 < g1) issue_in(grp + 1);
+        }
+
+        // ---------------- inner stages + decimation fold, per sub-problem pair
+        #pragma unroll 1
+        for (int ug = warp; ug < C::UNITS; ug += C::NWARPS) {
+            const int j = ug / (R1 / 2), jj = ug % (R1 / 2);
+            if (rbase + j >= rows) continue;
+            const long h = (rbase + j) / a.B;
+            uint32_t* rb = rowbuf + j * M;
+            const int ka = jj, kb = jj == 0 ? R1 / 2 : R1 - jj;
+            cpx za[8], zb[8], pp[8];
+            in.forward(rb, ka, g, t, za);
+            in.forward(rb, kb, g, t, zb);
+            // C = alpha~ conj(Z) + beta~ Z_partner  (= conj Z_y), in place.
+            const uint4* fa = a.kf + (size_t(h * R1 + ka) * 4) * 32 + lane;
+            const uint4* fb = a.kf + (size_t(h * R1 + kb) * 4) * 32 + lane;
+            if (jj != 0) {
+                // bins of sub-problem ka pair with sub-problem kb through lane ^ 31
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) pp[i] = shfl31(za[7 - i]);  // partners of zb
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = fa[q * 32];
+                    #pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        const int i = 2 * q + sl;
+                        za[i] = dit_fold<DT>(sl ? v.z : v.x, sl ? v.w : v.y, za[i], shfl31(zb[7 - i]));
+                    }
+                }
+            } else {
+                // sub-problem R1/2 pairs with itself through lane ^ 31; sub-problem 0
+                // pairs bin kappa with (256 - kappa) mod 256 of itself
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) pp[i] = shfl31(zb[7 - i]);
+                cpx* sc = scratch + (RP > 1 ? warp : 0) * 256;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) sc[(g + 8 * (i >> 2)) + 16 * (4 * (i & 3) + t)] = za[i];
+                __syncwarp();
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = fa[q * 32];
+                    #pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        const int i = 2 * q + sl;
+                        const int kap = (g + 8 * (i >> 2)) + 16 * (4 * (i & 3) + t);
+                        za[i] = dit_fold<DT>(sl ? v.z : v.x, sl ? v.w : v.y, za[i], sc[(256 - kap) & 255]);
+                    }
+                }
+                __syncwarp();
+            }
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = fb[q * 32];
+                #pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const int i = 2 * q + sl;
+                    zb[i] = dit_fold<DT>(sl ? v.z : v.x, sl ? v.w : v.y, zb[i], pp[i]);
+                }
+            }
+            // inverse inner stages, then the outer twiddle, back to the row buffer
+            #pragma unroll
+            for (int side = 0; side < 2; ++side) {
+                const int k1 = side ? kb : ka;
+                cpx w[8];
+                in.inverse(side ? zb : za, w);
+                const int X = ((k1 & 3) ^ ((t >> 1) & 1)) << 3;
+                uint32_t* s0 = rb + 256 * k1 + (((16 * t) ^ X) + g);
+                uint32_t* s1 = rb + 256 * k1 + (((16 * t + 8) ^ X) + g);
+                #pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const float4 tv = twi_t[(k1 * 4 + nt) * 32 + lane];
+                    const cpx v0 = cmul(w[nt], {tv.x, tv.y});
+                    const cpx v1 = cmul(w[4 + nt], {tv.z, tv.w});
+                    s0[64 * nt] = O::pack(v0.r, v0.i);
+                    s1[64 * nt] = O::pack(v1.r, v1.i);
+                }
             }
         }
-    }
-    __syncthreads();
-
-    // ---------------- inner stages + decimation fold, per sub-problem pair
-    for (int ug = warp; ug < C::UNITS; ug += C::NWARPS) {
-        const int j = ug / (R1 / 2), jj = ug % (R1 / 2);
-        if (row0 + j >= rows) continue;
-        const long h = (row0 + j) / B;
-        uint32_t* rb = rowbuf + j * M;
-        const int ka = jj, kb = jj == 0 ? R1 / 2 : R1 - jj;
-        cpx za[8], zb[8], pa[8], pb[8];
-        in.forward(rb, ka, g, t, za);
-        in.forward(rb, kb, g, t, zb);
-        #pragma unroll
-        for (int i = 0; i < 8; ++i) pb[i] = shfl31(jj == 0 ? zb[7 - i] : za[7 - i]);
-        if (jj != 0) {
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) pa[i] = shfl31(zb[7 - i]);
+        if (GATED) {
+            if (!wait_all(2, par)) {
+                if (threadIdx.x == 0 && grp + 1 < g1) mbar_wait_bounded(&bars[1], par ^ 1, kWaitLimit);
+                return;
+            }
         } else {
-            // sub-problem 0 pairs bin kappa with (256 - kappa) mod 256 of itself
-            cpx* sc = scratch + warp * 256;
-            __syncwarp();
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) sc[(g + 8 * (i >> 2)) + 16 * (4 * (i & 3) + t)] = za[i];
-            __syncwarp();
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int kap = (g + 8 * (i >> 2)) + 16 * (4 * (i & 3) + t);
-                pa[i] = sc[(256 - kap) & 255];
-            }
-            __syncwarp();
+            __syncthreads();
         }
-        // C = alpha~ conj(Z) + beta~ Z_partner  (= conj Z_y)
-        const uint4* fa = kf + (size_t(h * R1 + ka) * 4) * 32 + lane;
-        const uint4* fb = kf + (size_t(h * R1 + kb) * 4) * 32 + lane;
-        #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 va = fa[q * 32], vb = fb[q * 32];
-            #pragma unroll
-            for (int sl = 0; sl < 2; ++sl) {
-                const int i = 2 * q + sl;
-                const cpx al = O::unpack(sl ? va.z : va.x), be = O::unpack(sl ? va.w : va.y);
-                const cpx z = za[i], pz = pa[i];
-                za[i] = {al.r * z.r + al.i * z.i + be.r * pz.r - be.i * pz.i,
-                         al.i * z.r - al.r * z.i + be.r * pz.i + be.i * pz.r};
-                const cpx al2 = O::unpack(sl ? vb.z : vb.x), be2 = O::unpack(sl ? vb.w : vb.y);
-                const cpx z2 = zb[i], pz2 = pb[i];
-                zb[i] = {al2.r * z2.r + al2.i * z2.i + be2.r * pz2.r - be2.i * pz2.i,
-                         al2.i * z2.r - al2.r * z2.i + be2.r * pz2.i + be2.i * pz2.r};
-            }
-        }
-        // inverse inner stages, then the outer twiddle, back to the row buffer
-        #pragma unroll
-        for (int side = 0; side < 2; ++side) {
-            const int k1 = side ? kb : ka;
-            cpx w[8];
-            in.inverse(side ? zb : za, w);
-            #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const float4 tv = tb.twi[(k1 * 4 + nt) * 32 + lane];
-                const cpx v0 = cmul(w[nt], {tv.x, tv.y});
-                const cpx v1 = cmul(w[4 + nt], {tv.z, tv.w});
-                const int o0 = 16 * (4 * nt + t) + g;
-                rb[swz(256 * k1 + o0)] = O::pack(v0.r, v0.i);
-                rb[swz(256 * k1 + o0 + 8)] = O::pack(v1.r, v1.i);
-            }
-        }
-    }
-    __syncthreads();
 
-    // ---------------- outer inverse stage (first R1/2 outputs only) and store
-    for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
-        const int j = ntg >> 5, nt = ntg & 31;
-        if (row0 + j >= rows) continue;
-        const uint32_t* rb = rowbuf + j * M;
-        uint32_t bf[C::KS_I][2];
-        #pragma unroll
-        for (int s = 0; s < C::KS_I; ++s) {
-            bf[s][0] = rb[swz(256 * (8 * s + t) + 8 * nt + g)];
-            bf[s][1] = C::K8I ? 0u : rb[swz(256 * (8 * s + 4 + t) + 8 * nt + g)];
-        }
-        const long base = row_of(j) * N;
-        #pragma unroll
-        for (int m = 0; m < C::MT_I; ++m) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (C::K8I) {
-                uint4 a = tb.oi[m * 32 + lane];
-                O::mma8(acc, a.x, a.y, bf[0][0]);
-            } else {
-                #pragma unroll
-                for (int s = 0; s < C::KS_I; ++s) {
-                    uint4 a = tb.oi[(m * C::KS_I + s) * 32 + lane];
-                    const uint32_t af[4] = {a.x, a.y, a.z, a.w};
-                    O::mma16(acc, af, bf[s][0], bf[s][1]);
+        // ---------------- outer inverse stage (first R1/2 outputs only) and store
+        #pragma unroll 1
+        for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
+            const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
+            if (rbase + j >= rows) continue;
+            const uint32_t* rb = rowbuf + j * M + oi_base + 64 * i4;
+            uint32_t bf[C::KS_I][2];
+            #pragma unroll
+            for (int s = 0; s < C::KS_I; ++s) {
+                bf[s][0] = rb[256 * 8 * s];
+                bf[s][1] = C::K8I ? 0u : rb[256 * (8 * s + 4)];
+            }
+            const long base = row_of(rbase + j) * N;
+            #pragma unroll
+            for (int m = 0; m < C::MT_I; ++m) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (C::K8I) {
+                    const uint4 af = oi_t[m * 32 + lane];
+                    O::mma8(acc, af.x, af.y, bf[0][0]);
+                } else {
+                    #pragma unroll
+                    for (int s = 0; s < C::KS_I; ++s) {
+                        const uint4 af = oi_t[(m * C::KS_I + s) * 32 + lane];
+                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                    }
+                }
+                const int n1 = 8 * m + g;
+                if (n1 < HALF) {
+                    const int p = 256 * n1 + 8 * nt + 2 * t;  // complex index; reals 2p..2p+3
+                    float r0 = acc[0], i0 = -acc[2], r1 = acc[1], i1 = -acc[3];
+                    if (GATED) {
+                        const uint2 wv = *reinterpret_cast<const uint2*>(wobuf + (j * HALF + n1) * SEG + 8 * nt + 2 * t);
+                        const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
+                        r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
+                    }
+                    *reinterpret_cast<uint2*>(a.y + base + 2 * p) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
                 }
             }
-            const int n1 = 8 * m + g;
-            if (n1 < HALF) {
-                const long p = 256 * n1 + 8 * nt + 2 * t;  // complex index; reals 2p..2p+3
-                float r0 = acc[0], i0 = -acc[2], r1 = acc[1], i1 = -acc[3];
-                if (GATED) {
-                    const uint2 wv = *reinterpret_cast<const uint2*>(w_out + base + 2 * p);
-                    const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
-                    r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
-                }
-                *reinterpret_cast<uint2*>(y + base + 2 * p) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
-            }
         }
+        __syncthreads();
     }
 }
 

@@ -1,0 +1,87 @@
+"""The C-ABI library: loads, exports every declared symbol, host-side logic
+(no compute calls; runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fft_long_convolution_gb300 as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fftconv.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fftconv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = F.lib()
+    names = declared_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+    assert sorted(F.EXPORTED) == names
+
+
+def test_version_and_status_strings():
+    assert F.lib().fftconv_version().decode().count(".") == 2
+    for code in range(8):
+        s = F.status_string(code)
+        assert s and s != "unknown status"
+    assert F.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("N,R1", [(1024, 4), (2048, 8), (4096, 16), (8192, 32), (16384, 64)])
+def test_query_fused_factorization(N, R1):
+    for dt in (F.F16, F.BF16):
+        q = F.query(N, dt)
+        assert q["path"] == F.PATH_FUSED and q["order"] == 3
+        assert q["factors"] == [R1, 16, 16]
+        assert q["factors"][0] * 16 * 16 == N == q["M"]
+        assert q["kf_bytes_per_channel"] == 8 * N
+        assert q["workspace_bytes_per_row"] == 0
+
+
+@pytest.mark.parametrize("N", [0, 1000, 512, 3 << 12, 1 << 22])
+def test_query_rejects_unsupported_lengths(N):
+    with pytest.raises(F.FFTConvError) as e:
+        F.query(N, F.BF16)
+    assert e.value.status == 2
+
+
+def test_query_rejects_bad_order_and_dtype():
+    with pytest.raises(F.FFTConvError):
+        F.query(4096, F.BF16, order=2)
+    with pytest.raises(F.FFTConvError):
+        F.query(4096, 7)
+    assert F.lib().fftconv_plan_query(4096, 1, 0, None) == 1
+
+
+def test_null_plan_and_argument_validation_without_gpu():
+    L = F.lib()
+    vp = ctypes.c_void_p
+    assert L.fftconv_forward(None, vp(16), vp(16), vp(16), 1, 1, None) == 1
+    assert L.fftconv_forward_gated(None, vp(16), vp(16), vp(16), vp(16), vp(16), 1, 1, None) == 1
+    assert L.fftconv_kernel_fft(None, vp(16), vp(16), 1, None) == 1
+    assert L.fftconv_kf_bytes(None, 4) == 0
+    assert L.fftconv_workspace_bytes(None, 1, 1) == 0
+    assert L.fftconv_plan_destroy(None) == 0
+    assert L.fftconv_set_workspace(None, None, 0) == 1
+    h = ctypes.c_void_p()
+    assert L.fftconv_plan_create(ctypes.byref(h), 1000, 1, 0) == 2 and not h.value
+    assert L.fftconv_plan_create(None, 4096, 1, 0) == 1
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "fft_long_convolution_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "oracle/" not in text and "liboracle" not in text, f
