@@ -10,7 +10,7 @@
 #include <vector>
 
 #include "../../include/fftconv.h"
-#include "fused.cuh"
+#include "multipass.cuh"
 
 using namespace fftconv;
 
@@ -65,6 +65,8 @@ struct fftconv_plan_s {
     void* dev = nullptr;  // one allocation: tables + error word
     int* dev_err = nullptr;
     FusedTables tb{};
+    MPTables mp{};
+    int R0 = 1;  // outer factor through HBM (1 on the fused path)
     int num_sms = 0;
     void* workspace = nullptr;
     size_t workspace_bytes = 0;
@@ -91,7 +93,14 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
         q.factors[2] = 16;
         q.workspace_bytes_per_row = 0;
     } else {
-        return FFTCONV_ERR_UNSUPPORTED;  // multi-pass lengths: not built yet
+        // multi-pass: M = R0 * 64 * 16 * 16, outer factor R0 through HBM
+        q.path = FFTCONV_PATH_MULTIPASS;
+        q.order = 4;
+        q.factors[0] = int32_t(N / 16384);
+        q.factors[1] = 64;
+        q.factors[2] = 16;
+        q.factors[3] = 16;
+        q.workspace_bytes_per_row = 4 * N;  // 16-bit complex intermediate
     }
     if (order != 0 && order != q.order) return FFTCONV_ERR_UNSUPPORTED;
     q.kf_bytes_per_channel = q.M * 8;  // two 16-bit complex coefficients per bin
@@ -223,6 +232,30 @@ HostTables build_fused_tables(int R1, int dtype) {
     return T;
 }
 
+// A fragments of the full R-point DFT F_R/sqrt(R) (R a multiple of 16):
+// rows (k, ro) = (8m + (r&7), r>>3), K (n, ri) = (8s + (q>>1), q&1).
+std::vector<uint32_t> build_full_frags(int R, int dtype) {
+    const int MT = R / 8, KS = R / 8;
+    const double sc = 1.0 / std::sqrt(double(R));
+    std::vector<uint32_t> v(size_t(MT) * KS * 32 * 4, 0);
+    for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3;
+        for (int m = 0; m < MT; ++m)
+            for (int s = 0; s < KS; ++s) {
+                auto el = [&](int r, int q) {
+                    cd w = W(R, int64_t(8 * m + (r & 7)) * (8 * s + (q >> 1)));
+                    return embed(cd{w.r * sc, w.i * sc}, r >> 3, q & 1);
+                };
+                uint32_t* o = &v[((m * KS + s) * 32 + lane) * 4];
+                o[0] = pack2(el(g, 2 * t), el(g, 2 * t + 1), dtype);
+                o[1] = pack2(el(g + 8, 2 * t), el(g + 8, 2 * t + 1), dtype);
+                o[2] = pack2(el(g, 2 * t + 8), el(g, 2 * t + 9), dtype);
+                o[3] = pack2(el(g + 8, 2 * t + 8), el(g + 8, 2 * t + 9), dtype);
+            }
+    }
+    return v;
+}
+
 template <typename T>
 size_t append(std::vector<uint8_t>& blob, const std::vector<T>& v) {
     size_t off = (blob.size() + 255) & ~size_t(255);
@@ -281,6 +314,66 @@ cudaError_t launch_fused(const fftconv_plan_s* p, const void* u, const void* wi,
                  : launch_fused_r<1, false>(p, u, wi, wo, kf, y, B, H, st);
 }
 
+// ---- multi-pass dispatch
+template <typename K>
+cudaError_t prep(K fn, size_t smem, int threads, int* per_sm) {
+    if (*per_sm == 0) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem);
+        if (e != cudaSuccess) return e;
+        *per_sm = nb > 0 ? nb : 1;
+    }
+    return cudaSuccess;
+}
+
+template <int DT, int R0, bool G>
+cudaError_t launch_mp_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
+    constexpr int HALF = R0 / 2;
+    const size_t smem_a = size_t(HALF) * kSeg * 4 * (G ? 2 : 1) + 32;
+    const size_t smem_c = size_t(R0) * kSeg * 4 + (G ? size_t(HALF) * kSeg * 4 : 0) + 32;
+    static int na = 0, nb = 0, nc = 0;
+    cudaError_t e;
+    if ((e = prep(mp_pass_a<DT, R0, G>, smem_a, 256, &na)) != cudaSuccess) return e;
+    if ((e = prep(mp_pass_b<DT>, kMpBSmem, 512, &nb)) != cudaSuccess) return e;
+    if ((e = prep(mp_pass_c<DT, R0, G>, smem_c, 256, &nc)) != cudaSuccess) return e;
+    const int64_t items_ac = rows * (kMpL / 256), items_b = rows * (R0 / 2);
+    auto grid = [&](int64_t items, int per_sm) {
+        int64_t gsz = int64_t(p->num_sms) * per_sm;
+        return unsigned(gsz < items ? gsz : items);
+    };
+    mp_pass_a<DT, R0, G><<<grid(items_ac, na), 256, smem_a, st>>>(args);
+    mp_pass_b<DT><<<grid(items_b, nb), 512, kMpBSmem, st>>>(args);
+    mp_pass_c<DT, R0, G><<<grid(items_ac, nc), 256, smem_c, st>>>(args);
+    return cudaGetLastError();
+}
+
+template <int DT, bool G>
+cudaError_t launch_mp_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
+    switch (p->R0) {
+        case 2: return launch_mp_t<DT, 2, G>(p, args, rows, st);
+        case 4: return launch_mp_t<DT, 4, G>(p, args, rows, st);
+        case 8: return launch_mp_t<DT, 8, G>(p, args, rows, st);
+        case 16: return launch_mp_t<DT, 16, G>(p, args, rows, st);
+        case 32: return launch_mp_t<DT, 32, G>(p, args, rows, st);
+        case 64: return launch_mp_t<DT, 64, G>(p, args, rows, st);
+        case 128: return launch_mp_t<DT, 128, G>(p, args, rows, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_multipass(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
+                             const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+    MPArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
+                static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
+                static_cast<uint32_t*>(p->workspace), int(B), int(H), p->R0, p->mp, p->dev_err};
+    const bool gated = wi != nullptr;
+    if (p->info.dtype == FFTCONV_F16)
+        return gated ? launch_mp_r<0, true>(p, args, B * H, st) : launch_mp_r<0, false>(p, args, B * H, st);
+    return gated ? launch_mp_r<1, true>(p, args, B * H, st) : launch_mp_r<1, false>(p, args, B * H, st);
+}
+
 }  // namespace
 
 extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype,
@@ -294,13 +387,28 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     if (!p) return FFTCONV_ERR_ALLOC;
     p->info = info;
     p->R1 = info.factors[0];
+    const bool multi = info.path == FFTCONV_PATH_MULTIPASS;
+    p->R0 = multi ? info.factors[0] : 1;
+    p->R1 = multi ? kMpR1 : info.factors[0];
     HostTables T = build_fused_tables(p->R1, dtype);
+    HostTables T0;
+    std::vector<uint32_t> ofull;
+    if (multi) {
+        T0 = build_fused_tables(p->R0, dtype);
+        ofull = build_full_frags(kMpR1, dtype);
+    }
     std::vector<uint8_t> blob;
     const size_t o_err = append(blob, std::vector<int>(64, 0));
     const size_t o_lf = append(blob, T.lf), o_rf = append(blob, T.rf), o_tw = append(blob, T.tw);
     const size_t o_of = append(blob, T.of), o_oi = append(blob, T.oi);
     const size_t o_twf = append(blob, T.twf), o_twi = append(blob, T.twi);
     const size_t outer_end = o_twi + T.twi.size() * sizeof(float);
+    size_t o_ofa = 0, o_oic = 0, o_ofull = 0;
+    if (multi) {
+        o_ofa = append(blob, T0.of);
+        o_oic = append(blob, T0.oi);
+        o_ofull = append(blob, ofull);
+    }
     blob.resize((blob.size() + 255) & ~size_t(255));
     if (cudaMalloc(&p->dev, blob.size()) != cudaSuccess) {
         cudaGetLastError();
@@ -331,6 +439,16 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     p->tb.off_oi = uint32_t(o_oi - o_of);
     p->tb.off_twf = uint32_t(o_twf - o_of);
     p->tb.off_twi = uint32_t(o_twi - o_of);
+    if (multi) {
+        p->mp.lf = p->tb.lf;
+        p->mp.rf = p->tb.rf;
+        p->mp.tw = p->tb.tw;
+        p->mp.of_a = reinterpret_cast<const uint4*>(d + o_ofa);
+        p->mp.oi_c = reinterpret_cast<const uint4*>(d + o_oic);
+        p->mp.ofull = reinterpret_cast<const uint4*>(d + o_ofull);
+        p->mp.twf = reinterpret_cast<const float4*>(d + o_twf);
+        p->mp.twi = reinterpret_cast<const float4*>(d + o_twi);
+    }
     *out = p;
     return FFTCONV_OK;
 }
@@ -403,25 +521,30 @@ __device__ __forceinline__ uint32_t pack_dt(float lo, float hi, int dtype) {
     return dtype == FFTCONV_F16 ? Op<0>::pack(lo, hi) : Op<1>::pack(lo, hi);
 }
 
-// k_f for the fused layout: per (h, k1, q, lane) two bins, each with
-// alpha~ = conj(alpha), beta~ = conj(beta) of the decimation fold.
-__global__ void kfft_finalize_fused(const float2* __restrict__ K, uint4* __restrict__ kf, int64_t H,
-                                    int R1, int dtype) {
-    const int64_t M = int64_t(R1) * 256, L = 2 * M;
-    const int64_t total = H * R1 * 4 * 32;
+// k_f: per (h, k0, k1, q, lane) two bins, each with alpha~ = conj(alpha)
+// and beta~ = conj(beta) of the decimation fold, in the order the forward
+// kernels hold the bins: thread (g, t) of the warp that transforms
+// sub-problem k1 of sub-row k0 holds kappa' = (g + 8m) + 16(4nt + t), i.e.
+// frequency k = k0 + R0*(k1 + R1*kappa').  R0 = 1 on the fused path.
+__global__ void kfft_finalize(const float2* __restrict__ K, uint4* __restrict__ kf, int64_t H, int R0,
+                              int R1, int dtype) {
+    const int64_t M = int64_t(R0) * R1 * 256, L = 2 * M;
+    const int64_t total = H * R0 * R1 * 4 * 32;
     for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
          idx += int64_t(gridDim.x) * blockDim.x) {
         const int lane = int(idx & 31);
         const int q = int((idx >> 5) & 3);
         const int64_t hk = idx >> 7;
         const int k1 = int(hk % R1);
-        const int64_t h = hk / R1;
+        const int64_t hk0 = hk / R1;
+        const int k0 = int(hk0 % R0);
+        const int64_t h = hk0 / R0;
         const int g = lane >> 2, t = lane & 3;
         uint32_t words[4];
         for (int sl = 0; sl < 2; ++sl) {
             const int i = 2 * q + sl, m = i >> 2, nt = i & 3;
             const int64_t kap = (g + 8 * m) + 16 * (4 * nt + t);
-            const int64_t k = k1 + int64_t(R1) * kap;
+            const int64_t k = k0 + int64_t(R0) * (k1 + int64_t(R1) * kap);
             const float2 A = K[h * L + k], Bm = K[h * L + (M - k)];
             double st, ct;
             sincospi(double(k) / double(M), &st, &ct);  // theta = pi k / M
@@ -482,8 +605,8 @@ extern "C" fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float*
         a = b;
         b = tmp;
     }
-    kfft_finalize_fused<<<grid_for(H * plan->R1 * 128), 256, 0, st>>>(
-        a, static_cast<uint4*>(k_f), H, plan->R1, plan->info.dtype);
+    kfft_finalize<<<grid_for(H * plan->R0 * plan->R1 * 128), 256, 0, st>>>(
+        a, static_cast<uint4*>(k_f), H, plan->R0, plan->R1, plan->info.dtype);
     cudaError_t e = cudaGetLastError();
     cudaFreeAsync(buf, st);
     return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
@@ -506,7 +629,19 @@ static fftconv_status_t forward_impl(fftconv_plan_t plan, const void* u, const v
         (gated && (overlap(y, nb, w_in, nb) || overlap(y, nb, w_out, nb))))
         return FFTCONV_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_fused(plan, u, gated ? w_in : nullptr, gated ? w_out : nullptr, k_f, y, B, H, st);
+    cudaError_t e;
+    if (plan->info.path == FFTCONV_PATH_MULTIPASS) {
+        const size_t need = fftconv_workspace_bytes(plan, B, H);
+        if (!plan->workspace || plan->workspace_bytes < need) return FFTCONV_ERR_WORKSPACE;
+        const size_t nbw = need;
+        if (overlap(plan->workspace, nbw, u, nb) || overlap(plan->workspace, nbw, y, nb) ||
+            overlap(plan->workspace, nbw, k_f, kb) ||
+            (gated && (overlap(plan->workspace, nbw, w_in, nb) || overlap(plan->workspace, nbw, w_out, nb))))
+            return FFTCONV_ERR_INVALID;
+        e = launch_multipass(plan, u, gated ? w_in : nullptr, gated ? w_out : nullptr, k_f, y, B, H, st);
+    } else {
+        e = launch_fused(plan, u, gated ? w_in : nullptr, gated ? w_out : nullptr, k_f, y, B, H, st);
+    }
     if (e != cudaSuccess) return FFTCONV_ERR_CUDA;
     return FFTCONV_OK;
 }

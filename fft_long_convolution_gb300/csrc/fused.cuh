@@ -132,13 +132,11 @@ struct Inner {
         }
     }
 
-    // Forward 256-point sub-transform of sub-problem k1 of the row buffer:
-    // z[m*4+nt] = Z[k2 = g+8m][k3 = 4nt+t].
-    __device__ __forceinline__ void forward(const uint32_t* rb, int k1, int g, int t, cpx (&z)[8]) const {
-        // position 256*k1 + 16*(8s + 4j + t) + 8c + g, swizzled
-        const int X = ((k1 & 3) ^ ((t >> 1) & 1)) << 3;
-        const uint32_t* b0 = rb + 256 * k1 + (((16 * t) ^ X) + g);
-        const uint32_t* b1 = rb + 256 * k1 + (((16 * t + 8) ^ X) + g);
+    // Forward 256-point sub-transform of one sub-problem held in shared
+    // memory: b0 / b1 point at the words of (n2 = t, n3 = g) and (n2 = t,
+    // n3 = 8 + g); the other inputs sit at +128*s + 64*j (n2 = 8s + 4j + t).
+    // Result: z[m*4+nt] = Z[k2 = g+8m][k3 = 4nt+t].
+    __device__ __forceinline__ void forward_at(const uint32_t* b0, const uint32_t* b1, cpx (&z)[8]) const {
         uint32_t b[2][2][2];  // [s][c][reg]
         #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -157,6 +155,12 @@ struct Inner {
                 for (int s = 0; s < 2; ++s) O::mma16(d[m][c], lf[m][s], b[s][c][0], b[s][c][1]);
             }
         right_product(d, z);
+    }
+
+    // Same, sub-problem k1 of a swizzled row buffer (position 256*k1 + o).
+    __device__ __forceinline__ void forward(const uint32_t* rb, int k1, int g, int t, cpx (&z)[8]) const {
+        const int X = ((k1 & 3) ^ ((t >> 1) & 1)) << 3;
+        forward_at(rb + 256 * k1 + (((16 * t) ^ X) + g), rb + 256 * k1 + (((16 * t + 8) ^ X) + g), z);
     }
 
     // Twiddle the output of a left product and contract it with F16 from the

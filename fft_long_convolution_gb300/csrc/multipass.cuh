@@ -1,0 +1,413 @@
+// Multi-pass causal long convolution for N = M = R0 * 16384 (32K..2M).
+//
+// Partial fusion (FlashFFTConv page, section 3.4 "Kernel Fusion and
+// Recomputation Strategies" and the order-4 Algorithm 4): the outermost
+// Monarch factor R0 goes through HBM, everything inside it stays fused.
+//   n = L*n0 + n',  k = k0 + R0*kappa,  L = 16384
+//   pass A:  T[k0][n'] = W_M^(n'*k0) * sum_{n0 < R0/2} z[L*n0 + n'] W_R0^(n0*k0) / sqrt(R0)
+//            (implicit zero padding: z[n] = 0 for n >= M/2, i.e. n0 >= R0/2)
+//   pass B:  per pair of sub-rows (k0, R0-k0): the L-point transform of each
+//            sub-row as R1 = 64 outer factor x 16 x 16 (the fused machinery
+//            with a full outer stage), the decimation-in-time fold with the
+//            kernel spectrum (bin k pairs with M-k, which lives in sub-row
+//            R0-k0), the same stages back, and the W_M^(n'*k0) twiddle of
+//            the conjugate-trick inverse -> T (in place)
+//   pass C:  y_z[L*n0 + n'] = sum_{k0} W_R0^(n0*k0) T[k0][n'] / sqrt(R0), only
+//            n0 < R0/2 (causal truncation), conjugated (and gated) -> y.
+// T holds 16-bit complex words (the plan dtype); it is the caller's
+// workspace of B*H*N*4 bytes.  Each pass reads its operands with bulk copies
+// (TMA engine) into padded shared-memory segments and writes contiguous
+// 32-byte runs per output row.
+#pragma once
+#include "fused.cuh"
+
+namespace fftconv {
+
+constexpr int kMpL = 16384;   // sub-row length of pass B
+constexpr int kMpR1 = 64;     // outer factor inside pass B
+constexpr int kSeg = 264;     // staged 1 KB segment + 32 B pad (words)
+
+struct MPTables {
+    const uint4* lf;      // inner 16-point fragments (as the fused path)
+    const uint4* rf;
+    const float4* tw;
+    const uint4* of_a;    // pass A: F_R0/sqrt(R0) A fragments, half input   [m][s][lane]
+    const uint4* oi_c;    // pass C: F_R0/sqrt(R0) A fragments, half output  [m][s][lane]
+    const uint4* ofull;   // pass B: F_64/8 A fragments, full               [8][8][lane]
+    const float4* twf;    // pass B: W_L^(o*k1), outer-output order          [nt][m][lane]
+    const float4* twi;    // pass B: W_L^(o*k1), inner-output order          [k1][nt][lane]
+};
+
+struct MPArgs {
+    const uint16_t* u;
+    const uint16_t* w_in;
+    const uint16_t* w_out;
+    const uint4* kf;
+    uint16_t* y;
+    uint32_t* T;  // [rows][R0][L] 16-bit complex words
+    int B, H, R0;
+    MPTables tb;
+    int* err;
+};
+
+// W_M^j for M a power of two (exact angle: j / M is exact in float).
+__device__ __forceinline__ cpx twiddle_pow2(uint32_t j, uint32_t M) {
+    float s, c;
+    sincospif(-2.0f * (float(j) / float(M)), &s, &c);
+    return {c, s};
+}
+
+// Thread 0 waits (bounded) on a barrier phase, the CTA learns the outcome.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_fail, int* err) {
+    if (threadIdx.x == 0 && !mbar_wait_bounded(bar, parity, kWaitLimit)) {
+        *s_fail = 1;
+        atomicExch(err, 7);
+    }
+    __syncthreads();
+    if (*s_fail) return false;
+    mbar_wait_bounded(bar, parity, 4);
+    return true;
+}
+
+// ------------------------------------------------------------------ pass A
+template <int DT, int R0, bool GATED>
+__global__ void __launch_bounds__(256, 2) mp_pass_a(const MPArgs a) {
+    using O = Op<DT>;
+    constexpr int L = kMpL, HALF = R0 / 2, SEG = kSeg;
+    constexpr uint32_t M = uint32_t(R0) * L;
+    constexpr bool K8 = R0 <= 8;
+    constexpr int KS = K8 ? 1 : R0 / 16, MT = (R0 + 7) / 8;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t* su = reinterpret_cast<uint32_t*>(smem);  // [HALF][SEG]
+    uint32_t* sw = su + HALF * SEG;                     // gated: w_in
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sw + (GATED ? HALF * SEG : 0));
+    __shared__ int s_fail;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    const long rows = long(a.B) * a.H, tiles = L / 256, items = rows * tiles;
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t par = 0;
+    for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
+        const long row = item / tiles;
+        const int o_base = int(item % tiles) * 256;
+        const uint16_t* ur = a.u + row * long(M);
+        if (threadIdx.x == 0) {
+            mbar_expect_tx(bar, HALF * 1024u * (GATED ? 2u : 1u));
+            for (int n0 = 0; n0 < HALF; ++n0) {
+                bulk_g2s(su + n0 * SEG, ur + 2 * (long(L) * n0 + o_base), 1024, bar);
+                if (GATED) bulk_g2s(sw + n0 * SEG, a.w_in + row * long(M) + 2 * (long(L) * n0 + o_base), 1024, bar);
+            }
+        }
+        if (!cta_wait(bar, par, &s_fail, a.err)) return;
+        uint32_t* Trow = a.T + row * long(M);
+        #pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+            const int nt = warp + 8 * i;
+            uint32_t bf[KS][2];
+            #pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                const int na = 8 * s + t, nb = 8 * s + 4 + t;
+                uint32_t va = 0, vb = 0;
+                if (na < HALF) {
+                    va = su[na * SEG + 8 * nt + g];
+                    if (GATED) va = O::mul2(va, sw[na * SEG + 8 * nt + g]);
+                }
+                if (!K8 && nb < HALF) {
+                    vb = su[nb * SEG + 8 * nt + g];
+                    if (GATED) vb = O::mul2(vb, sw[nb * SEG + 8 * nt + g]);
+                }
+                bf[s][0] = va;
+                bf[s][1] = vb;
+            }
+            const uint32_t o = uint32_t(o_base + 8 * nt + 2 * t);
+            #pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                #pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    const uint4 af = a.tb.of_a[(m * KS + s) * 32 + lane];
+                    if (K8) {
+                        O::mma8(acc, af.x, af.y, bf[0][0]);
+                    } else {
+                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                    }
+                }
+                const uint32_t k0 = uint32_t(8 * m + g);
+                if (k0 < uint32_t(R0)) {
+                    const cpx v0 = cmul({acc[0], acc[2]}, twiddle_pow2((o * k0) & (M - 1), M));
+                    const cpx v1 = cmul({acc[1], acc[3]}, twiddle_pow2(((o + 1) * k0) & (M - 1), M));
+                    *reinterpret_cast<uint2*>(Trow + long(k0) * L + o) =
+                        make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+                }
+            }
+        }
+        __syncthreads();  // staging is reused by the next item
+    }
+}
+
+// ------------------------------------------------------------------ pass C
+template <int DT, int R0, bool GATED>
+__global__ void __launch_bounds__(256, 2) mp_pass_c(const MPArgs a) {
+    using O = Op<DT>;
+    constexpr int L = kMpL, HALF = R0 / 2, SEG = kSeg;
+    constexpr long M = long(R0) * L;
+    constexpr bool K8 = R0 <= 4;
+    constexpr int KS = K8 ? 1 : R0 / 8, MT = (R0 + 15) / 16;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t* st = reinterpret_cast<uint32_t*>(smem);  // [R0][SEG]
+    uint32_t* swo = st + R0 * SEG;                      // gated: w_out [HALF][SEG]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(swo + (GATED ? HALF * SEG : 0));
+    __shared__ int s_fail;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    const long rows = long(a.B) * a.H, tiles = L / 256, items = rows * tiles;
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t par = 0;
+    for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
+        const long row = item / tiles;
+        const int o_base = int(item % tiles) * 256;
+        if (threadIdx.x == 0) {
+            mbar_expect_tx(bar, R0 * 1024u + (GATED ? HALF * 1024u : 0u));
+            for (int k0 = 0; k0 < R0; ++k0)
+                bulk_g2s(st + k0 * SEG, a.T + row * M + long(k0) * L + o_base, 1024, bar);
+            if (GATED)
+                for (int n0 = 0; n0 < HALF; ++n0)
+                    bulk_g2s(swo + n0 * SEG, a.w_out + row * M + 2 * (long(L) * n0 + o_base), 1024, bar);
+        }
+        if (!cta_wait(bar, par, &s_fail, a.err)) return;
+        #pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+            const int nt = warp + 8 * i;
+            uint32_t bf[KS][2];
+            #pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                const int ka = 8 * s + t, kb = 8 * s + 4 + t;
+                bf[s][0] = ka < R0 ? st[ka * SEG + 8 * nt + g] : 0u;
+                bf[s][1] = (!K8 && kb < R0) ? st[kb * SEG + 8 * nt + g] : 0u;
+            }
+            #pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                #pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    const uint4 af = a.tb.oi_c[(m * KS + s) * 32 + lane];
+                    if (K8) {
+                        O::mma8(acc, af.x, af.y, bf[0][0]);
+                    } else {
+                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                    }
+                }
+                const int n0 = 8 * m + g;
+                if (n0 < HALF) {
+                    const long p = long(L) * n0 + o_base + 8 * nt + 2 * t;  // reals 2p..2p+3
+                    float r0 = acc[0], i0 = -acc[2], r1 = acc[1], i1 = -acc[3];
+                    if (GATED) {
+                        const uint2 wv = *reinterpret_cast<const uint2*>(swo + n0 * SEG + 8 * nt + 2 * t);
+                        const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
+                        r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
+                    }
+                    *reinterpret_cast<uint2*>(a.y + row * M + 2 * p) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ pass B
+constexpr size_t kMpBSmem = size_t(2) * kMpR1 * kSeg * 4 + 256 * 8 + 32;
+
+template <int DT>
+__global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
+    using O = Op<DT>;
+    constexpr int L = kMpL, R1 = kMpR1, SEG = kSeg;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t* rbuf = reinterpret_cast<uint32_t*>(smem);                 // [2][R1][SEG]
+    cpx* scratch = reinterpret_cast<cpx*>(rbuf + 2 * R1 * SEG);         // [256]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(scratch + 256);
+    __shared__ int s_fail;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    const int R0 = a.R0;
+    const uint32_t M = uint32_t(R0) * L;
+    const long rows = long(a.B) * a.H, pairs = R0 / 2, items = rows * pairs;
+    if (threadIdx.x == 0) {
+        s_fail = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    Inner<DT> in;
+    in.load({a.tb.lf, a.tb.rf, a.tb.tw, nullptr, 0, 0, 0, 0}, lane);
+    uint32_t par = 0;
+    for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
+        const long row = item / pairs;
+        const int p = int(item % pairs);
+        const int k0s[2] = {p == 0 ? 0 : p, p == 0 ? R0 / 2 : R0 - p};
+        const long h = row % a.H;
+        uint32_t* Trow = a.T + row * long(M);
+        if (threadIdx.x == 0) {
+            mbar_expect_tx(bar, 2u * R1 * 1024u);
+            for (int side = 0; side < 2; ++side)
+                for (int n1 = 0; n1 < R1; ++n1)
+                    bulk_g2s(rbuf + (side * R1 + n1) * SEG, Trow + long(k0s[side]) * L + 256 * n1, 1024, bar);
+        }
+        if (!cta_wait(bar, par, &s_fail, a.err)) return;
+
+        // full 64-point outer stage, in place (each warp owns 8 columns)
+        #pragma unroll 1
+        for (int job = warp; job < 64; job += 16) {
+            uint32_t* rs = rbuf + (job >> 5) * R1 * SEG;
+            const int nt = job & 31;
+            uint32_t bf[8][2];
+            #pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                bf[s][0] = rs[(8 * s + t) * SEG + 8 * nt + g];
+                bf[s][1] = rs[(8 * s + 4 + t) * SEG + 8 * nt + g];
+            }
+            #pragma unroll 1
+            for (int m = 0; m < 8; ++m) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                #pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint4 af = a.tb.ofull[(m * 8 + s) * 32 + lane];
+                    const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                    O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                }
+                const float4 w = a.tb.twf[(nt * 8 + m) * 32 + lane];
+                const cpx v0 = cmul({acc[0], acc[2]}, {w.x, w.y});
+                const cpx v1 = cmul({acc[1], acc[3]}, {w.z, w.w});
+                *reinterpret_cast<uint2*>(rs + (8 * m + g) * SEG + 8 * nt + 2 * t) =
+                    make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+            }
+        }
+        __syncthreads();
+
+        // sub-problem pairs: 256-point transforms, fold, and back
+        #pragma unroll 1
+        for (int un = warp; un < 64; un += 16) {
+            int sa, sb, ka, kb;
+            bool fusedlike = false;
+            if (p == 0 && un < 32) {  // sub-row 0 pairs with itself: kappa <-> L - kappa
+                fusedlike = true;
+                sa = sb = 0;
+                ka = un;
+                kb = un == 0 ? R1 / 2 : R1 - un;
+            } else if (p == 0) {      // sub-row R0/2 pairs with itself: kappa <-> L-1-kappa
+                sa = sb = 1;
+                ka = un - 32;
+                kb = R1 - 1 - ka;
+            } else {                  // sub-rows k0 and R0-k0: kappa <-> L-1-kappa
+                sa = 0;
+                sb = 1;
+                ka = un;
+                kb = R1 - 1 - un;
+            }
+            uint32_t* ra = rbuf + sa * R1 * SEG + ka * SEG + 16 * t + g;
+            uint32_t* rbp = rbuf + sb * R1 * SEG + kb * SEG + 16 * t + g;
+            cpx za[8], zb[8], pp[8];
+            in.forward_at(ra, ra + 8, za);
+            in.forward_at(rbp, rbp + 8, zb);
+            const uint4* fa = a.kf + (size_t((h * R0 + k0s[sa]) * R1 + ka) * 4) * 32 + lane;
+            const uint4* fb = a.kf + (size_t((h * R0 + k0s[sb]) * R1 + kb) * 4) * 32 + lane;
+            if (fusedlike && un == 0) {
+                // sub-problem R1/2 with itself through lane ^ 31; sub-problem 0
+                // pairs bin kappa' with (256 - kappa') mod 256 of itself
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) pp[i] = shfl31(zb[7 - i]);
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) scratch[(g + 8 * (i >> 2)) + 16 * (4 * (i & 3) + t)] = za[i];
+                __syncwarp();
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = fa[q * 32];
+                    #pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        const int i = 2 * q + sl;
+                        const int kap = (g + 8 * (i >> 2)) + 16 * (4 * (i & 3) + t);
+                        za[i] = dit_fold<DT>(sl ? v.z : v.x, sl ? v.w : v.y, za[i], scratch[(256 - kap) & 255]);
+                    }
+                }
+                __syncwarp();
+            } else {
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) pp[i] = shfl31(za[7 - i]);
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = fa[q * 32];
+                    #pragma unroll
+                    for (int sl = 0; sl < 2; ++sl) {
+                        const int i = 2 * q + sl;
+                        za[i] = dit_fold<DT>(sl ? v.z : v.x, sl ? v.w : v.y, za[i], shfl31(zb[7 - i]));
+                    }
+                }
+            }
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = fb[q * 32];
+                #pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const int i = 2 * q + sl;
+                    zb[i] = dit_fold<DT>(sl ? v.z : v.x, sl ? v.w : v.y, zb[i], pp[i]);
+                }
+            }
+            #pragma unroll
+            for (int side = 0; side < 2; ++side) {
+                const int k1 = side ? kb : ka;
+                uint32_t* dst = side ? rbp : ra;  // (n2 = t, n3 = g) of sub-problem k1
+                cpx w[8];
+                in.inverse(side ? zb : za, w);
+                #pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const float4 tv = a.tb.twi[(k1 * 4 + nt) * 32 + lane];
+                    const cpx v0 = cmul(w[nt], {tv.x, tv.y});
+                    const cpx v1 = cmul(w[4 + nt], {tv.z, tv.w});
+                    dst[64 * nt] = O::pack(v0.r, v0.i);
+                    dst[64 * nt + 8] = O::pack(v1.r, v1.i);
+                }
+            }
+        }
+        __syncthreads();
+
+        // full 64-point inverse outer stage, pass-A twiddle, back to T
+        #pragma unroll 1
+        for (int job = warp; job < 64; job += 16) {
+            const int side = job >> 5, nt = job & 31;
+            const uint32_t* rs = rbuf + side * R1 * SEG;
+            const uint32_t k0 = uint32_t(k0s[side]);
+            uint32_t bf[8][2];
+            #pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                bf[s][0] = rs[(8 * s + t) * SEG + 8 * nt + g];
+                bf[s][1] = rs[(8 * s + 4 + t) * SEG + 8 * nt + g];
+            }
+            uint32_t* To = Trow + long(k0) * L;
+            #pragma unroll 1
+            for (int m = 0; m < 8; ++m) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                #pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint4 af = a.tb.ofull[(m * 8 + s) * 32 + lane];
+                    const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                    O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                }
+                const uint32_t np = uint32_t(256 * (8 * m + g) + 8 * nt + 2 * t);
+                const cpx v0 = cmul({acc[0], acc[2]}, twiddle_pow2((np * k0) & (M - 1), M));
+                const cpx v1 = cmul({acc[1], acc[3]}, twiddle_pow2(((np + 1) * k0) & (M - 1), M));
+                *reinterpret_cast<uint2*>(To + np) = make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+            }
+        }
+        __syncthreads();  // the row buffers are refilled by the next item
+    }
+}
+
+}  // namespace fftconv

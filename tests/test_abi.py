@@ -46,6 +46,16 @@ def test_query_fused_factorization(N, R1):
         assert q["workspace_bytes_per_row"] == 0
 
 
+@pytest.mark.parametrize("N,R0", [(32768, 2), (262144, 16), (2097152, 128)])
+def test_query_multipass_factorization(N, R0):
+    q = F.query(N, F.BF16)
+    assert q["path"] == F.PATH_MULTIPASS and q["order"] == 4
+    assert q["factors"] == [R0, 64, 16, 16]
+    assert R0 * 64 * 16 * 16 == N
+    assert q["workspace_bytes_per_row"] == 4 * N
+    assert q["kf_bytes_per_channel"] == 8 * N
+
+
 @pytest.mark.parametrize("N", [0, 1000, 512, 3 << 12, 1 << 22])
 def test_query_rejects_unsupported_lengths(N):
     with pytest.raises(F.FFTConvError) as e:
