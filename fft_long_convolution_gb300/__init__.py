@@ -19,8 +19,8 @@ STATUS = {0: "OK", 1: "ERR_INVALID", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIGN", 4: "E
 
 EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy", "fftconv_plan_get_info",
             "fftconv_kf_bytes", "fftconv_workspace_bytes", "fftconv_set_workspace", "fftconv_kernel_fft",
-            "fftconv_forward", "fftconv_forward_gated", "fftconv_device_status", "fftconv_status_string",
-            "fftconv_version"]
+            "fftconv_forward", "fftconv_forward_gated", "fftconv_forward_noalloc", "fftconv_device_status",
+            "fftconv_status_string", "fftconv_version"]
 
 
 class FFTConvError(RuntimeError):
@@ -66,6 +66,7 @@ def lib(auto_build: bool = True):
         L.fftconv_kernel_fft.argtypes = [vp, vp, vp, i64, vp]
         L.fftconv_forward.argtypes = [vp, vp, vp, vp, i64, i64, vp]
         L.fftconv_forward_gated.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp]
+        L.fftconv_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, vp]
         L.fftconv_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         L.fftconv_status_string.argtypes = [ctypes.c_int]
         L.fftconv_status_string.restype = ctypes.c_char_p

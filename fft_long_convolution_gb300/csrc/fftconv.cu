@@ -686,3 +686,69 @@ extern "C" const char* fftconv_status_string(fftconv_status_t s) {
 }
 
 extern "C" const char* fftconv_version(void) { return "0.1.0"; }
+
+// --------------------------------------------------------------- no-allocation forward
+//
+// For callers that cannot allocate device memory: the multi-pass
+// intermediate lives in this file-scope array instead of a caller workspace.
+// Host code must not use the array's name as a pointer (it is a host-side
+// stand-in); the device address is looked up once per device below.
+
+static __device__ __align__(256) uint8_t g_static_scratch[FFTCONV_STATIC_SCRATCH_BYTES];
+
+#include <mutex>
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up the
+// first time each device asks; nullptr on failure).
+void* static_scratch_for_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_scratch_ptr[dev] = ptr;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" fftconv_status_t fftconv_forward_noalloc(fftconv_plan_t plan, const void* u, const void* k_f,
+                                                    void* y, int64_t B, int64_t H, fftconv_stream_t stream) {
+    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (B == 0 || H == 0) return FFTCONV_OK;
+    if (!u || !k_f || !y) return FFTCONV_ERR_INVALID;
+    if (misaligned(u) || misaligned(k_f) || misaligned(y)) return FFTCONV_ERR_ALIGN;
+    if (B * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    const size_t nb = size_t(B) * size_t(H) * size_t(plan->info.N) * 2;
+    const size_t kb = fftconv_kf_bytes(plan, H);
+    if (overlap(y, nb, u, nb) || overlap(y, nb, k_f, kb)) return FFTCONV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (plan->info.path == FFTCONV_PATH_MULTIPASS) {
+        if (fftconv_workspace_bytes(plan, B, H) > FFTCONV_STATIC_SCRATCH_BYTES) return FFTCONV_ERR_WORKSPACE;
+        void* scratch = static_scratch_for_current_device();
+        if (!scratch) return FFTCONV_ERR_CUDA;
+        MPArgs args{static_cast<const uint16_t*>(u), nullptr, nullptr, static_cast<const uint4*>(k_f),
+                    static_cast<uint16_t*>(y), static_cast<uint32_t*>(scratch), int(B), int(H), plan->R0,
+                    plan->mp, plan->dev_err};
+        e = plan->info.dtype == FFTCONV_F16 ? launch_mp_r<0, false>(plan, args, B * H, st)
+                                            : launch_mp_r<1, false>(plan, args, B * H, st);
+    } else {
+        e = launch_fused(plan, u, nullptr, nullptr, k_f, y, B, H, st);
+    }
+    return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+}

@@ -158,6 +158,39 @@ fftconv_status_t fftconv_forward_gated(fftconv_plan_t plan, const void *u, const
                                        const void *w_out, const void *k_f, void *y, int64_t B,
                                        int64_t H, fftconv_stream_t stream);
 
+/* Size of the library's own scratch array used by fftconv_forward_noalloc. */
+#define FFTCONV_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Forward convolution that allocates no device memory and takes no workspace.
+ *
+ * The FlashFFTConv page has no counterpart for this entry point.  It is for
+ * callers that cannot call cudaMalloc themselves: code that runs inside a
+ * host framework whose allocator owns every device byte, plug-ins that are
+ * handed only their input and output buffers, and services that fix their
+ * memory budget before they start.  Lengths above 16384 normally need the
+ * caller's workspace of B*H*N*4 bytes (fftconv_set_workspace); this call
+ * keeps that intermediate in one array of FFTCONV_STATIC_SCRATCH_BYTES
+ * (64 MiB) compiled into the library, which every GPU that loads the
+ * library reserves until the process exits.  Lengths up to 16384 use no
+ * scratch at all and run the ordinary fused kernel.
+ *
+ * - Arguments, layouts, arithmetic and results are those of fftconv_forward.
+ * - If B*H*N*4 exceeds FFTCONV_STATIC_SCRATCH_BYTES (for example more than
+ *   64 rows of N = 262144, or more than 8 rows of N = 2^21), the call
+ *   returns FFTCONV_ERR_WORKSPACE and launches nothing.
+ * - The first call on a device looks up the array's address for the current
+ *   device; make that first call before any stream capture on the device.
+ * - Every call shares the one array.  Calls that can overlap on the GPU (on
+ *   different streams or from different host threads) race and corrupt each
+ *   other's results: serialise them.  Nothing in the array has to start at
+ *   zero, since each call writes every word before it reads it.
+ * - No cudaMalloc, cudaFree or other allocating routine is called.
+ * Returns OK, INVALID, ALIGN, WORKSPACE or CUDA.
+ */
+fftconv_status_t fftconv_forward_noalloc(fftconv_plan_t plan, const void *u, const void *k_f, void *y,
+                                         int64_t B, int64_t H, fftconv_stream_t stream);
+
 /*
  * Read and clear the plan's device error word (waits for `stream`).
  * *out = 0 if no bounded on-device wait has given up since the last call,
