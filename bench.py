@@ -107,7 +107,7 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, pci_bus_id: str):
+    def __init__(self, device_index: int):
         import ctypes
         import threading
         self.samples = []
@@ -120,7 +120,15 @@ class ClockSampler:
             if nv.nvmlInit_v2() != 0:
                 return
             h = ctypes.c_void_p()
-            if nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) != 0:
+            ok = False
+            try:  # match the CUDA device by PCI location when torch exposes it
+                import torch
+                p = torch.cuda.get_device_properties(device_index)
+                bus = "%08x:%02x:%02x.0" % (int(p.pci_domain_id), int(p.pci_bus_id), int(p.pci_device_id))
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(h)) != 0:
                 if nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
                     return
             mx = ctypes.c_uint()
@@ -283,7 +291,7 @@ def main():
     for _ in range(max(args.warmup, 3)):
         step()
     barrier()
-    clocks = ClockSampler(torch.cuda.get_device_properties(dev).pci_bus_id if hasattr(torch.cuda.get_device_properties(dev), "pci_bus_id") else "")
+    clocks = ClockSampler(local)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)

@@ -157,9 +157,9 @@ HostTables build_fused_tables(int R1, int dtype) {
             for (int c = 0; c < 2; ++c)
                 for (int e = 0; e < 2; ++e) {
                     cd w = W(256, int64_t(8 * m + g) * (8 * c + 2 * t + e));
-                    float* o = &T.tw[lane * 16 + (m * 2 + c) * 4 + e * 2];
-                    o[0] = float(w.r);
-                    o[1] = float(w.i);
+                    float* o = &T.tw[lane * 16 + (m * 2 + c) * 4];
+                    o[e] = float(w.r);      // real parts of e = 0, 1
+                    o[2 + e] = float(w.i);  // imaginary parts
                 }
     }
     // outer stages
@@ -212,8 +212,8 @@ HostTables build_fused_tables(int R1, int dtype) {
                 if (k1 >= R1) continue;
                 for (int e = 0; e < 2; ++e) {
                     cd w = W(M, int64_t(8 * nt + 2 * t + e) * k1);
-                    o[2 * e] = float(w.r);
-                    o[2 * e + 1] = float(w.i);
+                    o[e] = float(w.r);      // (wr e=0, wr e=1, wi e=0, wi e=1)
+                    o[2 + e] = float(w.i);
                 }
             }
     T.twi.assign(size_t(R1) * 4 * 32 * 4, 0.f);
@@ -276,18 +276,19 @@ cudaError_t launch_fused_t(const fftconv_plan_s* p, const void* u, const void* w
                                              int(C::SMEM_BYTES));
         if (e != cudaSuccess) return e;
         int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, 256, C::SMEM_BYTES);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, C::THREADS, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         blocks_per_sm = nb > 0 ? nb : 1;
     }
     if (C::TSMEM && p->tb.outer_bytes > C::TAB_BYTES) return cudaErrorInvalidValue;
     const int64_t groups = (B * H + C::RP - 1) / C::RP;
     int64_t grid = int64_t(p->num_sms) * blocks_per_sm;
-    if (grid > groups) grid = groups;
+    const int64_t need = (groups + C::GROUPS - 1) / C::GROUPS;
+    if (grid > need) grid = need;
     FusedArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
                    static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
                    int(B), int(H), p->tb, p->dev_err};
-    fn<<<dim3(unsigned(grid)), dim3(256), C::SMEM_BYTES, st>>>(args);
+    fn<<<dim3(unsigned(grid)), dim3(C::THREADS), C::SMEM_BYTES, st>>>(args);
     return cudaGetLastError();
 }
 

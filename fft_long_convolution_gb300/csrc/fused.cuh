@@ -64,11 +64,11 @@ template <int R1, bool GATED>
 struct FusedCfg {
     static constexpr int M = R1 * 256;            // complex length = N
     static constexpr int N = M;                   // real samples per row
-    static constexpr int RP = R1 >= 16 ? 1 : 16 / R1;  // rows per CTA
+    static constexpr int RP = R1 >= 16 ? 1 : 16 / R1;  // rows per row group
     static constexpr int HALF = R1 / 2;           // nonzero outer inputs
     static constexpr int UNITS = RP * (R1 / 2);   // sub-problem pairs per row group
     static constexpr int NTILES = RP * 32;        // 8-vector tiles of the outer stage
-    static constexpr int NWARPS = 8;
+    static constexpr int NWARPS = 8;              // warps per row pipeline
     static constexpr int SEG = 264;               // staged segment: 256 words + 8 pad
     static constexpr bool K8F = R1 <= 8;          // forward outer uses K = 8
     static constexpr int KS_F = K8F ? 1 : R1 / 16;
@@ -77,6 +77,14 @@ struct FusedCfg {
     static constexpr int KS_I = K8I ? 1 : R1 / 8;
     static constexpr int MT_I = (R1 + 15) / 16;
     static constexpr bool TSMEM = R1 <= 16;       // outer tables resident in shared memory
+    // Short rows: one CTA per SM runs two independent 8-warp row pipelines that
+    // share one copy of the tables, and each pipeline keeps the k_f of its
+    // current channel(s) in shared memory (loaded by the TMA engine only when
+    // the channel changes).  Long rows: 8-warp CTAs, k_f read through L2.
+    static constexpr int GROUPS = R1 <= 16 ? 2 : 1;
+    static constexpr int THREADS = 256 * GROUPS;
+    static constexpr int MINB = GROUPS == 2 ? 1 : 2;
+    static constexpr bool KFS = R1 <= 16;
     static constexpr int NSPEC = RP > 1 ? NWARPS : 1;  // warps that own a self-paired sub-problem 0
     // shared-memory layout (bytes)
     static constexpr size_t TAB_BYTES = TSMEM ? (size_t(MT_F) * KS_F * 512 + size_t(MT_I) * KS_I * 512 +
@@ -87,12 +95,15 @@ struct FusedCfg {
     static constexpr size_t IN_BYTES = SEG_BYTES * (GATED ? 2 : 1);
     static constexpr size_t WO_BYTES = GATED ? SEG_BYTES : 0;
     static constexpr size_t SCR_BYTES = size_t(NSPEC) * 256 * 8;
-    static constexpr size_t OFF_ROW = TAB_BYTES;
-    static constexpr size_t OFF_IN = OFF_ROW + ROW_BYTES;
-    static constexpr size_t OFF_WO = OFF_IN + IN_BYTES;
-    static constexpr size_t OFF_SCR = OFF_WO + WO_BYTES;
-    static constexpr size_t OFF_BAR = OFF_SCR + SCR_BYTES;
-    static constexpr size_t SMEM_BYTES = OFF_BAR + 32;
+    static constexpr size_t KF_BYTES = KFS ? size_t(RP) * R1 * 2048 : 0;
+    static constexpr size_t G_ROW = 0;
+    static constexpr size_t G_IN = G_ROW + ROW_BYTES;
+    static constexpr size_t G_WO = G_IN + IN_BYTES;
+    static constexpr size_t G_SCR = G_WO + WO_BYTES;
+    static constexpr size_t G_KF = G_SCR + SCR_BYTES;
+    static constexpr size_t GROUP_BYTES = G_KF + KF_BYTES;
+    static constexpr size_t OFF_BAR = TAB_BYTES + GROUPS * GROUP_BYTES;
+    static constexpr size_t SMEM_BYTES = OFF_BAR + 64;
 };
 
 // Row-buffer swizzle (complex-word index): XOR bits 3-4 with bits of the
@@ -114,7 +125,7 @@ struct Inner {
     using O = Op<DT>;
     uint32_t lf[2][2][4];  // [m][s]
     uint32_t rf[2][4][2];  // [s][nt]
-    cpx tw[2][2][2];       // [m][c][e]
+    float4 tw[2][2];       // [m][c]: (wr e=0, wr e=1, wi e=0, wi e=1)
 
     __device__ __forceinline__ void load(const FusedTables& tb, int lane) {
         #pragma unroll
@@ -126,9 +137,7 @@ struct Inner {
             const int s = q >> 1, nt = 2 * (q & 1);
             rf[s][nt][0] = w.x; rf[s][nt][1] = w.y;
             rf[s][nt + 1][0] = w.z; rf[s][nt + 1][1] = w.w;
-            float4 x = tb.tw[lane * 4 + q];  // (m, c) = (q>>1, q&1), e = 0, 1
-            tw[q >> 1][q & 1][0] = {x.x, x.y};
-            tw[q >> 1][q & 1][1] = {x.z, x.w};
+            tw[q >> 1][q & 1] = tb.tw[lane * 4 + q];  // (m, c) = (q>>1, q&1)
         }
     }
 
@@ -170,14 +179,12 @@ struct Inner {
         uint32_t a[2][4];
         #pragma unroll
         for (int s = 0; s < 2; ++s) {
-            cpx x00 = cmul({d[0][s][0], d[0][s][2]}, tw[0][s][0]);
-            cpx x10 = cmul({d[1][s][0], d[1][s][2]}, tw[1][s][0]);
-            cpx x01 = cmul({d[0][s][1], d[0][s][3]}, tw[0][s][1]);
-            cpx x11 = cmul({d[1][s][1], d[1][s][3]}, tw[1][s][1]);
-            a[s][0] = O::pack(x00.r, x00.i);
-            a[s][1] = O::pack(x10.r, x10.i);
-            a[s][2] = O::pack(x01.r, x01.i);
-            a[s][3] = O::pack(x11.r, x11.i);
+            const float4 x0 = cmul2_split(d[0][s][0], d[0][s][1], d[0][s][2], d[0][s][3], tw[0][s]);
+            const float4 x1 = cmul2_split(d[1][s][0], d[1][s][1], d[1][s][2], d[1][s][3], tw[1][s]);
+            a[s][0] = O::pack(x0.x, x0.z);
+            a[s][1] = O::pack(x1.x, x1.z);
+            a[s][2] = O::pack(x0.y, x0.w);
+            a[s][3] = O::pack(x1.y, x1.w);
         }
         #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
@@ -207,6 +214,85 @@ struct Inner {
             }
         right_product(d, w);
     }
+
+    // Two independent sub-problems at once (instruction-level parallelism:
+    // both left products, then both twiddles, then both right products).
+    // p0[side] / p1[side] as the b0 / b1 of forward_at.
+    __device__ __forceinline__ void forward2(const uint32_t* const (&p0)[2], const uint32_t* const (&p1)[2],
+                                             cpx (&za)[8], cpx (&zb)[8]) const {
+        uint32_t b[2][2][2][2];  // [side][s][c][reg]
+        #pragma unroll
+        for (int sd = 0; sd < 2; ++sd)
+            #pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                b[sd][s][0][0] = p0[sd][128 * s];
+                b[sd][s][0][1] = p0[sd][128 * s + 64];
+                b[sd][s][1][0] = p1[sd][128 * s];
+                b[sd][s][1][1] = p1[sd][128 * s + 64];
+            }
+        float d[2][2][2][4];  // [side][m][c]
+        #pragma unroll
+        for (int sd = 0; sd < 2; ++sd)
+            #pragma unroll
+            for (int m = 0; m < 2; ++m)
+                #pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    d[sd][m][c][0] = d[sd][m][c][1] = d[sd][m][c][2] = d[sd][m][c][3] = 0.f;
+                    #pragma unroll
+                    for (int s = 0; s < 2; ++s) O::mma16(d[sd][m][c], lf[m][s], b[sd][s][c][0], b[sd][s][c][1]);
+                }
+        right_product2(d, za, zb);
+    }
+
+    __device__ __forceinline__ void right_product2(const float (&d)[2][2][2][4], cpx (&oa)[8], cpx (&ob)[8]) const {
+        uint32_t a[2][2][4];  // [side][s]
+        #pragma unroll
+        for (int sd = 0; sd < 2; ++sd)
+            #pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const float4 x0 = cmul2_split(d[sd][0][s][0], d[sd][0][s][1], d[sd][0][s][2], d[sd][0][s][3], tw[0][s]);
+                const float4 x1 = cmul2_split(d[sd][1][s][0], d[sd][1][s][1], d[sd][1][s][2], d[sd][1][s][3], tw[1][s]);
+                a[sd][s][0] = O::pack(x0.x, x0.z);
+                a[sd][s][1] = O::pack(x1.x, x1.z);
+                a[sd][s][2] = O::pack(x0.y, x0.w);
+                a[sd][s][3] = O::pack(x1.y, x1.w);
+            }
+        #pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            float ea[4] = {0.f, 0.f, 0.f, 0.f}, eb[4] = {0.f, 0.f, 0.f, 0.f};
+            #pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                O::mma16(ea, a[0][s], rf[s][nt][0], rf[s][nt][1]);
+                O::mma16(eb, a[1][s], rf[s][nt][0], rf[s][nt][1]);
+            }
+            oa[nt] = {ea[0], ea[1]};
+            oa[4 + nt] = {ea[2], ea[3]};
+            ob[nt] = {eb[0], eb[1]};
+            ob[4 + nt] = {eb[2], eb[3]};
+        }
+    }
+
+    __device__ __forceinline__ void inverse2(const cpx (&ca)[8], const cpx (&cb)[8], cpx (&wa)[8], cpx (&wb)[8]) const {
+        uint32_t p[2][8];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            p[0][i] = O::pack(ca[i].r, ca[i].i);
+            p[1][i] = O::pack(cb[i].r, cb[i].i);
+        }
+        float d[2][2][2][4];
+        #pragma unroll
+        for (int sd = 0; sd < 2; ++sd)
+            #pragma unroll
+            for (int m = 0; m < 2; ++m)
+                #pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    d[sd][m][n][0] = d[sd][m][n][1] = d[sd][m][n][2] = d[sd][m][n][3] = 0.f;
+                    #pragma unroll
+                    for (int s = 0; s < 2; ++s)
+                        O::mma16(d[sd][m][n], lf[m][s], p[sd][n * 4 + 2 * s], p[sd][n * 4 + 2 * s + 1]);
+                }
+        right_product2(d, wa, wb);
+    }
 };
 
 // One bin of the decimation-in-time fold with the kernel spectrum:
@@ -229,24 +315,37 @@ struct FusedArgs {
     int* err;
 };
 
-// Persistent fused kernel: each CTA walks a contiguous range of row groups
-// taken channel-major (row index h*B + b), so consecutive rows share k_f[h].
-// The next group's input is fetched by the TMA engine while the current
-// group runs its inner stages; w_out (gated) is fetched during the same
-// window into its own buffer.
+// Persistent fused kernel.  Each row pipeline (8 warps) walks a contiguous
+// range of row groups taken channel-major (row index h*B + b), so consecutive
+// rows share k_f[h].  The next group's input and the current w_out are
+// fetched by the TMA engine while the inner stages run.
 template <int DT, int R1, bool GATED>
-__global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(FusedCfg<R1, GATED>::THREADS, FusedCfg<R1, GATED>::MINB)
+fused_conv_kernel(const FusedArgs a) {
     using C = FusedCfg<R1, GATED>;
     using O = Op<DT>;
     constexpr int M = C::M, N = C::N, RP = C::RP, HALF = C::HALF, SEG = C::SEG;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint32_t* rowbuf = reinterpret_cast<uint32_t*>(smem + C::OFF_ROW);   // [RP][M]
-    uint32_t* stage_u = reinterpret_cast<uint32_t*>(smem + C::OFF_IN);   // [RP][HALF][SEG]
-    uint32_t* stage_w = stage_u + RP * HALF * SEG;                       // gated: w_in
-    uint32_t* wobuf = reinterpret_cast<uint32_t*>(smem + C::OFF_WO);     // gated: w_out
-    cpx* scratch = reinterpret_cast<cpx*>(smem + C::OFF_SCR);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);     // tab, in, wo
-    __shared__ int s_fail;
+    __shared__ int s_fail[2];
+    __shared__ long s_kfh[2][4];  // channel held by each k_f slot
+    __shared__ int s_kfwait[2];   // 1 when the group's k_f barrier has a phase in flight
+    __shared__ uint32_t s_kfpar[2];
+    __shared__ int s_row[2][4];   // row index b*H + h of each row of the current group (-1: none)
+    __shared__ int s_ch[2][4];    // its channel h
+
+    const int gi = C::GROUPS > 1 ? int(threadIdx.x >> 8) : 0;
+    const int tg = threadIdx.x & 255;
+    const int lane = tg & 31, warp = tg >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t* gb = smem + C::TAB_BYTES + gi * C::GROUP_BYTES;
+    uint32_t* rowbuf = reinterpret_cast<uint32_t*>(gb + C::G_ROW);   // [RP][M]
+    uint32_t* stage_u = reinterpret_cast<uint32_t*>(gb + C::G_IN);   // [RP][HALF][SEG]
+    uint32_t* stage_w = stage_u + RP * HALF * SEG;                   // gated: w_in
+    uint32_t* wobuf = reinterpret_cast<uint32_t*>(gb + C::G_WO);     // gated: w_out
+    cpx* scratch = reinterpret_cast<cpx*>(gb + C::G_SCR);
+    uint4* kfbuf = reinterpret_cast<uint4*>(gb + C::G_KF);            // [RP][R1][4][32]
+    uint64_t* bar_tab = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* bars = bar_tab + 1 + 3 * gi;                           // in, wo, kf
 
     const FusedTables& tb = a.tb;
     const uint4* of_t = reinterpret_cast<const uint4*>(C::TSMEM ? smem : tb.outer);
@@ -254,76 +353,131 @@ __global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
     const float4* twf_t = reinterpret_cast<const float4*>((C::TSMEM ? smem : tb.outer) + tb.off_twf);
     const float4* twi_t = reinterpret_cast<const float4*>((C::TSMEM ? smem : tb.outer) + tb.off_twi);
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const long rows = long(a.B) * a.H;
-    const long G = (rows + RP - 1) / RP;
-    const long g0 = long(blockIdx.x) * G / gridDim.x, g1 = long(blockIdx.x + 1) * G / gridDim.x;
-    if (g0 >= g1) return;
+    // Row bookkeeping in 32-bit: the host guarantees B*H < 2^30.
+    const int rows = a.B * a.H;
+    const int G = (rows + RP - 1) / RP;
+    const int V = int(gridDim.x) * C::GROUPS, v = int(blockIdx.x) * C::GROUPS + gi;
+    const int g0 = int(int64_t(v) * G / V), g1 = int(int64_t(v + 1) * G / V);
 
-    auto row_of = [&](long idx) -> long {  // channel-major index -> row b*H + h
-        const long h = idx / a.B, b = idx - h * a.B;
+    auto gsync = [&]() {
+        if (C::GROUPS == 1) __syncthreads();
+        else asm volatile("bar.sync %0, 256;" ::"r"(1 + gi) : "memory");
+    };
+    auto row_of = [&](int idx) -> int {  // channel-major index -> row b*H + h
+        const int h = int(unsigned(idx) / unsigned(a.B)), b = idx - h * a.B;
         return b * a.H + h;
     };
-    auto issue_in = [&](long grp) {  // thread 0: u (+ w_in) of a row group
-        uint32_t bytes = 0;
-        for (int j = 0; j < RP; ++j)
-            if (grp * RP + j < rows) bytes += HALF * 1024u * (GATED ? 2u : 1u);
-        mbar_expect_tx(&bars[1], bytes);
+    // Bulk copies of a row group, issued by the lanes of warp 0 together: lane
+    // 0 arms the barrier with the byte count, lane l issues copies l, l+32, ...
+    auto issue_in = [&](int grp) {  // u (+ w_in)
+        int nrows = 0;
+        for (int j = 0; j < RP; ++j) nrows += grp * RP + j < rows;
+        if (lane == 0) mbar_expect_tx(&bars[0], uint32_t(nrows) * HALF * 1024u * (GATED ? 2u : 1u));
+        const int ncopy = nrows * HALF * (GATED ? 2 : 1);
+        for (int c = lane; c < ncopy; c += 32) {
+            const int tsel = GATED ? (c & 1) : 0, jn = GATED ? (c >> 1) : c;
+            const int j = jn / HALF, n1 = jn - j * HALF;
+            const size_t base = size_t(row_of(grp * RP + j)) * N + 512 * n1;
+            bulk_g2s((tsel ? stage_w : stage_u) + (j * HALF + n1) * SEG, (tsel ? a.w_in : a.u) + base, 1024, &bars[0]);
+        }
+    };
+    auto issue_wo = [&](int grp) {  // w_out
+        int nrows = 0;
+        for (int j = 0; j < RP; ++j) nrows += grp * RP + j < rows;
+        if (lane == 0) mbar_expect_tx(&bars[1], uint32_t(nrows) * HALF * 1024u);
+        for (int c = lane; c < nrows * HALF; c += 32) {
+            const int j = c / HALF, n1 = c - j * HALF;
+            bulk_g2s(wobuf + (j * HALF + n1) * SEG, a.w_out + size_t(row_of(grp * RP + j)) * N + 512 * n1, 1024,
+                     &bars[1]);
+        }
+    };
+    // k_f of the group's channels into the slots (one slot per row of the
+    // group), skipping slots that already hold the right channel.  Warp 0.
+    auto issue_kf = [&](int grp) {
+        if (!C::KFS) return;
+        uint32_t need = 0;
         for (int j = 0; j < RP; ++j) {
-            if (grp * RP + j >= rows) break;
-            const long base = row_of(grp * RP + j) * N;
-            for (int n1 = 0; n1 < HALF; ++n1) {
-                bulk_g2s(stage_u + (j * HALF + n1) * SEG, a.u + base + 512 * n1, 1024, &bars[1]);
-                if (GATED) bulk_g2s(stage_w + (j * HALF + n1) * SEG, a.w_in + base + 512 * n1, 1024, &bars[1]);
+            const int idx = grp * RP + j;
+            if (idx < rows && s_kfh[gi][j] != long(unsigned(idx) / unsigned(a.B))) need |= 1u << j;
+        }
+        __syncwarp();
+        if (need) {
+            if (lane == 0) mbar_expect_tx(&bars[2], uint32_t(__popc(need)) * R1 * 2048u);
+            for (int j = 0; j < RP; ++j)
+                if ((need >> j) & 1) {
+                    const int hh = int(unsigned(grp * RP + j) / unsigned(a.B));
+                    // R1 * 2 KB per channel, in 1 KB copies spread over the lanes
+                    for (int c = lane; c < R1 * 2; c += 32)
+                        bulk_g2s(reinterpret_cast<uint8_t*>(kfbuf) + size_t(j) * R1 * 2048 + 1024 * c,
+                                 reinterpret_cast<const uint8_t*>(a.kf) + size_t(hh) * R1 * 2048 + 1024 * c, 1024,
+                                 &bars[2]);
+                }
+            __syncwarp();
+            if (lane == 0) {
+                for (int j = 0; j < RP; ++j)
+                    if ((need >> j) & 1) s_kfh[gi][j] = long(unsigned(grp * RP + j) / unsigned(a.B));
+                s_kfwait[gi] = 1;
             }
         }
+        __syncwarp();
     };
-    auto issue_wo = [&](long grp) {  // thread 0: w_out of a row group
-        uint32_t bytes = 0;
-        for (int j = 0; j < RP; ++j)
-            if (grp * RP + j < rows) bytes += HALF * 1024u;
-        mbar_expect_tx(&bars[2], bytes);
-        for (int j = 0; j < RP; ++j) {
-            if (grp * RP + j >= rows) break;
-            const long base = row_of(grp * RP + j) * N;
-            for (int n1 = 0; n1 < HALF; ++n1)
-                bulk_g2s(wobuf + (j * HALF + n1) * SEG, a.w_out + base + 512 * n1, 1024, &bars[2]);
-        }
-    };
-    // bounded wait by thread 0, broadcast of the outcome; false = give up
-    auto wait_all = [&](int b, uint32_t parity) -> bool {
-        if (threadIdx.x == 0 && !mbar_wait_bounded(&bars[b], parity, kWaitLimit)) {
-            s_fail = 1;
+    // bounded wait by the group's first thread, broadcast of the outcome
+    auto wait_grp = [&](int b, uint32_t parity) -> bool {
+        if (tg == 0 && !mbar_wait_bounded(&bars[b], parity, kWaitLimit)) {
+            s_fail[gi] = 1;
             atomicExch(a.err, 7);
         }
-        __syncthreads();
-        if (s_fail) return false;
+        gsync();
+        if (s_fail[gi]) return false;
         mbar_wait_bounded(&bars[b], parity, 4);  // completed phase: orders the copied bytes
         return true;
     };
+    // the group's k_f wait (if a load is in flight), folded into the next barrier
+    auto kf_ready = [&]() {
+        if (C::KFS && tg == 0 && s_kfwait[gi]) {
+            if (!mbar_wait_bounded(&bars[2], s_kfpar[gi], kWaitLimit)) {
+                s_fail[gi] = 1;
+                atomicExch(a.err, 7);
+            }
+            s_kfpar[gi] ^= 1;
+            s_kfwait[gi] = 0;
+        }
+    };
 
     if (threadIdx.x == 0) {
-        s_fail = 0;
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int i = 0; i < 1 + 3 * C::GROUPS; ++i) mbar_init(&bar_tab[i], 1);
         fence_mbar_init();
     }
+    if (tg == 0) {
+        s_fail[gi] = 0;
+        s_kfwait[gi] = 0;
+        s_kfpar[gi] = 0;
+        for (int j = 0; j < 4; ++j) s_kfh[gi][j] = -1;
+    }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        if (C::TSMEM) {
-            mbar_expect_tx(&bars[0], tb.outer_bytes);
-            bulk_g2s(smem, tb.outer, tb.outer_bytes, &bars[0]);
-        }
+    if (threadIdx.x == 0 && C::TSMEM) {
+        mbar_expect_tx(bar_tab, tb.outer_bytes);
+        bulk_g2s(smem, tb.outer, tb.outer_bytes, bar_tab);
+    }
+    if (warp == 0 && g0 < g1) {
         issue_in(g0);
+        issue_kf(g0);
     }
     Inner<DT> in;
     in.load(tb, lane);
-    if (C::TSMEM && !wait_all(0, 0)) {
-        if (threadIdx.x == 0) mbar_wait_bounded(&bars[1], 0, kWaitLimit);
-        return;
+    if (C::TSMEM) {  // every thread of the CTA reaches this barrier
+        if (threadIdx.x == 0 && !mbar_wait_bounded(bar_tab, 0, kWaitLimit)) {
+            s_fail[0] = s_fail[C::GROUPS - 1] = 1;
+            atomicExch(a.err, 7);
+        }
+        __syncthreads();
+        if (s_fail[gi]) {
+            if (tg == 0) mbar_wait_bounded(&bars[0], 0, kWaitLimit);
+            return;
+        }
+        mbar_wait_bounded(bar_tab, 0, 4);
     }
+    if (g0 >= g1) return;
 
     // per-thread address bases (see swz): warp w owns n-tiles w + 8i
     const int xs = (warp >> 2) & 1;
@@ -331,13 +485,19 @@ __global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
     const int oi_base = 256 * t + ((8 * warp + g) ^ (((t & 3) ^ xs) << 3));       // + 256(8s+4j) + 64i
 
     uint32_t it = 0;
-    for (long grp = g0; grp < g1; ++grp, ++it) {
+    for (int grp = g0; grp < g1; ++grp, ++it) {
         const uint32_t par = it & 1;
-        if (!wait_all(1, par)) {
-            if (threadIdx.x == 0 && GATED) mbar_wait_bounded(&bars[2], par ^ 1, kWaitLimit);
+        if (tg < RP) {  // this group's rows, once (read after the barrier below)
+            const int idx = grp * RP + tg;
+            const int hh = int(unsigned(idx) / unsigned(a.B));
+            s_row[gi][tg] = idx < rows ? (idx - hh * a.B) * a.H + hh : -1;
+            s_ch[gi][tg] = hh;
+        }
+        if (!wait_grp(0, par)) {
+            if (tg == 0 && GATED) mbar_wait_bounded(&bars[1], par ^ 1, kWaitLimit);
             return;
         }
-        const long rbase = grp * RP;
+        const int rbase = grp * RP;
 
         // ---------------- outer forward stage: k1 outputs of 8 vectors per tile
         #pragma unroll 1
@@ -378,33 +538,46 @@ __global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
                     }
                 }
                 if (8 * m + g < R1) {
-                    const float4 w = twf_t[(nt * C::MT_F + m) * 32 + lane];
-                    const cpx v0 = cmul({acc[0], acc[2]}, {w.x, w.y});
-                    const cpx v1 = cmul({acc[1], acc[3]}, {w.z, w.w});
-                    *reinterpret_cast<uint2*>(rb + 2048 * m) = make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+                    const float4 v = cmul2_split(acc[0], acc[1], acc[2], acc[3], twf_t[(nt * C::MT_F + m) * 32 + lane]);
+                    *reinterpret_cast<uint2*>(rb + 2048 * m) = make_uint2(O::pack(v.x, v.z), O::pack(v.y, v.w));
                 }
             }
         }
-        __syncthreads();
-        if (threadIdx.x == 0) {  // staging is free again: fetch ahead
+        kf_ready();
+        gsync();
+        if (s_fail[gi]) return;
+        if (warp == 0) {  // staging is free again: fetch ahead
             if (GATED) issue_wo(grp);
             if (grp + 1 < g1) issue_in(grp + 1);
+            if (!C::KFS && lane == 0 && grp + 1 < g1 &&
+                unsigned(grp * RP + RP) / unsigned(a.B) != unsigned(grp * RP) / unsigned(a.B)) {
+                const int hh = int(unsigned(grp * RP + RP) / unsigned(a.B));  // next channel's k_f into L2
+                bulk_prefetch_l2(a.kf + size_t(hh) * R1 * 128, R1 * 2048u);
+            }
         }
 
         // ---------------- inner stages + decimation fold, per sub-problem pair
         #pragma unroll 1
-        for (int ug = warp; ug < C::UNITS; ug += C::NWARPS) {
+        for (int ug = C::NWARPS - 1 - warp; ug < C::UNITS; ug += C::NWARPS) {
+            // (the self-paired sub-problem 0 of each row lands on a late warp,
+            // away from warp 0, which issues the bulk copies)
             const int j = ug / (R1 / 2), jj = ug % (R1 / 2);
             if (rbase + j >= rows) continue;
-            const long h = (rbase + j) / a.B;
+            const int h = s_ch[gi][j];
             uint32_t* rb = rowbuf + j * M;
             const int ka = jj, kb = jj == 0 ? R1 / 2 : R1 - jj;
             cpx za[8], zb[8], pp[8];
-            in.forward(rb, ka, g, t, za);
-            in.forward(rb, kb, g, t, zb);
+            const uint4* kfb = C::KFS ? kfbuf + size_t(j) * R1 * 128 : a.kf + size_t(h) * R1 * 128;
+            const uint4* fa = kfb + ka * 128 + lane;
+            const uint4* fb = kfb + kb * 128 + lane;
+            {
+                const int Xa = ((ka & 3) ^ ((t >> 1) & 1)) << 3, Xb = ((kb & 3) ^ ((t >> 1) & 1)) << 3;
+                const uint32_t* const p0[2] = {rb + 256 * ka + (((16 * t) ^ Xa) + g), rb + 256 * kb + (((16 * t) ^ Xb) + g)};
+                const uint32_t* const p1[2] = {rb + 256 * ka + (((16 * t + 8) ^ Xa) + g),
+                                               rb + 256 * kb + (((16 * t + 8) ^ Xb) + g)};
+                in.forward2(p0, p1, za, zb);
+            }
             // C = alpha~ conj(Z) + beta~ Z_partner  (= conj Z_y), in place.
-            const uint4* fa = a.kf + (size_t(h * R1 + ka) * 4) * 32 + lane;
-            const uint4* fb = a.kf + (size_t(h * R1 + kb) * 4) * 32 + lane;
             if (jj != 0) {
                 // bins of sub-problem ka pair with sub-problem kb through lane ^ 31
                 #pragma unroll
@@ -449,17 +622,23 @@ __global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
                 }
             }
             // inverse inner stages, then the outer twiddle, back to the row buffer
+            cpx wab[2][8];
+            in.inverse2(za, zb, wab[0], wab[1]);
+            float4 tvs[2][4];
+            #pragma unroll
+            for (int side = 0; side < 2; ++side)
+                #pragma unroll
+                for (int nt = 0; nt < 4; ++nt) tvs[side][nt] = twi_t[((side ? kb : ka) * 4 + nt) * 32 + lane];
             #pragma unroll
             for (int side = 0; side < 2; ++side) {
                 const int k1 = side ? kb : ka;
-                cpx w[8];
-                in.inverse(side ? zb : za, w);
+                const cpx (&w)[8] = wab[side];
                 const int X = ((k1 & 3) ^ ((t >> 1) & 1)) << 3;
                 uint32_t* s0 = rb + 256 * k1 + (((16 * t) ^ X) + g);
                 uint32_t* s1 = rb + 256 * k1 + (((16 * t + 8) ^ X) + g);
                 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
-                    const float4 tv = twi_t[(k1 * 4 + nt) * 32 + lane];
+                    const float4 tv = tvs[side][nt];
                     const cpx v0 = cmul(w[nt], {tv.x, tv.y});
                     const cpx v1 = cmul(w[4 + nt], {tv.z, tv.w});
                     s0[64 * nt] = O::pack(v0.r, v0.i);
@@ -468,13 +647,15 @@ __global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
             }
         }
         if (GATED) {
-            if (!wait_all(2, par)) {
-                if (threadIdx.x == 0 && grp + 1 < g1) mbar_wait_bounded(&bars[1], par ^ 1, kWaitLimit);
+            if (!wait_grp(1, par)) {
+                if (tg == 0 && grp + 1 < g1) mbar_wait_bounded(&bars[0], par ^ 1, kWaitLimit);
                 return;
             }
         } else {
-            __syncthreads();
+            gsync();
         }
+        // k_f slots are free until the next inner phase: fetch the next group's
+        if (warp == 0 && grp + 1 < g1) issue_kf(grp + 1);
 
         // ---------------- outer inverse stage (first R1/2 outputs only) and store
         #pragma unroll 1
@@ -488,7 +669,7 @@ __global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
                 bf[s][0] = rb[256 * 8 * s];
                 bf[s][1] = C::K8I ? 0u : rb[256 * (8 * s + 4)];
             }
-            const long base = row_of(rbase + j) * N;
+            const size_t base = size_t(s_row[gi][j]) * N;
             #pragma unroll
             for (int m = 0; m < C::MT_I; ++m) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -516,8 +697,9 @@ __global__ void __launch_bounds__(256, 2) fused_conv_kernel(const FusedArgs a) {
                 }
             }
         }
-        __syncthreads();
+        gsync();
     }
+    if (C::KFS && tg == 0 && s_kfwait[gi]) mbar_wait_bounded(&bars[2], s_kfpar[gi], kWaitLimit);
 }
 
 }  // namespace fftconv

@@ -20,6 +20,27 @@ __device__ __forceinline__ cpx cmul(cpx a, cpx b) {
     return {a.r * b.r - a.i * b.i, a.r * b.i + a.i * b.r};
 }
 
+// Two complex numbers held as a real pair (r0, r1) and an imaginary pair
+// (i0, i1) -- the layout of an mma accumulator's (c0, c1) and (c2, c3) --
+// times two twiddles given as (wr0, wr1, wi0, wi1), with packed f32x2
+// arithmetic.  Returns (re0, re1) in out.x/out.y and (im0, im1) in out.z/out.w.
+__device__ __forceinline__ float4 cmul2_split(float r0, float r1, float i0, float i1, float4 w) {
+    unsigned long long R, I, Wr, Wi, t, u, v, re, im;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(R) : "f"(r0), "f"(r1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(I) : "f"(i0), "f"(i1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(Wr) : "f"(w.x), "f"(w.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(Wi) : "f"(w.z), "f"(w.w));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(R), "l"(Wr));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(u) : "l"(I), "l"(Wi));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(re) : "l"(t), "l"(u));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(v) : "l"(R), "l"(Wi));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(im) : "l"(I), "l"(Wr), "l"(v));
+    float4 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(re));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.z), "=f"(o.w) : "l"(im));
+    return o;
+}
+
 // Operand-type traits: 16-bit packing, unpacking, packed product and the
 // m16n8k16 / m16n8k8 contractions with float32 accumulation.
 template <int DTYPE> struct Op;
@@ -133,6 +154,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// Hint the TMA engine to pull a contiguous range into L2 (no completion).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void fence_mbar_init() {

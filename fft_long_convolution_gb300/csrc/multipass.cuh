@@ -283,11 +283,9 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
                     const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
                     O::mma16(acc, a4, bf[s][0], bf[s][1]);
                 }
-                const float4 w = a.tb.twf[(nt * 8 + m) * 32 + lane];
-                const cpx v0 = cmul({acc[0], acc[2]}, {w.x, w.y});
-                const cpx v1 = cmul({acc[1], acc[3]}, {w.z, w.w});
+                const float4 v = cmul2_split(acc[0], acc[1], acc[2], acc[3], a.tb.twf[(nt * 8 + m) * 32 + lane]);
                 *reinterpret_cast<uint2*>(rs + (8 * m + g) * SEG + 8 * nt + 2 * t) =
-                    make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+                    make_uint2(O::pack(v.x, v.z), O::pack(v.y, v.w));
             }
         }
         __syncthreads();
