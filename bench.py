@@ -171,7 +171,7 @@ def dist_env():
     return rank, world, local
 
 
-def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 12.0):
+def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 10.0):
     """The oracle on the host cores over a bounded sample of rows."""
     import oracle
     cores = os.cpu_count() or 1
@@ -185,7 +185,7 @@ def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 12.0):
     t0 = time.perf_counter()
     run()
     dt = time.perf_counter() - t0
-    reps = max(1, min(int(budget_s / max(dt, 1e-3)), 50))
+    reps = max(1, min(int(budget_s / max(dt, 1e-3)), 100000))
     t0 = time.perf_counter()
     for _ in range(reps):
         run()

@@ -11,6 +11,7 @@
 
 #include "../../include/fftconv.h"
 #include "multipass.cuh"
+#include "tcconv.cuh"
 
 using namespace fftconv;
 
@@ -67,6 +68,8 @@ struct fftconv_plan_s {
     FusedTables tb{};
     MPTables mp{};
     int R0 = 1;  // outer factor through HBM (1 on the fused path)
+    bool tc64 = false;              // N = 4096: order-2 64 x 64 product on tcgen05
+    const uint32_t* fmat = nullptr;  // its DFT matrix rows (device)
     int num_sms = 0;
     void* workspace = nullptr;
     size_t workspace_bytes = 0;
@@ -84,7 +87,14 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
     q.N = N;
     q.M = N;
     q.dtype = dtype;
-    if (N <= 16384) {
+    if (N == 4096) {
+        // fused on the fifth-generation tensor cores: M = 64 * 64
+        q.path = FFTCONV_PATH_FUSED;
+        q.order = 2;
+        q.factors[0] = 64;
+        q.factors[1] = 64;
+        q.workspace_bytes_per_row = 0;
+    } else if (N <= 16384) {
         // fused: M = R1 * 16 * 16
         q.path = FFTCONV_PATH_FUSED;
         q.order = 3;
@@ -103,7 +113,9 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
         q.workspace_bytes_per_row = 4 * N;  // 16-bit complex intermediate
     }
     if (order != 0 && order != q.order) return FFTCONV_ERR_UNSUPPORTED;
-    q.kf_bytes_per_channel = q.M * 8;  // two 16-bit complex coefficients per bin
+    // two 16-bit complex coefficients per bin (plus zero padding bins on the
+    // 64 x 64 path, whose k_f follows the kernel's column layout)
+    q.kf_bytes_per_channel = N == 4096 ? int64_t(Tc64::KFB) : q.M * 8;
     *info = q;
     return FFTCONV_OK;
 }
@@ -256,6 +268,23 @@ std::vector<uint32_t> build_full_frags(int R, int dtype) {
     return v;
 }
 
+// Rows of F64/8 in the tensor-memory order of the 64 x 64 path (tcconv.cuh):
+// lane L = 32w + 16b + 8p + r holds output kappa = b ? 63 - 8w - r : 8w + r,
+// part p; word n holds the two K elements of input n (real, imaginary).
+std::vector<uint32_t> build_tc64_fmat(int dtype) {
+    std::vector<uint32_t> v(128 * 64, 0);
+    for (int L = 0; L < 128; ++L) {
+        const int w = L >> 5, b = (L >> 4) & 1, part = (L >> 3) & 1, r = L & 7;
+        const int kap = b ? 63 - 8 * w - r : 8 * w + r;
+        for (int n = 0; n < 64; ++n) {
+            cd x = W(64, int64_t(kap) * n);
+            x = {x.r / 8.0, x.i / 8.0};
+            v[size_t(L) * 64 + n] = pack2(embed(x, part, 0), embed(x, part, 1), dtype);
+        }
+    }
+    return v;
+}
+
 template <typename T>
 size_t append(std::vector<uint8_t>& blob, const std::vector<T>& v) {
     size_t off = (blob.size() + 255) & ~size_t(255);
@@ -293,8 +322,31 @@ cudaError_t launch_fused_t(const fftconv_plan_s* p, const void* u, const void* w
 }
 
 template <int DT, bool G>
+cudaError_t launch_tc64_t(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
+                          const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+    auto fn = tc64_conv_kernel<DT, G>;
+    static bool ready = false;  // per instantiation, set once per process
+    if (!ready) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Tc64::SMEM));
+        if (e != cudaSuccess) return e;
+        ready = true;
+    }
+    // one CTA per SM (its tensor-memory allocation takes all 512 columns);
+    // work items are pairs of rows of one channel, two pipelines per CTA
+    const int64_t items = (B + 1) / 2 * H;
+    const int64_t need = (items + 1) / 2;
+    const int64_t grid = need < p->num_sms ? need : p->num_sms;
+    Tc64Args args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
+                  static_cast<const uint16_t*>(wo), static_cast<const uint8_t*>(kf), static_cast<uint16_t*>(y),
+                  p->fmat, int(B), int(H), p->dev_err};
+    fn<<<dim3(unsigned(grid)), dim3(Tc64::THREADS), Tc64::SMEM, st>>>(args);
+    return cudaGetLastError();
+}
+
+template <int DT, bool G>
 cudaError_t launch_fused_r(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
                            const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+    if (p->tc64) return launch_tc64_t<DT, G>(p, u, wi, wo, kf, y, B, H, st);
     switch (p->R1) {
         case 4: return launch_fused_t<DT, 4, G>(p, u, wi, wo, kf, y, B, H, st);
         case 8: return launch_fused_t<DT, 8, G>(p, u, wi, wo, kf, y, B, H, st);
@@ -391,7 +443,10 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     const bool multi = info.path == FFTCONV_PATH_MULTIPASS;
     p->R0 = multi ? info.factors[0] : 1;
     p->R1 = multi ? kMpR1 : info.factors[0];
-    HostTables T = build_fused_tables(p->R1, dtype);
+    p->tc64 = N == 4096;
+    HostTables T = p->tc64 ? HostTables{} : build_fused_tables(p->R1, dtype);
+    std::vector<uint32_t> fmat;
+    if (p->tc64) fmat = build_tc64_fmat(dtype);
     HostTables T0;
     std::vector<uint32_t> ofull;
     if (multi) {
@@ -404,6 +459,7 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     const size_t o_of = append(blob, T.of), o_oi = append(blob, T.oi);
     const size_t o_twf = append(blob, T.twf), o_twi = append(blob, T.twi);
     const size_t outer_end = o_twi + T.twi.size() * sizeof(float);
+    const size_t o_fmat = p->tc64 ? append(blob, fmat) : 0;
     size_t o_ofa = 0, o_oic = 0, o_ofull = 0;
     if (multi) {
         o_ofa = append(blob, T0.of);
@@ -432,6 +488,7 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     }
     uint8_t* d = static_cast<uint8_t*>(p->dev);
     p->dev_err = reinterpret_cast<int*>(d + o_err);
+    if (p->tc64) p->fmat = reinterpret_cast<const uint32_t*>(d + o_fmat);
     p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);
     p->tb.rf = reinterpret_cast<const uint4*>(d + o_rf);
     p->tb.tw = reinterpret_cast<const float4*>(d + o_tw);
@@ -522,6 +579,29 @@ __device__ __forceinline__ uint32_t pack_dt(float lo, float hi, int dtype) {
     return dtype == FFTCONV_F16 ? Op<0>::pack(lo, hi) : Op<1>::pack(lo, hi);
 }
 
+// The two coefficients of bin k of the decimation fold Z_y[k] = alpha Z[k] +
+// beta conj Z[M-k], stored conjugated (alpha~, beta~) as 16-bit complex words,
+// from the 2M-point spectrum K of the channel.
+__device__ void fold_coeffs(const float2* __restrict__ Kh, int64_t k, int64_t M, int dtype, uint32_t* wa,
+                            uint32_t* wb) {
+    const float2 A = Kh[k], Bm = Kh[M - k];
+    double st, ct;
+    sincospi(double(k) / double(M), &st, &ct);  // theta = pi k / M
+    const double Pr = 0.5 * (1.0 - st), Pi = 0.5 * ct;
+    const double Qr = 0.5 * (1.0 + st), Qi = -0.5 * ct;
+    const double Ar = A.x, Ai = A.y, Br = Bm.x, Bi = -Bm.y;  // B = conj K[M-k]
+    const double PAr = Pr * Ar - Pi * Ai, PAi = Pr * Ai + Pi * Ar;
+    const double QBr = Qr * Br - Qi * Bi, QBi = Qr * Bi + Qi * Br;
+    const double Sr = PAr + QBr, Si = PAi + QBi, Dr = PAr - QBr, Di = PAi - QBi;
+    // (i/2) W^k D with W^k = (cos, -sin)
+    const double WDr = ct * Dr + st * Di, WDi = ct * Di - st * Dr;
+    const double Xr = -0.5 * WDi, Xi = 0.5 * WDr;
+    const double ar = 0.5 * Sr - Xr, ai = 0.5 * Si - Xi;
+    const double br = 0.5 * Sr + Xr, bi = 0.5 * Si + Xi;
+    *wa = pack_dt(float(ar), float(-ai), dtype);
+    *wb = pack_dt(float(br), float(-bi), dtype);
+}
+
 // k_f: per (h, k0, k1, q, lane) two bins, each with alpha~ = conj(alpha)
 // and beta~ = conj(beta) of the decimation fold, in the order the forward
 // kernels hold the bins: thread (g, t) of the warp that transforms
@@ -546,23 +626,40 @@ __global__ void kfft_finalize(const float2* __restrict__ K, uint4* __restrict__ 
             const int i = 2 * q + sl, m = i >> 2, nt = i & 3;
             const int64_t kap = (g + 8 * m) + 16 * (4 * nt + t);
             const int64_t k = k0 + int64_t(R0) * (k1 + int64_t(R1) * kap);
-            const float2 A = K[h * L + k], Bm = K[h * L + (M - k)];
-            double st, ct;
-            sincospi(double(k) / double(M), &st, &ct);  // theta = pi k / M
-            const double Pr = 0.5 * (1.0 - st), Pi = 0.5 * ct;
-            const double Qr = 0.5 * (1.0 + st), Qi = -0.5 * ct;
-            const double Ar = A.x, Ai = A.y, Br = Bm.x, Bi = -Bm.y;  // B = conj K[M-k]
-            const double PAr = Pr * Ar - Pi * Ai, PAi = Pr * Ai + Pi * Ar;
-            const double QBr = Qr * Br - Qi * Bi, QBi = Qr * Bi + Qi * Br;
-            const double Sr = PAr + QBr, Si = PAi + QBi, Dr = PAr - QBr, Di = PAi - QBi;
-            // (i/2) W^k D with W^k = (cos, -sin)
-            const double WDr = ct * Dr + st * Di, WDi = ct * Di - st * Dr;
-            const double Xr = -0.5 * WDi, Xi = 0.5 * WDr;
-            const double ar = 0.5 * Sr - Xr, ai = 0.5 * Si - Xi;
-            const double br = 0.5 * Sr + Xr, bi = 0.5 * Si + Xi;
-            words[2 * sl] = pack_dt(float(ar), float(-ai), dtype);
-            words[2 * sl + 1] = pack_dt(float(br), float(-bi), dtype);
+            fold_coeffs(K + h * L, k, M, dtype, &words[2 * sl], &words[2 * sl + 1]);
         }
+        kf[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+    }
+}
+
+// k_f of the 64 x 64 path: per (h, chunk j < 9, warp w, half, lane) four
+// words, in the order the fold of tc64_conv_kernel consumes them: half 0 =
+// bins (s0, k2a), (s1, k2b); half 1 = bins (s0, k2b), (s1, k2a), where lane =
+// 4r + q, k2a = 8w + r, k2b = 63 - k2a, s0 = 4j + q and s1 = 64 - s0 (j < 8),
+// s0 = 32 for j = 8, q = 0.  Bin (s, k2) is k = s + 64 k2; padding bins
+// (the copies of sub-problems 0 and 32, unused columns) are zero.
+__global__ void kfft_finalize_tc64(const float2* __restrict__ K, uint4* __restrict__ kf, int64_t H, int dtype) {
+    const int64_t M = 4096, L = 2 * M;
+    const int64_t total = H * 9 * 4 * 2 * 32;
+    for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+         idx += int64_t(gridDim.x) * blockDim.x) {
+        const int lane = int(idx & 31), half = int((idx >> 5) & 1), w = int((idx >> 6) & 3);
+        const int64_t hj = idx >> 8;
+        const int j = int(hj % 9);
+        const int64_t h = hj / 9;
+        const int r = lane >> 2, q = lane & 3, k2a = 8 * w + r, k2b = 63 - k2a;
+        int s0, s1;
+        if (j < 8) {
+            s0 = 4 * j + q;
+            s1 = s0 == 0 ? -1 : 64 - s0;
+        } else {
+            s0 = q == 0 ? 32 : -1;
+            s1 = -1;
+        }
+        const int sa[2] = {s0, s1}, ka[2] = {half ? k2b : k2a, half ? k2a : k2b};
+        uint32_t words[4] = {0, 0, 0, 0};
+        for (int i = 0; i < 2; ++i)
+            if (sa[i] >= 0) fold_coeffs(K + h * L, sa[i] + 64 * int64_t(ka[i]), M, dtype, &words[2 * i], &words[2 * i + 1]);
         kf[idx] = make_uint4(words[0], words[1], words[2], words[3]);
     }
 }
@@ -606,8 +703,12 @@ extern "C" fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float*
         a = b;
         b = tmp;
     }
-    kfft_finalize<<<grid_for(H * plan->R0 * plan->R1 * 128), 256, 0, st>>>(
-        a, static_cast<uint4*>(k_f), H, plan->R0, plan->R1, plan->info.dtype);
+    if (plan->tc64)
+        kfft_finalize_tc64<<<grid_for(H * 9 * 4 * 2 * 32), 256, 0, st>>>(a, static_cast<uint4*>(k_f), H,
+                                                                           plan->info.dtype);
+    else
+        kfft_finalize<<<grid_for(H * plan->R0 * plan->R1 * 128), 256, 0, st>>>(
+            a, static_cast<uint4*>(k_f), H, plan->R0, plan->R1, plan->info.dtype);
     cudaError_t e = cudaGetLastError();
     cudaFreeAsync(buf, st);
     return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;

@@ -1,0 +1,149 @@
+// Fifth-generation tensor-core (tcgen05) primitives: tensor-memory (TMEM)
+// allocation, register <-> TMEM moves, the MMA with the A operand in TMEM and
+// the B operand in shared memory, its completion through an mbarrier, and a
+// named-barrier vote.
+//
+// Conventions used by the kernels:
+// - cta_group::1.  M = 128: row i of A and D is TMEM lane i.  M = 64: rows
+//   16c .. 16c+15 are lanes 32c .. 32c+15 (c = 0..3), for A and for D.
+//   Warp w of a CTA reaches lanes 32*(w%4) .. 32*(w%4)+31.
+// - A (16-bit, K-major) in TMEM: lane = row, each 32-bit column holds two
+//   consecutive K elements (low half first) -- one complex word (re, im).
+// - B (16-bit, N rows x K, K-major) in shared memory without swizzle: 8 x 8
+//   core matrices of 8 rows x 16 contiguous bytes; element (n, k) at
+//   (n/8)*SBO + (k/8)*LBO + (n%8)*16 + (k%8)*2 bytes.  LBO and SBO are any
+//   multiples of 16, which lets a kernel pad rows against bank conflicts.
+// - D float32 in TMEM, one column per N index.
+// - ld16x256b: thread t of a warp receives, for every 8-column chunk, the
+//   columns 2(t%4), 2(t%4)+1 of lanes base + t/4 and base + 8 + t/4 (four
+//   registers per chunk, chunks in order).
+#pragma once
+#include <stdint.h>
+
+namespace fftconv {
+namespace tc {
+
+__device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+// Warp-wide: allocate ncols TMEM columns (power of two >= 32); the base
+// address is written to *dst (shared memory).
+__device__ __forceinline__ void alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(dst)), "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Generic-proxy shared-memory writes become visible to the tensor cores.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Store 16 consecutive columns of this thread's lane.
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// 16x256b loads of 1, 4 and 8 chunks of 8 columns (call wait_ld before use).
+__device__ __forceinline__ void ld16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ld16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void ld16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// a[i] += b[i] for float32 values held as raw words (packed f32x2 adds).
+template <int N>
+__device__ __forceinline__ void add_words(uint32_t (&a)[N], const uint32_t (&b)[N]) {
+    static_assert(N % 2 == 0, "pairs");
+    #pragma unroll
+    for (int i = 0; i < N; i += 2) {
+        unsigned long long x, y, z;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(a[i]), "r"(a[i + 1]));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "r"(b[i]), "r"(b[i + 1]));
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(a[i]), "=r"(a[i + 1]) : "l"(z));
+    }
+}
+
+// Shared-memory matrix descriptor, no swizzle (layout type 0), version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((smem_addr & 0x3FFFF) >> 4);
+    d |= uint64_t((lbo >> 4) & 0x3FFF) << 16;
+    d |= uint64_t((sbo >> 4) & 0x3FFF) << 32;
+    d |= uint64_t(1) << 46;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D float32, A and B both f16 (dt = 0) or
+// both bf16 (dt = 1), both K-major.
+__host__ __device__ constexpr uint32_t idesc(int dt, int M, int N) {
+    return (1u << 4) | (uint32_t(dt) << 7) | (uint32_t(dt) << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// D[tmem d] (+)= A[tmem a] * B[smem desc]; issued by one thread.
+__device__ __forceinline__ void mma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t id, uint32_t accumulate) {
+    asm volatile(
+        "{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier when every MMA issued so far by this thread is done.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+                 : "memory");
+}
+
+// Named barrier over `count` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_vote(uint32_t id, uint32_t count, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{.reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;}"
+        : "=r"(out)
+        : "r"(uint32_t(pred)), "r"(id), "r"(count)
+        : "memory");
+    return out != 0;
+}
+
+}  // namespace tc
+}  // namespace fftconv

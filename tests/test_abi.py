@@ -35,7 +35,7 @@ def test_version_and_status_strings():
     assert F.status_string(99) == "unknown status"
 
 
-@pytest.mark.parametrize("N,R1", [(1024, 4), (2048, 8), (4096, 16), (8192, 32), (16384, 64)])
+@pytest.mark.parametrize("N,R1", [(1024, 4), (2048, 8), (8192, 32), (16384, 64)])
 def test_query_fused_factorization(N, R1):
     for dt in (F.F16, F.BF16):
         q = F.query(N, dt)
@@ -43,6 +43,18 @@ def test_query_fused_factorization(N, R1):
         assert q["factors"] == [R1, 16, 16]
         assert q["factors"][0] * 16 * 16 == N == q["M"]
         assert q["kf_bytes_per_channel"] == 8 * N
+        assert q["workspace_bytes_per_row"] == 0
+
+
+def test_query_fused_order2_4096():
+    """N = 4096 runs as one 64 x 64 product on the fifth-generation tensor
+    cores; its k_f holds 36 KB per channel (4096 bins plus zero padding bins
+    in the kernel's column layout)."""
+    for dt in (F.F16, F.BF16):
+        q = F.query(4096, dt)
+        assert q["path"] == F.PATH_FUSED and q["order"] == 2
+        assert q["factors"] == [64, 64] and q["M"] == 4096
+        assert q["kf_bytes_per_channel"] == 9 * 4 * 2 * 32 * 16
         assert q["workspace_bytes_per_row"] == 0
 
 
@@ -65,7 +77,7 @@ def test_query_rejects_unsupported_lengths(N):
 
 def test_query_rejects_bad_order_and_dtype():
     with pytest.raises(F.FFTConvError):
-        F.query(4096, F.BF16, order=2)
+        F.query(4096, F.BF16, order=3)
     with pytest.raises(F.FFTConvError):
         F.query(4096, 7)
     assert F.lib().fftconv_plan_query(4096, 1, 0, None) == 1
