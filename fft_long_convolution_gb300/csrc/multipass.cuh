@@ -250,10 +250,12 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
     in.load({a.tb.lf, a.tb.rf, a.tb.tw, nullptr, 0, 0, 0, 0}, lane);
     uint32_t par = 0;
     for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
-        const long row = item / pairs;
-        const int p = int(item % pairs);
+        // items channel-major with b fastest: the B rows of one channel use the
+        // same k_f sub-rows at about the same time, so k_f is read from HBM once
+        const long b = item % a.B, hp = item / a.B;
+        const int p = int(hp % pairs);
+        const long h = hp / pairs, row = b * a.H + h;
         const int k0s[2] = {p == 0 ? 0 : p, p == 0 ? R0 / 2 : R0 - p};
-        const long h = row % a.H;
         uint32_t* Trow = a.T + row * long(M);
         if (threadIdx.x == 0) {
             mbar_expect_tx(bar, 2u * R1 * 1024u);

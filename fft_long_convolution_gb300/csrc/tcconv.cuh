@@ -44,9 +44,9 @@
 // matrix; while one pipeline waits for its contraction the other one does its
 // register work.  A pipeline has eight warps: two warpgroups on the same 128
 // TMEM lanes, each handling half of the columns of S1/S3/S4 and one row of
-// the fold.  k_f of a channel arrives by one bulk copy (TMA engine) when the
-// channel changes; u, w_in and w_out are read through L2 (prefetched by the
-// TMA engine one item ahead).
+// the fold.  u and w_in of an item are staged by bulk copies (TMA engine)
+// one item ahead, k_f of a channel when the channel changes; w_out is read
+// through L2 (prefetched by the TMA engine at the start of the item).
 #pragma once
 #include "mma.cuh"
 #include "tc.cuh"
@@ -70,20 +70,22 @@ struct Tc64 {
     // B operand layouts, two rows side by side along N: (LBO, SBO) in bytes.
     // B1: K = 64 (n1 < 32) x N = 128 (row, o).  B2: K = 128 (o) x N = 144
     // (row, slot).  B3: K = 128 (k2) x N = 128 (row, k1) plus a trash row
-    // group at row 128.  B4: K = 128 (k1) x N = 128 (row, o).  The paddings
-    // make every thread-to-shared store pattern of the kernel conflict free.
+    // group at row 128.  B4: K = 128 (k1) x N = 128 (row, o).  The 16-byte
+    // pad per core matrix makes the stores of S1 post and of the input pass
+    // conflict free and those of the fold and S3 post at most 2-way.
     static constexpr uint32_t LBO1 = 128, SBO1 = 1024;
     static constexpr uint32_t LBO2 = 144, SBO2 = 2304;
-    static constexpr uint32_t LBO3 = 192, SBO3 = 3072;
-    static constexpr uint32_t LBO4 = 192, SBO4 = 3072;
+    static constexpr uint32_t LBO3 = 144, SBO3 = 2304;
+    static constexpr uint32_t LBO4 = 144, SBO4 = 2304;
     static constexpr uint32_t TRASH = 16 * SBO3;
-    static constexpr uint32_t BBUF = 17 * SBO3;       // 52224 >= 18 * SBO2
+    static constexpr uint32_t BBUF = 18 * SBO2;       // 41472: B2, and B3 with its trash group
+    static constexpr uint32_t STG = 8192;             // one staged row of u or w_in (2048 words)
     static constexpr uint32_t KFB = 9 * 4 * 2 * 32 * 16;  // k_f of one channel: 36864
-    static constexpr uint32_t OFF_B = 0, OFF_KF = BBUF;
-    static constexpr uint32_t PIPE = OFF_KF + KFB;    // 89088 per pipeline
+    static constexpr uint32_t OFF_B = 0, OFF_ST = BBUF, OFF_KF = OFF_ST + 4 * STG;  // staging: u A, u B, w_in A, w_in B
+    static constexpr uint32_t PIPE = OFF_KF + KFB;    // 111104 per pipeline
     static constexpr uint32_t OFF_W64 = 2 * PIPE;     // W_64^o table (32 float4)
     static constexpr uint32_t OFF_BAR = OFF_W64 + 512;
-    static constexpr uint32_t SMEM = OFF_BAR + 4 * 8;
+    static constexpr uint32_t SMEM = OFF_BAR + 6 * 8;
     // TMEM columns: F64 at 0..63; pipeline g's accumulator at 64 + 192 g (144 columns).
     static constexpr uint32_t TMEM_COLS = 512;
 };
@@ -109,7 +111,8 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     uint8_t* bbuf = pb + C::OFF_B;
     const uint4* kfs = reinterpret_cast<const uint4*>(pb + C::OFF_KF);
     const float4* w64 = reinterpret_cast<const float4*>(smem + C::OFF_W64);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * g;  // kf, mma
+    const uint32_t* stg = reinterpret_cast<const uint32_t*>(pb + C::OFF_ST);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 3 * g;  // kf, mma, in
 
     // items: pairs of rows (b = 2p, 2p + 1) of one channel, channel-major
     const int P = (a.B + 1) >> 1, items = P * a.H;  // the host guarantees B*H < 2^30
@@ -118,7 +121,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
 
     // ---------------- set-up: barriers, TMEM, tables
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + i, 1);
+        for (int i = 0; i < 6; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + i, 1);
         fence_mbar_init();
     }
     if (threadIdx.x < 32) {
@@ -206,16 +209,16 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         valid = b < a.B;
         return (valid ? b : 0) * a.H + h;
     };
-    auto prefetch_item = [&](int it) {  // u, w_in (and w_out) of both rows into L2
-        for (int R = 0; R < 2; ++R) {
-            bool ok;
-            const size_t base = size_t(row_of(it, R, ok)) * C::M;
-            if (!ok) continue;
-            bulk_prefetch_l2(a.u + base, 8192);
-            if (GATED) {
-                bulk_prefetch_l2(a.w_in + base, 8192);
-                bulk_prefetch_l2(a.w_out + base, 8192);
-            }
+    // u and w_in of both rows into the staging buffers (one bulk copy each)
+    auto stage_item = [&](int it) {
+        bool okA, okB;
+        const size_t bA = size_t(row_of(it, 0, okA)) * C::M, bB = size_t(row_of(it, 1, okB)) * C::M;
+        mbar_expect_tx(&bars[2], C::STG * (okB ? 2u : 1u) * (GATED ? 2u : 1u));
+        bulk_g2s(pb + C::OFF_ST, a.u + bA, C::STG, &bars[2]);
+        if (okB) bulk_g2s(pb + C::OFF_ST + C::STG, a.u + bB, C::STG, &bars[2]);
+        if (GATED) {
+            bulk_g2s(pb + C::OFF_ST + 2 * C::STG, a.w_in + bA, C::STG, &bars[2]);
+            if (okB) bulk_g2s(pb + C::OFF_ST + 3 * C::STG, a.w_in + bB, C::STG, &bars[2]);
         }
     };
     auto issue_kf = [&](int h) {
@@ -224,14 +227,15 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     };
 
     // pending phases and the parity of the next phase to consume, per barrier
-    bool kf_pending = false, mma_pending = false;
-    uint32_t kfpar = 0, mmapar = 0;
+    bool kf_pending = false, mma_pending = false, in_pending = false;
+    uint32_t kfpar = 0, mmapar = 0, inpar = 0;
     if (i0 < i1) {
         if (tg == 0) {
-            prefetch_item(i0);
+            stage_item(i0);
             issue_kf(chan(i0));
         }
         kf_pending = true;
+        in_pending = true;
     }
     const uint32_t bar_id = 1 + g;
     bool failed = false;
@@ -241,19 +245,22 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         const bool has_next = it + 1 < i1;
         bool okA, okB;
         const int rowA = row_of(it, 0, okA), rowB = row_of(it, 1, okB);
-        if (tg == 0 && has_next) prefetch_item(it + 1);
+        if (GATED && tg == 32) {  // w_out of this item into L2 (read in S4 post)
+            bulk_prefetch_l2(a.w_out + size_t(rowA) * C::M, C::STG);
+            if (okB) bulk_prefetch_l2(a.w_out + size_t(rowB) * C::M, C::STG);
+        }
 
         // ---------------- input: z (times w_in) of row hf -> B1
-        {
-            const int row = hf ? rowB : rowA;
+        bool bad = !mbar_wait_bounded(&bars[2], inpar, kWaitLimit);
+        if (!bad) {
             const bool ok = hf ? okB : okA;
-            const uint32_t* ur = reinterpret_cast<const uint32_t*>(a.u) + size_t(row) * (C::M / 2);
-            const uint32_t* wr = reinterpret_cast<const uint32_t*>(a.w_in) + size_t(row) * (C::M / 2);
+            const uint32_t* ur = stg + hf * (C::STG / 4);
+            const uint32_t* wr = stg + (2 + hf) * (C::STG / 4);
             uint32_t z[16], zw[16];
             #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                z[i] = ok ? __ldg(ur + (16 * in_g + i) * 64 + in_o) : 0u;
-                if (GATED) zw[i] = ok ? __ldg(wr + (16 * in_g + i) * 64 + in_o) : 0u;
+                z[i] = ok ? ur[(16 * in_g + i) * 64 + in_o] : 0u;
+                if (GATED) zw[i] = ok ? wr[(16 * in_g + i) * 64 + in_o] : 0u;
             }
             #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -265,7 +272,9 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         }
         tc::fence_proxy_async();
         tc::fence_before();
-        if (tc::bar_vote(bar_id, 256, false)) { failed = true; break; }
+        if (tc::bar_vote(bar_id, 256, bad)) { failed = true; break; }
+        in_pending = false;
+        inpar ^= 1;
         if (tg == 0) {
             tc::fence_after();
             #pragma unroll
@@ -274,23 +283,30 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
             tc::commit(&bars[1]);
         }
         mma_pending = true;
+        if (has_next) {  // the staging is free: fetch the next item
+            if (tg == 64) stage_item(it + 1);
+            in_pending = true;
+        }
 
         // ---------------- S1 post: twiddle, -> B2 (slot rows)
-        bool bad = !mbar_wait_bounded(&bars[1], mmapar, kWaitLimit);
+        bad = !mbar_wait_bounded(&bars[1], mmapar, kWaitLimit);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
+            uint32_t vr[2][2][16];  // [row][block]: row 1's loads fly while row 0 is processed
+            tc::ld16x256b_x4(tD + laneA + 32 * hf, vr[0][0]);
+            tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
+            tc::wait_ld();
+            tc::ld16x256b_x4(tD + laneA + 64 + 32 * hf, vr[1][0]);
+            tc::ld16x256b_x4(tD + laneB + 64 + 32 * hf, vr[1][1]);
             #pragma unroll
             for (int R = 0; R < 2; ++R) {
                 float4 x0[4];   // k1 = 0 (block a): kept for the pre-twiddled copy
                 uint2 p32[4];   // k1 = 32 (block b): kept for the duplicate
-                uint32_t va[16], vb[16];
-                tc::ld16x256b_x4(tD + laneA + 64 * R + 32 * hf, va);
-                tc::ld16x256b_x4(tD + laneB + 64 * R + 32 * hf, vb);
-                tc::wait_ld();
+                if (R == 1) tc::wait_ld();
                 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
-                    const uint32_t* vv = b ? vb : va;
+                    const uint32_t* vv = vr[R][b];
                     uint8_t* dst = bbuf + row2[b] + 9 * R * C::SBO2 + kq2;
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
@@ -414,15 +430,18 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
+            uint32_t vr[2][2][16];  // [row][block]: row 1's loads fly while row 0 is processed
+            tc::ld16x256b_x4(tD + laneA + 32 * hf, vr[0][0]);
+            tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
+            tc::wait_ld();
+            tc::ld16x256b_x4(tD + laneA + 64 + 32 * hf, vr[1][0]);
+            tc::ld16x256b_x4(tD + laneB + 64 + 32 * hf, vr[1][1]);
             #pragma unroll
             for (int R = 0; R < 2; ++R) {
-                uint32_t va[16], vb[16];
-                tc::ld16x256b_x4(tD + laneA + 64 * R + 32 * hf, va);
-                tc::ld16x256b_x4(tD + laneB + 64 * R + 32 * hf, vb);
-                tc::wait_ld();
+                if (R == 1) tc::wait_ld();
                 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
-                    const uint32_t* vv = b ? vb : va;
+                    const uint32_t* vv = vr[R][b];
                     uint8_t* dst = bbuf + row4[b] + 8 * R * C::SBO4 + kq4;
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
@@ -496,6 +515,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         atomicExch(a.err, 7);
         if (mma_pending) mbar_wait_bounded(&bars[1], mmapar, kWaitLimit);
         if (kf_pending) mbar_wait_bounded(&bars[0], kfpar, kWaitLimit);
+        if (in_pending) mbar_wait_bounded(&bars[2], inpar, kWaitLimit);
     }
     tc::fence_before();
     __syncthreads();
