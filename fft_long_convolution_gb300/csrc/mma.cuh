@@ -145,6 +145,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Same, but each poll may suspend the thread for up to `hint_ns` nanoseconds
+// until the phase completes, so waiting warps do not compete for issue slots.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t limit, uint32_t hint_ns) {
+    uint32_t addr = smem_u32(bar);
+    for (uint32_t it = 0; it < limit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{.reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, "
+            "1, 0, p;}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
 // One-dimensional bulk copy global -> shared through the TMA engine,
 // completing on `bar` with its byte count.  Addresses 16-byte aligned, size a
 // multiple of 16.

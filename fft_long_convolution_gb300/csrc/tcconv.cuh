@@ -53,6 +53,10 @@
 
 namespace fftconv {
 
+// Bounded waits of this kernel: polls that may each suspend for up to 2 us
+// (at most about 2 s in total before the kernel reports a timeout).
+constexpr uint32_t kWaitSleepLimit = 1u << 20, kWaitHintNs = 2000;
+
 struct Tc64Args {
     const uint16_t* u;
     const uint16_t* w_in;
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         }
 
         // ---------------- input: z (times w_in) of row hf -> B1
-        bool bad = !mbar_wait_bounded(&bars[2], inpar, kWaitLimit);
+        bool bad = !mbar_wait_sleep(&bars[2], inpar, kWaitSleepLimit, kWaitHintNs);
         if (!bad) {
             const bool ok = hf ? okB : okA;
             const uint32_t* ur = stg + hf * (C::STG / 4);
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         }
 
         // ---------------- S1 post: twiddle, -> B2 (slot rows)
-        bad = !mbar_wait_bounded(&bars[1], mmapar, kWaitLimit);
+        bad = !mbar_wait_sleep(&bars[1], mmapar, kWaitSleepLimit, kWaitHintNs);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
@@ -352,8 +356,8 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         mma_pending = true;
 
         // ---------------- fold of row hf with the kernel spectrum -> B3
-        bad = !mbar_wait_bounded(&bars[1], mmapar, kWaitLimit);
-        if (kf_pending) bad |= !mbar_wait_bounded(&bars[0], kfpar, kWaitLimit);
+        bad = !mbar_wait_sleep(&bars[1], mmapar, kWaitSleepLimit, kWaitHintNs);
+        if (kf_pending) bad |= !mbar_wait_sleep(&bars[0], kfpar, kWaitSleepLimit, kWaitHintNs);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
@@ -426,7 +430,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         kf_pending = next_kf;
 
         // ---------------- S3 post: twiddle, -> B4
-        bad = !mbar_wait_bounded(&bars[1], mmapar, kWaitLimit);
+        bad = !mbar_wait_sleep(&bars[1], mmapar, kWaitSleepLimit, kWaitHintNs);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
                                            a.w_out + size_t(R ? rowB : rowA) * C::M + yin + 16 * jj))
                                      : make_uint2(0, 0);
         }
-        bad = !mbar_wait_bounded(&bars[1], mmapar, kWaitLimit);
+        bad = !mbar_wait_sleep(&bars[1], mmapar, kWaitSleepLimit, kWaitHintNs);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
