@@ -271,15 +271,19 @@ std::vector<uint32_t> build_full_frags(int R, int dtype) {
 // Rows of F64/8 in the tensor-memory order of the 64 x 64 path (tcconv.cuh):
 // lane L = 32w + 16b + 8p + r holds output kappa = b ? 63 - 8w - r : 8w + r,
 // part p; word n holds the two K elements of input n (real, imaginary).
+// Three copies: columns natural, then at positions tc64_p3(n), tc64_p4(n).
 std::vector<uint32_t> build_tc64_fmat(int dtype) {
-    std::vector<uint32_t> v(128 * 64, 0);
+    std::vector<uint32_t> v(3 * 128 * 64, 0);
     for (int L = 0; L < 128; ++L) {
         const int w = L >> 5, b = (L >> 4) & 1, part = (L >> 3) & 1, r = L & 7;
         const int kap = b ? 63 - 8 * w - r : 8 * w + r;
         for (int n = 0; n < 64; ++n) {
             cd x = W(64, int64_t(kap) * n);
             x = {x.r / 8.0, x.i / 8.0};
-            v[size_t(L) * 64 + n] = pack2(embed(x, part, 0), embed(x, part, 1), dtype);
+            const uint32_t word = pack2(embed(x, part, 0), embed(x, part, 1), dtype);
+            v[size_t(L) * 64 + n] = word;
+            v[size_t(128 + L) * 64 + tc64_p3(n)] = word;
+            v[size_t(256 + L) * 64 + tc64_p4(n)] = word;
         }
     }
     return v;

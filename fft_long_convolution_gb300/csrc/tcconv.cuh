@@ -63,7 +63,7 @@ struct Tc64Args {
     const uint16_t* w_out;
     const uint8_t* kf;      // [h][chunk 9][warp 4][half 2][lane 32] uint4
     uint16_t* y;
-    const uint32_t* fmat;   // [lane 128][64 words]: the permuted F64/8 rows
+    const uint32_t* fmat;   // [3][lane 128][64 words]: F64/8 with permuted rows; columns natural, P3, P4
     int B, H;
     int* err;
 };
@@ -90,11 +90,29 @@ struct Tc64 {
     static constexpr uint32_t OFF_W64 = 2 * PIPE;     // W_64^o table (32 float4)
     static constexpr uint32_t OFF_BAR = OFF_W64 + 512;
     static constexpr uint32_t SMEM = OFF_BAR + 6 * 8;
-    // TMEM columns: F64 at 0..63; pipeline g's accumulator at 64 + 192 g (144 columns).
+    // TMEM columns: F64 at 0..63 (columns natural, for S1 and S2), 64..127
+    // (columns in the order P3, for S3), 128..191 (order P4, for S4);
+    // pipeline g's accumulator at 192 + 160 g (144 columns).
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
-// Slot (S2 column within a row) of sub-problem s.
+// K positions of the B3 and B4 operands (and columns of the matching F64
+// copies): a permutation of the 64 inputs that makes the fold's and S3
+// post's shared-memory stores free of bank conflicts under the 144-byte pad.
+__host__ __device__ constexpr int tc64_p3(int k2) {
+    return k2 < 32 ? 4 * (k2 >> 3) + (k2 & 3) + 16 * ((k2 >> 2) & 1) : 32 + tc64_p3(63 - k2);
+}
+__host__ __device__ constexpr int tc64_p4(int s) {
+    return 4 * ((s >> 3) & 3) + 32 * (s >> 5) + 2 * ((s >> 1) & 1) + 16 * ((s >> 2) & 1) + (s & 1);
+}
+
+// Complex products of two values (real parts r0, r1, imaginary parts i0, i1)
+// with two twiddles given as (wr0, wr1, wi0, wi1); returns (re0, re1, im0, im1).
+__device__ __forceinline__ float4 cmul2_twiddle(float r0, float r1, float i0, float i1, float4 w) {
+    return cmul2_split(r0, r1, i0, i1, w);
+}
+
+// Slot (S2 column) of sub-problem s.
 __device__ __forceinline__ int tc64_slot(int s) {
     if (s <= 31) return 8 * (s >> 2) + 2 * (s & 3);
     if (s == 32) return 64;
@@ -145,12 +163,13 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tD = tmem + 64 + 192 * g;
+    const uint32_t tD = tmem + 192 + 160 * g;
     const uint32_t laneA = uint32_t(32 * w) << 16, laneB = uint32_t(32 * w + 16) << 16;
-    if (threadIdx.x < 128) {  // the DFT matrix: lane t <- row t
-        for (int c = 0; c < 4; ++c) {
+    if (threadIdx.x < 128) {  // the three DFT matrices: lane t <- row t
+        #pragma unroll 1
+        for (int c = 0; c < 12; ++c) {
             uint32_t rr[16];
-            const uint4* src = reinterpret_cast<const uint4*>(a.fmat + threadIdx.x * 64 + 16 * c);
+            const uint4* src = reinterpret_cast<const uint4*>(a.fmat + (c >> 2) * 128 * 64 + threadIdx.x * 64 + 16 * (c & 3));
             #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 x = src[i];
@@ -181,7 +200,8 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         }
     // per-thread shared-memory offsets (row R of the item adds 9R SBO2 / 8R SBO3 / 8R SBO4)
     const uint32_t kq2 = (q >> 1) * C::LBO2 + (q & 1) * 8 + 8 * hf * C::LBO2;
-    const uint32_t kq4 = (q >> 1) * C::LBO4 + (q & 1) * 8 + 8 * hf * C::LBO4;
+    // B4 K position of columns s = 8 (4 hf + jj) + 2q (+1): tc64_p4 = 4 jj + 32 hf + 2 (q&1) + 16 (q>>1)
+    const uint32_t kq4 = (4 * (q >> 1) + 8 * hf) * C::LBO4 + (q & 1) * 8;
     uint32_t row2[2], row4[2];
     #pragma unroll
     for (int b = 0; b < 2; ++b) {
@@ -197,7 +217,10 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
                              rowoff3(60 - q) + 8 * hf * C::SBO3};
     const uint32_t r3c0 = q == 0 ? C::TRASH : r3p[0];              // chunk 0: 64 - q, or the copy of 0
     const uint32_t r3s32 = q == 0 ? 4 * C::SBO3 + 8 * hf * C::SBO3 : C::TRASH;  // chunk 8: sub-problem 32
-    auto koff3 = [](int k2) -> uint32_t { return uint32_t(k2 >> 2) * C::LBO3 + uint32_t(k2 & 3) * 4; };
+    auto koff3 = [](int k2) -> uint32_t {  // B3 K position of input k2
+        const int pos = tc64_p3(k2);
+        return uint32_t(pos >> 2) * C::LBO3 + uint32_t(pos & 3) * 4;
+    };
     const uint32_t kAo = koff3(kapA), kBo = koff3(kapB);
     // input pass: row hf, column o, inputs n1 = 16 in_g .. 16 in_g + 15
     const int in_o = tg & 63, in_g = (tg >> 6) & 1;
@@ -314,7 +337,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
                     uint8_t* dst = bbuf + row2[b] + 9 * R * C::SBO2 + kq2;
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const float4 x = cmul2_split(__uint_as_float(vv[4 * jj]), __uint_as_float(vv[4 * jj + 1]),
+                        const float4 x = cmul2_twiddle(__uint_as_float(vv[4 * jj]), __uint_as_float(vv[4 * jj + 1]),
                                                      __uint_as_float(vv[4 * jj + 2]), __uint_as_float(vv[4 * jj + 3]),
                                                      tw[b][jj]);
                         const uint2 wd = make_uint2(O::pack(x.x, x.z), O::pack(x.y, x.w));
@@ -329,7 +352,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
                     for (int jj = 0; jj < 4; ++jj) wv[jj] = w64[4 * (4 * hf + jj) + q];
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const float4 y0 = cmul2_split(x0[jj].x, x0[jj].y, x0[jj].z, x0[jj].w, wv[jj]);
+                        const float4 y0 = cmul2_twiddle(x0[jj].x, x0[jj].y, x0[jj].z, x0[jj].w, wv[jj]);
                         *reinterpret_cast<uint2*>(bbuf + 9 * R * C::SBO2 + 16 + kq2 + 2 * jj * C::LBO2) =
                             make_uint2(O::pack(y0.x, y0.z), O::pack(y0.y, y0.w));
                     }
@@ -422,7 +445,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
             tc::fence_after();
             #pragma unroll
             for (int s = 0; s < 8; ++s)
-                tc::mma(tD, tmem + 8 * s, tc::sdesc(bsm + 2 * s * C::LBO3, C::LBO3, C::SBO3), id3, s > 0);
+                tc::mma(tD, tmem + 64 + 8 * s, tc::sdesc(bsm + 2 * s * C::LBO3, C::LBO3, C::SBO3), id3, s > 0);
             tc::commit(&bars[1]);
             if (next_kf) issue_kf(chan(it + 1));  // the k_f buffer is free: next channel's
         }
@@ -449,10 +472,10 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
                     uint8_t* dst = bbuf + row4[b] + 8 * R * C::SBO4 + kq4;
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
-                        const float4 x = cmul2_split(__uint_as_float(vv[4 * jj]), __uint_as_float(vv[4 * jj + 1]),
+                        const float4 x = cmul2_twiddle(__uint_as_float(vv[4 * jj]), __uint_as_float(vv[4 * jj + 1]),
                                                      __uint_as_float(vv[4 * jj + 2]), __uint_as_float(vv[4 * jj + 3]),
                                                      tw[b][jj]);
-                        *reinterpret_cast<uint2*>(dst + 2 * jj * C::LBO4) =
+                        *reinterpret_cast<uint2*>(dst + jj * C::LBO4) =
                             make_uint2(O::pack(x.x, x.z), O::pack(x.y, x.w));
                     }
                 }
@@ -467,7 +490,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
             tc::fence_after();
             #pragma unroll
             for (int s = 0; s < 8; ++s)
-                tc::mma(tD, tmem + 8 * s, tc::sdesc(bsm + 2 * s * C::LBO4, C::LBO4, C::SBO4), id4, s > 0);
+                tc::mma(tD, tmem + 128 + 8 * s, tc::sdesc(bsm + 2 * s * C::LBO4, C::LBO4, C::SBO4), id4, s > 0);
             tc::commit(&bars[1]);
         }
         mma_pending = true;
