@@ -279,6 +279,16 @@ def main():
     path = path_of(plan.info)
     k = dev_t(ins["k"])
     kf = plan.kernel_fft(k)
+    # the kernel spectrum is computed once per set of weights (outside the
+    # step); its time is reported beside the step
+    torch.cuda.synchronize()
+    kf_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    kf_ev[0].record()
+    for _ in range(3):
+        plan.kernel_fft(k, k_f=kf)
+    kf_ev[1].record()
+    torch.cuda.synchronize()
+    kernel_fft_ms = kf_ev[0].elapsed_time(kf_ev[1]) / 3
     u = dev_t(ins["u"])
     wi = dev_t(ins["w_in"]) if w.gated else None
     wo = dev_t(ins["w_out"]) if w.gated else None
@@ -377,6 +387,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": "outputs/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "clocks": clk,
+            "kernel_fft_ms": kernel_fft_ms,
         }
         if not args.no_cpu_baseline and world == 1:
             import oracle

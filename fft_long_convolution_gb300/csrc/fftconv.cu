@@ -569,10 +569,9 @@ __global__ void kfft_pass(const float2* __restrict__ x, float2* __restrict__ yv,
          i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t h = i / half, r = i - h * half;
         const int64_t j = r / p, kk = r - j * p;
-        double sw, cw;
-        sincospi(-double(kk) / double(p), &sw, &cw);
+        float wi, wr;  // p is a power of two: kk / p is exact in float
+        sincospif(-float(kk) / float(p), &wi, &wr);
         const float2 c0 = x[h * L + kk + j * p], c1 = x[h * L + kk + j * p + half];
-        const float wr = float(cw), wi = float(sw);
         const float tr = c1.x * wr - c1.y * wi, ti = c1.x * wi + c1.y * wr;
         yv[h * L + kk + 2 * j * p] = make_float2(c0.x + tr, c0.y + ti);
         yv[h * L + kk + 2 * j * p + p] = make_float2(c0.x - tr, c0.y - ti);
@@ -589,21 +588,21 @@ __device__ __forceinline__ uint32_t pack_dt(float lo, float hi, int dtype) {
 __device__ void fold_coeffs(const float2* __restrict__ Kh, int64_t k, int64_t M, int dtype, uint32_t* wa,
                             uint32_t* wb) {
     const float2 A = Kh[k], Bm = Kh[M - k];
-    double st, ct;
-    sincospi(double(k) / double(M), &st, &ct);  // theta = pi k / M
-    const double Pr = 0.5 * (1.0 - st), Pi = 0.5 * ct;
-    const double Qr = 0.5 * (1.0 + st), Qi = -0.5 * ct;
-    const double Ar = A.x, Ai = A.y, Br = Bm.x, Bi = -Bm.y;  // B = conj K[M-k]
-    const double PAr = Pr * Ar - Pi * Ai, PAi = Pr * Ai + Pi * Ar;
-    const double QBr = Qr * Br - Qi * Bi, QBi = Qr * Bi + Qi * Br;
-    const double Sr = PAr + QBr, Si = PAi + QBi, Dr = PAr - QBr, Di = PAi - QBi;
+    float st, ct;
+    sincospif(float(k) / float(M), &st, &ct);  // theta = pi k / M (M a power of two: exact)
+    const float Pr = 0.5f * (1.f - st), Pi = 0.5f * ct;
+    const float Qr = 0.5f * (1.f + st), Qi = -0.5f * ct;
+    const float Ar = A.x, Ai = A.y, Br = Bm.x, Bi = -Bm.y;  // B = conj K[M-k]
+    const float PAr = Pr * Ar - Pi * Ai, PAi = Pr * Ai + Pi * Ar;
+    const float QBr = Qr * Br - Qi * Bi, QBi = Qr * Bi + Qi * Br;
+    const float Sr = PAr + QBr, Si = PAi + QBi, Dr = PAr - QBr, Di = PAi - QBi;
     // (i/2) W^k D with W^k = (cos, -sin)
-    const double WDr = ct * Dr + st * Di, WDi = ct * Di - st * Dr;
-    const double Xr = -0.5 * WDi, Xi = 0.5 * WDr;
-    const double ar = 0.5 * Sr - Xr, ai = 0.5 * Si - Xi;
-    const double br = 0.5 * Sr + Xr, bi = 0.5 * Si + Xi;
-    *wa = pack_dt(float(ar), float(-ai), dtype);
-    *wb = pack_dt(float(br), float(-bi), dtype);
+    const float WDr = ct * Dr + st * Di, WDi = ct * Di - st * Dr;
+    const float Xr = -0.5f * WDi, Xi = 0.5f * WDr;
+    const float ar = 0.5f * Sr - Xr, ai = 0.5f * Si - Xi;
+    const float br = 0.5f * Sr + Xr, bi = 0.5f * Si + Xi;
+    *wa = pack_dt(ar, -ai, dtype);
+    *wb = pack_dt(br, -bi, dtype);
 }
 
 // k_f: per (h, k0, k1, q, lane) two bins, each with alpha~ = conj(alpha)
