@@ -314,6 +314,7 @@ cudaError_t launch_fused_t(const fftconv_plan_s* p, const void* u, const void* w
         blocks_per_sm = nb > 0 ? nb : 1;
     }
     if (C::TSMEM && p->tb.outer_bytes > C::TAB_BYTES) return cudaErrorInvalidValue;
+    if (C::FSMEM && p->tb.off_twf > C::TAB_BYTES) return cudaErrorInvalidValue;
     const int64_t groups = (B * H + C::RP - 1) / C::RP;
     int64_t grid = int64_t(p->num_sms) * blocks_per_sm;
     const int64_t need = (groups + C::GROUPS - 1) / C::GROUPS;

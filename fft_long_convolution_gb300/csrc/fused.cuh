@@ -76,32 +76,37 @@ struct FusedCfg {
     static constexpr bool K8I = R1 <= 4;          // inverse outer uses K = 8
     static constexpr int KS_I = K8I ? 1 : R1 / 8;
     static constexpr int MT_I = (R1 + 15) / 16;
-    static constexpr bool TSMEM = R1 <= 16;       // outer tables resident in shared memory
     // Short rows: one CTA per SM runs two independent 8-warp row pipelines that
     // share one copy of the tables, and each pipeline keeps the k_f of its
     // current channel(s) in shared memory (loaded by the TMA engine only when
-    // the channel changes).  Long rows: 8-warp CTAs, k_f read through L2.
-    static constexpr int GROUPS = R1 <= 16 ? 2 : 1;
-    static constexpr int THREADS = 256 * GROUPS;
-    static constexpr int MINB = GROUPS == 2 ? 1 : 2;
-    static constexpr bool KFS = R1 <= 16;
+    // the channel changes).  Long rows: two pipelines per CTA when their row
+    // buffers fit beside the outer DFT fragments (which are then resident; the
+    // outer twiddles and k_f are read through L2), else 8-warp CTAs.
+    static constexpr bool TSMEM = R1 <= 16;       // all outer tables resident in shared memory
     static constexpr int NSPEC = RP > 1 ? NWARPS : 1;  // warps that own a self-paired sub-problem 0
-    // shared-memory layout (bytes)
-    static constexpr size_t TAB_BYTES = TSMEM ? (size_t(MT_F) * KS_F * 512 + size_t(MT_I) * KS_I * 512 +
-                                                 size_t(MT_F) * 16384 + size_t(R1) * 2048 + 4 * 256)
-                                              : 0;
+    static constexpr size_t FRAG_BYTES = size_t(MT_F) * KS_F * 512 + size_t(MT_I) * KS_I * 512;
     static constexpr size_t ROW_BYTES = size_t(RP) * M * 4;
     static constexpr size_t SEG_BYTES = size_t(RP) * HALF * SEG * 4;
     static constexpr size_t IN_BYTES = SEG_BYTES * (GATED ? 2 : 1);
     static constexpr size_t WO_BYTES = GATED ? SEG_BYTES : 0;
     static constexpr size_t SCR_BYTES = size_t(NSPEC) * 256 * 8;
+    static constexpr bool KFS = R1 <= 16;
     static constexpr size_t KF_BYTES = KFS ? size_t(RP) * R1 * 2048 : 0;
+    static constexpr size_t GROUP_BYTES = ROW_BYTES + IN_BYTES + WO_BYTES + SCR_BYTES + KF_BYTES;
+    static constexpr bool PAIR_FITS = 2 * GROUP_BYTES + FRAG_BYTES + 64 <= 227 * 1024;
+    static constexpr int GROUPS = (R1 <= 16 || PAIR_FITS) ? 2 : 1;
+    static constexpr bool FSMEM = TSMEM || GROUPS == 2;  // outer DFT fragments resident
+    static constexpr int THREADS = 256 * GROUPS;
+    static constexpr int MINB = GROUPS == 2 ? 1 : 2;
+    // shared-memory layout (bytes)
+    static constexpr size_t TAB_BYTES = TSMEM ? (FRAG_BYTES + size_t(MT_F) * 16384 + size_t(R1) * 2048 + 4 * 256)
+                                              : (FSMEM ? FRAG_BYTES + 256 : 0);
     static constexpr size_t G_ROW = 0;
     static constexpr size_t G_IN = G_ROW + ROW_BYTES;
     static constexpr size_t G_WO = G_IN + IN_BYTES;
     static constexpr size_t G_SCR = G_WO + WO_BYTES;
     static constexpr size_t G_KF = G_SCR + SCR_BYTES;
-    static constexpr size_t GROUP_BYTES = G_KF + KF_BYTES;
+    static_assert(GROUP_BYTES == G_KF + KF_BYTES, "group layout");
     static constexpr size_t OFF_BAR = TAB_BYTES + GROUPS * GROUP_BYTES;
     static constexpr size_t SMEM_BYTES = OFF_BAR + 64;
 };
@@ -348,8 +353,8 @@ fused_conv_kernel(const FusedArgs a) {
     uint64_t* bars = bar_tab + 1 + 3 * gi;                           // in, wo, kf
 
     const FusedTables& tb = a.tb;
-    const uint4* of_t = reinterpret_cast<const uint4*>(C::TSMEM ? smem : tb.outer);
-    const uint4* oi_t = reinterpret_cast<const uint4*>((C::TSMEM ? smem : tb.outer) + tb.off_oi);
+    const uint4* of_t = reinterpret_cast<const uint4*>(C::FSMEM ? smem : tb.outer);
+    const uint4* oi_t = reinterpret_cast<const uint4*>((C::FSMEM ? smem : tb.outer) + tb.off_oi);
     const float4* twf_t = reinterpret_cast<const float4*>((C::TSMEM ? smem : tb.outer) + tb.off_twf);
     const float4* twi_t = reinterpret_cast<const float4*>((C::TSMEM ? smem : tb.outer) + tb.off_twi);
 
@@ -455,9 +460,10 @@ fused_conv_kernel(const FusedArgs a) {
         for (int j = 0; j < 4; ++j) s_kfh[gi][j] = -1;
     }
     __syncthreads();
-    if (threadIdx.x == 0 && C::TSMEM) {
-        mbar_expect_tx(bar_tab, tb.outer_bytes);
-        bulk_g2s(smem, tb.outer, tb.outer_bytes, bar_tab);
+    if (threadIdx.x == 0 && C::FSMEM) {  // resident tables: all (short rows) or the DFT fragments
+        const uint32_t nb = C::TSMEM ? tb.outer_bytes : tb.off_twf;
+        mbar_expect_tx(bar_tab, nb);
+        bulk_g2s(smem, tb.outer, nb, bar_tab);
     }
     if (warp == 0 && g0 < g1) {
         issue_in(g0);
@@ -465,7 +471,7 @@ fused_conv_kernel(const FusedArgs a) {
     }
     Inner<DT> in;
     in.load(tb, lane);
-    if (C::TSMEM) {  // every thread of the CTA reaches this barrier
+    if (C::FSMEM) {  // every thread of the CTA reaches this barrier
         if (threadIdx.x == 0 && !mbar_wait_bounded(bar_tab, 0, kWaitLimit)) {
             s_fail[0] = s_fail[C::GROUPS - 1] = 1;
             atomicExch(a.err, 7);
@@ -500,46 +506,87 @@ fused_conv_kernel(const FusedArgs a) {
         const int rbase = grp * RP;
 
         // ---------------- outer forward stage: k1 outputs of 8 vectors per tile
-        #pragma unroll 1
-        for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
-            const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
-            if (rbase + j >= rows) continue;
-            const uint32_t* su = stage_u + j * HALF * SEG + t * SEG + 8 * nt + g;
-            const uint32_t* sw = stage_w + j * HALF * SEG + t * SEG + 8 * nt + g;
-            uint32_t bf[C::KS_F][2];
-            #pragma unroll
-            for (int s = 0; s < C::KS_F; ++s) {
-                const int na = 8 * s + t, nb = 8 * s + 4 + t;
-                uint32_t va = 0, vb = 0;
-                if (na < HALF) {
-                    va = su[8 * s * SEG];
-                    if (GATED) va = O::mul2(va, sw[8 * s * SEG]);
+        if constexpr (C::FSMEM) {
+            #pragma unroll 1
+            for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
+                const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
+                if (rbase + j >= rows) continue;
+                const uint32_t* su = stage_u + j * HALF * SEG + t * SEG + 8 * nt + g;
+                const uint32_t* sw = stage_w + j * HALF * SEG + t * SEG + 8 * nt + g;
+                uint32_t bf[C::KS_F][2];
+                #pragma unroll
+                for (int s = 0; s < C::KS_F; ++s) {
+                    const int na = 8 * s + t, nb = 8 * s + 4 + t;
+                    uint32_t va = 0, vb = 0;
+                    if (na < HALF) {
+                        va = su[8 * s * SEG];
+                        if (GATED) va = O::mul2(va, sw[8 * s * SEG]);
+                    }
+                    if (!C::K8F && nb < HALF) {
+                        vb = su[(8 * s + 4) * SEG];
+                        if (GATED) vb = O::mul2(vb, sw[(8 * s + 4) * SEG]);
+                    }
+                    bf[s][0] = va;
+                    bf[s][1] = vb;
                 }
-                if (!C::K8F && nb < HALF) {
-                    vb = su[(8 * s + 4) * SEG];
-                    if (GATED) vb = O::mul2(vb, sw[(8 * s + 4) * SEG]);
-                }
-                bf[s][0] = va;
-                bf[s][1] = vb;
-            }
-            uint32_t* rb = rowbuf + j * M + st_base + 64 * i4;
-            #pragma unroll
-            for (int m = 0; m < C::MT_F; ++m) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                if (C::K8F) {
-                    const uint4 af = of_t[m * 32 + lane];
-                    O::mma8(acc, af.x, af.y, bf[0][0]);
-                } else {
-                    #pragma unroll
-                    for (int s = 0; s < C::KS_F; ++s) {
-                        const uint4 af = of_t[(m * C::KS_F + s) * 32 + lane];
-                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
-                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                uint32_t* rb = rowbuf + j * M + st_base + 64 * i4;
+                #pragma unroll
+                for (int m = 0; m < C::MT_F; ++m) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (C::K8F) {
+                        const uint4 af = of_t[m * 32 + lane];
+                        O::mma8(acc, af.x, af.y, bf[0][0]);
+                    } else {
+                        #pragma unroll
+                        for (int s = 0; s < C::KS_F; ++s) {
+                            const uint4 af = of_t[(m * C::KS_F + s) * 32 + lane];
+                            const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                            O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                        }
+                    }
+                    if (8 * m + g < R1) {
+                        const float4 v = cmul2_split(acc[0], acc[1], acc[2], acc[3], twf_t[(nt * C::MT_F + m) * 32 + lane]);
+                        *reinterpret_cast<uint2*>(rb + 2048 * m) = make_uint2(O::pack(v.x, v.z), O::pack(v.y, v.w));
                     }
                 }
-                if (8 * m + g < R1) {
-                    const float4 v = cmul2_split(acc[0], acc[1], acc[2], acc[3], twf_t[(nt * C::MT_F + m) * 32 + lane]);
-                    *reinterpret_cast<uint2*>(rb + 2048 * m) = make_uint2(O::pack(v.x, v.z), O::pack(v.y, v.w));
+            }
+        } else {
+            // fragments through L2: each A fragment once per row (m outer),
+            // the staged inputs re-read from shared memory per m
+            #pragma unroll 1
+            for (int m = 0; m < C::MT_F; ++m) {
+                uint32_t a4s[C::KS_F][4];
+                #pragma unroll
+                for (int s = 0; s < C::KS_F; ++s) {
+                    const uint4 af = of_t[(m * C::KS_F + s) * 32 + lane];
+                    a4s[s][0] = af.x; a4s[s][1] = af.y; a4s[s][2] = af.z; a4s[s][3] = af.w;
+                }
+                #pragma unroll 1
+                for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
+                    const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
+                    if (rbase + j >= rows) continue;
+                    const uint32_t* su = stage_u + j * HALF * SEG + t * SEG + 8 * nt + g;
+                    const uint32_t* sw = stage_w + j * HALF * SEG + t * SEG + 8 * nt + g;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    #pragma unroll
+                    for (int s = 0; s < C::KS_F; ++s) {
+                        const int na = 8 * s + t, nb = 8 * s + 4 + t;
+                        uint32_t va = 0, vb = 0;
+                        if (na < HALF) {
+                            va = su[8 * s * SEG];
+                            if (GATED) va = O::mul2(va, sw[8 * s * SEG]);
+                        }
+                        if (nb < HALF) {
+                            vb = su[(8 * s + 4) * SEG];
+                            if (GATED) vb = O::mul2(vb, sw[(8 * s + 4) * SEG]);
+                        }
+                        O::mma16(acc, a4s[s], va, vb);
+                    }
+                    if (8 * m + g < R1) {
+                        uint32_t* rb = rowbuf + j * M + st_base + 64 * i4;
+                        const float4 v = cmul2_split(acc[0], acc[1], acc[2], acc[3], twf_t[(nt * C::MT_F + m) * 32 + lane]);
+                        *reinterpret_cast<uint2*>(rb + 2048 * m) = make_uint2(O::pack(v.x, v.z), O::pack(v.y, v.w));
+                    }
                 }
             }
         }
@@ -658,42 +705,77 @@ fused_conv_kernel(const FusedArgs a) {
         if (warp == 0 && grp + 1 < g1) issue_kf(grp + 1);
 
         // ---------------- outer inverse stage (first R1/2 outputs only) and store
-        #pragma unroll 1
-        for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
-            const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
-            if (rbase + j >= rows) continue;
-            const uint32_t* rb = rowbuf + j * M + oi_base + 64 * i4;
-            uint32_t bf[C::KS_I][2];
-            #pragma unroll
-            for (int s = 0; s < C::KS_I; ++s) {
-                bf[s][0] = rb[256 * 8 * s];
-                bf[s][1] = C::K8I ? 0u : rb[256 * (8 * s + 4)];
-            }
-            const size_t base = size_t(s_row[gi][j]) * N;
-            #pragma unroll
-            for (int m = 0; m < C::MT_I; ++m) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                if (C::K8I) {
-                    const uint4 af = oi_t[m * 32 + lane];
-                    O::mma8(acc, af.x, af.y, bf[0][0]);
-                } else {
-                    #pragma unroll
-                    for (int s = 0; s < C::KS_I; ++s) {
-                        const uint4 af = oi_t[(m * C::KS_I + s) * 32 + lane];
-                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
-                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+        if constexpr (C::FSMEM) {
+            #pragma unroll 1
+            for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
+                const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
+                if (rbase + j >= rows) continue;
+                const uint32_t* rb = rowbuf + j * M + oi_base + 64 * i4;
+                uint32_t bf[C::KS_I][2];
+                #pragma unroll
+                for (int s = 0; s < C::KS_I; ++s) {
+                    bf[s][0] = rb[256 * 8 * s];
+                    bf[s][1] = C::K8I ? 0u : rb[256 * (8 * s + 4)];
+                }
+                const size_t base = size_t(s_row[gi][j]) * N;
+                #pragma unroll
+                for (int m = 0; m < C::MT_I; ++m) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (C::K8I) {
+                        const uint4 af = oi_t[m * 32 + lane];
+                        O::mma8(acc, af.x, af.y, bf[0][0]);
+                    } else {
+                        #pragma unroll
+                        for (int s = 0; s < C::KS_I; ++s) {
+                            const uint4 af = oi_t[(m * C::KS_I + s) * 32 + lane];
+                            const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                            O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                        }
+                    }
+                    const int n1 = 8 * m + g;
+                    if (n1 < HALF) {
+                        const int p = 256 * n1 + 8 * nt + 2 * t;  // complex index; reals 2p..2p+3
+                        float r0 = acc[0], i0 = -acc[2], r1 = acc[1], i1 = -acc[3];
+                        if (GATED) {
+                            const uint2 wv = *reinterpret_cast<const uint2*>(wobuf + (j * HALF + n1) * SEG + 8 * nt + 2 * t);
+                            const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
+                            r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
+                        }
+                        *reinterpret_cast<uint2*>(a.y + base + 2 * p) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
                     }
                 }
-                const int n1 = 8 * m + g;
-                if (n1 < HALF) {
-                    const int p = 256 * n1 + 8 * nt + 2 * t;  // complex index; reals 2p..2p+3
-                    float r0 = acc[0], i0 = -acc[2], r1 = acc[1], i1 = -acc[3];
-                    if (GATED) {
-                        const uint2 wv = *reinterpret_cast<const uint2*>(wobuf + (j * HALF + n1) * SEG + 8 * nt + 2 * t);
-                        const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
-                        r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
+            }
+        } else {
+            // fragments through L2: each A fragment once per row (m outer),
+            // the row buffer re-read per m
+            #pragma unroll 1
+            for (int m = 0; m < C::MT_I; ++m) {
+                uint32_t a4s[C::KS_I][4];
+                #pragma unroll
+                for (int s = 0; s < C::KS_I; ++s) {
+                    const uint4 af = oi_t[(m * C::KS_I + s) * 32 + lane];
+                    a4s[s][0] = af.x; a4s[s][1] = af.y; a4s[s][2] = af.z; a4s[s][3] = af.w;
+                }
+                #pragma unroll 1
+                for (int ntg = warp; ntg < C::NTILES; ntg += C::NWARPS) {
+                    const int j = ntg >> 5, nt = ntg & 31, i4 = (ntg >> 3) & 3;
+                    if (rbase + j >= rows) continue;
+                    const uint32_t* rb = rowbuf + j * M + oi_base + 64 * i4;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    #pragma unroll
+                    for (int s = 0; s < C::KS_I; ++s) O::mma16(acc, a4s[s], rb[256 * 8 * s], rb[256 * (8 * s + 4)]);
+                    const int n1 = 8 * m + g;
+                    if (n1 < HALF) {
+                        const size_t base = size_t(s_row[gi][j]) * N;
+                        const int p = 256 * n1 + 8 * nt + 2 * t;  // complex index; reals 2p..2p+3
+                        float r0 = acc[0], i0 = -acc[2], r1 = acc[1], i1 = -acc[3];
+                        if (GATED) {
+                            const uint2 wv = *reinterpret_cast<const uint2*>(wobuf + (j * HALF + n1) * SEG + 8 * nt + 2 * t);
+                            const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
+                            r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
+                        }
+                        *reinterpret_cast<uint2*>(a.y + base + 2 * p) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
                     }
-                    *reinterpret_cast<uint2*>(a.y + base + 2 * p) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
                 }
             }
         }

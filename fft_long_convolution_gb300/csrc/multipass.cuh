@@ -225,7 +225,8 @@ __global__ void __launch_bounds__(256, 2) mp_pass_c(const MPArgs a) {
 }
 
 // ------------------------------------------------------------------ pass B
-constexpr size_t kMpBSmem = size_t(2) * kMpR1 * kSeg * 4 + 256 * 8 + 32;
+constexpr size_t kMpBFrag = size_t(8) * 8 * 32 * 16;  // F_64/8 A fragments, resident in shared memory
+constexpr size_t kMpBSmem = size_t(2) * kMpR1 * kSeg * 4 + 256 * 8 + kMpBFrag + 32;
 
 template <int DT>
 __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
@@ -234,7 +235,8 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t* rbuf = reinterpret_cast<uint32_t*>(smem);                 // [2][R1][SEG]
     cpx* scratch = reinterpret_cast<cpx*>(rbuf + 2 * R1 * SEG);         // [256]
-    uint64_t* bar = reinterpret_cast<uint64_t*>(scratch + 256);
+    uint4* ofull = reinterpret_cast<uint4*>(scratch + 256);             // [8][8][lane]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(ofull + 8 * 8 * 32);    // items, table
     __shared__ int s_fail;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const int R0 = a.R0;
@@ -243,11 +245,15 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
     if (threadIdx.x == 0) {
         s_fail = 0;
         mbar_init(bar, 1);
+        mbar_init(bar + 1, 1);
         fence_mbar_init();
+        mbar_expect_tx(bar + 1, uint32_t(kMpBFrag));
+        bulk_g2s(ofull, a.tb.ofull, uint32_t(kMpBFrag), bar + 1);
     }
     __syncthreads();
     Inner<DT> in;
     in.load({a.tb.lf, a.tb.rf, a.tb.tw, nullptr, 0, 0, 0, 0}, lane);
+    if (!cta_wait(bar + 1, 0, &s_fail, a.err)) return;
     uint32_t par = 0;
     for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
         // items channel-major with b fastest: the B rows of one channel use the
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
-                    const uint4 af = a.tb.ofull[(m * 8 + s) * 32 + lane];
+                    const uint4 af = ofull[(m * 8 + s) * 32 + lane];
                     const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
                     O::mma16(acc, a4, bf[s][0], bf[s][1]);
                 }
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
-                    const uint4 af = a.tb.ofull[(m * 8 + s) * 32 + lane];
+                    const uint4 af = ofull[(m * 8 + s) * 32 + lane];
                     const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
                     O::mma16(acc, a4, bf[s][0], bf[s][1]);
                 }
