@@ -145,6 +145,26 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     if (threadIdx.x == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + i, 1);
         fence_mbar_init();
+        // the first item's inputs and k_f of both pipelines, overlapping the set-up below
+        for (int gp = 0; gp < 2; ++gp) {
+            const int vp = int(blockIdx.x) * 2 + gp;
+            const int j0 = int(int64_t(vp) * items / V), j1 = int(int64_t(vp + 1) * items / V);
+            if (j0 >= j1) continue;
+            uint8_t* pbp = smem + gp * C::PIPE;
+            uint64_t* bp = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 3 * gp;
+            const int h0 = int(unsigned(j0) / unsigned(P)), b0 = 2 * (j0 - h0 * P);
+            const bool okB0 = b0 + 1 < a.B;
+            const size_t bA = (size_t(b0) * a.H + h0) * C::M, bB = (size_t(okB0 ? b0 + 1 : 0) * a.H + h0) * C::M;
+            mbar_expect_tx(&bp[2], C::STG * (okB0 ? 2u : 1u) * (GATED ? 2u : 1u));
+            bulk_g2s(pbp + C::OFF_ST, a.u + bA, C::STG, &bp[2]);
+            if (okB0) bulk_g2s(pbp + C::OFF_ST + C::STG, a.u + bB, C::STG, &bp[2]);
+            if (GATED) {
+                bulk_g2s(pbp + C::OFF_ST + 2 * C::STG, a.w_in + bA, C::STG, &bp[2]);
+                if (okB0) bulk_g2s(pbp + C::OFF_ST + 3 * C::STG, a.w_in + bB, C::STG, &bp[2]);
+            }
+            mbar_expect_tx(&bp[0], C::KFB);
+            bulk_g2s(pbp + C::OFF_KF, a.kf + size_t(h0) * C::KFB, C::KFB, &bp[0]);
+        }
     }
     if (threadIdx.x < 32) {
         tc::alloc(&s_tmem, C::TMEM_COLS);
@@ -256,11 +276,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     // pending phases and the parity of the next phase to consume, per barrier
     bool kf_pending = false, mma_pending = false, in_pending = false;
     uint32_t kfpar = 0, mmapar = 0, inpar = 0;
-    if (i0 < i1) {
-        if (tg == 0) {
-            stage_item(i0);
-            issue_kf(chan(i0));
-        }
+    if (i0 < i1) {  // the first item's copies were issued during the set-up
         kf_pending = true;
         in_pending = true;
     }
