@@ -229,7 +229,8 @@ def run_reference(args, w: W.Workload):
 def path_of(plan_info: dict) -> dict:
     """The kernels one step launches for a plan (names as in the sources)."""
     if plan_info["path"] == 1:
-        return {"kernel": "mp_pass_a + mp_pass_b + mp_pass_c (the whole step)", "launches_per_step": 3}
+        b = "mp_pass_b_tc" if plan_info["order"] == 3 else "mp_pass_b"
+        return {"kernel": f"mp_pass_a + {b} + mp_pass_c (the whole step)", "launches_per_step": 3}
     if plan_info["order"] == 2:
         return {"kernel": "tc64_conv_kernel", "launches_per_step": 1}
     return {"kernel": "fused_conv_kernel", "launches_per_step": 1}

@@ -4,6 +4,7 @@ from __future__ import annotations
 import os
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
@@ -11,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfftconv_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["fftconv.cu"]
+SOURCES = ["fftconv.cu", "mp_l16k.cu", "mp_l4k.cu"]  # compiled in parallel, then linked
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 _lock = threading.Lock()
 
@@ -36,13 +37,24 @@ def build(force: bool = False, verbose: bool = False) -> str:
             return LIB_PATH
         os.makedirs(BUILD_DIR, exist_ok=True)
         nvcc = os.environ.get("NVCC", "nvcc")
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-               "-I", os.path.join(ROOT, "include"), "-o", tmp,
-               *[os.path.join(CSRC, s) for s in SOURCES]]
+        tag = f".tmp{os.getpid()}"
+        tmp = LIB_PATH + tag
+        flags = [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
         if verbose:
-            cmd.insert(1, "-Xptxas=-v")
-        subprocess.check_call(cmd)
+            flags.insert(0, "-Xptxas=-v")
+        objs = [os.path.join(BUILD_DIR, os.path.splitext(s)[0] + tag + ".o") for s in SOURCES]
+
+        def compile_one(i):
+            subprocess.check_call([nvcc, *flags, "-c", "-o", objs[i], os.path.join(CSRC, SOURCES[i])])
+
+        try:
+            with ThreadPoolExecutor(len(SOURCES)) as ex:
+                list(ex.map(compile_one, range(len(SOURCES))))
+            subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
+        finally:
+            for o in objs:
+                if os.path.exists(o):
+                    os.remove(o)
         os.replace(tmp, LIB_PATH)
         return LIB_PATH
 

@@ -10,8 +10,9 @@
 #include <vector>
 
 #include "../../include/fftconv.h"
-#include "multipass.cuh"
+#include "plan.h"
 #include "tcconv.cuh"
+#include "tcpass.cuh"
 
 using namespace fftconv;
 
@@ -60,20 +61,6 @@ bool is_pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
 
 }  // namespace
 
-struct fftconv_plan_s {
-    fftconv_plan_info_t info;
-    int R1 = 0;
-    void* dev = nullptr;  // one allocation: tables + error word
-    int* dev_err = nullptr;
-    FusedTables tb{};
-    MPTables mp{};
-    int R0 = 1;  // outer factor through HBM (1 on the fused path)
-    bool tc64 = false;              // N = 4096: order-2 64 x 64 product on tcgen05
-    const uint32_t* fmat = nullptr;  // its DFT matrix rows (device)
-    int num_sms = 0;
-    void* workspace = nullptr;
-    size_t workspace_bytes = 0;
-};
 
 // --------------------------------------------------------------- planning
 
@@ -102,6 +89,15 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
         q.factors[1] = 16;
         q.factors[2] = 16;
         q.workspace_bytes_per_row = 0;
+    } else if ((order == 0 || order == 3) && N <= (int64_t(1) << 19)) {
+        // multi-pass: M = R0 * 64 * 64, outer factor R0 through HBM, sub-rows
+        // of 4096 on the tensor cores (the default up to N = 512K)
+        q.path = FFTCONV_PATH_MULTIPASS;
+        q.order = 3;
+        q.factors[0] = int32_t(N / 4096);
+        q.factors[1] = 64;
+        q.factors[2] = 64;
+        q.workspace_bytes_per_row = 4 * N;  // 16-bit complex intermediate
     } else {
         // multi-pass: M = R0 * 64 * 16 * 16, outer factor R0 through HBM
         q.path = FFTCONV_PATH_MULTIPASS;
@@ -114,8 +110,13 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
     }
     if (order != 0 && order != q.order) return FFTCONV_ERR_UNSUPPORTED;
     // two 16-bit complex coefficients per bin (plus zero padding bins on the
-    // 64 x 64 path, whose k_f follows the kernel's column layout)
-    q.kf_bytes_per_channel = N == 4096 ? int64_t(Tc64::KFB) : q.M * 8;
+    // 64 x 64 paths, whose k_f follows the kernels' column layouts)
+    if (N == 4096)
+        q.kf_bytes_per_channel = int64_t(Tc64::KFB);
+    else if (q.path == FFTCONV_PATH_MULTIPASS && q.order == 3)
+        q.kf_bytes_per_channel = int64_t(q.factors[0] / 2) * TcB::KFP * 16;
+    else
+        q.kf_bytes_per_channel = q.M * 8;
     *info = q;
     return FFTCONV_OK;
 }
@@ -372,64 +373,14 @@ cudaError_t launch_fused(const fftconv_plan_s* p, const void* u, const void* wi,
                  : launch_fused_r<1, false>(p, u, wi, wo, kf, y, B, H, st);
 }
 
-// ---- multi-pass dispatch
-template <typename K>
-cudaError_t prep(K fn, size_t smem, int threads, int* per_sm) {
-    if (*per_sm == 0) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return e;
-        int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem);
-        if (e != cudaSuccess) return e;
-        *per_sm = nb > 0 ? nb : 1;
-    }
-    return cudaSuccess;
-}
-
-template <int DT, int R0, bool G>
-cudaError_t launch_mp_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    constexpr int HALF = R0 / 2;
-    const size_t smem_a = size_t(HALF) * kSeg * 4 * (G ? 2 : 1) + 32;
-    const size_t smem_c = size_t(R0) * kSeg * 4 + (G ? size_t(HALF) * kSeg * 4 : 0) + 32;
-    static int na = 0, nb = 0, nc = 0;
-    cudaError_t e;
-    if ((e = prep(mp_pass_a<DT, R0, G>, smem_a, 256, &na)) != cudaSuccess) return e;
-    if ((e = prep(mp_pass_b<DT>, kMpBSmem, 512, &nb)) != cudaSuccess) return e;
-    if ((e = prep(mp_pass_c<DT, R0, G>, smem_c, 256, &nc)) != cudaSuccess) return e;
-    const int64_t items_ac = rows * (kMpL / 256), items_b = rows * (R0 / 2);
-    auto grid = [&](int64_t items, int per_sm) {
-        int64_t gsz = int64_t(p->num_sms) * per_sm;
-        return unsigned(gsz < items ? gsz : items);
-    };
-    mp_pass_a<DT, R0, G><<<grid(items_ac, na), 256, smem_a, st>>>(args);
-    mp_pass_b<DT><<<grid(items_b, nb), 512, kMpBSmem, st>>>(args);
-    mp_pass_c<DT, R0, G><<<grid(items_ac, nc), 256, smem_c, st>>>(args);
-    return cudaGetLastError();
-}
-
-template <int DT, bool G>
-cudaError_t launch_mp_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    switch (p->R0) {
-        case 2: return launch_mp_t<DT, 2, G>(p, args, rows, st);
-        case 4: return launch_mp_t<DT, 4, G>(p, args, rows, st);
-        case 8: return launch_mp_t<DT, 8, G>(p, args, rows, st);
-        case 16: return launch_mp_t<DT, 16, G>(p, args, rows, st);
-        case 32: return launch_mp_t<DT, 32, G>(p, args, rows, st);
-        case 64: return launch_mp_t<DT, 64, G>(p, args, rows, st);
-        case 128: return launch_mp_t<DT, 128, G>(p, args, rows, st);
-    }
-    return cudaErrorInvalidValue;
-}
-
+// ---- multi-pass dispatch (T: the intermediate, B*H*N*4 bytes)
 cudaError_t launch_multipass(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
-                             const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+                             const void* kf, void* y, void* T, int64_t B, int64_t H, cudaStream_t st) {
     MPArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
                 static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
-                static_cast<uint32_t*>(p->workspace), int(B), int(H), p->R0, p->mp, p->dev_err};
+                static_cast<uint32_t*>(T), int(B), int(H), p->R0, p->mp, p->dev_err};
     const bool gated = wi != nullptr;
-    if (p->info.dtype == FFTCONV_F16)
-        return gated ? launch_mp_r<0, true>(p, args, B * H, st) : launch_mp_r<0, false>(p, args, B * H, st);
-    return gated ? launch_mp_r<1, true>(p, args, B * H, st) : launch_mp_r<1, false>(p, args, B * H, st);
+    return p->mpL == kMpLtc ? launch_mp_l4k(p, args, B * H, gated, st) : launch_mp_l16k(p, args, B * H, gated, st);
 }
 
 }  // namespace
@@ -449,9 +400,11 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     p->R0 = multi ? info.factors[0] : 1;
     p->R1 = multi ? kMpR1 : info.factors[0];
     p->tc64 = N == 4096;
+    p->mpL = multi ? (info.order == 3 ? kMpLtc : kMpL) : 0;
+    const bool need_fmat = p->tc64 || p->mpL == kMpLtc;
     HostTables T = p->tc64 ? HostTables{} : build_fused_tables(p->R1, dtype);
     std::vector<uint32_t> fmat;
-    if (p->tc64) fmat = build_tc64_fmat(dtype);
+    if (need_fmat) fmat = build_tc64_fmat(dtype);
     HostTables T0;
     std::vector<uint32_t> ofull;
     if (multi) {
@@ -464,7 +417,7 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     const size_t o_of = append(blob, T.of), o_oi = append(blob, T.oi);
     const size_t o_twf = append(blob, T.twf), o_twi = append(blob, T.twi);
     const size_t outer_end = o_twi + T.twi.size() * sizeof(float);
-    const size_t o_fmat = p->tc64 ? append(blob, fmat) : 0;
+    const size_t o_fmat = need_fmat ? append(blob, fmat) : 0;
     size_t o_ofa = 0, o_oic = 0, o_ofull = 0;
     if (multi) {
         o_ofa = append(blob, T0.of);
@@ -493,7 +446,7 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     }
     uint8_t* d = static_cast<uint8_t*>(p->dev);
     p->dev_err = reinterpret_cast<int*>(d + o_err);
-    if (p->tc64) p->fmat = reinterpret_cast<const uint32_t*>(d + o_fmat);
+    if (need_fmat) p->fmat = reinterpret_cast<const uint32_t*>(d + o_fmat);
     p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);
     p->tb.rf = reinterpret_cast<const uint4*>(d + o_rf);
     p->tb.tw = reinterpret_cast<const float4*>(d + o_tw);
@@ -668,6 +621,58 @@ __global__ void kfft_finalize_tc64(const float2* __restrict__ K, uint4* __restri
     }
 }
 
+// k_f of the multi-pass path with 4096-point sub-rows (tcpass.cuh): per (h,
+// pair p, chunk c < 17, warp w, half, lane) four words, in the order the fold
+// of mp_pass_b_tc consumes them.  lane = 4r + q, k2a = 8w + r, k2b = 63 - k2a;
+// half 0 = bins (s0, k2a), (s1, k2b), half 1 = bins (s0, k2b), (s1, k2a);
+// bin (sub-row k0, s, k2) is k = k0 + R0 (s + 64 k2).
+// - p > 0, c < 16: s0 = 4c + q of sub-row p, s1 = 63 - s0 of sub-row R0 - p.
+// - p = 0, c < 9: sub-row 0 as the N = 4096 kernel (s0 = 4c + q, s1 = 64 - s0,
+//   c = 8: s0 = 32 for q = 0); c >= 9: s0 = 4(c - 9) + q and s1 = 63 - s0,
+//   both of sub-row R0/2.
+// Bins that do not exist (copies, padding, chunk 16 of p > 0) are zero.
+__global__ void kfft_finalize_tcmp(const float2* __restrict__ K, uint4* __restrict__ kf, int64_t H, int R0,
+                                   int dtype) {
+    const int64_t M = int64_t(R0) * 4096, L2 = 2 * M;
+    const int pairs = R0 / 2;
+    const int64_t total = H * pairs * TcB::KFP;
+    for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+         idx += int64_t(gridDim.x) * blockDim.x) {
+        const int lane = int(idx & 31), half = int((idx >> 5) & 1), w = int((idx >> 6) & 3);
+        const int64_t hpc = idx >> 8;
+        const int c = int(hpc % TcB::KF_CHUNKS);
+        const int64_t hp = hpc / TcB::KF_CHUNKS;
+        const int p = int(hp % pairs);
+        const int64_t h = hp / pairs;
+        const int r = lane >> 2, q = lane & 3, k2a = 8 * w + r, k2b = 63 - k2a;
+        int s0 = -1, s1 = -1, kr0 = 0, kr1 = 0;  // sub-problems and their sub-rows
+        if (p > 0) {
+            if (c < 16) {
+                s0 = 4 * c + q;
+                s1 = 63 - s0;
+                kr0 = p;
+                kr1 = R0 - p;
+            }
+        } else if (c < 8) {
+            s0 = 4 * c + q;
+            s1 = s0 == 0 ? -1 : 64 - s0;
+        } else if (c == 8) {
+            s0 = q == 0 ? 32 : -1;
+        } else {
+            s0 = 4 * (c - 9) + q;
+            s1 = 63 - s0;
+            kr0 = kr1 = pairs;
+        }
+        const int sa[2] = {s0, s1}, ra[2] = {kr0, kr1}, ka[2] = {half ? k2b : k2a, half ? k2a : k2b};
+        uint32_t words[4] = {0, 0, 0, 0};
+        for (int i = 0; i < 2; ++i)
+            if (sa[i] >= 0)
+                fold_coeffs(K + h * L2, ra[i] + int64_t(R0) * (sa[i] + 64 * int64_t(ka[i])), M, dtype, &words[2 * i],
+                            &words[2 * i + 1]);
+        kf[idx] = make_uint4(words[0], words[1], words[2], words[3]);
+    }
+}
+
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -710,6 +715,9 @@ extern "C" fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float*
     if (plan->tc64)
         kfft_finalize_tc64<<<grid_for(H * 9 * 4 * 2 * 32), 256, 0, st>>>(a, static_cast<uint4*>(k_f), H,
                                                                            plan->info.dtype);
+    else if (plan->mpL == kMpLtc)
+        kfft_finalize_tcmp<<<grid_for(H * (plan->R0 / 2) * TcB::KFP), 256, 0, st>>>(
+            a, static_cast<uint4*>(k_f), H, plan->R0, plan->info.dtype);
     else
         kfft_finalize<<<grid_for(H * plan->R0 * plan->R1 * 128), 256, 0, st>>>(
             a, static_cast<uint4*>(k_f), H, plan->R0, plan->R1, plan->info.dtype);
@@ -744,7 +752,8 @@ static fftconv_status_t forward_impl(fftconv_plan_t plan, const void* u, const v
             overlap(plan->workspace, nbw, k_f, kb) ||
             (gated && (overlap(plan->workspace, nbw, w_in, nb) || overlap(plan->workspace, nbw, w_out, nb))))
             return FFTCONV_ERR_INVALID;
-        e = launch_multipass(plan, u, gated ? w_in : nullptr, gated ? w_out : nullptr, k_f, y, B, H, st);
+        e = launch_multipass(plan, u, gated ? w_in : nullptr, gated ? w_out : nullptr, k_f, y, plan->workspace, B,
+                             H, st);
     } else {
         e = launch_fused(plan, u, gated ? w_in : nullptr, gated ? w_out : nullptr, k_f, y, B, H, st);
     }
@@ -848,11 +857,7 @@ extern "C" fftconv_status_t fftconv_forward_noalloc(fftconv_plan_t plan, const v
         if (fftconv_workspace_bytes(plan, B, H) > FFTCONV_STATIC_SCRATCH_BYTES) return FFTCONV_ERR_WORKSPACE;
         void* scratch = static_scratch_for_current_device();
         if (!scratch) return FFTCONV_ERR_CUDA;
-        MPArgs args{static_cast<const uint16_t*>(u), nullptr, nullptr, static_cast<const uint4*>(k_f),
-                    static_cast<uint16_t*>(y), static_cast<uint32_t*>(scratch), int(B), int(H), plan->R0,
-                    plan->mp, plan->dev_err};
-        e = plan->info.dtype == FFTCONV_F16 ? launch_mp_r<0, false>(plan, args, B * H, st)
-                                            : launch_mp_r<1, false>(plan, args, B * H, st);
+        e = launch_multipass(plan, u, nullptr, nullptr, k_f, y, scratch, B, H, st);
     } else {
         e = launch_fused(plan, u, nullptr, nullptr, k_f, y, B, H, st);
     }

@@ -1,0 +1,56 @@
+// Multi-pass launches with sub-rows of 4096 points (pass B on the
+// fifth-generation tensor cores, tcpass.cuh).
+#include "plan.h"
+#include "tcpass.cuh"
+
+namespace fftconv {
+namespace {
+
+template <int DT, int R0, bool G>
+cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
+    constexpr int HALF = R0 / 2, L = kMpLtc;
+    const size_t smem_a = size_t(HALF) * kSeg * 4 * (G ? 2 : 1) + 32;
+    const size_t smem_c = size_t(R0) * kSeg * 4 + (G ? size_t(HALF) * kSeg * 4 : 0) + 32;
+    static int na = 0, nb = 0, nc = 0;
+    cudaError_t e;
+    if ((e = prep_kernel(mp_pass_a<DT, R0, G, L>, smem_a, 256, &na)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_b_tc<DT>, TcB::SMEM, TcB::THREADS, &nb)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true>, smem_c, 256, &nc)) != cudaSuccess) return e;
+    const int64_t items_ac = rows * (L / 256);
+    auto grid = [&](int64_t items, int per_sm) {
+        int64_t gsz = int64_t(p->num_sms) * per_sm;
+        return unsigned(gsz < items ? gsz : items);
+    };
+    // pass B: one CTA per SM (its tensor-memory allocation takes all 512
+    // columns), two item pipelines per CTA
+    const int64_t items_b = rows * (R0 / 2), need_b = (items_b + 1) / 2;
+    if (items_b >= (int64_t(1) << 30)) return cudaErrorInvalidValue;  // pass B counts items in int
+    const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);
+    TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err};
+    mp_pass_a<DT, R0, G, L><<<grid(items_ac, na), 256, smem_a, st>>>(args);
+    mp_pass_b_tc<DT><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
+    mp_pass_c<DT, R0, G, L, true><<<grid(items_ac, nc), 256, smem_c, st>>>(args);
+    return cudaGetLastError();
+}
+
+template <int DT, bool G>
+cudaError_t launch_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
+    switch (p->R0) {
+        case 8: return launch_t<DT, 8, G>(p, args, rows, st);
+        case 16: return launch_t<DT, 16, G>(p, args, rows, st);
+        case 32: return launch_t<DT, 32, G>(p, args, rows, st);
+        case 64: return launch_t<DT, 64, G>(p, args, rows, st);
+        case 128: return launch_t<DT, 128, G>(p, args, rows, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_mp_l4k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st) {
+    if (p->info.dtype == FFTCONV_F16)
+        return gated ? launch_r<0, true>(p, args, rows, st) : launch_r<0, false>(p, args, rows, st);
+    return gated ? launch_r<1, true>(p, args, rows, st) : launch_r<1, false>(p, args, rows, st);
+}
+
+}  // namespace fftconv

@@ -1,17 +1,20 @@
-// Multi-pass causal long convolution for N = M = R0 * 16384 (32K..2M).
+// Multi-pass causal long convolution for N = M = R0 * L (32K..2M), with
+// sub-rows of L = 16384 (pass B on warp-level MMAs, below) or L = 4096 (pass B
+// on the fifth-generation tensor cores, tcpass.cuh).
 //
 // Partial fusion (FlashFFTConv page, section 3.4 "Kernel Fusion and
 // Recomputation Strategies" and the order-4 Algorithm 4): the outermost
 // Monarch factor R0 goes through HBM, everything inside it stays fused.
-//   n = L*n0 + n',  k = k0 + R0*kappa,  L = 16384
+//   n = L*n0 + n',  k = k0 + R0*kappa
 //   pass A:  T[k0][n'] = W_M^(n'*k0) * sum_{n0 < R0/2} z[L*n0 + n'] W_R0^(n0*k0) / sqrt(R0)
 //            (implicit zero padding: z[n] = 0 for n >= M/2, i.e. n0 >= R0/2)
 //   pass B:  per pair of sub-rows (k0, R0-k0): the L-point transform of each
-//            sub-row as R1 = 64 outer factor x 16 x 16 (the fused machinery
-//            with a full outer stage), the decimation-in-time fold with the
-//            kernel spectrum (bin k pairs with M-k, which lives in sub-row
-//            R0-k0), the same stages back, and the W_M^(n'*k0) twiddle of
-//            the conjugate-trick inverse -> T (in place)
+//            sub-row, the decimation-in-time fold with the kernel spectrum
+//            (bin k pairs with M-k, which lives in sub-row R0-k0), the same
+//            stages back, then the W_M^(n'*k0) twiddle of the conjugate-trick
+//            inverse -> T (in place).  L = 16384: R1 = 64 outer factor x 16 x
+//            16 (the fused machinery with a full outer stage).  L = 4096: 64 x
+//            64 on the tensor cores, and the twiddle moves into pass C.
 //   pass C:  y_z[L*n0 + n'] = sum_{k0} W_R0^(n0*k0) T[k0][n'] / sqrt(R0), only
 //            n0 < R0/2 (causal truncation), conjugated (and gated) -> y.
 // T holds 16-bit complex words (the plan dtype); it is the caller's
@@ -23,7 +26,8 @@
 
 namespace fftconv {
 
-constexpr int kMpL = 16384;   // sub-row length of pass B
+constexpr int kMpL = 16384;   // sub-row length of the warp-level pass B
+constexpr int kMpLtc = 4096;  // sub-row length of the tensor-core pass B
 constexpr int kMpR1 = 64;     // outer factor inside pass B
 constexpr int kSeg = 264;     // staged 1 KB segment + 32 B pad (words)
 
@@ -70,10 +74,10 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_
 }
 
 // ------------------------------------------------------------------ pass A
-template <int DT, int R0, bool GATED>
+template <int DT, int R0, bool GATED, int L>
 __global__ void __launch_bounds__(256, 2) mp_pass_a(const MPArgs a) {
     using O = Op<DT>;
-    constexpr int L = kMpL, HALF = R0 / 2, SEG = kSeg;
+    constexpr int HALF = R0 / 2, SEG = kSeg;
     constexpr uint32_t M = uint32_t(R0) * L;
     constexpr bool K8 = R0 <= 8;
     constexpr int KS = K8 ? 1 : R0 / 16, MT = (R0 + 7) / 8;
@@ -151,10 +155,13 @@ __global__ void __launch_bounds__(256, 2) mp_pass_a(const MPArgs a) {
 }
 
 // ------------------------------------------------------------------ pass C
-template <int DT, int R0, bool GATED>
+// TWID: T still lacks the W_M^(n'*k0) twiddle (tensor-core pass B); it is
+// applied here to each element before the contraction, as the chain
+// W_M^(n' t) * W_M^(8 n')^s (and * W_M^(4 n')) for k0 = 8s + t (+ 4).
+template <int DT, int R0, bool GATED, int L, bool TWID>
 __global__ void __launch_bounds__(256, 2) mp_pass_c(const MPArgs a) {
     using O = Op<DT>;
-    constexpr int L = kMpL, HALF = R0 / 2, SEG = kSeg;
+    constexpr int HALF = R0 / 2, SEG = kSeg;
     constexpr long M = long(R0) * L;
     constexpr bool K8 = R0 <= 4;
     constexpr int KS = K8 ? 1 : R0 / 8, MT = (R0 + 15) / 16;
@@ -193,6 +200,22 @@ __global__ void __launch_bounds__(256, 2) mp_pass_c(const MPArgs a) {
                 const int ka = 8 * s + t, kb = 8 * s + 4 + t;
                 bf[s][0] = ka < R0 ? st[ka * SEG + 8 * nt + g] : 0u;
                 bf[s][1] = (!K8 && kb < R0) ? st[kb * SEG + 8 * nt + g] : 0u;
+            }
+            if constexpr (TWID) {
+                static_assert(!K8 && R0 % 8 == 0, "twiddled pass C needs R0 >= 8");
+                const uint32_t np = uint32_t(o_base + 8 * nt + g);
+                const uint32_t mask = uint32_t(M) - 1;
+                cpx wa = twiddle_pow2((np * uint32_t(t)) & mask, uint32_t(M));
+                const cpx w4 = twiddle_pow2((4 * np) & mask, uint32_t(M));
+                const cpx w8 = twiddle_pow2((8 * np) & mask, uint32_t(M));
+                #pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    const cpx xa = cmul(O::unpack(bf[s][0]), wa);
+                    const cpx xb = cmul(O::unpack(bf[s][1]), cmul(wa, w4));
+                    bf[s][0] = O::pack(xa.r, xa.i);
+                    bf[s][1] = O::pack(xb.r, xb.i);
+                    wa = cmul(wa, w8);
+                }
             }
             #pragma unroll
             for (int m = 0; m < MT; ++m) {

@@ -1,0 +1,48 @@
+// The plan object shared by the library's translation units, and the
+// multi-pass launchers that live in their own units (compiled in parallel).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/fftconv.h"
+#include "multipass.cuh"
+
+struct fftconv_plan_s {
+    fftconv_plan_info_t info;
+    int R1 = 0;
+    void* dev = nullptr;  // one allocation: tables + error word
+    int* dev_err = nullptr;
+    fftconv::FusedTables tb{};
+    fftconv::MPTables mp{};
+    int R0 = 1;     // outer factor through HBM (1 on the fused path)
+    int mpL = 0;    // multi-pass sub-row length: 16384 (warp-level pass B) or 4096 (tensor-core pass B)
+    bool tc64 = false;               // N = 4096: order-2 64 x 64 product on tcgen05
+    const uint32_t* fmat = nullptr;  // the 64 x 64 DFT matrix rows (device), N = 4096 and mpL = 4096
+    int num_sms = 0;
+    void* workspace = nullptr;
+    size_t workspace_bytes = 0;
+};
+
+namespace fftconv {
+
+// Pass A, pass B, pass C of one forward call (args.T is the intermediate).
+cudaError_t launch_mp_l16k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st);
+cudaError_t launch_mp_l4k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st);
+
+// Dynamic shared memory opt-in and resident blocks per SM of a kernel (once).
+template <typename K>
+cudaError_t prep_kernel(K fn, size_t smem, int threads, int* per_sm) {
+    if (*per_sm == 0) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        int nb = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem);
+        if (e != cudaSuccess) return e;
+        *per_sm = nb > 0 ? nb : 1;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace fftconv

@@ -58,14 +58,34 @@ def test_query_fused_order2_4096():
         assert q["workspace_bytes_per_row"] == 0
 
 
-@pytest.mark.parametrize("N,R0", [(32768, 2), (262144, 16), (2097152, 128)])
-def test_query_multipass_factorization(N, R0):
+@pytest.mark.parametrize("N,R0", [(32768, 8), (262144, 64), (524288, 128)])
+def test_query_multipass_order3_factorization(N, R0):
+    """Sub-rows of 64 x 64 on the tensor cores: the default up to N = 512K."""
     q = F.query(N, F.BF16)
+    assert q["path"] == F.PATH_MULTIPASS and q["order"] == 3
+    assert q["factors"] == [R0, 64, 64]
+    assert R0 * 64 * 64 == N
+    assert q["workspace_bytes_per_row"] == 4 * N
+    # per pair of sub-rows: 17 chunks x 4 warps x 2 halves x 32 lanes x 16 bytes
+    assert q["kf_bytes_per_channel"] == R0 // 2 * 17 * 4 * 2 * 32 * 16
+    assert F.query(N, F.BF16, order=3) == q
+
+
+@pytest.mark.parametrize("N,R0,order", [(32768, 2, 4), (262144, 16, 4), (1048576, 64, 0), (2097152, 128, 0)])
+def test_query_multipass_order4_factorization(N, R0, order):
+    """Sub-rows of 64 x 16 x 16: on request, and the default above N = 512K."""
+    q = F.query(N, F.BF16, order=order)
     assert q["path"] == F.PATH_MULTIPASS and q["order"] == 4
     assert q["factors"] == [R0, 64, 16, 16]
     assert R0 * 64 * 16 * 16 == N
     assert q["workspace_bytes_per_row"] == 4 * N
     assert q["kf_bytes_per_channel"] == 8 * N
+
+
+def test_query_multipass_order3_limit():
+    with pytest.raises(F.FFTConvError) as e:
+        F.query(1048576, F.BF16, order=3)
+    assert e.value.status == 2
 
 
 @pytest.mark.parametrize("N", [0, 1000, 512, 3 << 12, 1 << 22])

@@ -46,6 +46,25 @@ def test_multipass_matches_oracle(N, dtype, gated, B, H):
     assert plan.device_status() == 0
 
 
+@pytest.mark.parametrize("N,dtype,gated,B,H", [
+    (32768, "bf16", True, 2, 2),
+    (262144, "fp16", False, 1, 2),
+])
+def test_multipass_order4_matches_oracle(N, dtype, gated, B, H):
+    """The 64 x 16 x 16 sub-rows on request at lengths whose default is 64 x 64."""
+    w = W.Workload("t", B, H, N, dtype, gated, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=11)
+    plan = F.Plan(N, torch_dtype(dtype), order=4)
+    assert plan.info["path"] == F.PATH_MULTIPASS and plan.info["order"] == 4
+    y, _ = run_gpu(plan, ins, gated)
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle_rows(ins, gated, threads=8)
+    rel = rel_l2(got, ref)
+    print(f"order 4 N={N} {dtype} gated={gated} rel-L2={rel:.3e}")
+    assert rel <= TOL[dtype]
+    assert plan.device_status() == 0
+
+
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_multipass_delta_kernels(dtype):
     N, H = 65536, 4
