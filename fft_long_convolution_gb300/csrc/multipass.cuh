@@ -108,45 +108,71 @@ __global__ void __launch_bounds__(256, 2) mp_pass_a(const MPArgs a) {
         }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
         uint32_t* Trow = a.T + row * long(M);
+        // NT column groups of 8 per iteration share each DFT fragment load; the
+        // twiddle of output (k0 = 8m + g, o) is W_M^(o g) * W_M^(8 o)^m, a
+        // product chain over the output tiles m
+        constexpr int NT = 2;
         #pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
-            const int nt = warp + 8 * i;
-            uint32_t bf[KS][2];
+        for (int i = 0; i < 4 / NT; ++i) {
+            uint32_t bf[NT][KS][2];
+            cpx tw[NT][2], ts[NT][2];
             #pragma unroll
-            for (int s = 0; s < KS; ++s) {
-                const int na = 8 * s + t, nb = 8 * s + 4 + t;
-                uint32_t va = 0, vb = 0;
-                if (na < HALF) {
-                    va = su[na * SEG + 8 * nt + g];
-                    if (GATED) va = O::mul2(va, sw[na * SEG + 8 * nt + g]);
+            for (int j = 0; j < NT; ++j) {
+                const int nt = warp + 8 * (NT * i + j);
+                #pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    const int na = 8 * s + t, nb = 8 * s + 4 + t;
+                    uint32_t va = 0, vb = 0;
+                    if (na < HALF) {
+                        va = su[na * SEG + 8 * nt + g];
+                        if (GATED) va = O::mul2(va, sw[na * SEG + 8 * nt + g]);
+                    }
+                    if (!K8 && nb < HALF) {
+                        vb = su[nb * SEG + 8 * nt + g];
+                        if (GATED) vb = O::mul2(vb, sw[nb * SEG + 8 * nt + g]);
+                    }
+                    bf[j][s][0] = va;
+                    bf[j][s][1] = vb;
                 }
-                if (!K8 && nb < HALF) {
-                    vb = su[nb * SEG + 8 * nt + g];
-                    if (GATED) vb = O::mul2(vb, sw[nb * SEG + 8 * nt + g]);
+                #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t o = uint32_t(o_base + 8 * nt + 2 * t + e);
+                    tw[j][e] = twiddle_pow2((o * uint32_t(g)) & (M - 1), M);
+                    ts[j][e] = twiddle_pow2((8 * o) & (M - 1), M);
                 }
-                bf[s][0] = va;
-                bf[s][1] = vb;
             }
-            const uint32_t o = uint32_t(o_base + 8 * nt + 2 * t);
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float acc[NT][4];
+                #pragma unroll
+                for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     const uint4 af = a.tb.of_a[(m * KS + s) * 32 + lane];
-                    if (K8) {
-                        O::mma8(acc, af.x, af.y, bf[0][0]);
-                    } else {
-                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
-                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                    #pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        if (K8) {
+                            O::mma8(acc[j], af.x, af.y, bf[j][0][0]);
+                        } else {
+                            const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                            O::mma16(acc[j], a4, bf[j][s][0], bf[j][s][1]);
+                        }
                     }
                 }
                 const uint32_t k0 = uint32_t(8 * m + g);
-                if (k0 < uint32_t(R0)) {
-                    const cpx v0 = cmul({acc[0], acc[2]}, twiddle_pow2((o * k0) & (M - 1), M));
-                    const cpx v1 = cmul({acc[1], acc[3]}, twiddle_pow2(((o + 1) * k0) & (M - 1), M));
-                    *reinterpret_cast<uint2*>(Trow + long(k0) * L + o) =
-                        make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+                #pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    if (k0 < uint32_t(R0)) {
+                        const uint32_t o = uint32_t(o_base + 8 * (warp + 8 * (NT * i + j)) + 2 * t);
+                        const cpx v0 = cmul({acc[j][0], acc[j][2]}, tw[j][0]);
+                        const cpx v1 = cmul({acc[j][1], acc[j][3]}, tw[j][1]);
+                        *reinterpret_cast<uint2*>(Trow + long(k0) * L + o) =
+                            make_uint2(O::pack(v0.r, v0.i), O::pack(v1.r, v1.i));
+                    }
+                    if (m + 1 < MT) {
+                        tw[j][0] = cmul(tw[j][0], ts[j][0]);
+                        tw[j][1] = cmul(tw[j][1], ts[j][1]);
+                    }
                 }
             }
         }
@@ -191,55 +217,70 @@ __global__ void __launch_bounds__(256, 2) mp_pass_c(const MPArgs a) {
                     bulk_g2s(swo + n0 * SEG, a.w_out + row * M + 2 * (long(L) * n0 + o_base), 1024, bar);
         }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
+        // NT column groups of 8 per iteration share each DFT fragment load
+        constexpr int NT = KS <= 8 ? 2 : 1;
         #pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
-            const int nt = warp + 8 * i;
-            uint32_t bf[KS][2];
+        for (int i = 0; i < 4 / NT; ++i) {
+            uint32_t bf[NT][KS][2];
             #pragma unroll
-            for (int s = 0; s < KS; ++s) {
-                const int ka = 8 * s + t, kb = 8 * s + 4 + t;
-                bf[s][0] = ka < R0 ? st[ka * SEG + 8 * nt + g] : 0u;
-                bf[s][1] = (!K8 && kb < R0) ? st[kb * SEG + 8 * nt + g] : 0u;
-            }
-            if constexpr (TWID) {
-                static_assert(!K8 && R0 % 8 == 0, "twiddled pass C needs R0 >= 8");
-                const uint32_t np = uint32_t(o_base + 8 * nt + g);
-                const uint32_t mask = uint32_t(M) - 1;
-                cpx wa = twiddle_pow2((np * uint32_t(t)) & mask, uint32_t(M));
-                const cpx w4 = twiddle_pow2((4 * np) & mask, uint32_t(M));
-                const cpx w8 = twiddle_pow2((8 * np) & mask, uint32_t(M));
+            for (int j = 0; j < NT; ++j) {
+                const int nt = warp + 8 * (NT * i + j);
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
-                    const cpx xa = cmul(O::unpack(bf[s][0]), wa);
-                    const cpx xb = cmul(O::unpack(bf[s][1]), cmul(wa, w4));
-                    bf[s][0] = O::pack(xa.r, xa.i);
-                    bf[s][1] = O::pack(xb.r, xb.i);
-                    wa = cmul(wa, w8);
+                    const int ka = 8 * s + t, kb = 8 * s + 4 + t;
+                    bf[j][s][0] = ka < R0 ? st[ka * SEG + 8 * nt + g] : 0u;
+                    bf[j][s][1] = (!K8 && kb < R0) ? st[kb * SEG + 8 * nt + g] : 0u;
+                }
+                if constexpr (TWID) {
+                    static_assert(!K8 && R0 % 8 == 0, "twiddled pass C needs R0 >= 8");
+                    const uint32_t np = uint32_t(o_base + 8 * nt + g);
+                    const uint32_t mask = uint32_t(M) - 1;
+                    cpx wa = twiddle_pow2((np * uint32_t(t)) & mask, uint32_t(M));
+                    const cpx w4 = twiddle_pow2((4 * np) & mask, uint32_t(M));
+                    const cpx w8 = twiddle_pow2((8 * np) & mask, uint32_t(M));
+                    #pragma unroll
+                    for (int s = 0; s < KS; ++s) {
+                        const cpx xa = cmul(O::unpack(bf[j][s][0]), wa);
+                        const cpx xb = cmul(O::unpack(bf[j][s][1]), cmul(wa, w4));
+                        bf[j][s][0] = O::pack(xa.r, xa.i);
+                        bf[j][s][1] = O::pack(xb.r, xb.i);
+                        if (s + 1 < KS) wa = cmul(wa, w8);
+                    }
                 }
             }
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float acc[NT][4];
+                #pragma unroll
+                for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     const uint4 af = a.tb.oi_c[(m * KS + s) * 32 + lane];
-                    if (K8) {
-                        O::mma8(acc, af.x, af.y, bf[0][0]);
-                    } else {
-                        const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
-                        O::mma16(acc, a4, bf[s][0], bf[s][1]);
+                    #pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        if (K8) {
+                            O::mma8(acc[j], af.x, af.y, bf[j][0][0]);
+                        } else {
+                            const uint32_t a4[4] = {af.x, af.y, af.z, af.w};
+                            O::mma16(acc[j], a4, bf[j][s][0], bf[j][s][1]);
+                        }
                     }
                 }
                 const int n0 = 8 * m + g;
                 if (n0 < HALF) {
-                    const long p = long(L) * n0 + o_base + 8 * nt + 2 * t;  // reals 2p..2p+3
-                    float r0 = acc[0], i0 = -acc[2], r1 = acc[1], i1 = -acc[3];
-                    if (GATED) {
-                        const uint2 wv = *reinterpret_cast<const uint2*>(swo + n0 * SEG + 8 * nt + 2 * t);
-                        const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
-                        r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
+                    #pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const int nt = warp + 8 * (NT * i + j);
+                        const long p = long(L) * n0 + o_base + 8 * nt + 2 * t;  // reals 2p..2p+3
+                        float r0 = acc[j][0], i0 = -acc[j][2], r1 = acc[j][1], i1 = -acc[j][3];
+                        if (GATED) {
+                            const uint2 wv = *reinterpret_cast<const uint2*>(swo + n0 * SEG + 8 * nt + 2 * t);
+                            const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
+                            r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
+                        }
+                        *reinterpret_cast<uint2*>(a.y + row * M + 2 * p) =
+                            make_uint2(O::pack(r0, i0), O::pack(r1, i1));
                     }
-                    *reinterpret_cast<uint2*>(a.y + row * M + 2 * p) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
                 }
             }
         }
