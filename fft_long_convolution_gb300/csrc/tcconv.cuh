@@ -185,18 +185,21 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     const uint32_t tmem = s_tmem;
     const uint32_t tD = tmem + 192 + 160 * g;
     const uint32_t laneA = uint32_t(32 * w) << 16, laneB = uint32_t(32 * w + 16) << 16;
-    if (threadIdx.x < 128) {  // the three DFT matrices: lane t <- row t
-        #pragma unroll 1
-        for (int c = 0; c < 12; ++c) {
-            uint32_t rr[16];
-            const uint4* src = reinterpret_cast<const uint4*>(a.fmat + (c >> 2) * 128 * 64 + threadIdx.x * 64 + 16 * (c & 3));
+    {  // the three DFT matrices, lane t <- row t; each warpgroup moves three of the twelve 16-column chunks
+        const int grp = threadIdx.x >> 7, row = 32 * w + lane;
+        uint32_t rr[3][16];
+        #pragma unroll
+        for (int c3 = 0; c3 < 3; ++c3) {
+            const int c = 3 * grp + c3;
+            const uint4* src = reinterpret_cast<const uint4*>(a.fmat + (c >> 2) * 128 * 64 + row * 64 + 16 * (c & 3));
             #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 x = src[i];
-                rr[4 * i] = x.x; rr[4 * i + 1] = x.y; rr[4 * i + 2] = x.z; rr[4 * i + 3] = x.w;
+                rr[c3][4 * i] = x.x; rr[c3][4 * i + 1] = x.y; rr[c3][4 * i + 2] = x.z; rr[c3][4 * i + 3] = x.w;
             }
-            tc::st16(tmem + laneA + 16 * c, rr);
         }
+        #pragma unroll
+        for (int c3 = 0; c3 < 3; ++c3) tc::st16(tmem + laneA + 16 * (3 * grp + c3), rr[c3]);
         tc::wait_st();
     }
     tc::fence_before();

@@ -120,7 +120,11 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
         for (int gp = 0; gp < 2; ++gp) {  // the first item of both pipelines, overlapping the set-up
             const int vp = int(blockIdx.x) * 2 + gp;
             const int j0 = int(int64_t(vp) * items / V), j1 = int(int64_t(vp + 1) * items / V);
-            if (j0 < j1) stage_item(j0, smem + gp * C::PIPE, reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * gp);
+            if (j0 < j1) {
+                stage_item(j0, smem + gp * C::PIPE, reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * gp);
+                const Item x = decode(j0);
+                bulk_prefetch_l2(a.kf + (size_t(x.h) * pairs + x.p) * C::KFP, C::KFP * 16);
+            }
         }
     }
     if (threadIdx.x < 32) {
@@ -154,18 +158,21 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
     const uint32_t tmem = s_tmem;
     const uint32_t tD = tmem + 192 + 160 * g;
     const uint32_t laneA = uint32_t(32 * w) << 16, laneB = uint32_t(32 * w + 16) << 16;
-    if (threadIdx.x < 128) {  // the three DFT matrices: lane t <- row t
-        #pragma unroll 1
-        for (int c = 0; c < 12; ++c) {
-            uint32_t rr[16];
-            const uint4* src = reinterpret_cast<const uint4*>(a.fmat + (c >> 2) * 128 * 64 + threadIdx.x * 64 + 16 * (c & 3));
+    {  // the three DFT matrices, lane t <- row t; each warpgroup moves three of the twelve 16-column chunks
+        const int grp = threadIdx.x >> 7, row = 32 * w + lane;
+        uint32_t rr[3][16];
+        #pragma unroll
+        for (int c3 = 0; c3 < 3; ++c3) {
+            const int c = 3 * grp + c3;
+            const uint4* src = reinterpret_cast<const uint4*>(a.fmat + (c >> 2) * 128 * 64 + row * 64 + 16 * (c & 3));
             #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 x = src[i];
-                rr[4 * i] = x.x; rr[4 * i + 1] = x.y; rr[4 * i + 2] = x.z; rr[4 * i + 3] = x.w;
+                rr[c3][4 * i] = x.x; rr[c3][4 * i + 1] = x.y; rr[c3][4 * i + 2] = x.z; rr[c3][4 * i + 3] = x.w;
             }
-            tc::st16(tmem + laneA + 16 * c, rr);
         }
+        #pragma unroll
+        for (int c3 = 0; c3 < 3; ++c3) tc::st16(tmem + laneA + 16 * (3 * grp + c3), rr[c3]);
         tc::wait_st();
     }
     tc::fence_before();
@@ -197,6 +204,11 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
         const Item x = decode(it);
         const bool sp = x.p == 0;
         const bool has_next = it + 1 < i1;
+        if (tg == 32 && has_next) {  // the next item's k_f into L2 (read by the next fold)
+            const Item xn = decode(it + 1);
+            if (xn.p != x.p || xn.h != x.h)
+                bulk_prefetch_l2(a.kf + (size_t(xn.h) * pairs + xn.p) * C::KFP, C::KFP * 16);
+        }
 
         // ---------------- input: sub-row hf -> B1
         bool bad = !mbar_wait_sleep(&bars[1], inpar, kWaitSleepLimit, kWaitHintNs);

@@ -84,7 +84,13 @@ typedef struct {
 /*
  * Describe the plan that fftconv_plan_create would build, without touching
  * the GPU.  N must be a power of two with 2^10 <= N <= 2^21.  order = 0 picks
- * the factorization; a nonzero order is honoured or rejected.
+ * the factorization; a nonzero order is honoured or rejected.  Factorizations
+ * (outer factor first; "Higher-order decompositions" of section 3.4):
+ *   N = 4096:             order 2, 64 x 64 (fused, tensor-memory kernel)
+ *   N <= 16384 otherwise: order 3, N/256 x 16 x 16 (fused)
+ *   32768 <= N <= 2^19:   order 3, N/4096 x 64 x 64 (multi-pass; the default),
+ *                         or order 4 on request
+ *   N >= 2^20:            order 4, N/16384 x 64 x 16 x 16 (multi-pass)
  * Returns OK, INVALID (info NULL) or UNSUPPORTED.
  */
 fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype, int order,
