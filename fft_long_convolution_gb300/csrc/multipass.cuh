@@ -75,7 +75,7 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_
 
 // ------------------------------------------------------------------ pass A
 template <int DT, int R0, bool GATED, int L>
-__global__ void __launch_bounds__(256, 2) mp_pass_a(const MPArgs a) {
+__global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_a(const MPArgs a) {
     using O = Op<DT>;
     constexpr int HALF = R0 / 2, SEG = kSeg;
     constexpr uint32_t M = uint32_t(R0) * L;
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(256, 2) mp_pass_a(const MPArgs a) {
 // applied here to each element before the contraction, as the chain
 // W_M^(n' t) * W_M^(8 n')^s (and * W_M^(4 n')) for k0 = 8s + t (+ 4).
 template <int DT, int R0, bool GATED, int L, bool TWID>
-__global__ void __launch_bounds__(256, 2) mp_pass_c(const MPArgs a) {
+__global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_c(const MPArgs a) {
     using O = Op<DT>;
     constexpr int HALF = R0 / 2, SEG = kSeg;
     constexpr long M = long(R0) * L;
