@@ -137,3 +137,19 @@ def test_workload_full_size_sampled(name):
     print(f"{name}: sampled rows {len(flat)} worst rel-L2 {max(rels):.3e}")
     assert torch.isfinite(y.float()).all()
     assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("dtype,gated", [("bf16", True), ("fp16", False)])
+def test_tc64_many_items_every_row(dtype, gated):
+    """N = 4096 with several row pairs per pipeline and an odd batch (the
+    last pair of every channel has no second row); every row checked."""
+    w = W.Workload("t", 7, 180, 4096, dtype, gated, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=13)
+    plan = _plan(4096, dtype)
+    y, _ = run_gpu(plan, ins, gated)
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle_rows(ins, gated, threads=8)
+    worst = max(rel_l2(got[b, h], ref[b, h]) for b in range(w.B) for h in range(w.H))
+    print(f"N=4096 {dtype} gated={gated} rows={w.rows} worst row rel-L2={worst:.3e}")
+    assert worst <= TOL[dtype]
+    assert plan.device_status() == 0

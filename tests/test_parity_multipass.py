@@ -127,3 +127,22 @@ def test_workload_full_size_sampled(name, nrows):
     print(f"{name}: sampled rows {flat} worst rel-L2 {worst:.3e}")
     assert torch.isfinite(y.float()).all()
     assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("N,dtype,gated,B,H", [
+    (32768, "bf16", False, 3, 100),
+    (65536, "fp16", True, 2, 40),
+])
+def test_multipass_many_items_every_row(N, dtype, gated, B, H):
+    """Several work items per pipeline (next-item staging, pair changes,
+    k_f prefetch) with every row compared with the oracle."""
+    w = W.Workload("t", B, H, N, dtype, gated, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=12)
+    plan = F.Plan(N, torch_dtype(dtype))
+    y, _ = run_gpu(plan, ins, gated)
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle_rows(ins, gated, threads=8)
+    worst = max(rel_l2(got[b, h], ref[b, h]) for b in range(B) for h in range(H))
+    print(f"N={N} {dtype} gated={gated} rows={B * H} worst row rel-L2={worst:.3e}")
+    assert worst <= TOL[dtype]
+    assert plan.device_status() == 0
