@@ -19,8 +19,8 @@ STATUS = {0: "OK", 1: "ERR_INVALID", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIGN", 4: "E
 
 EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy", "fftconv_plan_get_info",
             "fftconv_kf_bytes", "fftconv_workspace_bytes", "fftconv_set_workspace", "fftconv_kernel_fft",
-            "fftconv_forward", "fftconv_forward_gated", "fftconv_forward_noalloc", "fftconv_device_status",
-            "fftconv_status_string", "fftconv_version"]
+            "fftconv_forward", "fftconv_forward_gated", "fftconv_forward_noalloc", "fftconv_host_scratch_bytes",
+            "fftconv_forward_host", "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
 
 
 class FFTConvError(RuntimeError):
@@ -67,6 +67,9 @@ def lib(auto_build: bool = True):
         L.fftconv_forward.argtypes = [vp, vp, vp, vp, i64, i64, vp]
         L.fftconv_forward_gated.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp]
         L.fftconv_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, vp]
+        L.fftconv_host_scratch_bytes.argtypes = [vp, i64, i64, ctypes.c_int]
+        L.fftconv_host_scratch_bytes.restype = sz
+        L.fftconv_forward_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp, sz, vp]
         L.fftconv_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         L.fftconv_status_string.argtypes = [ctypes.c_int]
         L.fftconv_status_string.restype = ctypes.c_char_p
@@ -119,6 +122,7 @@ class Plan:
         _check(lib().fftconv_plan_get_info(self._h, ctypes.byref(info)), "fftconv_plan_get_info")
         self.info = info.as_dict()
         self._workspace = None
+        self._host_scratch = None
 
     def close(self):
         if getattr(self, "_h", None):
@@ -180,6 +184,29 @@ class Plan:
         self._ensure_workspace(B, H, u.device)
         _check(lib().fftconv_forward_gated(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y),
                                            B, H, _stream(stream)), "fftconv_forward_gated")
+        return y
+
+    def forward_host(self, u, k_f, w_in=None, w_out=None, y=None, stream=None):
+        """u (and w_in, w_out): host tensors [B, H, N] in the plan dtype,
+        page-locked for the copies to overlap -> y (host).  Chunks of rows are
+        copied in, convolved and copied back with the three steps overlapped;
+        y is complete once the stream has been synchronised."""
+        import torch
+        for t in (u, w_in, w_out, y):
+            if t is not None and (t.is_cuda or not t.is_contiguous() or t.dtype != self.torch_dtype):
+                raise ValueError("host tensors must be contiguous CPU tensors of the plan dtype")
+        if (w_in is None) != (w_out is None):
+            raise ValueError("w_in and w_out go together")
+        B, H, N = u.shape
+        if y is None:
+            y = torch.empty(u.shape, dtype=u.dtype, pin_memory=True)
+        gated = w_in is not None
+        need = int(lib().fftconv_host_scratch_bytes(self._h, B, H, int(gated)))
+        if need and (self._host_scratch is None or self._host_scratch.numel() < need):
+            self._host_scratch = torch.empty(need, dtype=torch.uint8, device=k_f.device)
+        n = 0 if self._host_scratch is None else self._host_scratch.numel()
+        _check(lib().fftconv_forward_host(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y), B, H,
+                                          _ptr(self._host_scratch), n, _stream(stream)), "fftconv_forward_host")
         return y
 
     def device_status(self, stream=None) -> int:

@@ -3,6 +3,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -472,6 +473,10 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
 extern "C" fftconv_status_t fftconv_plan_destroy(fftconv_plan_t plan) {
     if (!plan) return FFTCONV_OK;
     cudaError_t e = cudaSuccess;
+    for (cudaEvent_t& ev : plan->ev)
+        if (ev) cudaEventDestroy(ev);
+    if (plan->s_in) cudaStreamDestroy(plan->s_in);
+    if (plan->s_out) cudaStreamDestroy(plan->s_out);
     if (plan->dev) e = cudaFree(plan->dev);
     delete plan;
     return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
@@ -862,4 +867,142 @@ extern "C" fftconv_status_t fftconv_forward_noalloc(fftconv_plan_t plan, const v
         e = launch_fused(plan, u, nullptr, nullptr, k_f, y, B, H, st);
     }
     return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+}
+
+// --------------------------------------------------------------- host-buffer forward
+//
+// Rows that live in host memory pass through three device buffer sets in
+// chunks; the copy of chunk c to the device (stream s_in), the convolution of
+// chunk c - 1 (the caller's stream) and the copy back of chunk c - 2 (stream
+// s_out) overlap.  Events order each buffer set's reuse: its inputs are
+// overwritten only after the convolution that read them, its output only
+// after the copy that drained it.
+
+namespace {
+
+constexpr int kHostSets = 3;
+constexpr int64_t kHostChunks = 8;  // target number of chunks per call
+
+struct HostChunks {
+    bool by_b;       // chunks of whole batch entries; else (B = 1) ranges of channels
+    int64_t per, n;  // batch entries (or channels) per chunk, number of chunks
+    int64_t rows;    // rows of the largest chunk
+};
+
+HostChunks host_chunks(int64_t B, int64_t H) {
+    HostChunks c{};
+    c.by_b = B >= 2;
+    const int64_t ext = c.by_b ? B : H;
+    c.per = (ext + kHostChunks - 1) / kHostChunks;
+    c.n = (ext + c.per - 1) / c.per;
+    c.rows = c.by_b ? c.per * H : c.per;
+    return c;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct HostLayout {
+    size_t buf, set, ws, total;  // one chunk buffer, one set, the multi-pass intermediate, all
+};
+
+HostLayout host_layout(const fftconv_plan_s* p, int64_t B, int64_t H, bool gated) {
+    const HostChunks c = host_chunks(B, H);
+    HostLayout l{};
+    l.buf = align256(size_t(c.rows) * size_t(p->info.N) * 2);
+    l.set = l.buf * (gated ? 4 : 2);
+    l.ws = p->info.path == FFTCONV_PATH_MULTIPASS ? align256(size_t(c.rows) * size_t(p->info.N) * 4) : 0;
+    l.total = kHostSets * l.set + l.ws;
+    return l;
+}
+
+cudaError_t host_pipeline_init(fftconv_plan_s* p) {
+    if (p->s_in) return cudaSuccess;
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (cudaEvent_t& ev : p->ev)
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" size_t fftconv_host_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H, int gated) {
+    if (!plan || B <= 0 || H <= 0) return 0;
+    return host_layout(plan, B, H, gated != 0).total;
+}
+
+extern "C" fftconv_status_t fftconv_forward_host(fftconv_plan_t plan, const void* u, const void* w_in,
+                                                 const void* w_out, const void* k_f, void* y, int64_t B,
+                                                 int64_t H, void* scratch, size_t scratch_bytes,
+                                                 fftconv_stream_t stream) {
+    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (B == 0 || H == 0) return FFTCONV_OK;
+    if (!u || !k_f || !y || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
+    const bool gated = w_in != nullptr;
+    if (misaligned(k_f)) return FFTCONV_ERR_ALIGN;
+    if (B * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    const size_t nb = size_t(B) * size_t(H) * size_t(plan->info.N) * 2;
+    if (overlap(y, nb, u, nb) || (gated && (overlap(y, nb, w_in, nb) || overlap(y, nb, w_out, nb))))
+        return FFTCONV_ERR_INVALID;
+    const HostLayout lay = host_layout(plan, B, H, gated);
+    if (!scratch || scratch_bytes < lay.total) return FFTCONV_ERR_WORKSPACE;
+    if (misaligned(scratch)) return FFTCONV_ERR_ALIGN;
+    if (host_pipeline_init(plan) != cudaSuccess) {
+        cudaGetLastError();
+        return FFTCONV_ERR_CUDA;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaEvent_t ev_start = plan->ev[0], ev_end = plan->ev[1];
+    cudaEvent_t* ev_in = plan->ev + 2;
+    cudaEvent_t* ev_done = plan->ev + 2 + kHostSets;
+    cudaEvent_t* ev_out = plan->ev + 2 + 2 * kHostSets;
+    uint8_t* sb = static_cast<uint8_t*>(scratch);
+    void* ws = sb + kHostSets * lay.set;
+    const HostChunks c = host_chunks(B, H);
+    const size_t row_bytes = size_t(plan->info.N) * 2;
+    const size_t kfc = size_t(plan->info.kf_bytes_per_channel);
+    auto hptr = [](const void* base, size_t off) { return static_cast<const uint8_t*>(base) + off; };
+    cudaError_t e = cudaEventRecord(ev_start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->s_in, ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->s_out, ev_start, 0);
+    for (int64_t ci = 0; ci < c.n && e == cudaSuccess; ++ci) {
+        const int s = int(ci % kHostSets);
+        // the chunk's rows are contiguous: batch entries [b0, b0 + nbc) x all
+        // channels, or (B = 1) channels [h0, h0 + nhc)
+        const int64_t b0 = c.by_b ? ci * c.per : 0, h0 = c.by_b ? 0 : ci * c.per;
+        const int64_t nbc = c.by_b ? std::min(c.per, B - b0) : 1;
+        const int64_t nhc = c.by_b ? H : std::min(c.per, H - h0);
+        const size_t off = size_t(b0 * H + h0) * row_bytes, bytes = size_t(nbc * nhc) * row_bytes;
+        uint8_t* du = sb + size_t(s) * lay.set;
+        uint8_t* dy = du + lay.buf;
+        uint8_t* dwi = gated ? dy + lay.buf : nullptr;
+        uint8_t* dwo = gated ? dwi + lay.buf : nullptr;
+        if (ci >= kHostSets) e = cudaStreamWaitEvent(plan->s_in, ev_done[s], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(du, hptr(u, off), bytes, cudaMemcpyHostToDevice, plan->s_in);
+        if (gated && e == cudaSuccess)
+            e = cudaMemcpyAsync(dwi, hptr(w_in, off), bytes, cudaMemcpyHostToDevice, plan->s_in);
+        if (gated && e == cudaSuccess)
+            e = cudaMemcpyAsync(dwo, hptr(w_out, off), bytes, cudaMemcpyHostToDevice, plan->s_in);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_in[s], plan->s_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in[s], 0);
+        if (e == cudaSuccess && ci >= kHostSets) e = cudaStreamWaitEvent(st, ev_out[s], 0);
+        if (e != cudaSuccess) break;
+        const void* kfp = hptr(k_f, size_t(h0) * kfc);
+        e = plan->info.path == FFTCONV_PATH_MULTIPASS
+                ? launch_multipass(plan, du, dwi, dwo, kfp, dy, ws, nbc, nhc, st)
+                : launch_fused(plan, du, dwi, dwo, kfp, dy, nbc, nhc, st);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_done[s], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->s_out, ev_done[s], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t*>(y) + off, dy, bytes, cudaMemcpyDeviceToHost, plan->s_out);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_out[s], plan->s_out);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ev_end, plan->s_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_end, 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FFTCONV_ERR_CUDA;
+    }
+    return FFTCONV_OK;
 }

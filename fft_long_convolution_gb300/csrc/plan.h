@@ -23,6 +23,11 @@ struct fftconv_plan_s {
     int num_sms = 0;
     void* workspace = nullptr;
     size_t workspace_bytes = 0;
+    // host-buffer forward: two copy streams and the events that order its
+    // three device buffer sets (start, end, then per set: in, done, out),
+    // created on first use
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev[11] = {};
 };
 
 namespace fftconv {

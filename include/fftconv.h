@@ -198,6 +198,40 @@ fftconv_status_t fftconv_forward_noalloc(fftconv_plan_t plan, const void *u, con
                                          int64_t B, int64_t H, fftconv_stream_t stream);
 
 /*
+ * Forward convolution of rows that live in host memory: u (and w_in, w_out)
+ * are copied to the device, convolved as fftconv_forward(_gated) would, and
+ * y is copied back, all ordered on `stream`.  The rows are cut into chunks
+ * (whole batch entries, or ranges of channels when B = 1) that pass through
+ * three device buffer sets, so the copy of one chunk to the device, the
+ * convolution of the one before and the copy back of the one before that
+ * overlap (the plan keeps two internal copy streams for this, created on the
+ * first call and released by fftconv_plan_destroy).  The FlashFFTConv page
+ * has no counterpart: it assumes device-resident inputs; this call serves
+ * callers whose sequences are produced and consumed on the host.
+ *
+ * - u, w_in, w_out, y: host memory, [B][H][N] in the plan dtype.  Page-locked
+ *   memory (cudaHostAlloc / cudaHostRegister) is needed for the copies to
+ *   overlap; pageable memory works but serialises them.  w_in and w_out are
+ *   both NULL (plain convolution) or both non-NULL (gated).  y must not
+ *   overlap the inputs.
+ * - k_f: device, as for fftconv_forward.
+ * - scratch: caller-owned device memory of at least
+ *   fftconv_host_scratch_bytes(plan, B, H, gated) bytes, 16-byte aligned; it
+ *   holds the three buffer sets and the multi-pass intermediate of one chunk,
+ *   so no workspace needs to be attached.  It must not be used by anything
+ *   else until the work on `stream` has completed.
+ * - Returns OK, INVALID, ALIGN, WORKSPACE (scratch missing or too small) or
+ *   CUDA.  When the call returns OK the copies and launches are queued; y is
+ *   complete once `stream` has been synchronised.
+ * - One plan must not run this call concurrently from two host threads.
+ */
+size_t fftconv_host_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H, int gated);
+fftconv_status_t fftconv_forward_host(fftconv_plan_t plan, const void *u, const void *w_in,
+                                      const void *w_out, const void *k_f, void *y, int64_t B,
+                                      int64_t H, void *scratch, size_t scratch_bytes,
+                                      fftconv_stream_t stream);
+
+/*
  * Read and clear the plan's device error word (waits for `stream`).
  * *out = 0 if no bounded on-device wait has given up since the last call,
  * else FFTCONV_ERR_TIMEOUT.  Returns OK, INVALID or CUDA.
