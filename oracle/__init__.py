@@ -59,6 +59,11 @@ def _load():
         lib.oracle_direct_causal_conv_at.argtypes = [_dp, _dp, i64, i64]
         lib.oracle_direct_causal_conv_at.restype = ctypes.c_double
         lib.oracle_direct_causal_conv.argtypes = [_dp, _dp, _dp, i64]
+        lib.oracle_causal_corr.argtypes = [_dp, _dp, _dp, i64]
+        lib.oracle_direct_causal_corr_at.argtypes = [_dp, _dp, i64, i64]
+        lib.oracle_direct_causal_corr_at.restype = ctypes.c_double
+        lib.oracle_input_grad_rows.argtypes = [_dp, _dp, _dp, _dp, _dp, i64, i64, i64, i64]
+        lib.oracle_kernel_grad_channels.argtypes = [_dp, _dp, _dp, _dp, _dp, i64, i64, i64, i64, i64]
         _lib = lib
     return _lib
 
@@ -149,3 +154,71 @@ def causal_conv_batch(u: np.ndarray, k: np.ndarray, w_in: Optional[np.ndarray] =
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda r: run(r, r + 1), r_list))
     return y.reshape(shape)
+
+
+# ---------------------------------------------------------------- backward
+
+def causal_corr(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """One row: out[i] = sum_{t>=i} a[t] b[t-i], through the 2N-point DFT."""
+    a, b = _f64(a), _f64(b)
+    out = np.empty_like(a)
+    if _load().oracle_causal_corr(_ptr(a), _ptr(b), _ptr(out), a.size):
+        raise ValueError("N must be a power of two")
+    return out
+
+
+def direct_causal_corr_at(a: np.ndarray, b: np.ndarray, i: int) -> float:
+    """One correlation output by the definition (compensated sum), O(N - i)."""
+    a, b = _f64(a), _f64(b)
+    return float(_load().oracle_direct_causal_corr_at(_ptr(a), _ptr(b), a.size, int(i)))
+
+
+def input_grad_batch(dy: np.ndarray, k: np.ndarray, w_in: Optional[np.ndarray] = None,
+                     w_out: Optional[np.ndarray] = None, threads: int = 1) -> np.ndarray:
+    """du for dy [B, H, N], k [H, N]; gated when both gates are given:
+    du = w_in * corr(w_out * dy, k)."""
+    k = _f64(k)
+    H, N = k.shape
+    dy = _f64(dy)
+    shape = dy.shape
+    d2 = dy.reshape(-1, N)
+    gi = _f64(w_in).reshape(-1, N) if w_in is not None else None
+    go = _f64(w_out).reshape(-1, N) if w_out is not None else None
+    du = np.zeros_like(d2)
+    lib = _load()
+
+    def run(r0: int, r1: int):
+        rc = lib.oracle_input_grad_rows(_ptr(d2), _ptr(gi), _ptr(go), _ptr(k), _ptr(du), H, N, r0, r1)
+        if rc:
+            raise ValueError("oracle_input_grad_rows failed")
+
+    _split(run, d2.shape[0], threads)
+    return du.reshape(shape)
+
+
+def kernel_grad(u: np.ndarray, dy: np.ndarray, w_in: Optional[np.ndarray] = None,
+                w_out: Optional[np.ndarray] = None, threads: int = 1) -> np.ndarray:
+    """dk [H, N] = sum_b corr(w_out * dy_b, w_in * u_b) for u, dy [B, H, N]."""
+    u, dy = _f64(u), _f64(dy)
+    B, H, N = u.shape
+    gi = _f64(w_in) if w_in is not None else None
+    go = _f64(w_out) if w_out is not None else None
+    dk = np.zeros((H, N))
+    lib = _load()
+
+    def run(h0: int, h1: int):
+        rc = lib.oracle_kernel_grad_channels(_ptr(u), _ptr(dy), _ptr(gi), _ptr(go), _ptr(dk), B, H, N, h0, h1)
+        if rc:
+            raise ValueError("oracle_kernel_grad_channels failed")
+
+    _split(run, H, threads)
+    return dk
+
+
+def _split(run, n: int, threads: int):
+    if threads <= 1 or n <= 1:
+        run(0, n)
+        return
+    step = (n + threads - 1) // threads
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda r0: run(r0, min(n, r0 + step)), range(0, n, step)))

@@ -194,3 +194,103 @@ int oracle_direct_causal_conv(const double *u, const double *k, double *y, int64
     for (int64_t t = 0; t < N; ++t) y[t] = oracle_direct_causal_conv_at(u, k, N, t);
     return 0;
 }
+
+/*
+ * Backward pass (FlashFFTConv page, section 3.4 "Kernel Fusion and
+ * Recomputation Strategies", recomputation in the backward pass: gradients
+ * of the convolution output with respect to the input u and the kernel k).
+ * For y[t] = sum_{j<=t} u[j] k[t-j] and an output gradient dy:
+ *   du[j] = sum_{t=j}^{N-1} dy[t] k[t-j]            (correlation of dy with k)
+ *   dk[i] = sum_b sum_{t=i}^{N-1} dy_b[t] u_b[t-i]   (correlation of dy with u, summed over the batch)
+ * Through the DFT: with zero padding to 2N, sum_t a[t] b[t-i] is the first
+ * N outputs of IDFT_{2N}(DFT(a0) . conj(DFT(b0))), because the padded b is
+ * zero at the indices t - i + 2N >= N that the circular form adds.
+ */
+int oracle_causal_corr(const double *a, const double *b, double *out, int64_t N)
+{
+    if (!is_pow2(N)) return -1;
+    int64_t L = 2 * N;
+    double *ar = calloc((size_t)L, sizeof(double)), *ai = calloc((size_t)L, sizeof(double));
+    double *br = calloc((size_t)L, sizeof(double)), *bi = calloc((size_t)L, sizeof(double));
+    if (!ar || !ai || !br || !bi) { free(ar); free(ai); free(br); free(bi); return -1; }
+    memcpy(ar, a, (size_t)N * sizeof(double));
+    memcpy(br, b, (size_t)N * sizeof(double));
+    oracle_fft(ar, ai, L, -1);
+    oracle_fft(br, bi, L, -1);
+    for (int64_t i = 0; i < L; ++i) {  /* A . conj(B) */
+        double pr = ar[i] * br[i] + ai[i] * bi[i];
+        double pi = ai[i] * br[i] - ar[i] * bi[i];
+        ar[i] = pr; ai[i] = pi;
+    }
+    oracle_fft(ar, ai, L, 1);
+    memcpy(out, ar, (size_t)N * sizeof(double));
+    free(ar); free(ai); free(br); free(bi);
+    return 0;
+}
+
+/* One correlation output sum_{t=i}^{N-1} a[t] b[t-i] by the definition (compensated sum). */
+double oracle_direct_causal_corr_at(const double *a, const double *b, int64_t N, int64_t i)
+{
+    if (i < 0 || i >= N) return NAN;
+    double s = 0.0, c = 0.0;
+    for (int64_t t = i; t < N; ++t) {
+        double v = a[t] * b[t - i];
+        double nt = s + v;
+        if (fabs(s) >= fabs(v)) c += (s - nt) + v;
+        else c += (v - nt) + s;
+        s = nt;
+    }
+    return s + c;
+}
+
+/*
+ * Input gradient of rows [row_begin, row_end) of a [rows][N] batch (row r =
+ * b*H + h uses k[h]).  Gated (y = w_out . conv(u . w_in, k)):
+ * du = w_in . corr(w_out . dy, k); w_in / w_out NULL for the plain form.
+ */
+int oracle_input_grad_rows(const double *dy, const double *w_in, const double *w_out,
+                           const double *k, double *du, int64_t H, int64_t N,
+                           int64_t row_begin, int64_t row_end)
+{
+    double *g = malloc((size_t)N * sizeof(double));
+    if (!g) return -1;
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        int64_t h = r % H;
+        for (int64_t t = 0; t < N; ++t) g[t] = w_out ? dy[r * N + t] * w_out[r * N + t] : dy[r * N + t];
+        int rc = oracle_causal_corr(g, k + h * N, du + r * N, N);
+        if (rc) { free(g); return rc; }
+        if (w_in)
+            for (int64_t t = 0; t < N; ++t) du[r * N + t] *= w_in[r * N + t];
+    }
+    free(g);
+    return 0;
+}
+
+/*
+ * Kernel gradient of channels [h_begin, h_end): dk[h] = sum_b corr(g_b, x_b)
+ * with g = w_out . dy and x = u . w_in (plain form: g = dy, x = u).  u, dy,
+ * w_in, w_out are [B][H][N]; dk is [H][N].
+ */
+int oracle_kernel_grad_channels(const double *u, const double *dy, const double *w_in,
+                                const double *w_out, double *dk, int64_t B, int64_t H,
+                                int64_t N, int64_t h_begin, int64_t h_end)
+{
+    double *g = malloc((size_t)N * sizeof(double)), *x = malloc((size_t)N * sizeof(double));
+    double *c = malloc((size_t)N * sizeof(double));
+    if (!g || !x || !c) { free(g); free(x); free(c); return -1; }
+    for (int64_t h = h_begin; h < h_end; ++h) {
+        for (int64_t i = 0; i < N; ++i) dk[h * N + i] = 0.0;
+        for (int64_t b = 0; b < B; ++b) {
+            int64_t r = b * H + h;
+            for (int64_t t = 0; t < N; ++t) {
+                g[t] = w_out ? dy[r * N + t] * w_out[r * N + t] : dy[r * N + t];
+                x[t] = w_in ? u[r * N + t] * w_in[r * N + t] : u[r * N + t];
+            }
+            int rc = oracle_causal_corr(g, x, c, N);
+            if (rc) { free(g); free(x); free(c); return rc; }
+            for (int64_t i = 0; i < N; ++i) dk[h * N + i] += c[i];
+        }
+    }
+    free(g); free(x); free(c);
+    return 0;
+}
