@@ -209,20 +209,20 @@ int oracle_direct_causal_conv(const double *u, const double *k, double *y, int64
 int oracle_causal_corr(const double *a, const double *b, double *out, int64_t N)
 {
     if (!is_pow2(N)) return -1;
-    int64_t L = 2 * N;
-    double *ar = calloc((size_t)L, sizeof(double)), *ai = calloc((size_t)L, sizeof(double));
-    double *br = calloc((size_t)L, sizeof(double)), *bi = calloc((size_t)L, sizeof(double));
+    const int64_t L2 = 2 * N;
+    double *ar = calloc((size_t)L2, sizeof(double)), *ai = calloc((size_t)L2, sizeof(double));
+    double *br = calloc((size_t)L2, sizeof(double)), *bi = calloc((size_t)L2, sizeof(double));
     if (!ar || !ai || !br || !bi) { free(ar); free(ai); free(br); free(bi); return -1; }
     memcpy(ar, a, (size_t)N * sizeof(double));
     memcpy(br, b, (size_t)N * sizeof(double));
-    oracle_fft(ar, ai, L, -1);
-    oracle_fft(br, bi, L, -1);
-    for (int64_t i = 0; i < L; ++i) {  /* A . conj(B) */
+    oracle_fft(ar, ai, L2, -1);
+    oracle_fft(br, bi, L2, -1);
+    for (int64_t i = 0; i < L2; ++i) {  /* A . conj(B) */
         double pr = ar[i] * br[i] + ai[i] * bi[i];
         double pi = ai[i] * br[i] - ar[i] * bi[i];
         ar[i] = pr; ai[i] = pi;
     }
-    oracle_fft(ar, ai, L, 1);
+    oracle_fft(ar, ai, L2, 1);
     memcpy(out, ar, (size_t)N * sizeof(double));
     free(ar); free(ai); free(br); free(bi);
     return 0;

@@ -87,3 +87,66 @@ def test_direct_conv_and_corr_are_mutual_adjoints_brute_force():
     N = 16
     u, k, dy = rng.standard_normal(N), rng.standard_normal(N), rng.standard_normal(N)
     assert abs(np.dot(_direct_conv(u, k), dy) - np.dot(u, _direct_corr(dy, k))) < 1e-12
+
+
+BACKWARD_MUTANTS = {
+    "correlation without the conjugate": ("double pi = ai[i] * br[i] - ar[i] * bi[i];",
+                                          "double pi = ai[i] * br[i] + ar[i] * bi[i];"),
+    "correlation without zero padding": ("const int64_t L2 = 2 * N;", "const int64_t L2 = N;"),
+    "input gradient gate swapped": ("g[t] = w_out ? dy[r * N + t] * w_out[r * N + t] : dy[r * N + t];\n        int rc",
+                                    "g[t] = w_out ? dy[r * N + t] * w_in[r * N + t] : dy[r * N + t];\n        int rc"),
+    "kernel gradient misses a batch row": ("for (int64_t b = 0; b < B; ++b) {", "for (int64_t b = 1; b < B; ++b) {"),
+    "direct sum starts one late": ("for (int64_t t = i; t < N; ++t) {", "for (int64_t t = i + 1; t < N; ++t) {"),
+}
+
+
+def _backward_pins_pass(lib) -> bool:
+    import ctypes
+    P = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    lib.oracle_direct_causal_corr_at.restype = ctypes.c_double
+    rng = np.random.default_rng(0)
+    ok = True
+    B, H, N = 3, 2, 32
+    u, dy = rng.standard_normal((B, H, N)), rng.standard_normal((B, H, N))
+    wi, wo = rng.standard_normal((B, H, N)), rng.standard_normal((B, H, N))
+    k = rng.standard_normal((H, N))
+    for gated in (False, True):
+        gi, go = (wi, wo) if gated else (None, None)
+        du = np.zeros((B * H, N))
+        lib.oracle_input_grad_rows(P(dy), P(gi) if gated else None, P(go) if gated else None, P(k), P(du),
+                                   ctypes.c_int64(H), ctypes.c_int64(N), ctypes.c_int64(0), ctypes.c_int64(B * H))
+        dk = np.zeros((H, N))
+        lib.oracle_kernel_grad_channels(P(u), P(dy), P(gi) if gated else None, P(go) if gated else None, P(dk),
+                                        ctypes.c_int64(B), ctypes.c_int64(H), ctypes.c_int64(N), ctypes.c_int64(0),
+                                        ctypes.c_int64(H))
+        g = dy * wo if gated else dy
+        x = u * wi if gated else u
+        for b in range(B):
+            for h in range(H):
+                ref = _direct_corr(g[b, h], k[h]) * (wi[b, h] if gated else 1.0)
+                ok &= np.allclose(du[b * H + h], ref, atol=1e-10)
+        for h in range(H):
+            ref = sum(_direct_corr(g[b, h], x[b, h]) for b in range(B))
+            ok &= np.allclose(dk[h], ref, atol=1e-10)
+    a, c = rng.standard_normal(N), rng.standard_normal(N)
+    ref = _direct_corr(a, c)
+    for i in range(N):
+        ok &= abs(lib.oracle_direct_causal_corr_at(P(a), P(c), ctypes.c_int64(N), ctypes.c_int64(i)) - ref[i]) < 1e-10
+    return bool(ok)
+
+
+def test_backward_pins_catch_planted_mistakes(tmp_path):
+    import ctypes
+    import os
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "fftconv_oracle.c")).read()
+    base = tmp_path / "base.c"
+    base.write_text(src)
+    subprocess.check_call(["gcc", "-O1", "-fPIC", "-shared", str(base), "-o", str(base) + ".so", "-lm"])
+    assert _backward_pins_pass(ctypes.CDLL(str(base) + ".so"))
+    for name, (old, new) in BACKWARD_MUTANTS.items():
+        assert src.count(old) == 1, name
+        path = tmp_path / f"m_{abs(hash(name))}.c"
+        path.write_text(src.replace(old, new))
+        subprocess.check_call(["gcc", "-O1", "-fPIC", "-shared", str(path), "-o", str(path) + ".so", "-lm"])
+        assert not _backward_pins_pass(ctypes.CDLL(str(path) + ".so")), f"planted mistake not caught: {name}"
