@@ -20,7 +20,9 @@ STATUS = {0: "OK", 1: "ERR_INVALID", 2: "ERR_UNSUPPORTED", 3: "ERR_ALIGN", 4: "E
 EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy", "fftconv_plan_get_info",
             "fftconv_kf_bytes", "fftconv_workspace_bytes", "fftconv_set_workspace", "fftconv_kernel_fft",
             "fftconv_forward", "fftconv_forward_gated", "fftconv_forward_noalloc", "fftconv_host_scratch_bytes",
-            "fftconv_forward_host", "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
+            "fftconv_forward_host", "fftconv_kernel_fft_adjoint", "fftconv_backward_du",
+            "fftconv_backward_du_gated", "fftconv_backward_dk_scratch_bytes", "fftconv_backward_dk",
+            "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
 
 
 class FFTConvError(RuntimeError):
@@ -70,6 +72,12 @@ def lib(auto_build: bool = True):
         L.fftconv_host_scratch_bytes.argtypes = [vp, i64, i64, ctypes.c_int]
         L.fftconv_host_scratch_bytes.restype = sz
         L.fftconv_forward_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp, sz, vp]
+        L.fftconv_kernel_fft_adjoint.argtypes = [vp, vp, vp, i64, vp]
+        L.fftconv_backward_du.argtypes = [vp, vp, vp, vp, i64, i64, vp]
+        L.fftconv_backward_du_gated.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp]
+        L.fftconv_backward_dk_scratch_bytes.argtypes = [vp, i64, i64]
+        L.fftconv_backward_dk_scratch_bytes.restype = sz
+        L.fftconv_backward_dk.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp, sz, vp]
         L.fftconv_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         L.fftconv_status_string.argtypes = [ctypes.c_int]
         L.fftconv_status_string.restype = ctypes.c_char_p
@@ -208,6 +216,47 @@ class Plan:
         _check(lib().fftconv_forward_host(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y), B, H,
                                           _ptr(self._host_scratch), n, _stream(stream)), "fftconv_forward_host")
         return y
+
+    # ---- backward (gradients in u and k)
+
+    def kernel_fft_adjoint(self, k, k_f=None, stream=None):
+        """k: float32 [H, N] -> opaque adjoint k_f (correlation with k)."""
+        import torch
+        H = k.shape[0]
+        if k.dtype != torch.float32 or not k.is_contiguous() or k.shape[-1] != self.N:
+            raise ValueError("k must be contiguous float32 [H, N]")
+        if k_f is None:
+            k_f = torch.empty(self.kf_bytes(H), dtype=torch.uint8, device=k.device)
+        _check(lib().fftconv_kernel_fft_adjoint(self._h, _ptr(k), _ptr(k_f), H, _stream(stream)),
+               "fftconv_kernel_fft_adjoint")
+        return k_f
+
+    def backward_du(self, dy, k_f_adj, w_in=None, w_out=None, du=None, stream=None):
+        """du = corr(dy, k) (gated: w_in * corr(w_out * dy, k))."""
+        import torch
+        B, H, N = dy.shape
+        if du is None:
+            du = torch.empty_like(dy)
+        self._ensure_workspace(B, H, dy.device)
+        if w_in is None:
+            st = lib().fftconv_backward_du(self._h, _ptr(dy), _ptr(k_f_adj), _ptr(du), B, H, _stream(stream))
+        else:
+            st = lib().fftconv_backward_du_gated(self._h, _ptr(dy), _ptr(w_in), _ptr(w_out), _ptr(k_f_adj),
+                                                 _ptr(du), B, H, _stream(stream))
+        _check(st, "fftconv_backward_du")
+        return du
+
+    def backward_dk(self, u, dy, w_in=None, w_out=None, dk=None, stream=None):
+        """dk [H, N] float32 = sum_b corr(w_out * dy_b, w_in * u_b)."""
+        import torch
+        B, H, N = u.shape
+        if dk is None:
+            dk = torch.empty(H, N, dtype=torch.float32, device=u.device)
+        need = int(lib().fftconv_backward_dk_scratch_bytes(self._h, B, H))
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=u.device)
+        _check(lib().fftconv_backward_dk(self._h, _ptr(u), _ptr(dy), _ptr(w_in), _ptr(w_out), _ptr(dk), B, H,
+                                         _ptr(scratch), need, _stream(stream)), "fftconv_backward_dk")
+        return dk
 
     def device_status(self, stream=None) -> int:
         v = ctypes.c_int()

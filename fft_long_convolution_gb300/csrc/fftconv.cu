@@ -693,8 +693,33 @@ int grid_for(int64_t work) {
 
 }  // namespace
 
+namespace {
+
+// conj of every spectrum value (the adjoint k_f: correlation instead of convolution)
+__global__ void kfft_conj(float2* __restrict__ x, int64_t n) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
+        x[i].y = -x[i].y;
+}
+
+fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f, int64_t H,
+                                 fftconv_stream_t stream, bool adjoint);
+
+}  // namespace
+
 extern "C" fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float* k, void* k_f, int64_t H,
                                                fftconv_stream_t stream) {
+    return kernel_fft_impl(plan, k, k_f, H, stream, false);
+}
+
+extern "C" fftconv_status_t fftconv_kernel_fft_adjoint(fftconv_plan_t plan, const float* k, void* k_f, int64_t H,
+                                                       fftconv_stream_t stream) {
+    return kernel_fft_impl(plan, k, k_f, H, stream, true);
+}
+
+namespace {
+
+fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f, int64_t H,
+                                 fftconv_stream_t stream, bool adjoint) {
     if (!plan || H < 0) return FFTCONV_ERR_INVALID;
     if (H == 0) return FFTCONV_OK;
     if (!k || !k_f) return FFTCONV_ERR_INVALID;
@@ -717,6 +742,7 @@ extern "C" fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float*
         a = b;
         b = tmp;
     }
+    if (adjoint) kfft_conj<<<grid_for(H * L), 256, 0, st>>>(a, H * L);
     if (plan->tc64)
         kfft_finalize_tc64<<<grid_for(H * 9 * 4 * 2 * 32), 256, 0, st>>>(a, static_cast<uint4*>(k_f), H,
                                                                            plan->info.dtype);
@@ -730,6 +756,8 @@ extern "C" fftconv_status_t fftconv_kernel_fft(fftconv_plan_t plan, const float*
     cudaFreeAsync(buf, st);
     return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
 }
+
+}  // namespace
 
 // --------------------------------------------------------------- forward
 
@@ -789,6 +817,135 @@ extern "C" fftconv_status_t fftconv_device_status(fftconv_plan_t plan, fftconv_s
     }
     *out = v;
     return FFTCONV_OK;
+}
+
+// --------------------------------------------------------------- backward
+//
+// Gradients of the convolution (FlashFFTConv page, section 3.4, "Kernel
+// Fusion and Recomputation Strategies": the backward pass recomputes the
+// transforms instead of storing them).  For y = conv(u, k) and the output
+// gradient dy: du[j] = sum_{t>=j} dy[t] k[t-j] is the causal convolution
+// machinery run with conj(rfft(k, 2N)) (fftconv_kernel_fft_adjoint); dk[h] =
+// sum_b sum_{t>=i} dy_b[t] u_b[t-i] is the batch sum of the cross spectra
+// DY_b conj(U_b), transformed back.
+
+extern "C" fftconv_status_t fftconv_backward_du(fftconv_plan_t plan, const void* dy, const void* k_f_adj, void* du,
+                                                int64_t B, int64_t H, fftconv_stream_t stream) {
+    return forward_impl(plan, dy, nullptr, nullptr, k_f_adj, du, B, H, stream, false);
+}
+
+extern "C" fftconv_status_t fftconv_backward_du_gated(fftconv_plan_t plan, const void* dy, const void* w_in,
+                                                      const void* w_out, const void* k_f_adj, void* du, int64_t B,
+                                                      int64_t H, fftconv_stream_t stream) {
+    // du = w_in * corr(w_out * dy, k): the gated kernels with the gates swapped
+    return forward_impl(plan, dy, w_out, w_in, k_f_adj, du, B, H, stream, true);
+}
+
+namespace {
+
+// z[r][n] = g[n] + i x[n] (n < N), 0 above: g = dy (* w_out), x = u (* w_in)
+template <int DT>
+__global__ void dk_pack(const uint16_t* __restrict__ u, const uint16_t* __restrict__ dy,
+                        const uint16_t* __restrict__ w_in, const uint16_t* __restrict__ w_out,
+                        float2* __restrict__ z, int64_t rows, int64_t N) {
+    using O = Op<DT>;
+    const int64_t L = 2 * N;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows * L;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r = i / L, n = i - r * L;
+        float g = 0.f, x = 0.f;
+        if (n < N) {
+            const int64_t j = r * N + n;
+            g = O::unpack(uint32_t(dy[j])).r;
+            x = O::unpack(uint32_t(u[j])).r;
+            if (w_out) g *= O::unpack(uint32_t(w_out[j])).r;
+            if (w_in) x *= O::unpack(uint32_t(w_in[j])).r;
+        }
+        z[i] = make_float2(g, x);
+    }
+}
+
+// P~[h][f] = conj(sum_b G_b[f] conj X_b[f]) with G = (Z[f] + conj Z[-f]) / 2 and
+// X = (Z[f] - conj Z[-f]) / (2i), the spectra of the real rows g and x packed
+// as Z = DFT(g + i x); the conjugate lets a forward DFT compute the inverse.
+__global__ void dk_reduce(const float2* __restrict__ Z, float2* __restrict__ P, int64_t B, int64_t H, int64_t L) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * L;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = i / L, f = i - h * L, fm = (L - f) & (L - 1);
+        float pr = 0.f, pi = 0.f;
+        for (int64_t b = 0; b < B; ++b) {
+            const float2* Zr = Z + (b * H + h) * L;
+            const float2 a = Zr[f], c = Zr[fm];  // Z[f], Z[-f]
+            const float gr = 0.5f * (a.x + c.x), gi = 0.5f * (a.y - c.y);     // G = (Z[f] + conj Z[-f]) / 2
+            const float xr = 0.5f * (a.y + c.y), xi = -0.5f * (a.x - c.x);    // X = (Z[f] - conj Z[-f]) / (2i)
+            pr += gr * xr + gi * xi;  // G conj X
+            pi += gi * xr - gr * xi;
+        }
+        P[i] = make_float2(pr, -pi);
+    }
+}
+
+// dk[h][n] = Re(DFT(conj P)[n]) / L = Re(IDFT(P)[n]), n < N
+__global__ void dk_extract(const float2* __restrict__ Y, float* __restrict__ dk, int64_t H, int64_t N) {
+    const int64_t L = 2 * N;
+    const float s = 1.f / float(L);
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * N;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = i / N, n = i - h * N;
+        dk[i] = Y[h * L + n].x * s;
+    }
+}
+
+}  // namespace
+
+extern "C" size_t fftconv_backward_dk_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H) {
+    if (!plan || B <= 0 || H <= 0) return 0;
+    return 2 * size_t(B) * size_t(H) * size_t(2 * plan->info.N) * sizeof(float2);
+}
+
+extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void* u, const void* dy, const void* w_in,
+                                                const void* w_out, float* dk, int64_t B, int64_t H, void* scratch,
+                                                size_t scratch_bytes, fftconv_stream_t stream) {
+    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (H == 0) return FFTCONV_OK;
+    if (!dk || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
+    const int64_t N = plan->info.N, L = 2 * N;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (misaligned(dk)) return FFTCONV_ERR_ALIGN;
+    if (B == 0) {  // no rows: the gradient is zero
+        return cudaMemsetAsync(dk, 0, size_t(H) * size_t(N) * 4, st) == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+    }
+    if (!u || !dy) return FFTCONV_ERR_INVALID;
+    if (misaligned(u) || misaligned(dy) || (w_in && (misaligned(w_in) || misaligned(w_out)))) return FFTCONV_ERR_ALIGN;
+    const size_t nb = size_t(B) * size_t(H) * size_t(N) * 2, kb = size_t(H) * size_t(N) * 4;
+    if (overlap(dk, kb, u, nb) || overlap(dk, kb, dy, nb) || (w_in && (overlap(dk, kb, w_in, nb) || overlap(dk, kb, w_out, nb))))
+        return FFTCONV_ERR_INVALID;
+    const size_t need = fftconv_backward_dk_scratch_bytes(plan, B, H);
+    if (!scratch || scratch_bytes < need) return FFTCONV_ERR_WORKSPACE;
+    if (misaligned(scratch)) return FFTCONV_ERR_ALIGN;
+    const int64_t rows = B * H;
+    float2* a = static_cast<float2*>(scratch);
+    float2* b = a + rows * L;
+    if (plan->info.dtype == FFTCONV_F16)
+        dk_pack<0><<<grid_for(rows * L), 256, 0, st>>>(static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy),
+                                                       static_cast<const uint16_t*>(w_in),
+                                                       static_cast<const uint16_t*>(w_out), a, rows, N);
+    else
+        dk_pack<1><<<grid_for(rows * L), 256, 0, st>>>(static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy),
+                                                       static_cast<const uint16_t*>(w_in),
+                                                       static_cast<const uint16_t*>(w_out), a, rows, N);
+    for (int64_t p = 1; p < L; p *= 2) {  // Z = DFT(g + i x) of every row
+        kfft_pass<<<grid_for(rows * L / 2), 256, 0, st>>>(a, b, rows, L, p);
+        std::swap(a, b);
+    }
+    dk_reduce<<<grid_for(H * L), 256, 0, st>>>(a, b, B, H, L);
+    std::swap(a, b);
+    for (int64_t p = 1; p < L; p *= 2) {  // DFT of conj P per channel
+        kfft_pass<<<grid_for(H * L / 2), 256, 0, st>>>(a, b, H, L, p);
+        std::swap(a, b);
+    }
+    dk_extract<<<grid_for(H * N), 256, 0, st>>>(a, dk, H, N);
+    return cudaGetLastError() == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
 }
 
 extern "C" const char* fftconv_status_string(fftconv_status_t s) {

@@ -232,6 +232,44 @@ fftconv_status_t fftconv_forward_host(fftconv_plan_t plan, const void *u, const 
                                       fftconv_stream_t stream);
 
 /*
+ * Backward pass (FlashFFTConv page, section 3.4, "Kernel Fusion and
+ * Recomputation Strategies": the gradients with respect to u and k, with the
+ * transforms recomputed rather than stored).  For y = conv(u, k) (causal, as
+ * fftconv_forward) and an output gradient dy [B][H][N] in the plan dtype:
+ *   du[b,h,j] = sum_{t=j}^{N-1} dy[b,h,t] k[h,t-j]              (correlation with k)
+ *   dk[h,i]   = sum_b sum_{t=i}^{N-1} dy[b,h,t] u[b,h,t-i]       (batch sum of correlations with u)
+ * and for the gated form y = w_out . conv(u . w_in, k):
+ *   du = w_in . corr(w_out . dy, k),  dk[h] = sum_b corr(w_out . dy, u . w_in)
+ * (the gate gradients, dw_in = u . corr(w_out . dy, k) and
+ * dw_out = dy . conv(u . w_in, k), follow from du-style and forward calls).
+ *
+ * fftconv_kernel_fft_adjoint: as fftconv_kernel_fft, for conj(rfft(k, 2N));
+ *   a forward call with this k_f computes the correlation with k.
+ * fftconv_backward_du(_gated): du through the forward kernels with the
+ *   adjoint k_f (the gated form swaps the gates); arguments, layouts,
+ *   workspace and errors as fftconv_forward(_gated).
+ * fftconv_backward_dk: dk float32 [H][N] on the device; w_in / w_out both
+ *   NULL or both given; scratch: device memory of at least
+ *   fftconv_backward_dk_scratch_bytes(plan, B, H) bytes (16-byte aligned), the
+ *   float32 spectra of all rows (two buffers of B*H*2N complex).  Computed in
+ *   float32: one radix-2 transform of g + i x per row (g = w_out . dy,
+ *   x = u . w_in), the per-channel sum over b of the cross spectra, one
+ *   inverse transform per channel.  B = 0 writes zeros.  Returns OK, INVALID,
+ *   ALIGN, WORKSPACE or CUDA.
+ */
+fftconv_status_t fftconv_kernel_fft_adjoint(fftconv_plan_t plan, const float *k, void *k_f, int64_t H,
+                                            fftconv_stream_t stream);
+fftconv_status_t fftconv_backward_du(fftconv_plan_t plan, const void *dy, const void *k_f_adj, void *du,
+                                     int64_t B, int64_t H, fftconv_stream_t stream);
+fftconv_status_t fftconv_backward_du_gated(fftconv_plan_t plan, const void *dy, const void *w_in,
+                                           const void *w_out, const void *k_f_adj, void *du, int64_t B,
+                                           int64_t H, fftconv_stream_t stream);
+size_t fftconv_backward_dk_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H);
+fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void *u, const void *dy, const void *w_in,
+                                     const void *w_out, float *dk, int64_t B, int64_t H, void *scratch,
+                                     size_t scratch_bytes, fftconv_stream_t stream);
+
+/*
  * Read and clear the plan's device error word (waits for `stream`).
  * *out = 0 if no bounded on-device wait has given up since the last call,
  * else FFTCONV_ERR_TIMEOUT.  Returns OK, INVALID or CUDA.
