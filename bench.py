@@ -17,6 +17,7 @@ the host cores over a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -243,6 +244,87 @@ def config_of(w: W.Workload) -> dict:
             else "L2 flushed between steps"}
 
 
+def run_backward(args, w: W.Workload):
+    """One step = the input gradient (through the forward kernels with the
+    adjoint spectrum) and the kernel gradient (float32 spectral path) of the
+    workload, inputs and output gradient resident on the device."""
+    import torch
+    import fft_long_convolution_gb300 as F
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    F.build_library()
+    ins = W.make_inputs(w, seed=rank)
+    dy_in = W.make_inputs(dataclasses.replace(w, gated=False), seed=rank + 1000)["u"]  # the output gradient
+    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+
+    def dev_t(r):
+        if r.dtype == "fp32":
+            return torch.from_numpy(r.bits).to(dev)
+        return torch.from_numpy(r.bits.view(np.int16)).view(tdt).to(dev)
+
+    plan = F.Plan(w.N, tdt)
+    kfa = plan.kernel_fft_adjoint(dev_t(ins["k"]))
+    u, dy = dev_t(ins["u"]), dev_t(dy_in)
+    wi = dev_t(ins["w_in"]) if w.gated else None
+    wo = dev_t(ins["w_out"]) if w.gated else None
+    du = torch.empty_like(u)
+    dk = torch.empty(w.H, w.N, dtype=torch.float32, device=dev)
+    L = F.lib()
+    need = int(L.fftconv_backward_dk_scratch_bytes(plan._h, w.B, w.H))
+    scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.backward_du(dy, kfa, wi, wo, du=du, stream=stream)
+        F._check(L.fftconv_backward_dk(plan._h, u.data_ptr(), dy.data_ptr(), F._ptr(wi), F._ptr(wo), dk.data_ptr(),
+                                       w.B, w.H, scratch.data_ptr(), need, stream.cuda_stream), "fftconv_backward_dk")
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(1, min(args.steps, 50))
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / steps
+    assert plan.device_status() == 0
+    t = torch.tensor([ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    if rank == 0:
+        peaks = measured_peaks()
+        s = 2
+        rows = w.rows
+        nbytes = rows * w.N * s * (3 + (2 if w.gated else 0)) + w.H * w.N * 4 + w.H * (w.N + 1) * 4
+        lg = int(np.log2(2 * w.N))
+        launches = path_of(plan.info)["launches_per_step"] + 1 + lg + 1 + lg + 1
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        out = {"metric": METRIC + " (backward: du + dk)", "value": world * w.outputs / (ms * 1e-3),
+               "unit": "outputs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
+               "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": {"fp16": "f16", "bf16": "bf16"}[w.dtype], "data": "synthetic",
+               "config": config_of(w),
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                            "algorithmic_bytes_per_launch": nbytes,
+                            "kernel": "du: " + path_of(plan.info)["kernel"] + "; dk: dk_pack + kfft_pass + "
+                                      "dk_reduce + kfft_pass + dk_extract"},
+               "gpu_launches": steps * launches, "clocks": clk}
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -251,10 +333,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                    help="backward: input and kernel gradients (du + dk) per step")
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if args.which == "backward":
+        run_backward(args, w)
         return
 
     import torch

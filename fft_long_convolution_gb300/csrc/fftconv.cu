@@ -512,29 +512,87 @@ namespace {
 
 __global__ void kfft_init(const float* __restrict__ k, float2* __restrict__ buf, int64_t H, int64_t N) {
     const int64_t L = 2 * N;
+    int lgL = 0;
+    while ((int64_t(1) << lgL) < L) ++lgL;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * L;
          i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t h = i / L, n = i - h * L;
+        const int64_t h = i >> lgL, n = i & (L - 1);
         buf[i] = make_float2(n < N ? k[h * N + n] : 0.f, 0.f);
     }
 }
 
-// One radix-2 Stockham pass (self-sorting, out of place) of a length-L DFT
-// with exponent sign -1, for every channel.
-__global__ void kfft_pass(const float2* __restrict__ x, float2* __restrict__ yv, int64_t H, int64_t L,
-                          int64_t p) {
-    const int64_t half = L / 2;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * half;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t h = i / half, r = i - h * half;
-        const int64_t j = r / p, kk = r - j * p;
-        float wi, wr;  // p is a power of two: kk / p is exact in float
-        sincospif(-float(kk) / float(p), &wi, &wr);
-        const float2 c0 = x[h * L + kk + j * p], c1 = x[h * L + kk + j * p + half];
+// Stockham passes (self-sorting, out of place) of length-L DFTs with exponent
+// sign -1, one per row, L = 2^lgL.  A pass of radix R with current span Ns
+// (the product of the radices before it): element j = kk + Ns jj of the
+// R-way split reads x[j + r L/R] (r < R), multiplies by W_{R Ns}^(kk r), takes
+// the R-point DFT and writes y[kk + R Ns jj + q Ns] (q < R).  Powers of two
+// throughout, so every index is a shift or a mask.
+__global__ void kfft_pass2(const float2* __restrict__ x, float2* __restrict__ yv, int64_t H, int lgL, int lgNs) {
+    const int64_t L = int64_t(1) << lgL, n = H << (lgL - 1);
+    const int64_t Ns = int64_t(1) << lgNs;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = i >> (lgL - 1), j = i & ((L >> 1) - 1);
+        const int64_t kk = j & (Ns - 1), jj = j >> lgNs;
+        float wi, wr;  // kk / Ns is exact in float
+        sincospif(-float(kk) / float(Ns), &wi, &wr);
+        const float2* xr = x + (h << lgL);
+        const float2 c0 = xr[j], c1 = xr[j + (L >> 1)];
         const float tr = c1.x * wr - c1.y * wi, ti = c1.x * wi + c1.y * wr;
-        yv[h * L + kk + 2 * j * p] = make_float2(c0.x + tr, c0.y + ti);
-        yv[h * L + kk + 2 * j * p + p] = make_float2(c0.x - tr, c0.y - ti);
+        float2* yr = yv + (h << lgL) + kk + (jj << (lgNs + 1));
+        yr[0] = make_float2(c0.x + tr, c0.y + ti);
+        yr[Ns] = make_float2(c0.x - tr, c0.y - ti);
     }
+}
+
+__global__ void kfft_pass4(const float2* __restrict__ x, float2* __restrict__ yv, int64_t H, int lgL, int lgNs) {
+    const int64_t L = int64_t(1) << lgL, Q = L >> 2, n = H << (lgL - 2);
+    const int64_t Ns = int64_t(1) << lgNs;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = i >> (lgL - 2), j = i & (Q - 1);
+        const int64_t kk = j & (Ns - 1), jj = j >> lgNs;
+        const float2* xr = x + (h << lgL);
+        float2 v0 = xr[j], v1 = xr[j + Q], v2 = xr[j + 2 * Q], v3 = xr[j + 3 * Q];
+        float s1, c1;  // W_{4 Ns}^kk; kk / (2 Ns) is exact in float
+        sincospif(-float(kk) / float(2 * Ns), &s1, &c1);
+        const float c2 = c1 * c1 - s1 * s1, s2 = 2.f * c1 * s1;
+        const float c3 = c2 * c1 - s2 * s1, s3 = c2 * s1 + s2 * c1;
+        v1 = make_float2(v1.x * c1 - v1.y * s1, v1.x * s1 + v1.y * c1);
+        v2 = make_float2(v2.x * c2 - v2.y * s2, v2.x * s2 + v2.y * c2);
+        v3 = make_float2(v3.x * c3 - v3.y * s3, v3.x * s3 + v3.y * c3);
+        const float2 a0 = make_float2(v0.x + v2.x, v0.y + v2.y), a1 = make_float2(v0.x - v2.x, v0.y - v2.y);
+        const float2 a2 = make_float2(v1.x + v3.x, v1.y + v3.y);
+        const float2 a3 = make_float2(v1.y - v3.y, v3.x - v1.x);  // -i (v1 - v3)
+        float2* yr = yv + (h << lgL) + kk + (jj << (lgNs + 2));
+        yr[0] = make_float2(a0.x + a2.x, a0.y + a2.y);
+        yr[Ns] = make_float2(a1.x + a3.x, a1.y + a3.y);
+        yr[2 * Ns] = make_float2(a0.x - a2.x, a0.y - a2.y);
+        yr[3 * Ns] = make_float2(a1.x - a3.x, a1.y - a3.y);
+    }
+}
+
+int ilog2(int64_t v) {
+    int l = 0;
+    while ((int64_t(1) << l) < v) ++l;
+    return l;
+}
+
+int grid_for(int64_t work);
+
+// DFT of every row of a [H][L] (L a power of two >= 2), ping-ponging between
+// a and b; returns the buffer that holds the result.
+float2* fft_rows(float2* a, float2* b, int64_t H, int64_t L, cudaStream_t st) {
+    const int lgL = ilog2(L);
+    int lgNs = 0;
+    if (lgL & 1) {
+        kfft_pass2<<<grid_for(H * L / 2), 256, 0, st>>>(a, b, H, lgL, 0);
+        std::swap(a, b);
+        lgNs = 1;
+    }
+    for (; lgNs < lgL; lgNs += 2) {
+        kfft_pass4<<<grid_for(H * L / 4), 256, 0, st>>>(a, b, H, lgL, lgNs);
+        std::swap(a, b);
+    }
+    return a;
 }
 
 __device__ __forceinline__ uint32_t pack_dt(float lo, float hi, int dtype) {
@@ -736,12 +794,7 @@ fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f,
     float2* a = buf;
     float2* b = buf + H * L;
     kfft_init<<<grid_for(H * L), 256, 0, st>>>(k, a, H, N);
-    for (int64_t p = 1; p < L; p *= 2) {
-        kfft_pass<<<grid_for(H * L / 2), 256, 0, st>>>(a, b, H, L, p);
-        float2* tmp = a;
-        a = b;
-        b = tmp;
-    }
+    a = fft_rows(a, b, H, L, st);
     if (adjoint) kfft_conj<<<grid_for(H * L), 256, 0, st>>>(a, H * L);
     if (plan->tc64)
         kfft_finalize_tc64<<<grid_for(H * 9 * 4 * 2 * 32), 256, 0, st>>>(a, static_cast<uint4*>(k_f), H,
@@ -850,9 +903,11 @@ __global__ void dk_pack(const uint16_t* __restrict__ u, const uint16_t* __restri
                         float2* __restrict__ z, int64_t rows, int64_t N) {
     using O = Op<DT>;
     const int64_t L = 2 * N;
+    int lgL = 0;
+    while ((int64_t(1) << lgL) < L) ++lgL;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows * L;
          i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t r = i / L, n = i - r * L;
+        const int64_t r = i >> lgL, n = i & (L - 1);
         float g = 0.f, x = 0.f;
         if (n < N) {
             const int64_t j = r * N + n;
@@ -869,9 +924,11 @@ __global__ void dk_pack(const uint16_t* __restrict__ u, const uint16_t* __restri
 // X = (Z[f] - conj Z[-f]) / (2i), the spectra of the real rows g and x packed
 // as Z = DFT(g + i x); the conjugate lets a forward DFT compute the inverse.
 __global__ void dk_reduce(const float2* __restrict__ Z, float2* __restrict__ P, int64_t B, int64_t H, int64_t L) {
+    int lgL = 0;
+    while ((int64_t(1) << lgL) < L) ++lgL;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * L;
          i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t h = i / L, f = i - h * L, fm = (L - f) & (L - 1);
+        const int64_t h = i >> lgL, f = i & (L - 1), fm = (L - f) & (L - 1);
         float pr = 0.f, pi = 0.f;
         for (int64_t b = 0; b < B; ++b) {
             const float2* Zr = Z + (b * H + h) * L;
@@ -889,9 +946,11 @@ __global__ void dk_reduce(const float2* __restrict__ Z, float2* __restrict__ P, 
 __global__ void dk_extract(const float2* __restrict__ Y, float* __restrict__ dk, int64_t H, int64_t N) {
     const int64_t L = 2 * N;
     const float s = 1.f / float(L);
+    int lgN = 0;
+    while ((int64_t(1) << lgN) < N) ++lgN;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * N;
          i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t h = i / N, n = i - h * N;
+        const int64_t h = i >> lgN, n = i & (N - 1);
         dk[i] = Y[h * L + n].x * s;
     }
 }
@@ -934,16 +993,10 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
         dk_pack<1><<<grid_for(rows * L), 256, 0, st>>>(static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy),
                                                        static_cast<const uint16_t*>(w_in),
                                                        static_cast<const uint16_t*>(w_out), a, rows, N);
-    for (int64_t p = 1; p < L; p *= 2) {  // Z = DFT(g + i x) of every row
-        kfft_pass<<<grid_for(rows * L / 2), 256, 0, st>>>(a, b, rows, L, p);
-        std::swap(a, b);
-    }
-    dk_reduce<<<grid_for(H * L), 256, 0, st>>>(a, b, B, H, L);
-    std::swap(a, b);
-    for (int64_t p = 1; p < L; p *= 2) {  // DFT of conj P per channel
-        kfft_pass<<<grid_for(H * L / 2), 256, 0, st>>>(a, b, H, L, p);
-        std::swap(a, b);
-    }
+    float2* z = fft_rows(a, b, rows, L, st);  // Z = DFT(g + i x) of every row
+    float2* pb = z == a ? b : a;
+    dk_reduce<<<grid_for(H * L), 256, 0, st>>>(z, pb, B, H, L);
+    a = fft_rows(pb, z, H, L, st);  // DFT of conj P per channel
     dk_extract<<<grid_for(H * N), 256, 0, st>>>(a, dk, H, N);
     return cudaGetLastError() == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
 }
