@@ -955,10 +955,115 @@ __global__ void dk_extract(const float2* __restrict__ Y, float* __restrict__ dk,
     }
 }
 
+// The kernel gradient of whole channels for 2N <= 8192, in shared memory: one
+// CTA per channel transforms each batch row g + i x (Stockham radix-4 /
+// radix-2 passes between two shared buffers), adds the row's cross spectrum
+// G conj X to per-thread accumulators (bins f = tid + 512 m), and after the
+// batch transforms conj P once more and writes dk.  Only u, dy (and the gates)
+// are read and dk written.
+constexpr int kDkThreads = 512, kDkMaxL = 8192;
+
+__device__ void smem_fft(float2* a, float2* b, int lgL, float2** out) {
+    const int L = 1 << lgL;
+    int lgNs = 0;
+    if (lgL & 1) {  // radix-2 pass
+        for (int j = threadIdx.x; j < L / 2; j += blockDim.x) {
+            const float2 c0 = a[j], c1 = a[j + L / 2];
+            b[2 * j] = make_float2(c0.x + c1.x, c0.y + c1.y);
+            b[2 * j + 1] = make_float2(c0.x - c1.x, c0.y - c1.y);
+        }
+        __syncthreads();
+        float2* t = a; a = b; b = t;
+        lgNs = 1;
+    }
+    for (; lgNs < lgL; lgNs += 2) {
+        const int Ns = 1 << lgNs, Q = L >> 2;
+        for (int j = threadIdx.x; j < Q; j += blockDim.x) {
+            const int kk = j & (Ns - 1), jj = j >> lgNs;
+            float2 v0 = a[j], v1 = a[j + Q], v2 = a[j + 2 * Q], v3 = a[j + 3 * Q];
+            float s1, c1;
+            sincospif(-float(kk) / float(2 * Ns), &s1, &c1);
+            const float c2 = c1 * c1 - s1 * s1, s2 = 2.f * c1 * s1;
+            const float c3 = c2 * c1 - s2 * s1, s3 = c2 * s1 + s2 * c1;
+            v1 = make_float2(v1.x * c1 - v1.y * s1, v1.x * s1 + v1.y * c1);
+            v2 = make_float2(v2.x * c2 - v2.y * s2, v2.x * s2 + v2.y * c2);
+            v3 = make_float2(v3.x * c3 - v3.y * s3, v3.x * s3 + v3.y * c3);
+            const float2 a0 = make_float2(v0.x + v2.x, v0.y + v2.y), a1 = make_float2(v0.x - v2.x, v0.y - v2.y);
+            const float2 a2 = make_float2(v1.x + v3.x, v1.y + v3.y);
+            const float2 a3 = make_float2(v1.y - v3.y, v3.x - v1.x);
+            float2* y = b + kk + (jj << (lgNs + 2));
+            y[0] = make_float2(a0.x + a2.x, a0.y + a2.y);
+            y[Ns] = make_float2(a1.x + a3.x, a1.y + a3.y);
+            y[2 * Ns] = make_float2(a0.x - a2.x, a0.y - a2.y);
+            y[3 * Ns] = make_float2(a1.x - a3.x, a1.y - a3.y);
+        }
+        __syncthreads();
+        float2* t = a; a = b; b = t;
+    }
+    *out = a;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kDkThreads, 1) dk_channel_smem(const uint16_t* __restrict__ u, const uint16_t* __restrict__ dy,
+                                                                 const uint16_t* __restrict__ w_in,
+                                                                 const uint16_t* __restrict__ w_out,
+                                                                 float* __restrict__ dk, int64_t B, int64_t H, int lgN) {
+    using O = Op<DT>;
+    extern __shared__ __align__(16) float2 sbuf[];
+    const int N = 1 << lgN, L = 2 * N, lgL = lgN + 1;
+    constexpr int PER = kDkMaxL / kDkThreads;  // accumulated bins per thread (at most)
+    for (int64_t h = blockIdx.x; h < H; h += gridDim.x) {
+        float pr[PER], pi[PER];
+        #pragma unroll
+        for (int m = 0; m < PER; ++m) pr[m] = pi[m] = 0.f;
+        for (int64_t b = 0; b < B; ++b) {
+            const int64_t r = b * H + h;
+            for (int n = threadIdx.x; n < L; n += blockDim.x) {
+                float g = 0.f, x = 0.f;
+                if (n < N) {
+                    const int64_t j = r * N + n;
+                    g = O::unpack(uint32_t(dy[j])).r;
+                    x = O::unpack(uint32_t(u[j])).r;
+                    if (w_out) g *= O::unpack(uint32_t(w_out[j])).r;
+                    if (w_in) x *= O::unpack(uint32_t(w_in[j])).r;
+                }
+                sbuf[n] = make_float2(g, x);
+            }
+            __syncthreads();
+            float2* z;
+            smem_fft(sbuf, sbuf + L, lgL, &z);
+            #pragma unroll
+            for (int m = 0; m < PER; ++m) {
+                const int f = threadIdx.x + kDkThreads * m;
+                if (f < L) {
+                    const float2 a = z[f], c = z[(L - f) & (L - 1)];
+                    const float gr = 0.5f * (a.x + c.x), gi = 0.5f * (a.y - c.y);
+                    const float xr = 0.5f * (a.y + c.y), xi = -0.5f * (a.x - c.x);
+                    pr[m] += gr * xr + gi * xi;
+                    pi[m] += gi * xr - gr * xi;
+                }
+            }
+            __syncthreads();  // the buffers are refilled by the next row
+        }
+        #pragma unroll
+        for (int m = 0; m < PER; ++m) {
+            const int f = threadIdx.x + kDkThreads * m;
+            if (f < L) sbuf[f] = make_float2(pr[m], -pi[m]);
+        }
+        __syncthreads();
+        float2* y;
+        smem_fft(sbuf, sbuf + L, lgL, &y);
+        const float sc = 1.f / float(L);
+        for (int n = threadIdx.x; n < N; n += blockDim.x) dk[h * N + n] = y[n].x * sc;
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 extern "C" size_t fftconv_backward_dk_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H) {
     if (!plan || B <= 0 || H <= 0) return 0;
+    if (2 * plan->info.N <= kDkMaxL) return 0;  // whole channels in shared memory
     return 2 * size_t(B) * size_t(H) * size_t(2 * plan->info.N) * sizeof(float2);
 }
 
@@ -980,6 +1085,25 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
     if (overlap(dk, kb, u, nb) || overlap(dk, kb, dy, nb) || (w_in && (overlap(dk, kb, w_in, nb) || overlap(dk, kb, w_out, nb))))
         return FFTCONV_ERR_INVALID;
     const size_t need = fftconv_backward_dk_scratch_bytes(plan, B, H);
+    if (L <= kDkMaxL) {
+        const size_t smem = size_t(2) * L * sizeof(float2);
+        static bool ready[2] = {false, false};
+        auto fn = plan->info.dtype == FFTCONV_F16 ? dk_channel_smem<0> : dk_channel_smem<1>;
+        const int di = plan->info.dtype == FFTCONV_F16 ? 0 : 1;
+        if (!ready[di]) {
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * kDkMaxL * sizeof(float2))) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return FFTCONV_ERR_CUDA;
+            }
+            ready[di] = true;
+        }
+        const int64_t grid = H < 65535 ? H : 65535;
+        fn<<<unsigned(grid), kDkThreads, smem, st>>>(static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy),
+                                                     static_cast<const uint16_t*>(w_in),
+                                                     static_cast<const uint16_t*>(w_out), dk, B, H, ilog2(N));
+        return cudaGetLastError() == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+    }
     if (!scratch || scratch_bytes < need) return FFTCONV_ERR_WORKSPACE;
     if (misaligned(scratch)) return FFTCONV_ERR_ALIGN;
     const int64_t rows = B * H;

@@ -57,8 +57,10 @@ def test_input_grad_matches_oracle(N, dtype, gated, B, H, order):
 
 
 @pytest.mark.parametrize("N,dtype,gated,B,H", [
-    (1024, "fp16", False, 3, 2),
+    (1024, "fp16", False, 3, 2),      # shared-memory channels
     (4096, "bf16", True, 4, 3),
+    (4096, "fp16", False, 1, 5),
+    (8192, "fp16", True, 2, 2),       # spectra through HBM
     (32768, "bf16", False, 2, 2),
 ])
 def test_kernel_grad_matches_oracle(N, dtype, gated, B, H):
@@ -101,8 +103,12 @@ def test_kernel_grad_edge_cases():
     assert L.fftconv_backward_dk(plan._h, None, None, None, None, dk.data_ptr(), 0, 2, None, 0, None) == 0
     torch.cuda.synchronize()
     assert float(dk.abs().max()) == 0.0  # B = 0: zero gradient
-    u = torch.zeros(1, 2, 1024, dtype=torch.float16, device="cuda")
-    need = L.fftconv_backward_dk_scratch_bytes(plan._h, 1, 2)
-    assert need == 2 * 2 * 2048 * 8
-    assert L.fftconv_backward_dk(plan._h, u.data_ptr(), u.data_ptr(), None, None, dk.data_ptr(), 1, 2, None, 0,
+    # 2N <= 8192: whole channels in shared memory, no scratch
+    assert L.fftconv_backward_dk_scratch_bytes(plan._h, 1, 2) == 0
+    big = F.Plan(8192, torch.float16)
+    u = torch.zeros(1, 2, 8192, dtype=torch.float16, device="cuda")
+    dk8 = torch.empty(2, 8192, device="cuda")
+    need = L.fftconv_backward_dk_scratch_bytes(big._h, 1, 2)
+    assert need == 2 * 2 * 16384 * 8
+    assert L.fftconv_backward_dk(big._h, u.data_ptr(), u.data_ptr(), None, None, dk8.data_ptr(), 1, 2, None, 0,
                                  None) == 4
