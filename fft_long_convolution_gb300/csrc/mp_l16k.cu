@@ -13,7 +13,7 @@ cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, 
     cudaError_t e;
     if ((e = prep_kernel(mp_pass_a<DT, R0, G, L>, smem_a, 256, &na)) != cudaSuccess) return e;
     if ((e = prep_kernel(mp_pass_b<DT>, kMpBSmem, 512, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, false>, smem_c, 256, &nc)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, false>, smem_c, 32 * mp_pass_c_warps<R0>(), &nc)) != cudaSuccess) return e;
     const int64_t items_ac = rows * (L / 256), items_b = rows * (R0 / 2);
     auto grid = [&](int64_t items, int per_sm) {
         int64_t gsz = int64_t(p->num_sms) * per_sm;
@@ -21,7 +21,7 @@ cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, 
     };
     mp_pass_a<DT, R0, G, L><<<grid(items_ac, na), 256, smem_a, st>>>(args);
     mp_pass_b<DT><<<grid(items_b, nb), 512, kMpBSmem, st>>>(args);
-    mp_pass_c<DT, R0, G, L, false><<<grid(items_ac, nc), 256, smem_c, st>>>(args);
+    mp_pass_c<DT, R0, G, L, false><<<grid(items_ac, nc), 32 * mp_pass_c_warps<R0>(), smem_c, st>>>(args);
     return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@ cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, 
     cudaError_t e;
     if ((e = prep_kernel(mp_pass_a<DT, R0, G, L>, smem_a, 256, &na)) != cudaSuccess) return e;
     if ((e = prep_kernel(mp_pass_b_tc<DT>, TcB::SMEM, TcB::THREADS, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true>, smem_c, 256, &nc)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true>, smem_c, 32 * mp_pass_c_warps<R0>(), &nc)) != cudaSuccess) return e;
     const int64_t items_ac = rows * (L / 256);
     auto grid = [&](int64_t items, int per_sm) {
         int64_t gsz = int64_t(p->num_sms) * per_sm;
@@ -29,7 +29,7 @@ cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, 
     TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err};
     mp_pass_a<DT, R0, G, L><<<grid(items_ac, na), 256, smem_a, st>>>(args);
     mp_pass_b_tc<DT><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
-    mp_pass_c<DT, R0, G, L, true><<<grid(items_ac, nc), 256, smem_c, st>>>(args);
+    mp_pass_c<DT, R0, G, L, true><<<grid(items_ac, nc), 32 * mp_pass_c_warps<R0>(), smem_c, st>>>(args);
     return cudaGetLastError();
 }
 

@@ -181,11 +181,15 @@ __global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_a(const MPArgs 
 }
 
 // ------------------------------------------------------------------ pass C
+// Warps per CTA: 16 when the staged segments leave room for one CTA per SM.
+template <int R0>
+__host__ __device__ constexpr int mp_pass_c_warps() { return R0 >= 128 ? 16 : 8; }
+
 // TWID: T still lacks the W_M^(n'*k0) twiddle (tensor-core pass B); it is
 // applied here to each element before the contraction, as the chain
 // W_M^(n' t) * W_M^(8 n')^s (and * W_M^(4 n')) for k0 = 8s + t (+ 4).
 template <int DT, int R0, bool GATED, int L, bool TWID>
-__global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_c(const MPArgs a) {
+__global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), R0 <= 64 ? 3 : 1) mp_pass_c(const MPArgs a) {
     using O = Op<DT>;
     constexpr int HALF = R0 / 2, SEG = kSeg;
     constexpr long M = long(R0) * L;
@@ -218,13 +222,13 @@ __global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_c(const MPArgs 
         }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
         // NT column groups of 8 per iteration share each DFT fragment load
-        constexpr int NT = KS <= 8 ? 2 : 1;
+        constexpr int NT = KS <= 8 ? 2 : 1, NW = mp_pass_c_warps<R0>();
         #pragma unroll 1
-        for (int i = 0; i < 4 / NT; ++i) {
+        for (int i = 0; i < 32 / NW / NT; ++i) {
             uint32_t bf[NT][KS][2];
             #pragma unroll
             for (int j = 0; j < NT; ++j) {
-                const int nt = warp + 8 * (NT * i + j);
+                const int nt = warp + NW * (NT * i + j);
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     const int ka = 8 * s + t, kb = 8 * s + 4 + t;
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_c(const MPArgs 
                 if (n0 < HALF) {
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        const int nt = warp + 8 * (NT * i + j);
+                        const int nt = warp + NW * (NT * i + j);
                         const long p = long(L) * n0 + o_base + 8 * nt + 2 * t;  // reals 2p..2p+3
                         float r0 = acc[j][0], i0 = -acc[j][2], r1 = acc[j][1], i1 = -acc[j][3];
                         if (GATED) {
