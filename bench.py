@@ -165,6 +165,23 @@ class ClockSampler:
                 "source": "nvml"}
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (every rank gets it): the step of a weakly
+    scaled job ends when its last replica ends."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(outputs_per_rank: int, world: int, ms_slowest: float) -> float:
+    """Whole-job outputs/s: every rank convolves its own copy of the workload
+    (rows are independent; no collective on the data path)."""
+    return world * outputs_per_rank / (ms_slowest * 1e-3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -297,10 +314,7 @@ def run_backward(args, w: W.Workload):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / steps
     assert plan.device_status() == 0
-    t = torch.tensor([ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     if rank == 0:
         peaks = measured_peaks()
         s = 2
@@ -309,7 +323,7 @@ def run_backward(args, w: W.Workload):
         lg = int(np.log2(2 * w.N))
         launches = path_of(plan.info)["launches_per_step"] + 1 + lg + 1 + lg + 1
         achieved = nbytes / (ms * 1e-3) / 1e9
-        out = {"metric": METRIC + " (backward: du + dk)", "value": world * w.outputs / (ms * 1e-3),
+        out = {"metric": METRIC + " (backward: du + dk)", "value": job_value(w.outputs, world, ms),
                "unit": "outputs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": {"fp16": "f16", "bf16": "bf16"}[w.dtype], "data": "synthetic",
@@ -418,11 +432,8 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     step_ms = sum(kernel_ms) / len(kernel_ms) if flush is not None else total_ms / args.steps
     assert plan.device_status() == 0
-    t = torch.tensor([step_ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    step_ms_max = float(t.item())
-    value = world * w.outputs / (step_ms_max * 1e-3)
+    step_ms_max = max_over_ranks(step_ms, world, dev)
+    value = job_value(w.outputs, world, step_ms_max)
 
     # end to end through the public API with host buffers (pinned)
     hu = torch.from_numpy(ins["u"].bits.view(np.int16)).view(tdt).pin_memory()
@@ -449,10 +460,7 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e_steps
-    te = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = world * w.outputs / (float(te.item()) * 1e-3)
+    e2e_value = job_value(w.outputs, world, max_over_ranks(e2e_ms, world, dev))
 
     if rank == 0:
         peaks = measured_peaks()
