@@ -64,6 +64,9 @@ def _load():
         lib.oracle_direct_causal_corr_at.restype = ctypes.c_double
         lib.oracle_input_grad_rows.argtypes = [_dp, _dp, _dp, _dp, _dp, i64, i64, i64, i64]
         lib.oracle_kernel_grad_channels.argtypes = [_dp, _dp, _dp, _dp, _dp, i64, i64, i64, i64, i64]
+        lib.oracle_partial_conv.argtypes = [_dp, _dp, _dp, i64, i64]
+        lib.oracle_direct_partial_conv_at.argtypes = [_dp, _dp, i64, i64, i64]
+        lib.oracle_direct_partial_conv_at.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -222,3 +225,20 @@ def _split(run, n: int, threads: int):
     step = (n + threads - 1) // threads
     with ThreadPoolExecutor(threads) as ex:
         list(ex.map(lambda r0: run(r0, min(n, r0 + step)), range(0, n, step)))
+
+
+# ---------------------------------------------------------------- partial convolution
+
+def partial_conv(u: np.ndarray, k: np.ndarray, T: int) -> np.ndarray:
+    """One row: y[t] = sum_{t-T < j <= t} u[j] k[t-j] (k cut to T taps)."""
+    u, k = _f64(u), _f64(k)
+    y = np.empty_like(u)
+    if _load().oracle_partial_conv(_ptr(u), _ptr(k), _ptr(y), u.size, int(T)):
+        raise ValueError("N must be a power of two and 1 <= T <= N")
+    return y
+
+
+def direct_partial_conv_at(u: np.ndarray, k: np.ndarray, T: int, t: int) -> float:
+    """One partial-convolution output by the definition, O(T)."""
+    u, k = _f64(u), _f64(k)
+    return float(_load().oracle_direct_partial_conv_at(_ptr(u), _ptr(k), u.size, int(T), int(t)))

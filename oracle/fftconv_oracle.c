@@ -294,3 +294,38 @@ int oracle_kernel_grad_channels(const double *u, const double *dy, const double 
     free(g); free(x); free(c);
     return 0;
 }
+
+/*
+ * Partial convolution (FlashFFTConv page, "Architectural Extensions: Partial
+ * and Frequency-Sparse Convolutions": the kernel is zero beyond its first T
+ * taps, so each output only sees the last T inputs):
+ *   y[t] = sum_{j = max(0, t-T+1)}^{t} u[j] k[t-j],  t = 0..N-1.
+ * Computed as the causal convolution of u with k cut to its first T taps
+ * (N a power of two).
+ */
+int oracle_partial_conv(const double *u, const double *k, double *y, int64_t N, int64_t T)
+{
+    if (T < 1 || T > N) return -1;
+    double *kt = calloc((size_t)N, sizeof(double));
+    if (!kt) return -1;
+    memcpy(kt, k, (size_t)T * sizeof(double));
+    int rc = oracle_causal_conv(u, kt, y, N);
+    free(kt);
+    return rc;
+}
+
+/* One partial-convolution output by the definition (compensated sum), any N. */
+double oracle_direct_partial_conv_at(const double *u, const double *k, int64_t N, int64_t T, int64_t t)
+{
+    if (t < 0 || t >= N || T < 1) return NAN;
+    double s = 0.0, c = 0.0;
+    int64_t j0 = t - T + 1 > 0 ? t - T + 1 : 0;
+    for (int64_t j = j0; j <= t; ++j) {
+        double v = u[j] * k[t - j];
+        double nt = s + v;
+        if (fabs(s) >= fabs(v)) c += (s - nt) + v;
+        else c += (v - nt) + s;
+        s = nt;
+    }
+    return s + c;
+}
