@@ -22,6 +22,7 @@ EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy",
             "fftconv_forward", "fftconv_forward_gated", "fftconv_forward_noalloc", "fftconv_host_scratch_bytes",
             "fftconv_forward_host", "fftconv_kernel_fft_adjoint", "fftconv_backward_du",
             "fftconv_backward_du_gated", "fftconv_backward_dk_scratch_bytes", "fftconv_backward_dk",
+            "fftconv_partial_scratch_bytes", "fftconv_forward_partial",
             "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
 
 
@@ -78,6 +79,9 @@ def lib(auto_build: bool = True):
         L.fftconv_backward_dk_scratch_bytes.argtypes = [vp, i64, i64]
         L.fftconv_backward_dk_scratch_bytes.restype = sz
         L.fftconv_backward_dk.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp, sz, vp]
+        L.fftconv_partial_scratch_bytes.argtypes = [vp, i64, i64, i64, ctypes.c_int]
+        L.fftconv_partial_scratch_bytes.restype = sz
+        L.fftconv_forward_partial.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
         L.fftconv_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         L.fftconv_status_string.argtypes = [ctypes.c_int]
         L.fftconv_status_string.restype = ctypes.c_char_p
@@ -215,6 +219,32 @@ class Plan:
         n = 0 if self._host_scratch is None else self._host_scratch.numel()
         _check(lib().fftconv_forward_host(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y), B, H,
                                           _ptr(self._host_scratch), n, _stream(stream)), "fftconv_forward_host")
+        return y
+
+    # ---- partial convolution (kernels of at most N/2 taps, sequences of any multiple of N/2)
+
+    def kernel_fft_partial(self, k, k_f=None, stream=None):
+        """k: float32 [H, T] with T <= N/2 taps -> k_f for forward_partial."""
+        import torch
+        H, T = k.shape
+        if T > self.N // 2:
+            raise ValueError(f"a partial-convolution kernel has at most {self.N // 2} taps")
+        kp = torch.zeros(H, self.N, dtype=torch.float32, device=k.device)
+        kp[:, :T] = k
+        return self.kernel_fft(kp, k_f=k_f, stream=stream)
+
+    def forward_partial(self, u, k_f, w_in=None, w_out=None, y=None, stream=None):
+        """u: [B, H, N'] with N' a multiple of N/2 -> the causal convolution with
+        the kernel of kernel_fft_partial (gated when w_in, w_out are given)."""
+        import torch
+        B, H, Np = u.shape
+        if y is None:
+            y = torch.empty_like(u)
+        gated = w_in is not None
+        need = int(lib().fftconv_partial_scratch_bytes(self._h, B, H, Np, int(gated)))
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=u.device)
+        _check(lib().fftconv_forward_partial(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y), B, H, Np,
+                                             _ptr(scratch), need, _stream(stream)), "fftconv_forward_partial")
         return y
 
     # ---- backward (gradients in u and k)

@@ -60,6 +60,8 @@ uint32_t pack2(double lo, double hi, int dtype) {
 
 bool is_pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
 
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
 }  // namespace
 
 
@@ -1125,6 +1127,113 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
     return cudaGetLastError() == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
 }
 
+// --------------------------------------------------------------- partial convolution
+//
+// Kernels with at most C = W/2 taps (FlashFFTConv page, "Architectural
+// Extensions: Partial and Frequency-Sparse Convolutions"): the sequence of
+// any length N (a multiple of C) runs as overlapping windows of W = 2C
+// inputs, window w covering inputs [(w-1)C, (w+1)C) (zeros before the
+// start); its causal convolution with the kernel is exact on window
+// positions [C, 2C), i.e. outputs [wC, (w+1)C), which are kept.
+
+namespace {
+
+// windows of one [B][H][N] tensor: out[(b*nwin + w)*H + h][j] = in[b][h][(w-1)C + j] (0 before the start)
+__global__ void partial_gather(const uint4* __restrict__ in, uint4* __restrict__ out, int64_t B, int64_t H,
+                               int64_t N, int64_t C, int64_t nwin) {
+    const int64_t W8 = (2 * C) / 8, C8 = C / 8, N8 = N / 8;  // 16-byte units (8 values)
+    const int64_t total = B * nwin * H * W8;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t j = i % W8, r = i / W8, h = r % H, bw = r / H, w = bw % nwin, b = bw / nwin;
+        const int64_t src = (w - 1) * C8 + j;  // 16-byte unit inside the row
+        out[i] = src >= 0 ? in[(b * H + h) * N8 + src] : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// kept outputs: y[b][h][wC + i] = yw[(b*nwin + w)*H + h][C + i]
+__global__ void partial_scatter(const uint4* __restrict__ yw, uint4* __restrict__ y, int64_t B, int64_t H,
+                                int64_t N, int64_t C, int64_t nwin) {
+    const int64_t W8 = (2 * C) / 8, C8 = C / 8, N8 = N / 8;
+    const int64_t total = B * H * N8;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t n = i % N8, r = i / N8, h = r % H, b = r / H, w = n / C8, c = n - w * C8;
+        y[i] = yw[((b * nwin + w) * H + h) * W8 + C8 + c];
+    }
+}
+
+struct PartialLayout {
+    int64_t C, nwin;
+    size_t buf, ws, total;  // one windowed tensor, the multi-pass intermediate, all
+};
+
+PartialLayout partial_layout(const fftconv_plan_s* p, int64_t B, int64_t H, int64_t N, bool gated) {
+    PartialLayout l{};
+    const int64_t W = p->info.N;
+    l.C = W / 2;
+    l.nwin = N / l.C;
+    const size_t rows = size_t(B) * size_t(l.nwin) * size_t(H);
+    l.buf = align256(rows * size_t(W) * 2);
+    l.ws = p->info.path == FFTCONV_PATH_MULTIPASS ? align256(rows * size_t(W) * 4) : 0;
+    l.total = l.buf * (gated ? 4 : 2) + l.ws;
+    return l;
+}
+
+}  // namespace
+
+extern "C" size_t fftconv_partial_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H, int64_t N, int gated) {
+    if (!plan || B <= 0 || H <= 0 || N <= 0) return 0;
+    const int64_t C = plan->info.N / 2;
+    if (N % C != 0) return 0;
+    return partial_layout(plan, B, H, N, gated != 0).total;
+}
+
+extern "C" fftconv_status_t fftconv_forward_partial(fftconv_plan_t plan, const void* u, const void* w_in,
+                                                    const void* w_out, const void* k_f, void* y, int64_t B,
+                                                    int64_t H, int64_t N, void* scratch, size_t scratch_bytes,
+                                                    fftconv_stream_t stream) {
+    if (!plan || B < 0 || H < 0 || N < 0) return FFTCONV_ERR_INVALID;
+    if (B == 0 || H == 0 || N == 0) return FFTCONV_OK;
+    if (!u || !k_f || !y || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
+    const bool gated = w_in != nullptr;
+    const int64_t C = plan->info.N / 2;
+    if (N % C != 0) return FFTCONV_ERR_UNSUPPORTED;
+    if (misaligned(u) || misaligned(k_f) || misaligned(y) || (gated && (misaligned(w_in) || misaligned(w_out))))
+        return FFTCONV_ERR_ALIGN;
+    const PartialLayout lay = partial_layout(plan, B, H, N, gated);
+    if (B * lay.nwin * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    const size_t nb = size_t(B) * size_t(H) * size_t(N) * 2;
+    if (overlap(y, nb, u, nb) || (gated && (overlap(y, nb, w_in, nb) || overlap(y, nb, w_out, nb))))
+        return FFTCONV_ERR_INVALID;
+    if (!scratch || scratch_bytes < lay.total) return FFTCONV_ERR_WORKSPACE;
+    if (misaligned(scratch)) return FFTCONV_ERR_ALIGN;
+    if (overlap(scratch, lay.total, u, nb) || overlap(scratch, lay.total, y, nb)) return FFTCONV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* sb = static_cast<uint8_t*>(scratch);
+    uint4* uw = reinterpret_cast<uint4*>(sb);
+    uint4* yw = reinterpret_cast<uint4*>(sb + lay.buf);
+    uint4* wiw = gated ? reinterpret_cast<uint4*>(sb + 2 * lay.buf) : nullptr;
+    uint4* wow = gated ? reinterpret_cast<uint4*>(sb + 3 * lay.buf) : nullptr;
+    void* ws = sb + lay.buf * (gated ? 4 : 2);
+    const int64_t Bw = B * lay.nwin, units = Bw * H * (2 * C) / 8;
+    partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(u), uw, B, H, N, C, lay.nwin);
+    if (gated) {
+        partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(w_in), wiw, B, H, N, C, lay.nwin);
+        partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(w_out), wow, B, H, N, C, lay.nwin);
+    }
+    cudaError_t e = plan->info.path == FFTCONV_PATH_MULTIPASS
+                        ? launch_multipass(plan, uw, wiw, wow, k_f, yw, ws, Bw, H, st)
+                        : launch_fused(plan, uw, wiw, wow, k_f, yw, Bw, H, st);
+    if (e == cudaSuccess) {
+        partial_scatter<<<grid_for(B * H * N / 8), 256, 0, st>>>(yw, static_cast<uint4*>(y), B, H, N, C, lay.nwin);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FFTCONV_ERR_CUDA;
+    }
+    return FFTCONV_OK;
+}
+
 extern "C" const char* fftconv_status_string(fftconv_status_t s) {
     switch (s) {
         case FFTCONV_OK: return "ok";
@@ -1232,8 +1341,6 @@ HostChunks host_chunks(int64_t B, int64_t H) {
     c.rows = c.by_b ? c.per * H : c.per;
     return c;
 }
-
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct HostLayout {
     size_t buf, set, ws, total;  // one chunk buffer, one set, the multi-pass intermediate, all

@@ -270,6 +270,32 @@ fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void *u, const v
                                      size_t scratch_bytes, fftconv_stream_t stream);
 
 /*
+ * Partial convolution (FlashFFTConv page, "Architectural Extensions: Partial
+ * and Frequency-Sparse Convolutions"): a kernel with at most C taps, where
+ * C = W/2 and W is the plan's length, over sequences of any length N that is
+ * a multiple of C (N may exceed 2^21):
+ *   y[b,h,t] = sum_{j = max(0, t-C+1)}^{t} u[b,h,j] k[h,t-j]   (gated: w_out . conv(u . w_in, k))
+ * k_f: fftconv_kernel_fft of the plan on k [H][W] whose taps at lags >= C
+ * are zero (a shorter kernel, zero-padded).  The rows are cut into windows of
+ * W inputs overlapping by C (window w covers inputs [(w-1)C, (w+1)C), zeros
+ * before the start); each window is convolved by the plan's kernels and its
+ * last C outputs are kept, so the convolution work per output is that of a
+ * length-W transform.
+ * - u, w_in, w_out, y: device, [B][H][N] in the plan dtype, 16-byte aligned;
+ *   w_in, w_out both NULL or both given.
+ * - scratch: device memory of fftconv_partial_scratch_bytes(plan, B, H, N,
+ *   gated) bytes (the windowed inputs and outputs: two or four times the size
+ *   of u, plus the multi-pass intermediate of the windows).
+ * - Returns OK, INVALID, UNSUPPORTED (N not a multiple of C, or too many
+ *   windowed rows), ALIGN, WORKSPACE or CUDA.
+ */
+size_t fftconv_partial_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H, int64_t N, int gated);
+fftconv_status_t fftconv_forward_partial(fftconv_plan_t plan, const void *u, const void *w_in,
+                                         const void *w_out, const void *k_f, void *y, int64_t B, int64_t H,
+                                         int64_t N, void *scratch, size_t scratch_bytes,
+                                         fftconv_stream_t stream);
+
+/*
  * Read and clear the plan's device error word (waits for `stream`).
  * *out = 0 if no bounded on-device wait has given up since the last call,
  * else FFTCONV_ERR_TIMEOUT.  Returns OK, INVALID or CUDA.
