@@ -67,6 +67,7 @@ def _load():
         lib.oracle_partial_conv.argtypes = [_dp, _dp, _dp, i64, i64]
         lib.oracle_direct_partial_conv_at.argtypes = [_dp, _dp, i64, i64, i64]
         lib.oracle_direct_partial_conv_at.restype = ctypes.c_double
+        lib.oracle_circular_conv.argtypes = [_dp, _dp, _dp, i64]
         _lib = lib
     return _lib
 
@@ -242,3 +243,14 @@ def direct_partial_conv_at(u: np.ndarray, k: np.ndarray, T: int, t: int) -> floa
     """One partial-convolution output by the definition, O(T)."""
     u, k = _f64(u), _f64(k)
     return float(_load().oracle_direct_partial_conv_at(_ptr(u), _ptr(k), u.size, int(T), int(t)))
+
+
+# ---------------------------------------------------------------- circular convolution
+
+def circular_conv(u: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """One row: y[t] = sum_j u[j] k[(t - j) mod N], through the N-point DFT."""
+    u, k = _f64(u), _f64(k)
+    y = np.empty_like(u)
+    if _load().oracle_circular_conv(_ptr(u), _ptr(k), _ptr(y), u.size):
+        raise ValueError("N must be a power of two")
+    return y

@@ -329,3 +329,30 @@ double oracle_direct_partial_conv_at(const double *u, const double *k, int64_t N
     }
     return s + c;
 }
+
+/*
+ * Circular (non-causal) convolution of length N (FlashFFTConv page, the
+ * convolution theorem without zero padding; the pages' non-causal
+ * workloads): y[t] = sum_{j=0}^{N-1} u[j] k[(t - j) mod N], through the
+ * N-point DFT: y = IDFT_N(DFT_N(u) . DFT_N(k)).  N a power of two.
+ */
+int oracle_circular_conv(const double *u, const double *k, double *y, int64_t N)
+{
+    if (!is_pow2(N)) return -1;
+    double *ur = malloc((size_t)N * sizeof(double)), *ui = calloc((size_t)N, sizeof(double));
+    double *kr = malloc((size_t)N * sizeof(double)), *ki = calloc((size_t)N, sizeof(double));
+    if (!ur || !ui || !kr || !ki) { free(ur); free(ui); free(kr); free(ki); return -1; }
+    memcpy(ur, u, (size_t)N * sizeof(double));
+    memcpy(kr, k, (size_t)N * sizeof(double));
+    oracle_fft(ur, ui, N, -1);
+    oracle_fft(kr, ki, N, -1);
+    for (int64_t i = 0; i < N; ++i) {
+        double cr = ur[i] * kr[i] - ui[i] * ki[i];
+        double ci = ur[i] * ki[i] + ui[i] * kr[i];
+        ur[i] = cr; ui[i] = ci;
+    }
+    oracle_fft(ur, ui, N, 1);
+    memcpy(y, ur, (size_t)N * sizeof(double));
+    free(ur); free(ui); free(kr); free(ki);
+    return 0;
+}
