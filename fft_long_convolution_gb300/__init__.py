@@ -22,7 +22,8 @@ EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy",
             "fftconv_forward", "fftconv_forward_gated", "fftconv_forward_noalloc", "fftconv_host_scratch_bytes",
             "fftconv_forward_host", "fftconv_kernel_fft_adjoint", "fftconv_backward_du",
             "fftconv_backward_du_gated", "fftconv_backward_dk_scratch_bytes", "fftconv_backward_dk",
-            "fftconv_partial_scratch_bytes", "fftconv_forward_partial",
+            "fftconv_partial_scratch_bytes", "fftconv_forward_partial", "fftconv_circular_scratch_bytes",
+            "fftconv_forward_circular",
             "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
 
 
@@ -82,6 +83,9 @@ def lib(auto_build: bool = True):
         L.fftconv_partial_scratch_bytes.argtypes = [vp, i64, i64, i64, ctypes.c_int]
         L.fftconv_partial_scratch_bytes.restype = sz
         L.fftconv_forward_partial.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        L.fftconv_circular_scratch_bytes.argtypes = [vp, i64, i64, ctypes.c_int]
+        L.fftconv_circular_scratch_bytes.restype = sz
+        L.fftconv_forward_circular.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp, sz, vp]
         L.fftconv_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         L.fftconv_status_string.argtypes = [ctypes.c_int]
         L.fftconv_status_string.restype = ctypes.c_char_p
@@ -245,6 +249,22 @@ class Plan:
         scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=u.device)
         _check(lib().fftconv_forward_partial(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y), B, H, Np,
                                              _ptr(scratch), need, _stream(stream)), "fftconv_forward_partial")
+        return y
+
+    def forward_circular(self, u, k_f, w_in=None, w_out=None, y=None, stream=None):
+        """u: [B, H, N/2] -> circular convolution of length N/2 with the kernel
+        of kernel_fft_partial (its N/2 taps)."""
+        import torch
+        B, H, C = u.shape
+        if C != self.N // 2:
+            raise ValueError(f"circular length must be {self.N // 2} for this plan")
+        if y is None:
+            y = torch.empty_like(u)
+        gated = w_in is not None
+        need = int(lib().fftconv_circular_scratch_bytes(self._h, B, H, int(gated)))
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=u.device)
+        _check(lib().fftconv_forward_circular(self._h, _ptr(u), _ptr(w_in), _ptr(w_out), _ptr(k_f), _ptr(y), B, H,
+                                              _ptr(scratch), need, _stream(stream)), "fftconv_forward_circular")
         return y
 
     # ---- backward (gradients in u and k)

@@ -1139,14 +1139,16 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
 namespace {
 
 // windows of one [B][H][N] tensor: out[(b*nwin + w)*H + h][j] = in[b][h][(w-1)C + j] (0 before the start)
+// (wrap: the part before the start is taken from the end of the row instead)
 __global__ void partial_gather(const uint4* __restrict__ in, uint4* __restrict__ out, int64_t B, int64_t H,
-                               int64_t N, int64_t C, int64_t nwin) {
+                               int64_t N, int64_t C, int64_t nwin, bool wrap) {
     const int64_t W8 = (2 * C) / 8, C8 = C / 8, N8 = N / 8;  // 16-byte units (8 values)
     const int64_t total = B * nwin * H * W8;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t j = i % W8, r = i / W8, h = r % H, bw = r / H, w = bw % nwin, b = bw / nwin;
         const int64_t src = (w - 1) * C8 + j;  // 16-byte unit inside the row
-        out[i] = src >= 0 ? in[(b * H + h) * N8 + src] : make_uint4(0, 0, 0, 0);
+        out[i] = src >= 0 ? in[(b * H + h) * N8 + src]
+                          : (wrap ? in[(b * H + h) * N8 + src + N8] : make_uint4(0, 0, 0, 0));
     }
 }
 
@@ -1187,10 +1189,44 @@ extern "C" size_t fftconv_partial_scratch_bytes(fftconv_plan_t plan, int64_t B, 
     return partial_layout(plan, B, H, N, gated != 0).total;
 }
 
+namespace {
+
+fftconv_status_t windowed_forward(fftconv_plan_t plan, const void* u, const void* w_in, const void* w_out,
+                                  const void* k_f, void* y, int64_t B, int64_t H, int64_t N, void* scratch,
+                                  size_t scratch_bytes, fftconv_stream_t stream, bool wrap);
+
+}  // namespace
+
 extern "C" fftconv_status_t fftconv_forward_partial(fftconv_plan_t plan, const void* u, const void* w_in,
                                                     const void* w_out, const void* k_f, void* y, int64_t B,
                                                     int64_t H, int64_t N, void* scratch, size_t scratch_bytes,
                                                     fftconv_stream_t stream) {
+    return windowed_forward(plan, u, w_in, w_out, k_f, y, B, H, N, scratch, scratch_bytes, stream, false);
+}
+
+// Circular convolution of length C = W/2: y[t] = sum_j u[j] k[(t - j) mod C]
+// equals outputs [C, 2C) of the causal convolution of [u, u] with [k, 0]
+// (the first copy supplies the wrapped-around terms): one window of the
+// partial form whose first half wraps instead of being zero.
+extern "C" size_t fftconv_circular_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H, int gated) {
+    if (!plan) return 0;
+    return fftconv_partial_scratch_bytes(plan, B, H, plan->info.N / 2, gated);
+}
+
+extern "C" fftconv_status_t fftconv_forward_circular(fftconv_plan_t plan, const void* u, const void* w_in,
+                                                     const void* w_out, const void* k_f, void* y, int64_t B,
+                                                     int64_t H, void* scratch, size_t scratch_bytes,
+                                                     fftconv_stream_t stream) {
+    if (!plan) return FFTCONV_ERR_INVALID;
+    return windowed_forward(plan, u, w_in, w_out, k_f, y, B, H, plan->info.N / 2, scratch, scratch_bytes, stream,
+                            true);
+}
+
+namespace {
+
+fftconv_status_t windowed_forward(fftconv_plan_t plan, const void* u, const void* w_in, const void* w_out,
+                                  const void* k_f, void* y, int64_t B, int64_t H, int64_t N, void* scratch,
+                                  size_t scratch_bytes, fftconv_stream_t stream, bool wrap) {
     if (!plan || B < 0 || H < 0 || N < 0) return FFTCONV_ERR_INVALID;
     if (B == 0 || H == 0 || N == 0) return FFTCONV_OK;
     if (!u || !k_f || !y || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
@@ -1215,10 +1251,12 @@ extern "C" fftconv_status_t fftconv_forward_partial(fftconv_plan_t plan, const v
     uint4* wow = gated ? reinterpret_cast<uint4*>(sb + 3 * lay.buf) : nullptr;
     void* ws = sb + lay.buf * (gated ? 4 : 2);
     const int64_t Bw = B * lay.nwin, units = Bw * H * (2 * C) / 8;
-    partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(u), uw, B, H, N, C, lay.nwin);
+    partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(u), uw, B, H, N, C, lay.nwin, wrap);
     if (gated) {
-        partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(w_in), wiw, B, H, N, C, lay.nwin);
-        partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(w_out), wow, B, H, N, C, lay.nwin);
+        partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(w_in), wiw, B, H, N, C, lay.nwin,
+                                                        wrap);
+        partial_gather<<<grid_for(units), 256, 0, st>>>(static_cast<const uint4*>(w_out), wow, B, H, N, C, lay.nwin,
+                                                        wrap);
     }
     cudaError_t e = plan->info.path == FFTCONV_PATH_MULTIPASS
                         ? launch_multipass(plan, uw, wiw, wow, k_f, yw, ws, Bw, H, st)
@@ -1233,6 +1271,8 @@ extern "C" fftconv_status_t fftconv_forward_partial(fftconv_plan_t plan, const v
     }
     return FFTCONV_OK;
 }
+
+}  // namespace
 
 extern "C" const char* fftconv_status_string(fftconv_status_t s) {
     switch (s) {

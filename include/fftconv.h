@@ -296,6 +296,23 @@ fftconv_status_t fftconv_forward_partial(fftconv_plan_t plan, const void *u, con
                                          fftconv_stream_t stream);
 
 /*
+ * Circular (non-causal) convolution of length C = W/2, W the plan's length
+ * (the convolution theorem without zero padding or truncation):
+ *   y[b,h,t] = sum_{j=0}^{C-1} u[b,h,j] k[h,(t-j) mod C]   (gated: w_out . conv(u . w_in, k))
+ * k_f: fftconv_kernel_fft of the plan on k [H][W] holding the C taps followed
+ * by C zeros.  Computed as outputs [C, 2C) of the plan's causal convolution of
+ * [u, u] with [k, 0] (the first copy supplies the wrapped terms), i.e. one
+ * window of fftconv_forward_partial whose first half wraps around.
+ * u, w_in, w_out, y: device [B][H][C]; scratch: device memory of
+ * fftconv_circular_scratch_bytes(plan, B, H, gated) bytes.  Errors as
+ * fftconv_forward_partial.
+ */
+size_t fftconv_circular_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H, int gated);
+fftconv_status_t fftconv_forward_circular(fftconv_plan_t plan, const void *u, const void *w_in,
+                                          const void *w_out, const void *k_f, void *y, int64_t B, int64_t H,
+                                          void *scratch, size_t scratch_bytes, fftconv_stream_t stream);
+
+/*
  * Read and clear the plan's device error word (waits for `stream`).
  * *out = 0 if no bounded on-device wait has given up since the last call,
  * else FFTCONV_ERR_TIMEOUT.  Returns OK, INVALID or CUDA.
