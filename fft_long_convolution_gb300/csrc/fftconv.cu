@@ -92,6 +92,16 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
         q.factors[1] = 16;
         q.factors[2] = 16;
         q.workspace_bytes_per_row = 0;
+    } else if ((order == 0 || order == 4) && N >= (int64_t(1) << 20)) {
+        // multi-pass: M = RA * 64 * 64 * 64, the outer factor R0 = RA * 64 through
+        // HBM in two levels, sub-rows of 4096 on the tensor cores
+        q.path = FFTCONV_PATH_MULTIPASS;
+        q.order = 4;
+        q.factors[0] = int32_t(N >> 18);
+        q.factors[1] = 64;
+        q.factors[2] = 64;
+        q.factors[3] = 64;
+        q.workspace_bytes_per_row = 4 * N;  // 16-bit complex intermediate
     } else if ((order == 0 || order == 3) && N <= (int64_t(1) << 19)) {
         // multi-pass: M = R0 * 64 * 64, outer factor R0 through HBM, sub-rows
         // of 4096 on the tensor cores (the default up to N = 512K)
@@ -118,6 +128,8 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
         q.kf_bytes_per_channel = int64_t(Tc64::KFB);
     else if (q.path == FFTCONV_PATH_MULTIPASS && q.order == 3)
         q.kf_bytes_per_channel = int64_t(q.factors[0] / 2) * TcB::KFP * 16;
+    else if (q.path == FFTCONV_PATH_MULTIPASS && q.factors[3] == 64)  // two-level outer factor
+        q.kf_bytes_per_channel = int64_t(q.factors[0] * 64 / 2) * TcB::KFP * 16;
     else
         q.kf_bytes_per_channel = q.M * 8;
     *info = q;
@@ -383,6 +395,7 @@ cudaError_t launch_multipass(const fftconv_plan_s* p, const void* u, const void*
                 static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
                 static_cast<uint32_t*>(T), int(B), int(H), p->R0, p->mp, p->dev_err};
     const bool gated = wi != nullptr;
+    if (p->mp2) return launch_mp_l4k_2level(p, args, B * H, gated, st);
     return p->mpL == kMpLtc ? launch_mp_l4k(p, args, B * H, gated, st) : launch_mp_l16k(p, args, B * H, gated, st);
 }
 
@@ -403,7 +416,9 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     p->R0 = multi ? info.factors[0] : 1;
     p->R1 = multi ? kMpR1 : info.factors[0];
     p->tc64 = N == 4096;
-    p->mpL = multi ? (info.order == 3 ? kMpLtc : kMpL) : 0;
+    p->mp2 = multi && info.order == 4 && info.factors[3] == 64;
+    if (p->mp2) p->R0 = info.factors[0] * 64;  // the sub-row count of pass B
+    p->mpL = multi ? ((info.order == 3 || p->mp2) ? kMpLtc : kMpL) : 0;
     const bool need_fmat = p->tc64 || p->mpL == kMpLtc;
     HostTables T = p->tc64 ? HostTables{} : build_fused_tables(p->R1, dtype);
     std::vector<uint32_t> fmat;
@@ -411,7 +426,7 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
     HostTables T0;
     std::vector<uint32_t> ofull;
     if (multi) {
-        T0 = build_fused_tables(p->R0, dtype);
+        T0 = build_fused_tables(p->mp2 ? info.factors[0] : p->R0, dtype);  // fragments of the outermost factor
         ofull = build_full_frags(kMpR1, dtype);
     }
     std::vector<uint8_t> blob;

@@ -73,14 +73,29 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_
     return true;
 }
 
+// Dynamic shared memory of pass A (half or full input rows, gated) and pass C.
+template <int R0, bool GATED, bool FULL = false>
+constexpr size_t mp_pass_a_smem() {
+    return size_t(FULL ? R0 : R0 / 2) * kSeg * 4 * (GATED ? 2 : 1) + 32;
+}
+template <int R0, bool GATED>
+constexpr size_t mp_pass_c_smem() {
+    return size_t(R0) * kSeg * 4 + (GATED ? size_t(R0 / 2) * kSeg * 4 : 0) + 32;
+}
+
 // ------------------------------------------------------------------ pass A
-template <int DT, int R0, bool GATED, int L>
-__global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_a(const MPArgs a) {
+// FULL: an inner outer stage of a two-level outer factor: all R0 input rows
+// are nonzero and come from T itself (16-bit complex words, rows of length
+// R0*L), the result overwrites them (each item stages its whole tile first).
+template <int DT, int R0, bool GATED, int L, bool FULL = false>
+__global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(const MPArgs a) {
     using O = Op<DT>;
-    constexpr int HALF = R0 / 2, SEG = kSeg;
+    static_assert(!(FULL && GATED), "the inner stage has no gates");
+    constexpr int HALF = FULL ? R0 : R0 / 2, SEG = kSeg;  // input rows staged
     constexpr uint32_t M = uint32_t(R0) * L;
-    constexpr bool K8 = R0 <= 8;
-    constexpr int KS = K8 ? 1 : R0 / 16, MT = (R0 + 7) / 8;
+    constexpr bool K8 = !FULL && R0 <= 8;
+    constexpr int KS = K8 ? 1 : HALF / 8, MT = (R0 + 7) / 8;
+    const uint4* frag = FULL ? a.tb.ofull : a.tb.of_a;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t* su = reinterpret_cast<uint32_t*>(smem);  // [HALF][SEG]
     uint32_t* sw = su + HALF * SEG;                     // gated: w_in
@@ -102,7 +117,10 @@ __global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_a(const MPArgs 
         if (threadIdx.x == 0) {
             mbar_expect_tx(bar, HALF * 1024u * (GATED ? 2u : 1u));
             for (int n0 = 0; n0 < HALF; ++n0) {
-                bulk_g2s(su + n0 * SEG, ur + 2 * (long(L) * n0 + o_base), 1024, bar);
+                if (FULL)
+                    bulk_g2s(su + n0 * SEG, a.T + row * long(M) + long(L) * n0 + o_base, 1024, bar);
+                else
+                    bulk_g2s(su + n0 * SEG, ur + 2 * (long(L) * n0 + o_base), 1024, bar);
                 if (GATED) bulk_g2s(sw + n0 * SEG, a.w_in + row * long(M) + 2 * (long(L) * n0 + o_base), 1024, bar);
             }
         }
@@ -148,7 +166,7 @@ __global__ void __launch_bounds__(256, R0 <= 64 ? 3 : 2) mp_pass_a(const MPArgs 
                 for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
-                    const uint4 af = a.tb.of_a[(m * KS + s) * 32 + lane];
+                    const uint4 af = frag[(m * KS + s) * 32 + lane];
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         if (K8) {
@@ -188,13 +206,19 @@ __host__ __device__ constexpr int mp_pass_c_warps() { return R0 >= 128 ? 16 : 8;
 // TWID: T still lacks the W_M^(n'*k0) twiddle (tensor-core pass B); it is
 // applied here to each element before the contraction, as the chain
 // W_M^(n' t) * W_M^(8 n')^s (and * W_M^(4 n')) for k0 = 8s + t (+ 4).
-template <int DT, int R0, bool GATED, int L, bool TWID>
-__global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), R0 <= 64 ? 3 : 1) mp_pass_c(const MPArgs a) {
+// TOT: an inner outer stage of a two-level outer factor: all R0 outputs,
+// neither conjugated nor gated, written back over the staged tile of T.
+template <int DT, int R0, bool GATED, int L, bool TWID, bool TOT = false>
+__global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT) ? 3 : (R0 <= 64 ? 2 : 1))
+    mp_pass_c(const MPArgs a) {
     using O = Op<DT>;
+    static_assert(!(TOT && GATED), "the inner stage has no gates");
     constexpr int HALF = R0 / 2, SEG = kSeg;
+    constexpr int NOUT = TOT ? R0 : HALF;  // outputs kept
     constexpr long M = long(R0) * L;
     constexpr bool K8 = R0 <= 4;
-    constexpr int KS = K8 ? 1 : R0 / 8, MT = (R0 + 15) / 16;
+    constexpr int KS = K8 ? 1 : R0 / 8, MT = (NOUT + 7) / 8;
+    const uint4* frag = TOT ? a.tb.ofull : a.tb.oi_c;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t* st = reinterpret_cast<uint32_t*>(smem);  // [R0][SEG]
     uint32_t* swo = st + R0 * SEG;                      // gated: w_out [HALF][SEG]
@@ -235,8 +259,14 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), R0 <= 64 ? 3 : 1) 
                     bf[j][s][0] = ka < R0 ? st[ka * SEG + 8 * nt + g] : 0u;
                     bf[j][s][1] = (!K8 && kb < R0) ? st[kb * SEG + 8 * nt + g] : 0u;
                 }
-                if constexpr (TWID) {
-                    static_assert(!K8 && R0 % 8 == 0, "twiddled pass C needs R0 >= 8");
+                if constexpr (TWID && K8) {  // one input k0 = t per thread
+                    const uint32_t np = uint32_t(o_base + 8 * nt + g);
+                    const cpx w = twiddle_pow2((np * uint32_t(t)) & (uint32_t(M) - 1), uint32_t(M));
+                    const cpx xa = cmul(O::unpack(bf[j][0][0]), w);
+                    bf[j][0][0] = O::pack(xa.r, xa.i);
+                }
+                if constexpr (TWID && !K8) {
+                    static_assert(R0 % 8 == 0, "twiddled pass C needs R0 = 4 or a multiple of 8");
                     const uint32_t np = uint32_t(o_base + 8 * nt + g);
                     const uint32_t mask = uint32_t(M) - 1;
                     cpx wa = twiddle_pow2((np * uint32_t(t)) & mask, uint32_t(M));
@@ -259,7 +289,7 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), R0 <= 64 ? 3 : 1) 
                 for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
-                    const uint4 af = a.tb.oi_c[(m * KS + s) * 32 + lane];
+                    const uint4 af = frag[(m * KS + s) * 32 + lane];
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         if (K8) {
@@ -271,7 +301,14 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), R0 <= 64 ? 3 : 1) 
                     }
                 }
                 const int n0 = 8 * m + g;
-                if (n0 < HALF) {
+                if (TOT && n0 < NOUT) {
+                    #pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const int nt = warp + NW * (NT * i + j);
+                        *reinterpret_cast<uint2*>(a.T + row * M + long(L) * n0 + o_base + 8 * nt + 2 * t) =
+                            make_uint2(O::pack(acc[j][0], acc[j][2]), O::pack(acc[j][1], acc[j][3]));
+                    }
+                } else if (!TOT && n0 < HALF) {
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         const int nt = warp + NW * (NT * i + j);

@@ -18,6 +18,7 @@ struct fftconv_plan_s {
     fftconv::MPTables mp{};
     int R0 = 1;     // outer factor through HBM (1 on the fused path)
     int mpL = 0;    // multi-pass sub-row length: 16384 (warp-level pass B) or 4096 (tensor-core pass B)
+    bool mp2 = false;  // sub-rows of 4096 with the outer factor R0 = RA * 64 in two levels (N >= 2^20)
     bool tc64 = false;               // N = 4096: order-2 64 x 64 product on tcgen05
     const uint32_t* fmat = nullptr;  // the 64 x 64 DFT matrix rows (device), N = 4096 and mpL = 4096
     int num_sms = 0;
@@ -35,6 +36,8 @@ namespace fftconv {
 // Pass A, pass B, pass C of one forward call (args.T is the intermediate).
 cudaError_t launch_mp_l16k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st);
 cudaError_t launch_mp_l4k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st);
+cudaError_t launch_mp_l4k_2level(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
+                                 cudaStream_t st);
 
 // Dynamic shared memory opt-in and resident blocks per SM of a kernel (once).
 template <typename K>

@@ -42,6 +42,8 @@ struct TcBArgs {
     const uint32_t* fmat;   // the three DFT matrices of the N = 4096 kernel
     int B, H, R0;
     int* err;
+    int RA;                 // 0: sub-row k0 at position k0; else (two-level outer factor R0 = RA * 64)
+                            // at position (k0 mod RA) * 64 + k0 / RA
 };
 
 struct TcB {
@@ -101,10 +103,11 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
         uint32_t* TA;  // sub-row A (k0 = p), B (k0 = p ? R0 - p : R0/2)
         uint32_t* TB;
     };
+    auto pos = [&](int k0) -> size_t { return a.RA ? size_t(k0 % a.RA) * 64 + size_t(k0 / a.RA) : size_t(k0); };
     auto decode = [&](int it) -> Item {
         const int b = it % a.B, hp = it / a.B, p = hp % pairs, h = hp / pairs;
         uint32_t* Trow = a.T + (size_t(b) * a.H + h) * M;
-        return {p, h, Trow + size_t(p) * C::L, Trow + size_t(p ? a.R0 - p : pairs) * C::L};
+        return {p, h, Trow + pos(p) * C::L, Trow + pos(p ? a.R0 - p : pairs) * C::L};
     };
     auto stage_item = [&](int it, uint8_t* pbp, uint64_t* bp) {
         const Item x = decode(it);

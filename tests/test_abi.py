@@ -71,9 +71,21 @@ def test_query_multipass_order3_factorization(N, R0):
     assert F.query(N, F.BF16, order=3) == q
 
 
-@pytest.mark.parametrize("N,R0,order", [(32768, 2, 4), (262144, 16, 4), (1048576, 64, 0), (2097152, 128, 0)])
+@pytest.mark.parametrize("N,RA", [(1048576, 4), (2097152, 8)])
+def test_query_multipass_two_level_factorization(N, RA):
+    """Above N = 512K: the outer factor RA * 64 in two levels, sub-rows of 64 x 64."""
+    q = F.query(N, F.BF16)
+    assert q["path"] == F.PATH_MULTIPASS and q["order"] == 4
+    assert q["factors"] == [RA, 64, 64, 64]
+    assert RA * 64 * 64 * 64 == N
+    assert q["workspace_bytes_per_row"] == 4 * N
+    assert q["kf_bytes_per_channel"] == RA * 64 // 2 * 17 * 4 * 2 * 32 * 16
+    assert F.query(N, F.BF16, order=4) == q
+
+
+@pytest.mark.parametrize("N,R0,order", [(32768, 2, 4), (262144, 16, 4), (524288, 32, 4)])
 def test_query_multipass_order4_factorization(N, R0, order):
-    """Sub-rows of 64 x 16 x 16: on request, and the default above N = 512K."""
+    """Sub-rows of 64 x 16 x 16 on request up to N = 512K."""
     q = F.query(N, F.BF16, order=order)
     assert q["path"] == F.PATH_MULTIPASS and q["order"] == 4
     assert q["factors"] == [R0, 64, 16, 16]
