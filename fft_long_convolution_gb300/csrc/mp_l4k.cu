@@ -9,14 +9,13 @@ namespace {
 template <int DT, int R0, bool G>
 cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
     constexpr int HALF = R0 / 2, L = kMpLtc;
-    const size_t smem_a = size_t(HALF) * kSeg * 4 * (G ? 2 : 1) + 32;
-    const size_t smem_c = size_t(R0) * kSeg * 4 + (G ? size_t(HALF) * kSeg * 4 : 0) + 32;
+    const size_t smem_a = mp_pass_a_smem<R0, G>(), smem_c = mp_pass_c_smem<R0, G>();
     static int na = 0, nb = 0, nc = 0;
     cudaError_t e;
     if ((e = prep_kernel(mp_pass_a<DT, R0, G, L>, smem_a, 256, &na)) != cudaSuccess) return e;
     if ((e = prep_kernel(mp_pass_b_tc<DT>, TcB::SMEM, TcB::THREADS, &nb)) != cudaSuccess) return e;
     if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true>, smem_c, 32 * mp_pass_c_warps<R0>(), &nc)) != cudaSuccess) return e;
-    const int64_t items_ac = rows * (L / 256);
+    const int64_t items_ac = rows * (L / mp_tile<R0>());
     auto grid = [&](int64_t items, int per_sm) {
         int64_t gsz = int64_t(p->num_sms) * per_sm;
         return unsigned(gsz < items ? gsz : items);
@@ -68,7 +67,7 @@ cudaError_t launch_2l_t(const fftconv_plan_s* p, const MPArgs& args, int64_t row
         int64_t gsz = int64_t(p->num_sms) * per_sm;
         return unsigned(gsz < items ? gsz : items);
     };
-    const int64_t items1 = rows * (L1 / 256), items2 = rows * RA * (L / 256);
+    const int64_t items1 = rows * (L1 / mp_tile<RA>()), items2 = rows * RA * (L / mp_tile<64>());
     const int64_t items_b = rows * (R0 / 2), need_b = (items_b + 1) / 2;
     if (items_b >= (int64_t(1) << 30) || rows * RA >= (int64_t(1) << 30)) return cudaErrorInvalidValue;
     const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);

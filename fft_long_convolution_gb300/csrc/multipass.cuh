@@ -73,14 +73,22 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* s_
     return true;
 }
 
+// Columns per pass A / C item (wider where few segments are staged, so the
+// per-item staging, barrier and twiddle set-up are amortized) and the padded
+// staged segment in words (row stride = 8 banks, conflict free).
+template <int R0>
+__host__ __device__ constexpr int mp_tile() { return R0 <= 8 ? 2048 : 256; }
+template <int R0>
+__host__ __device__ constexpr int mp_seg() { return mp_tile<R0>() + 8; }
+
 // Dynamic shared memory of pass A (half or full input rows, gated) and pass C.
 template <int R0, bool GATED, bool FULL = false>
 constexpr size_t mp_pass_a_smem() {
-    return size_t(FULL ? R0 : R0 / 2) * kSeg * 4 * (GATED ? 2 : 1) + 32;
+    return size_t(FULL ? R0 : R0 / 2) * mp_seg<R0>() * 4 * (GATED ? 2 : 1) + 32;
 }
 template <int R0, bool GATED>
 constexpr size_t mp_pass_c_smem() {
-    return size_t(R0) * kSeg * 4 + (GATED ? size_t(R0 / 2) * kSeg * 4 : 0) + 32;
+    return size_t(R0) * mp_seg<R0>() * 4 + (GATED ? size_t(R0 / 2) * mp_seg<R0>() * 4 : 0) + 32;
 }
 
 // ------------------------------------------------------------------ pass A
@@ -91,7 +99,7 @@ template <int DT, int R0, bool GATED, int L, bool FULL = false>
 __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(const MPArgs a) {
     using O = Op<DT>;
     static_assert(!(FULL && GATED), "the inner stage has no gates");
-    constexpr int HALF = FULL ? R0 : R0 / 2, SEG = kSeg;  // input rows staged
+    constexpr int HALF = FULL ? R0 : R0 / 2, SEG = mp_seg<R0>(), TILE = mp_tile<R0>();  // input rows staged
     constexpr uint32_t M = uint32_t(R0) * L;
     constexpr bool K8 = !FULL && R0 <= 8;
     constexpr int KS = K8 ? 1 : HALF / 8, MT = (R0 + 7) / 8;
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
     uint64_t* bar = reinterpret_cast<uint64_t*>(sw + (GATED ? HALF * SEG : 0));
     __shared__ int s_fail;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const long rows = long(a.B) * a.H, tiles = L / 256, items = rows * tiles;
+    const long rows = long(a.B) * a.H, tiles = L / TILE, items = rows * tiles;
     if (threadIdx.x == 0) {
         s_fail = 0;
         mbar_init(bar, 1);
@@ -112,16 +120,16 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
     uint32_t par = 0;
     for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
         const long row = item / tiles;
-        const int o_base = int(item % tiles) * 256;
+        const int o_base = int(item % tiles) * TILE;
         const uint16_t* ur = a.u + row * long(M);
         if (threadIdx.x == 0) {
-            mbar_expect_tx(bar, HALF * 1024u * (GATED ? 2u : 1u));
+            mbar_expect_tx(bar, HALF * TILE * 4u * (GATED ? 2u : 1u));
             for (int n0 = 0; n0 < HALF; ++n0) {
                 if (FULL)
-                    bulk_g2s(su + n0 * SEG, a.T + row * long(M) + long(L) * n0 + o_base, 1024, bar);
+                    bulk_g2s(su + n0 * SEG, a.T + row * long(M) + long(L) * n0 + o_base, TILE * 4, bar);
                 else
-                    bulk_g2s(su + n0 * SEG, ur + 2 * (long(L) * n0 + o_base), 1024, bar);
-                if (GATED) bulk_g2s(sw + n0 * SEG, a.w_in + row * long(M) + 2 * (long(L) * n0 + o_base), 1024, bar);
+                    bulk_g2s(su + n0 * SEG, ur + 2 * (long(L) * n0 + o_base), TILE * 4, bar);
+                if (GATED) bulk_g2s(sw + n0 * SEG, a.w_in + row * long(M) + 2 * (long(L) * n0 + o_base), TILE * 4, bar);
             }
         }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
         // product chain over the output tiles m
         constexpr int NT = 2;
         #pragma unroll 1
-        for (int i = 0; i < 4 / NT; ++i) {
+        for (int i = 0; i < TILE / 64 / NT; ++i) {
             uint32_t bf[NT][KS][2];
             cpx tw[NT][2], ts[NT][2];
             #pragma unroll
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
                 for (int e = 0; e < 2; ++e) {
                     const uint32_t o = uint32_t(o_base + 8 * nt + 2 * t + e);
                     tw[j][e] = twiddle_pow2((o * uint32_t(g)) & (M - 1), M);
-                    ts[j][e] = twiddle_pow2((8 * o) & (M - 1), M);
+                    if (MT > 1) ts[j][e] = twiddle_pow2((8 * o) & (M - 1), M);
                 }
             }
             #pragma unroll
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
     mp_pass_c(const MPArgs a) {
     using O = Op<DT>;
     static_assert(!(TOT && GATED), "the inner stage has no gates");
-    constexpr int HALF = R0 / 2, SEG = kSeg;
+    constexpr int HALF = R0 / 2, SEG = mp_seg<R0>(), TILE = mp_tile<R0>();
     constexpr int NOUT = TOT ? R0 : HALF;  // outputs kept
     constexpr long M = long(R0) * L;
     constexpr bool K8 = R0 <= 4;
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
     uint64_t* bar = reinterpret_cast<uint64_t*>(swo + (GATED ? HALF * SEG : 0));
     __shared__ int s_fail;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-    const long rows = long(a.B) * a.H, tiles = L / 256, items = rows * tiles;
+    const long rows = long(a.B) * a.H, tiles = L / TILE, items = rows * tiles;
     if (threadIdx.x == 0) {
         s_fail = 0;
         mbar_init(bar, 1);
@@ -235,20 +243,20 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
     uint32_t par = 0;
     for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
         const long row = item / tiles;
-        const int o_base = int(item % tiles) * 256;
+        const int o_base = int(item % tiles) * TILE;
         if (threadIdx.x == 0) {
-            mbar_expect_tx(bar, R0 * 1024u + (GATED ? HALF * 1024u : 0u));
+            mbar_expect_tx(bar, (R0 + (GATED ? HALF : 0)) * TILE * 4u);
             for (int k0 = 0; k0 < R0; ++k0)
-                bulk_g2s(st + k0 * SEG, a.T + row * M + long(k0) * L + o_base, 1024, bar);
+                bulk_g2s(st + k0 * SEG, a.T + row * M + long(k0) * L + o_base, TILE * 4, bar);
             if (GATED)
                 for (int n0 = 0; n0 < HALF; ++n0)
-                    bulk_g2s(swo + n0 * SEG, a.w_out + row * M + 2 * (long(L) * n0 + o_base), 1024, bar);
+                    bulk_g2s(swo + n0 * SEG, a.w_out + row * M + 2 * (long(L) * n0 + o_base), TILE * 4, bar);
         }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
         // NT column groups of 8 per iteration share each DFT fragment load
         constexpr int NT = KS <= 8 ? 2 : 1, NW = mp_pass_c_warps<R0>();
         #pragma unroll 1
-        for (int i = 0; i < 32 / NW / NT; ++i) {
+        for (int i = 0; i < TILE / 8 / NW / NT; ++i) {
             uint32_t bf[NT][KS][2];
             #pragma unroll
             for (int j = 0; j < NT; ++j) {
