@@ -89,8 +89,9 @@ typedef struct {
  *   N = 4096:             order 2, 64 x 64 (fused, tensor-memory kernel)
  *   N <= 16384 otherwise: order 3, N/256 x 16 x 16 (fused)
  *   32768 <= N <= 2^19:   order 3, N/4096 x 64 x 64 (multi-pass; the default),
- *                         or order 4 on request
- *   N >= 2^20:            order 4, N/16384 x 64 x 16 x 16 (multi-pass)
+ *                         or order 4, N/16384 x 64 x 16 x 16, on request
+ *   N >= 2^20:            order 4, N/2^18 x 64 x 64 x 64 (multi-pass, the outer
+ *                         factor in two HBM levels)
  * Returns OK, INVALID (info NULL) or UNSUPPORTED.
  */
 fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype, int order,
