@@ -23,7 +23,7 @@ EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy",
             "fftconv_forward_host", "fftconv_kernel_fft_adjoint", "fftconv_backward_du",
             "fftconv_backward_du_gated", "fftconv_backward_dk_scratch_bytes", "fftconv_backward_dk",
             "fftconv_partial_scratch_bytes", "fftconv_forward_partial", "fftconv_circular_scratch_bytes",
-            "fftconv_forward_circular",
+            "fftconv_forward_circular", "fftconv_selftest_wait",
             "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
 
 
@@ -86,6 +86,7 @@ def lib(auto_build: bool = True):
         L.fftconv_circular_scratch_bytes.argtypes = [vp, i64, i64, ctypes.c_int]
         L.fftconv_circular_scratch_bytes.restype = sz
         L.fftconv_forward_circular.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, vp, sz, vp]
+        L.fftconv_selftest_wait.argtypes = [vp, ctypes.c_int, vp]
         L.fftconv_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         L.fftconv_status_string.argtypes = [ctypes.c_int]
         L.fftconv_status_string.restype = ctypes.c_char_p

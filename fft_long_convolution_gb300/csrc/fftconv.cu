@@ -889,6 +889,37 @@ extern "C" fftconv_status_t fftconv_device_status(fftconv_plan_t plan, fftconv_s
     return FFTCONV_OK;
 }
 
+// --------------------------------------------------------------- failure-detection self-test
+//
+// One CTA waits, with the library's own bounded waits, on an mbarrier phase
+// that nothing ever completes (no arrival, no copy): the wait must give up,
+// record FFTCONV_ERR_TIMEOUT in the plan's error word and return, leaving the
+// context usable.  No fault, trap or unbounded loop is involved.
+
+namespace {
+
+__global__ void selftest_wait_kernel(int* err, int sleep) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool done = sleep ? mbar_wait_sleep(&bar, 0, kWaitSleepLimit, kWaitHintNs)
+                                : mbar_wait_bounded(&bar, 0, kWaitLimit);
+        if (!done) atomicExch(err, FFTCONV_ERR_TIMEOUT);
+    }
+}
+
+}  // namespace
+
+extern "C" fftconv_status_t fftconv_selftest_wait(fftconv_plan_t plan, int sleep, fftconv_stream_t stream) {
+    if (!plan) return FFTCONV_ERR_INVALID;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(plan->dev_err, sleep);
+    return cudaGetLastError() == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+}
+
 // --------------------------------------------------------------- backward
 //
 // Gradients of the convolution (FlashFFTConv page, section 3.4, "Kernel

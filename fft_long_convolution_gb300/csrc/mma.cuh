@@ -128,10 +128,23 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Wait until phase `parity` of the barrier completes; gives up after
-// `limit` polls.  Returns true when the phase completed.
+// Wall-clock bound of every on-device wait: about one second (a poll can
+// suspend for a system-dependent time, so a poll count alone does not bound
+// the time).
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until phase `parity` of the barrier completes; gives up after `limit`
+// polls or about kWaitNs, whichever comes first.  Returns true when the phase
+// completed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
     uint32_t addr = smem_u32(bar);
+    uint64_t t0 = 0;
     for (uint32_t it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile(
@@ -141,6 +154,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             : "r"(addr), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((it & 63) == 0) {
+            const uint64_t t = globaltimer_ns();
+            if (it == 0) t0 = t;
+            else if (t - t0 > kWaitNs) return false;
+        }
     }
     return false;
 }
@@ -149,6 +167,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // until the phase completes, so waiting warps do not compete for issue slots.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t limit, uint32_t hint_ns) {
     uint32_t addr = smem_u32(bar);
+    uint64_t t0 = 0;
     for (uint32_t it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile(
@@ -158,6 +177,11 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
             : "r"(addr), "r"(parity), "r"(hint_ns)
             : "memory");
         if (done) return true;
+        if ((it & 63) == 0) {
+            const uint64_t t = globaltimer_ns();
+            if (it == 0) t0 = t;
+            else if (t - t0 > kWaitNs) return false;
+        }
     }
     return false;
 }

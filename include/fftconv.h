@@ -320,6 +320,16 @@ fftconv_status_t fftconv_forward_circular(fftconv_plan_t plan, const void *u, co
  */
 fftconv_status_t fftconv_device_status(fftconv_plan_t plan, fftconv_stream_t stream, int *out);
 
+/*
+ * Failure-detection self-test: one CTA waits, with the same bounded waits the
+ * kernels use (sleep != 0: the suspending form, at most about 2 s; else the
+ * polling form), on an mbarrier phase that nothing completes.  The wait gives
+ * up, records FFTCONV_ERR_TIMEOUT in the plan's error word (read it with
+ * fftconv_device_status) and returns; the context stays usable.  Returns OK,
+ * INVALID or CUDA.
+ */
+fftconv_status_t fftconv_selftest_wait(fftconv_plan_t plan, int sleep, fftconv_stream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char *fftconv_status_string(fftconv_status_t s);
 
