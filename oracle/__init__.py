@@ -68,6 +68,8 @@ def _load():
         lib.oracle_direct_partial_conv_at.argtypes = [_dp, _dp, i64, i64, i64]
         lib.oracle_direct_partial_conv_at.restype = ctypes.c_double
         lib.oracle_circular_conv.argtypes = [_dp, _dp, _dp, i64]
+        lib.oracle_masked_causal_conv.argtypes = [_dp, _dp, _dp, _dp, i64]
+        lib.oracle_direct_masked_causal_conv.argtypes = [_dp, _dp, _dp, _dp, i64]
         _lib = lib
     return _lib
 
@@ -254,3 +256,76 @@ def circular_conv(u: np.ndarray, k: np.ndarray) -> np.ndarray:
     if _load().oracle_circular_conv(_ptr(u), _ptr(k), _ptr(y), u.size):
         raise ValueError("N must be a power of two")
     return y
+
+
+# ---------------------------------------------------------------- frequency-sparse convolution
+
+def band_mask(N: int, factors, band) -> np.ndarray:
+    """Weights (0 or 1) of the spectrum bins f = 0..N for a frequency-sparse
+    pattern on the decomposition's frequency digits (FlashFFTConv page,
+    "Architectural Extensions", frequency-sparse part, and its pattern of
+    zeroing whole rows along each axis of the reshaped k_f).
+
+    The transform the decomposition runs has length M = N (complex, after
+    the real-input packing); its frequency index r = f mod M is written in
+    mixed radix over the factors, outer factor first:
+    r = r_1 + M_1 r_2 + M_1 M_2 r_3 + ...  Bin f is kept when every digit is
+    within its band in cyclic distance: min(r_j, M_j - r_j) < band[j].  A
+    band of M_j/2 + 1 or more keeps the whole axis; a band of 0 zeroes it.
+    """
+    factors, band = [int(x) for x in factors], [int(x) for x in band]
+    if len(factors) != len(band) or int(np.prod(factors)) != N:
+        raise ValueError("one band per factor, and the factors must multiply to N")
+    r = np.arange(N + 1, dtype=np.int64) % N
+    keep = np.ones(N + 1, dtype=bool)
+    for Mj, bj in zip(factors, band):
+        d = r % Mj
+        r = r // Mj
+        keep &= np.minimum(d, Mj - d) < bj
+    return keep.astype(np.float64)
+
+
+def masked_causal_conv(u: np.ndarray, k: np.ndarray, mask: np.ndarray) -> np.ndarray:
+    """One row of the frequency-sparse convolution: the 2N-point spectrum of
+    k weighted by mask[f] (f = 0..N, mirrored to 2N - f) before the product."""
+    u, k, mask = _f64(u), _f64(k), _f64(mask)
+    if mask.size != u.size + 1:
+        raise ValueError("mask needs N + 1 entries")
+    y = np.empty_like(u)
+    if _load().oracle_masked_causal_conv(_ptr(u), _ptr(k), _ptr(mask), _ptr(y), u.size):
+        raise ValueError("N must be a power of two")
+    return y
+
+
+def direct_masked_causal_conv(u: np.ndarray, k: np.ndarray, mask: np.ndarray) -> np.ndarray:
+    """The same row from DFT sums over bins 0..N (no FFT), O(N^2)."""
+    u, k, mask = _f64(u), _f64(k), _f64(mask)
+    if mask.size != u.size + 1:
+        raise ValueError("mask needs N + 1 entries")
+    y = np.empty_like(u)
+    _load().oracle_direct_masked_causal_conv(_ptr(u), _ptr(k), _ptr(mask), _ptr(y), u.size)
+    return y
+
+
+def masked_causal_conv_batch(u: np.ndarray, k: np.ndarray, mask: np.ndarray, w_in: Optional[np.ndarray] = None,
+                             w_out: Optional[np.ndarray] = None, threads: int = 1,
+                             rows: Optional[range] = None) -> np.ndarray:
+    """u: [B, H, N], k: [H, N]; y = w_out . masked_conv(u . w_in, k) per row
+    (gates optional).  rows selects flat rows b*H + h (default all)."""
+    u, k = _f64(u), _f64(k)
+    B, H, N = u.shape
+    sel = list(rows) if rows is not None else list(range(B * H))
+    uf = u.reshape(B * H, N)
+    wi = _f64(w_in).reshape(B * H, N) if w_in is not None else None
+    wo = _f64(w_out).reshape(B * H, N) if w_out is not None else None
+    out = np.empty((len(sel), N))
+
+    def run(i0, i1):
+        for i in range(i0, i1):
+            r = sel[i]
+            x = uf[r] * wi[r] if wi is not None else uf[r]
+            y = masked_causal_conv(x, k[r % H], mask)
+            out[i] = y * wo[r] if wo is not None else y
+
+    _split(run, len(sel), threads)
+    return out

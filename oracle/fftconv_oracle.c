@@ -356,3 +356,76 @@ int oracle_circular_conv(const double *u, const double *k, double *y, int64_t N)
     free(ur); free(ui); free(kr); free(ki);
     return 0;
 }
+
+/*
+ * Frequency-sparse causal convolution (FlashFFTConv page, "Architectural
+ * Extensions: Partial and Frequency-Sparse Convolutions", the
+ * frequency-sparse part): part of the kernel's spectrum is set to zero
+ * before the product.  mask[f], f = 0..N, weighs bin f of the 2N-point
+ * spectrum of the real kernel; bin 2N - f (f = 1..N-1) takes the same
+ * weight, so the weighted spectrum keeps the conjugate symmetry of a real
+ * signal and the result is real:
+ *   y = first N outputs of IDFT_2N( DFT_2N(u0) . DFT_2N(k0) . m ),
+ *   m[f] = mask[f] for f <= N, mask[2N - f] for f > N.
+ * N a power of two.  Returns 0 or -1.
+ */
+int oracle_masked_causal_conv(const double *u, const double *k, const double *mask, double *y, int64_t N)
+{
+    if (!is_pow2(N)) return -1;
+    int64_t L = 2 * N;
+    double *ur = calloc((size_t)L, sizeof(double)), *ui = calloc((size_t)L, sizeof(double));
+    double *kr = calloc((size_t)L, sizeof(double)), *ki = calloc((size_t)L, sizeof(double));
+    if (!ur || !ui || !kr || !ki) { free(ur); free(ui); free(kr); free(ki); return -1; }
+    memcpy(ur, u, (size_t)N * sizeof(double));
+    memcpy(kr, k, (size_t)N * sizeof(double));
+    oracle_fft(ur, ui, L, -1);
+    oracle_fft(kr, ki, L, -1);
+    for (int64_t f = 0; f < L; ++f) {
+        double w = f <= N ? mask[f] : mask[L - f];
+        double pr = (ur[f] * kr[f] - ui[f] * ki[f]) * w;
+        double pi = (ur[f] * ki[f] + ui[f] * kr[f]) * w;
+        ur[f] = pr; ui[f] = pi;
+    }
+    oracle_fft(ur, ui, L, 1);
+    memcpy(y, ur, (size_t)N * sizeof(double));
+    free(ur); free(ui); free(kr); free(ki);
+    return 0;
+}
+
+/*
+ * The same outputs from the definition of the DFT, with no FFT (brute
+ * force, O(N^2), any N >= 1).  Only the bins f = 0..N are formed:
+ *   U[f] = sum_n u[n] exp(-i pi f n / N), K[f] likewise, P[f] = mask[f] U[f] K[f];
+ * the other half of the spectrum is the conjugate of this one, so the
+ * inverse transform of length 2N reads
+ *   y[t] = (1 / 2N) (P[0] + (-1)^t P[N] + 2 sum_{f=1}^{N-1} Re(P[f] exp(+i pi f t / N))).
+ * Angles are reduced exactly (f n mod 2N) before cos / sin.
+ */
+int oracle_direct_masked_causal_conv(const double *u, const double *k, const double *mask, double *y, int64_t N)
+{
+    if (N < 1) return -1;
+    int64_t L = 2 * N;
+    double *pr = malloc((size_t)(N + 1) * sizeof(double)), *pi = malloc((size_t)(N + 1) * sizeof(double));
+    if (!pr || !pi) { free(pr); free(pi); return -1; }
+    for (int64_t f = 0; f <= N; ++f) {
+        double Ur = 0.0, Ui = 0.0, Kr = 0.0, Ki = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double a = ORACLE_PI * (double)((f * n) % L) / (double)N;
+            double c = cos(a), s = sin(a);
+            Ur += u[n] * c; Ui -= u[n] * s;
+            Kr += k[n] * c; Ki -= k[n] * s;
+        }
+        pr[f] = (Ur * Kr - Ui * Ki) * mask[f];
+        pi[f] = (Ur * Ki + Ui * Kr) * mask[f];
+    }
+    for (int64_t t = 0; t < N; ++t) {
+        double s = pr[0] + ((t & 1) ? -pr[N] : pr[N]);
+        for (int64_t f = 1; f < N; ++f) {
+            double a = ORACLE_PI * (double)((f * t) % L) / (double)N;
+            s += 2.0 * (pr[f] * cos(a) - pi[f] * sin(a));
+        }
+        y[t] = s / (double)L;
+    }
+    free(pr); free(pi);
+    return 0;
+}
