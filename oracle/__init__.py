@@ -310,14 +310,16 @@ def direct_masked_causal_conv(u: np.ndarray, k: np.ndarray, mask: np.ndarray) ->
 def masked_causal_conv_batch(u: np.ndarray, k: np.ndarray, mask: np.ndarray, w_in: Optional[np.ndarray] = None,
                              w_out: Optional[np.ndarray] = None, threads: int = 1,
                              rows: Optional[range] = None) -> np.ndarray:
-    """u: [B, H, N], k: [H, N]; y = w_out . masked_conv(u . w_in, k) per row
-    (gates optional).  rows selects flat rows b*H + h (default all)."""
+    """u: [B, H, N] (or [rows, N] with H = k.shape[0]), k: [H, N];
+    y = w_out . masked_conv(u . w_in, k) per row (gates optional).  rows
+    selects flat rows b*H + h (default all)."""
     u, k = _f64(u), _f64(k)
-    B, H, N = u.shape
-    sel = list(rows) if rows is not None else list(range(B * H))
-    uf = u.reshape(B * H, N)
-    wi = _f64(w_in).reshape(B * H, N) if w_in is not None else None
-    wo = _f64(w_out).reshape(B * H, N) if w_out is not None else None
+    H, N = k.shape
+    R = u.size // N
+    sel = list(rows) if rows is not None else list(range(R))
+    uf = u.reshape(R, N)
+    wi = _f64(w_in).reshape(R, N) if w_in is not None else None
+    wo = _f64(w_out).reshape(R, N) if w_out is not None else None
     out = np.empty((len(sel), N))
 
     def run(i0, i1):

@@ -372,21 +372,21 @@ int oracle_circular_conv(const double *u, const double *k, double *y, int64_t N)
 int oracle_masked_causal_conv(const double *u, const double *k, const double *mask, double *y, int64_t N)
 {
     if (!is_pow2(N)) return -1;
-    int64_t L = 2 * N;
-    double *ur = calloc((size_t)L, sizeof(double)), *ui = calloc((size_t)L, sizeof(double));
-    double *kr = calloc((size_t)L, sizeof(double)), *ki = calloc((size_t)L, sizeof(double));
+    int64_t L2 = 2 * N;
+    double *ur = calloc((size_t)L2, sizeof(double)), *ui = calloc((size_t)L2, sizeof(double));
+    double *kr = calloc((size_t)L2, sizeof(double)), *ki = calloc((size_t)L2, sizeof(double));
     if (!ur || !ui || !kr || !ki) { free(ur); free(ui); free(kr); free(ki); return -1; }
     memcpy(ur, u, (size_t)N * sizeof(double));
     memcpy(kr, k, (size_t)N * sizeof(double));
-    oracle_fft(ur, ui, L, -1);
-    oracle_fft(kr, ki, L, -1);
-    for (int64_t f = 0; f < L; ++f) {
-        double w = f <= N ? mask[f] : mask[L - f];
+    oracle_fft(ur, ui, L2, -1);
+    oracle_fft(kr, ki, L2, -1);
+    for (int64_t f = 0; f < L2; ++f) {
+        double w = f <= N ? mask[f] : mask[L2 - f];
         double pr = (ur[f] * kr[f] - ui[f] * ki[f]) * w;
         double pi = (ur[f] * ki[f] + ui[f] * kr[f]) * w;
         ur[f] = pr; ui[f] = pi;
     }
-    oracle_fft(ur, ui, L, 1);
+    oracle_fft(ur, ui, L2, 1);
     memcpy(y, ur, (size_t)N * sizeof(double));
     free(ur); free(ui); free(kr); free(ki);
     return 0;
@@ -404,13 +404,13 @@ int oracle_masked_causal_conv(const double *u, const double *k, const double *ma
 int oracle_direct_masked_causal_conv(const double *u, const double *k, const double *mask, double *y, int64_t N)
 {
     if (N < 1) return -1;
-    int64_t L = 2 * N;
+    int64_t L2 = 2 * N;
     double *pr = malloc((size_t)(N + 1) * sizeof(double)), *pi = malloc((size_t)(N + 1) * sizeof(double));
     if (!pr || !pi) { free(pr); free(pi); return -1; }
     for (int64_t f = 0; f <= N; ++f) {
         double Ur = 0.0, Ui = 0.0, Kr = 0.0, Ki = 0.0;
         for (int64_t n = 0; n < N; ++n) {
-            double a = ORACLE_PI * (double)((f * n) % L) / (double)N;
+            double a = ORACLE_PI * (double)((f * n) % L2) / (double)N;
             double c = cos(a), s = sin(a);
             Ur += u[n] * c; Ui -= u[n] * s;
             Kr += k[n] * c; Ki -= k[n] * s;
@@ -421,10 +421,10 @@ int oracle_direct_masked_causal_conv(const double *u, const double *k, const dou
     for (int64_t t = 0; t < N; ++t) {
         double s = pr[0] + ((t & 1) ? -pr[N] : pr[N]);
         for (int64_t f = 1; f < N; ++f) {
-            double a = ORACLE_PI * (double)((f * t) % L) / (double)N;
+            double a = ORACLE_PI * (double)((f * t) % L2) / (double)N;
             s += 2.0 * (pr[f] * cos(a) - pi[f] * sin(a));
         }
-        y[t] = s / (double)L;
+        y[t] = s / (double)L2;
     }
     free(pr); free(pi);
     return 0;

@@ -143,10 +143,10 @@ def test_batch_rows_use_their_channel_and_gates():
 
 
 SPARSE_MUTANTS = {
-    "mask not mirrored to the upper half": ("double w = f <= N ? mask[f] : mask[L - f];",
+    "mask not mirrored to the upper half": ("double w = f <= N ? mask[f] : mask[L2 - f];",
                                             "double w = f <= N ? mask[f] : 1.0;"),
-    "mirror off by one": ("double w = f <= N ? mask[f] : mask[L - f];",
-                          "double w = f <= N ? mask[f] : mask[L - f - 1];"),
+    "mirror off by one": ("double w = f <= N ? mask[f] : mask[L2 - f];",
+                          "double w = f <= N ? mask[f] : mask[L2 - f - 1];"),
     "mask on the real part only": ("double pi = (ur[f] * ki[f] + ui[f] * kr[f]) * w;",
                                    "double pi = (ur[f] * ki[f] + ui[f] * kr[f]);"),
     "direct sums: conjugated U": ("Ur += u[n] * c; Ui -= u[n] * s;", "Ur += u[n] * c; Ui += u[n] * s;"),
