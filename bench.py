@@ -25,6 +25,7 @@ import statistics
 import subprocess
 import sys
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -189,8 +190,9 @@ def dist_env():
     return rank, world, local
 
 
-def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 10.0):
-    """The oracle on the host cores over a bounded sample of rows."""
+def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 10.0, mask=None):
+    """The oracle on the host cores over a bounded sample of rows (the
+    masked convolution for a frequency-sparse run)."""
     import oracle
     cores = os.cpu_count() or 1
     rows = min(w.rows, max(cores, 1))
@@ -198,7 +200,10 @@ def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 10.0):
     sl = {n: (r.f64.reshape(-1, w.N)[:rows] if n != "k" else r.f64) for n, r in ins.items()}
 
     def run():
-        oracle.causal_conv_batch(sl["u"], sl["k"], sl.get("w_in"), sl.get("w_out"), threads=cores)
+        if mask is None:
+            oracle.causal_conv_batch(sl["u"], sl["k"], sl.get("w_in"), sl.get("w_out"), threads=cores)
+        else:
+            oracle.masked_causal_conv_batch(sl["u"], sl["k"], mask, sl.get("w_in"), sl.get("w_out"), threads=cores)
 
     t0 = time.perf_counter()
     run()
@@ -213,6 +218,11 @@ def cpu_baseline(w: W.Workload, ins: dict, budget_s: float = 10.0):
             "sample": f"{rows} rows x {reps} repeats of {w.name} (N={w.N}) in {dt:.1f} s"}
 
 
+def _factors(w: W.Workload) -> list:
+    import fft_long_convolution_gb300 as F
+    return F.query(w.N, F.F16 if w.dtype == "fp16" else F.BF16)["factors"]
+
+
 def run_reference(args, w: W.Workload):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -222,9 +232,16 @@ def run_reference(args, w: W.Workload):
     small = W.scaled(w, B=1, H=min(w.H, (os.cpu_count() or 1)))
     ins = W.make_inputs(small, seed=0)
     cores = os.cpu_count() or 1
-    fn = lambda: oracle.causal_conv_batch(  # noqa: E731
-        ins["u"].f64, ins["k"].f64, ins["w_in"].f64 if w.gated else None,
-        ins["w_out"].f64 if w.gated else None, threads=cores)
+    band = parse_band(args.band)
+    mask = band_mask_for(w, band)
+    if mask is None:
+        fn = lambda: oracle.causal_conv_batch(  # noqa: E731
+            ins["u"].f64, ins["k"].f64, ins["w_in"].f64 if w.gated else None,
+            ins["w_out"].f64 if w.gated else None, threads=cores)
+    else:
+        fn = lambda: oracle.masked_causal_conv_batch(  # noqa: E731
+            ins["u"].f64, ins["k"].f64, mask, ins["w_in"].f64 if w.gated else None,
+            ins["w_out"].f64 if w.gated else None, threads=cores)
     for _ in range(args.warmup):
         fn()
     t0 = time.perf_counter()
@@ -238,27 +255,55 @@ def run_reference(args, w: W.Workload):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "outputs/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(w),
+        "data": "synthetic",
+        "config": config_of(w, band, None if band is None else _factors(w)),
         "cpu_baseline": {"value": v, "unit": "outputs/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "outputs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 
-def path_of(plan_info: dict) -> dict:
-    """The kernels one step launches for a plan (names as in the sources)."""
+def path_of(plan_info: dict, pairs_run: Optional[int] = None) -> dict:
+    """The kernels one step launches for a plan (names as in the sources);
+    pass B is not launched when a frequency-sparse plan skips every pair."""
     if plan_info["path"] == 1:
+        nb = 0 if pairs_run == 0 else 1
+        if plan_info["order"] == 4 and plan_info["factors"][3] == 64:  # outer factor in two HBM levels
+            return {"kernel": "mp_pass_a x2 + mp_pass_b_tc + mp_pass_c x2 (the whole step)",
+                    "launches_per_step": 4 + nb}
         b = "mp_pass_b_tc" if plan_info["order"] == 3 else "mp_pass_b"
-        return {"kernel": f"mp_pass_a + {b} + mp_pass_c (the whole step)", "launches_per_step": 3}
+        return {"kernel": f"mp_pass_a + {b} + mp_pass_c (the whole step)", "launches_per_step": 2 + nb}
     if plan_info["order"] == 2:
         return {"kernel": "tc64_conv_kernel", "launches_per_step": 1}
     return {"kernel": "fused_conv_kernel", "launches_per_step": 1}
 
 
-def config_of(w: W.Workload) -> dict:
-    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "gated": w.gated, "dtype": w.dtype,
-            "u": w.u_kind, "k": w.k_kind,
-            "l2": "no flush: inputs+outputs exceed L2" if algorithmic(w)["bytes"] > L2_BYTES
-            else "L2 flushed between steps"}
+def config_of(w: W.Workload, band: Optional[list] = None, factors: Optional[list] = None) -> dict:
+    c = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "gated": w.gated, "dtype": w.dtype,
+         "u": w.u_kind, "k": w.k_kind,
+         "l2": "no flush: inputs+outputs exceed L2" if algorithmic(w)["bytes"] > L2_BYTES
+         else "L2 flushed between steps"}
+    if band is not None:
+        # frequency-sparse: kept fraction of the spectrum, prod_j kept_j / N
+        kept = 1
+        for b, Mj in zip(band, factors):
+            kept *= 0 if b <= 0 else min(Mj, 2 * b - 1)
+        c["band"] = list(band)
+        c["spectrum_kept"] = kept / w.N
+    return c
+
+
+def parse_band(text: Optional[str]) -> Optional[list]:
+    return None if not text else [int(x) for x in text.split(",")]
+
+
+def band_mask_for(w: W.Workload, band: Optional[list]):
+    """The oracle's 0/1 pattern for a frequency-sparse run (None: dense)."""
+    if band is None:
+        return None
+    import oracle
+    import fft_long_convolution_gb300 as F
+    info = F.query(w.N, F.F16 if w.dtype == "fp16" else F.BF16)
+    return oracle.band_mask(w.N, info["factors"], band)
 
 
 def run_backward(args, w: W.Workload):
@@ -347,6 +392,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--band", default=None,
+                    help="frequency-sparse forward: one band per plan factor, comma separated (e.g. 16,33,33)")
     ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
                     help="backward: input and kernel gradients (du + dk) per step")
     args = ap.parse_args()
@@ -377,8 +424,10 @@ def main():
             return torch.from_numpy(r.bits).to(dev)
         return torch.from_numpy(r.bits.view(np.int16)).view(tdt).to(dev)
 
-    plan = F.Plan(w.N, tdt)
-    path = path_of(plan.info)
+    band = parse_band(args.band)
+    plan = F.Plan(w.N, tdt, band=band)
+    bd = plan.band()
+    path = path_of(plan.info, bd["pairs_run"] if band is not None else None)
     k = dev_t(ins["k"])
     kf = plan.kernel_fft(k)
     # the kernel spectrum is computed once per set of weights (outside the
@@ -477,7 +526,8 @@ def main():
             "warmup": max(args.warmup, 3), "ms_per_step": step_ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": {"fp16": "f16", "bf16": "bf16"}[w.dtype],
             "data": "synthetic (seeded SplitMix64 / Box-Muller, see workloads/)",
-            "config": config_of(w), "roofline": roof, "gpu_launches": args.steps * path["launches_per_step"],
+            "config": config_of(w, band, plan.info["factors"]), "roofline": roof,
+            "gpu_launches": args.steps * path["launches_per_step"],
             "e2e": {"value": e2e_value, "unit": "outputs/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "clocks": clk,
@@ -486,7 +536,10 @@ def main():
         if not args.no_cpu_baseline and world == 1:
             import oracle
             oracle.build()
-            out["cpu_baseline"] = cpu_baseline(w, ins)
+            out["cpu_baseline"] = cpu_baseline(w, ins, mask=band_mask_for(w, band))
+        if band is not None:
+            out["config"]["pairs_run"] = bd["pairs_run"]
+            out["config"]["pairs_total"] = bd["pairs_total"]
         print(json.dumps(out))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -23,7 +23,8 @@ EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy",
             "fftconv_forward_host", "fftconv_kernel_fft_adjoint", "fftconv_backward_du",
             "fftconv_backward_du_gated", "fftconv_backward_dk_scratch_bytes", "fftconv_backward_dk",
             "fftconv_partial_scratch_bytes", "fftconv_forward_partial", "fftconv_circular_scratch_bytes",
-            "fftconv_forward_circular", "fftconv_selftest_wait",
+            "fftconv_forward_circular", "fftconv_selftest_wait", "fftconv_plan_create_sparse",
+            "fftconv_plan_get_band", "fftconv_sparse_query",
             "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
 
 
@@ -60,6 +61,13 @@ def lib(auto_build: bool = True):
         vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
         L.fftconv_plan_query.argtypes = [i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(PlanInfo)]
         L.fftconv_plan_create.argtypes = [ctypes.POINTER(vp), i64, ctypes.c_int, ctypes.c_int]
+        L.fftconv_plan_create_sparse.argtypes = [ctypes.POINTER(vp), i64, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
+        L.fftconv_sparse_query.argtypes = [i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.POINTER(ctypes.c_int32)]
+        L.fftconv_plan_get_band.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                            ctypes.POINTER(ctypes.c_int32)]
         L.fftconv_plan_destroy.argtypes = [vp]
         L.fftconv_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
         L.fftconv_kf_bytes.argtypes = [vp, i64]
@@ -106,6 +114,15 @@ def query(N: int, dtype: int, order: int = 0) -> dict:
     return info.as_dict()
 
 
+def sparse_query(N: int, dtype: int, band, order: int = 0) -> dict:
+    """Pairs of sub-rows a frequency-sparse plan would transform (no GPU)."""
+    arr = (ctypes.c_int32 * max(1, len(band)))(*[int(b) for b in band])
+    run, tot = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().fftconv_sparse_query(N, dtype, order, arr, len(band), ctypes.byref(run), ctypes.byref(tot)),
+           "fftconv_sparse_query")
+    return {"pairs_run": run.value, "pairs_total": tot.value}
+
+
 def _dtype_code(torch_dtype) -> int:
     import torch
     if torch_dtype == torch.float16:
@@ -128,18 +145,32 @@ def _stream(stream) -> Optional[int]:
 class Plan:
     """A plan for one sequence length N and dtype (torch.float16 / bfloat16)."""
 
-    def __init__(self, N: int, dtype, order: int = 0):
+    def __init__(self, N: int, dtype, order: int = 0, band=None):
+        """band: one int per factor (outer first) for a frequency-sparse plan;
+        None for the dense convolution."""
         self.N = int(N)
         self.torch_dtype = dtype
         self.dtype = _dtype_code(dtype)
         h = ctypes.c_void_p()
-        _check(lib().fftconv_plan_create(ctypes.byref(h), self.N, self.dtype, order), "fftconv_plan_create")
+        if band is None:
+            _check(lib().fftconv_plan_create(ctypes.byref(h), self.N, self.dtype, order), "fftconv_plan_create")
+        else:
+            arr = (ctypes.c_int32 * max(1, len(band)))(*[int(b) for b in band])
+            _check(lib().fftconv_plan_create_sparse(ctypes.byref(h), self.N, self.dtype, order, arr, len(band)),
+                   "fftconv_plan_create_sparse")
         self._h = h
         info = PlanInfo()
         _check(lib().fftconv_plan_get_info(self._h, ctypes.byref(info)), "fftconv_plan_get_info")
         self.info = info.as_dict()
         self._workspace = None
         self._host_scratch = None
+
+    def band(self) -> dict:
+        """The plan's band per factor and the pass-B pairs that run / exist."""
+        b = (ctypes.c_int32 * 8)()
+        run, tot = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().fftconv_plan_get_band(self._h, b, ctypes.byref(run), ctypes.byref(tot)), "fftconv_plan_get_band")
+        return {"band": list(b[: self.info["order"]]), "pairs_run": run.value, "pairs_total": tot.value}
 
     def close(self):
         if getattr(self, "_h", None):

@@ -393,24 +393,95 @@ cudaError_t launch_multipass(const fftconv_plan_s* p, const void* u, const void*
                              const void* kf, void* y, void* T, int64_t B, int64_t H, cudaStream_t st) {
     MPArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
                 static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
-                static_cast<uint32_t*>(T), int(B), int(H), p->R0, p->mp, p->dev_err};
+                static_cast<uint32_t*>(T), int(B), int(H), p->R0, p->mp, p->dev_err,
+                p->zbits, 1, p->pairs_run, p->plist};
     const bool gated = wi != nullptr;
+    if (p->zbits) {  // frequency-sparse plan with pairs of sub-rows to skip
+        if (p->mp2) return launch_mp_l4k_2level_sparse(p, args, B * H, gated, st);
+        return p->mpL == kMpLtc ? launch_mp_l4k_sparse(p, args, B * H, gated, st)
+                                : launch_mp_l16k_sparse(p, args, B * H, gated, st);
+    }
     if (p->mp2) return launch_mp_l4k_2level(p, args, B * H, gated, st);
     return p->mpL == kMpLtc ? launch_mp_l4k(p, args, B * H, gated, st) : launch_mp_l16k(p, args, B * H, gated, st);
 }
 
 }  // namespace
 
-extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype,
-                                                int order) {
+namespace {
+
+// Frequency-sparse skipping on the multi-pass path.  Sub-row k0 of pass B
+// holds the bins whose leading digits (r_1, or r_1 + RA r_2 for a two-level
+// outer factor) make up k0; it is all zero when one of those digits is out of
+// its band or an inner axis keeps nothing.  Pass B's pair (k0, R0 - k0) (pair
+// 0: sub-rows 0 and R0/2) is skipped when both of its sub-rows are; then no
+// pass reads or writes its sub-rows.  Outputs: the pairs that run, and the
+// dead bits per sub-row ([RA][2] words for two levels, [1][2] otherwise).
+struct SparseTables {
+    std::vector<uint16_t> plist;
+    std::vector<unsigned long long> zbits;
+    bool any_skipped = false;
+};
+
+SparseTables sparse_tables(const fftconv_plan_info_t& info, const int32_t* band, int R0, bool two_level) {
+    const int nlead = two_level ? 2 : 1;
+    bool inner_empty = false;
+    for (int j = nlead; j < info.order; ++j) inner_empty |= band[j] == 0;
+    auto out_of_band = [&](int d, int j) {
+        const int Mj = info.factors[j];
+        return std::min(d, Mj - d) >= band[j];
+    };
+    std::vector<char> zero_sub(size_t(R0), 0);
+    for (int k0 = 0; k0 < R0; ++k0) {
+        bool z = inner_empty;
+        if (two_level) {
+            const int RA = info.factors[0];
+            z |= out_of_band(k0 % RA, 0) || out_of_band(k0 / RA, 1);
+        } else {
+            z |= out_of_band(k0, 0);
+        }
+        zero_sub[size_t(k0)] = z;
+    }
+    SparseTables t;
+    std::vector<char> dead(size_t(R0), 0);
+    for (int pr = 0; pr < R0 / 2; ++pr) {
+        const int a = pr, b = pr ? R0 - pr : R0 / 2;
+        if (zero_sub[size_t(a)] && zero_sub[size_t(b)]) {
+            dead[size_t(a)] = dead[size_t(b)] = 1;
+            t.any_skipped = true;
+        } else {
+            t.plist.push_back(uint16_t(pr));
+        }
+    }
+    const int groups = two_level ? info.factors[0] : 1;
+    t.zbits.assign(size_t(groups) * 2, 0ull);
+    for (int k0 = 0; k0 < R0; ++k0) {
+        if (!dead[size_t(k0)]) continue;
+        const int g = two_level ? k0 % groups : 0, bit = two_level ? k0 / groups : k0;  // bit < 128
+        t.zbits[size_t(g) * 2 + size_t(bit >> 6)] |= 1ull << (bit & 63);
+    }
+    return t;
+}
+
+fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype, int order,
+                                  const int32_t* band, int nband) {
     if (!out) return FFTCONV_ERR_INVALID;
     *out = nullptr;
     fftconv_plan_info_t info;
     fftconv_status_t st = fftconv_plan_query(N, dtype, order, &info);
     if (st != FFTCONV_OK) return st;
+    if (band) {
+        if (nband != info.order) return FFTCONV_ERR_INVALID;
+        for (int j = 0; j < nband; ++j)
+            if (band[j] < 0) return FFTCONV_ERR_INVALID;
+    }
     fftconv_plan_s* p = new (std::nothrow) fftconv_plan_s();
     if (!p) return FFTCONV_ERR_ALLOC;
     p->info = info;
+    for (int j = 0; j < info.order; ++j) {
+        const int32_t full = info.factors[j] / 2 + 1;  // keeps every digit value
+        p->band[j] = band ? std::min(band[j], full) : full;
+        p->sparse |= p->band[j] < full;
+    }
     p->R1 = info.factors[0];
     const bool multi = info.path == FFTCONV_PATH_MULTIPASS;
     p->R0 = multi ? info.factors[0] : 1;
@@ -441,6 +512,18 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
         o_ofa = append(blob, T0.of);
         o_oic = append(blob, T0.oi);
         o_ofull = append(blob, ofull);
+    }
+    SparseTables sp;
+    size_t o_plist = 0, o_zbits = 0;
+    p->pairs_run = multi ? p->R0 / 2 : 0;
+    if (multi && p->sparse) {
+        sp = sparse_tables(info, p->band, p->R0, p->mp2);
+        if (sp.any_skipped) {
+            p->pairs_run = int(sp.plist.size());
+            if (sp.plist.empty()) sp.plist.push_back(0);  // nothing runs; keep the table non-empty
+            o_plist = append(blob, sp.plist);
+            o_zbits = append(blob, sp.zbits);
+        }
     }
     blob.resize((blob.size() + 255) & ~size_t(255));
     if (cudaMalloc(&p->dev, blob.size()) != cudaSuccess) {
@@ -483,7 +566,61 @@ extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, 
         p->mp.twf = reinterpret_cast<const float4*>(d + o_twf);
         p->mp.twi = reinterpret_cast<const float4*>(d + o_twi);
     }
+    if (sp.any_skipped) {
+        p->plist = reinterpret_cast<const uint16_t*>(d + o_plist);
+        p->zbits = reinterpret_cast<const unsigned long long*>(d + o_zbits);
+    }
     *out = p;
+    return FFTCONV_OK;
+}
+
+}  // namespace
+
+extern "C" fftconv_status_t fftconv_plan_create(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype,
+                                                int order) {
+    return plan_create_impl(out, N, dtype, order, nullptr, 0);
+}
+
+extern "C" fftconv_status_t fftconv_plan_create_sparse(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype,
+                                                       int order, const int32_t* band, int nband) {
+    if (!band) return FFTCONV_ERR_INVALID;
+    return plan_create_impl(out, N, dtype, order, band, nband);
+}
+
+extern "C" fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtype, int order, const int32_t* band,
+                                                 int nband, int32_t* pairs_run, int32_t* pairs_total) {
+    fftconv_plan_info_t info;
+    fftconv_status_t st = fftconv_plan_query(N, dtype, order, &info);
+    if (st != FFTCONV_OK) return st;
+    if (!band || nband != info.order) return FFTCONV_ERR_INVALID;
+    int32_t b[8] = {};
+    bool sparse = false;
+    for (int j = 0; j < nband; ++j) {
+        if (band[j] < 0) return FFTCONV_ERR_INVALID;
+        const int32_t full = info.factors[j] / 2 + 1;
+        b[j] = std::min(band[j], full);
+        sparse |= b[j] < full;
+    }
+    int run = 0, total = 0;
+    if (info.path == FFTCONV_PATH_MULTIPASS) {
+        const bool two_level = info.order == 4 && info.factors[3] == 64;
+        const int R0 = two_level ? info.factors[0] * 64 : info.factors[0];
+        total = run = R0 / 2;
+        if (sparse) run = int(sparse_tables(info, b, R0, two_level).plist.size());
+    }
+    if (pairs_run) *pairs_run = run;
+    if (pairs_total) *pairs_total = total;
+    return FFTCONV_OK;
+}
+
+extern "C" fftconv_status_t fftconv_plan_get_band(fftconv_plan_t plan, int32_t* band, int32_t* pairs_run,
+                                                  int32_t* pairs_total) {
+    if (!plan) return FFTCONV_ERR_INVALID;
+    if (band)
+        for (int j = 0; j < 8; ++j) band[j] = j < plan->info.order ? plan->band[j] : 0;
+    const bool multi = plan->info.path == FFTCONV_PATH_MULTIPASS;
+    if (pairs_run) *pairs_run = multi ? plan->pairs_run : 0;
+    if (pairs_total) *pairs_total = multi ? plan->R0 / 2 : 0;
     return FFTCONV_OK;
 }
 
@@ -770,6 +907,33 @@ int grid_for(int64_t work) {
 
 namespace {
 
+// The band pattern of a frequency-sparse plan (factors outer first).
+struct BandSpec {
+    int n;
+    int f[4];
+    int b[4];
+};
+
+// Zero the bins f = 0..M of every channel's 2M-point spectrum that the band
+// pattern drops: r = f mod M in mixed radix over the factors (outer digit
+// first) keeps bin f when min(r_j, M_j - r_j) < band_j for every j.  Only
+// these bins feed the decimation fold.
+__global__ void kfft_band(float2* __restrict__ K, int64_t H, int64_t M, BandSpec bs) {
+    const int64_t bins = M + 1;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * bins;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t h = i / bins, f = i % bins;
+        int64_t r = f & (M - 1);
+        bool keep = true;
+        for (int j = 0; j < bs.n; ++j) {
+            const int d = int(r % bs.f[j]);
+            r /= bs.f[j];
+            keep &= min(d, bs.f[j] - d) < bs.b[j];
+        }
+        if (!keep) K[h * 2 * M + f] = make_float2(0.f, 0.f);
+    }
+}
+
 // conj of every spectrum value (the adjoint k_f: correlation instead of convolution)
 __global__ void kfft_conj(float2* __restrict__ x, int64_t n) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
@@ -813,6 +977,14 @@ fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f,
     kfft_init<<<grid_for(H * L), 256, 0, st>>>(k, a, H, N);
     a = fft_rows(a, b, H, L, st);
     if (adjoint) kfft_conj<<<grid_for(H * L), 256, 0, st>>>(a, H * L);
+    if (plan->sparse) {
+        BandSpec bs{plan->info.order, {1, 1, 1, 1}, {1, 1, 1, 1}};
+        for (int j = 0; j < plan->info.order && j < 4; ++j) {
+            bs.f[j] = plan->info.factors[j];
+            bs.b[j] = plan->band[j];
+        }
+        kfft_band<<<grid_for(H * (N + 1)), 256, 0, st>>>(a, H, N, bs);
+    }
     if (plan->tc64)
         kfft_finalize_tc64<<<grid_for(H * 9 * 4 * 2 * 32), 256, 0, st>>>(a, static_cast<uint4*>(k_f), H,
                                                                            plan->info.dtype);
@@ -1119,6 +1291,7 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
                                                 const void* w_out, float* dk, int64_t B, int64_t H, void* scratch,
                                                 size_t scratch_bytes, fftconv_stream_t stream) {
     if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (plan->sparse) return FFTCONV_ERR_UNSUPPORTED;  // the kernel gradient is not band-limited here
     if (H == 0) return FFTCONV_OK;
     if (!dk || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
     const int64_t N = plan->info.N, L = 2 * N;
@@ -1274,6 +1447,7 @@ fftconv_status_t windowed_forward(fftconv_plan_t plan, const void* u, const void
                                   const void* k_f, void* y, int64_t B, int64_t H, int64_t N, void* scratch,
                                   size_t scratch_bytes, fftconv_stream_t stream, bool wrap) {
     if (!plan || B < 0 || H < 0 || N < 0) return FFTCONV_ERR_INVALID;
+    if (plan->sparse) return FFTCONV_ERR_UNSUPPORTED;  // windows of a band-limited kernel are not defined here
     if (B == 0 || H == 0 || N == 0) return FFTCONV_OK;
     if (!u || !k_f || !y || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
     const bool gated = w_in != nullptr;

@@ -1,110 +1,15 @@
-// Multi-pass launches with sub-rows of 4096 points (pass B on the
-// fifth-generation tensor cores, tcpass.cuh).
-#include "plan.h"
-#include "tcpass.cuh"
+// Multi-pass launches with sub-rows of 4096 points, dense plans.
+#include "mp_l4k.cuh"
 
 namespace fftconv {
-namespace {
 
-template <int DT, int R0, bool G>
-cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    constexpr int HALF = R0 / 2, L = kMpLtc;
-    const size_t smem_a = mp_pass_a_smem<R0, G>(), smem_c = mp_pass_c_smem<R0, G>();
-    static int na = 0, nb = 0, nc = 0;
-    cudaError_t e;
-    if ((e = prep_kernel(mp_pass_a<DT, R0, G, L>, smem_a, 256, &na)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_b_tc<DT>, TcB::SMEM, TcB::THREADS, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true>, smem_c, 32 * mp_pass_c_warps<R0>(), &nc)) != cudaSuccess) return e;
-    const int64_t items_ac = rows * (L / mp_tile<R0>());
-    auto grid = [&](int64_t items, int per_sm) {
-        int64_t gsz = int64_t(p->num_sms) * per_sm;
-        return unsigned(gsz < items ? gsz : items);
-    };
-    // pass B: one CTA per SM (its tensor-memory allocation takes all 512
-    // columns), two item pipelines per CTA
-    const int64_t items_b = rows * (R0 / 2), need_b = (items_b + 1) / 2;
-    if (items_b >= (int64_t(1) << 30)) return cudaErrorInvalidValue;  // pass B counts items in int
-    const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);
-    TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, 0};
-    mp_pass_a<DT, R0, G, L><<<grid(items_ac, na), 256, smem_a, st>>>(args);
-    mp_pass_b_tc<DT><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
-    mp_pass_c<DT, R0, G, L, true><<<grid(items_ac, nc), 32 * mp_pass_c_warps<R0>(), smem_c, st>>>(args);
-    return cudaGetLastError();
+cudaError_t launch_mp_l4k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st) {
+    return launch_l4k<false>(p, args, rows, gated, st);
 }
-
-template <int DT, bool G>
-cudaError_t launch_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    switch (p->R0) {
-        case 8: return launch_t<DT, 8, G>(p, args, rows, st);
-        case 16: return launch_t<DT, 16, G>(p, args, rows, st);
-        case 32: return launch_t<DT, 32, G>(p, args, rows, st);
-        case 64: return launch_t<DT, 64, G>(p, args, rows, st);
-        case 128: return launch_t<DT, 128, G>(p, args, rows, st);
-    }
-    return cudaErrorInvalidValue;
-}
-
-// Two-level outer factor R0 = RA * 64 (N = RA * 64 * 64 * 64): pass A over RA
-// sub-blocks of L1 = N / RA, the inner 64-point stage in place (all inputs),
-// pass B on sub-rows of 4096 (sub-row k0 = a + RA k at position 64 a + k),
-// the inner inverse stage in place (all outputs), the last pass over RA.
-template <int DT, int RA, bool G>
-cudaError_t launch_2l_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    constexpr int L = kMpLtc, L1 = 64 * L, R0 = RA * 64;  // N = RA * L1
-    const size_t smem_a1 = mp_pass_a_smem<RA, G>(), smem_c1 = mp_pass_c_smem<RA, G>();
-    const size_t smem_a2 = mp_pass_a_smem<64, false, true>(), smem_c2 = mp_pass_c_smem<64, false>();
-    static int na1 = 0, na2 = 0, nb = 0, nc2 = 0, nc1 = 0;
-    cudaError_t e;
-    if ((e = prep_kernel(mp_pass_a<DT, RA, G, L1>, smem_a1, 256, &na1)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_a<DT, 64, false, L, true>, smem_a2, 256, &na2)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_b_tc<DT>, TcB::SMEM, TcB::THREADS, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, 64, false, L, true, true>, smem_c2, 32 * mp_pass_c_warps<64>(), &nc2)) !=
-        cudaSuccess)
-        return e;
-    if ((e = prep_kernel(mp_pass_c<DT, RA, G, L1, true>, smem_c1, 32 * mp_pass_c_warps<RA>(), &nc1)) != cudaSuccess)
-        return e;
-    auto grid = [&](int64_t items, int per_sm) {
-        int64_t gsz = int64_t(p->num_sms) * per_sm;
-        return unsigned(gsz < items ? gsz : items);
-    };
-    const int64_t items1 = rows * (L1 / mp_tile<RA>()), items2 = rows * RA * (L / mp_tile<64>());
-    const int64_t items_b = rows * (R0 / 2), need_b = (items_b + 1) / 2;
-    if (items_b >= (int64_t(1) << 30) || rows * RA >= (int64_t(1) << 30)) return cudaErrorInvalidValue;
-    const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);
-    MPArgs inner = args;  // the RA sub-blocks of every row as rows of length 64 * 4096
-    inner.B = args.B * RA;
-    inner.w_in = inner.w_out = nullptr;
-    TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, RA};
-    mp_pass_a<DT, RA, G, L1><<<grid(items1, na1), 256, smem_a1, st>>>(args);
-    mp_pass_a<DT, 64, false, L, true><<<grid(items2, na2), 256, smem_a2, st>>>(inner);
-    mp_pass_b_tc<DT><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
-    mp_pass_c<DT, 64, false, L, true, true><<<grid(items2, nc2), 32 * mp_pass_c_warps<64>(), smem_c2, st>>>(inner);
-    mp_pass_c<DT, RA, G, L1, true><<<grid(items1, nc1), 32 * mp_pass_c_warps<RA>(), smem_c1, st>>>(args);
-    return cudaGetLastError();
-}
-
-template <int DT, bool G>
-cudaError_t launch_2l_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    switch (p->R0 / 64) {
-        case 4: return launch_2l_t<DT, 4, G>(p, args, rows, st);
-        case 8: return launch_2l_t<DT, 8, G>(p, args, rows, st);
-    }
-    return cudaErrorInvalidValue;
-}
-
-}  // namespace
 
 cudaError_t launch_mp_l4k_2level(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
                                  cudaStream_t st) {
-    if (p->info.dtype == FFTCONV_F16)
-        return gated ? launch_2l_r<0, true>(p, args, rows, st) : launch_2l_r<0, false>(p, args, rows, st);
-    return gated ? launch_2l_r<1, true>(p, args, rows, st) : launch_2l_r<1, false>(p, args, rows, st);
-}
-
-cudaError_t launch_mp_l4k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st) {
-    if (p->info.dtype == FFTCONV_F16)
-        return gated ? launch_r<0, true>(p, args, rows, st) : launch_r<0, false>(p, args, rows, st);
-    return gated ? launch_r<1, true>(p, args, rows, st) : launch_r<1, false>(p, args, rows, st);
+    return launch_l4k_2level<false>(p, args, rows, gated, st);
 }
 
 }  // namespace fftconv

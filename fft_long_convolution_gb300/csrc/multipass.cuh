@@ -52,7 +52,19 @@ struct MPArgs {
     int B, H, R0;
     MPTables tb;
     int* err;
+    // frequency-sparse plans: sub-rows whose pair of pass B is skipped (bit k0
+    // of [row % zmod][2], k0 < 128) are not written by pass A and read as
+    // zeros by pass C; pass B runs only the np pairs listed in plist
+    const unsigned long long* zbits = nullptr;  // null: every sub-row is live
+    int zmod = 1;
+    int np = 0;                                 // pass-B pairs that run (R0 / 2 when plist is null)
+    const uint16_t* plist = nullptr;
 };
+
+// Bit k0 (< 128) of a dead-sub-row pair of words.
+__device__ __forceinline__ bool zbit(unsigned long long z0, unsigned long long z1, int k0) {
+    return ((k0 < 64 ? z0 >> k0 : z1 >> (k0 - 64)) & 1ull) != 0;
+}
 
 // W_M^j for M a power of two (exact angle: j / M is exact in float).
 __device__ __forceinline__ cpx twiddle_pow2(uint32_t j, uint32_t M) {
@@ -95,7 +107,8 @@ constexpr size_t mp_pass_c_smem() {
 // FULL: an inner outer stage of a two-level outer factor: all R0 input rows
 // are nonzero and come from T itself (16-bit complex words, rows of length
 // R0*L), the result overwrites them (each item stages its whole tile first).
-template <int DT, int R0, bool GATED, int L, bool FULL = false>
+// SP: frequency-sparse plan: outputs of dead sub-rows (a.zbits) are not stored.
+template <int DT, int R0, bool GATED, int L, bool FULL = false, bool SP = false>
 __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(const MPArgs a) {
     using O = Op<DT>;
     static_assert(!(FULL && GATED), "the inner stage has no gates");
@@ -109,6 +122,7 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
     uint32_t* sw = su + HALF * SEG;                     // gated: w_in
     uint64_t* bar = reinterpret_cast<uint64_t*>(sw + (GATED ? HALF * SEG : 0));
     __shared__ int s_fail;
+    __shared__ unsigned long long s_z[2];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const long rows = long(a.B) * a.H, tiles = L / TILE, items = rows * tiles;
     if (threadIdx.x == 0) {
@@ -132,8 +146,22 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
                 if (GATED) bulk_g2s(sw + n0 * SEG, a.w_in + row * long(M) + 2 * (long(L) * n0 + o_base), TILE * 4, bar);
             }
         }
+        if constexpr (SP) {
+            if (threadIdx.x == 32) {  // outputs k0 that nothing reads
+                s_z[0] = a.zbits ? __ldg(a.zbits + 2 * (row % a.zmod)) : 0ull;
+                s_z[1] = a.zbits ? __ldg(a.zbits + 2 * (row % a.zmod) + 1) : 0ull;
+            }
+        }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
         uint32_t* Trow = a.T + row * long(M);
+        uint32_t lm = 0;  // SP: bit m set when this thread's output k0 = 8m + g exists and is read later
+        if constexpr (SP) {
+            #pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const int k0 = 8 * m + g;
+                if (k0 < R0 && !((s_z[k0 >> 6] >> (k0 & 63)) & 1ull)) lm |= 1u << m;
+            }
+        }
         // NT column groups of 8 per iteration share each DFT fragment load; the
         // twiddle of output (k0 = 8m + g, o) is W_M^(o g) * W_M^(8 o)^m, a
         // product chain over the output tiles m
@@ -185,10 +213,13 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
                         }
                     }
                 }
+                // SP: outputs that nothing reads are not stored (their HBM writes
+                // are the saving; the contraction itself stays branch free)
                 const uint32_t k0 = uint32_t(8 * m + g);
+                const bool live = SP ? ((lm >> m) & 1u) != 0 : k0 < uint32_t(R0);
                 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    if (k0 < uint32_t(R0)) {
+                    if (live) {
                         const uint32_t o = uint32_t(o_base + 8 * (warp + 8 * (NT * i + j)) + 2 * t);
                         const cpx v0 = cmul({acc[j][0], acc[j][2]}, tw[j][0]);
                         const cpx v1 = cmul({acc[j][1], acc[j][3]}, tw[j][1]);
@@ -216,7 +247,8 @@ __host__ __device__ constexpr int mp_pass_c_warps() { return R0 >= 128 ? 16 : 8;
 // W_M^(n' t) * W_M^(8 n')^s (and * W_M^(4 n')) for k0 = 8s + t (+ 4).
 // TOT: an inner outer stage of a two-level outer factor: all R0 outputs,
 // neither conjugated nor gated, written back over the staged tile of T.
-template <int DT, int R0, bool GATED, int L, bool TWID, bool TOT = false>
+// SP: frequency-sparse plan: dead sub-rows (a.zbits) are zeros, not loaded.
+template <int DT, int R0, bool GATED, int L, bool TWID, bool TOT = false, bool SP = false>
 __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT) ? 3 : (R0 <= 64 ? 2 : 1))
     mp_pass_c(const MPArgs a) {
     using O = Op<DT>;
@@ -241,18 +273,48 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
     }
     __syncthreads();
     uint32_t par = 0;
+    __shared__ unsigned long long s_z[2], s_zs[2];  // SP: dead sub-rows of this item; staged ones holding zeros
+    if (SP && threadIdx.x == 0) s_zs[0] = s_zs[1] = 0ull;
     for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
         const long row = item / tiles;
         const int o_base = int(item % tiles) * TILE;
         if (threadIdx.x == 0) {
-            mbar_expect_tx(bar, (R0 + (GATED ? HALF : 0)) * TILE * 4u);
-            for (int k0 = 0; k0 < R0; ++k0)
-                bulk_g2s(st + k0 * SEG, a.T + row * M + long(k0) * L + o_base, TILE * 4, bar);
+            if constexpr (!SP) {
+                mbar_expect_tx(bar, (R0 + (GATED ? HALF : 0)) * TILE * 4u);
+                for (int k0 = 0; k0 < R0; ++k0)
+                    bulk_g2s(st + k0 * SEG, a.T + row * M + long(k0) * L + o_base, TILE * 4, bar);
+            } else {  // dead sub-rows are zeros, not loaded
+                const unsigned long long z0 = a.zbits ? __ldg(a.zbits + 2 * (row % a.zmod)) : 0ull;
+                const unsigned long long z1 = a.zbits ? __ldg(a.zbits + 2 * (row % a.zmod) + 1) : 0ull;
+                s_z[0] = z0;
+                s_z[1] = z1;
+                const int live = R0 - __popcll(z0) - __popcll(z1);  // bits exist for k0 < R0 only
+                mbar_expect_tx(bar, (live + (GATED ? HALF : 0)) * TILE * 4u);
+                for (int k0 = 0; k0 < R0; ++k0)
+                    if (!zbit(z0, z1, k0))
+                        bulk_g2s(st + k0 * SEG, a.T + row * M + long(k0) * L + o_base, TILE * 4, bar);
+            }
             if (GATED)
                 for (int n0 = 0; n0 < HALF; ++n0)
                     bulk_g2s(swo + n0 * SEG, a.w_out + row * M + 2 * (long(L) * n0 + o_base), TILE * 4, bar);
         }
+        if constexpr (SP) {  // newly dead sub-rows: clear their staged segments
+            __syncthreads();
+            const unsigned long long n0 = s_z[0] & ~s_zs[0], n1 = s_z[1] & ~s_zs[1];
+            if (n0 | n1) {
+                for (int k0 = 0; k0 < R0; ++k0)
+                    if (zbit(n0, n1, k0))
+                        for (int c = threadIdx.x; c < TILE / 4; c += blockDim.x)
+                            reinterpret_cast<uint4*>(st + k0 * SEG)[c] = make_uint4(0u, 0u, 0u, 0u);
+                // the cleared segments may be bulk-copy targets of a later item
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+        }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
+        if (SP && threadIdx.x == 0) {  // every live sub-row was overwritten by this item's copies
+            s_zs[0] = s_z[0];
+            s_zs[1] = s_z[1];
+        }
         // NT column groups of 8 per iteration share each DFT fragment load
         constexpr int NT = KS <= 8 ? 2 : 1, NW = mp_pass_c_warps<R0>();
         #pragma unroll 1
@@ -341,7 +403,8 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
 constexpr size_t kMpBFrag = size_t(8) * 8 * 32 * 16;  // F_64/8 A fragments, resident in shared memory
 constexpr size_t kMpBSmem = size_t(2) * kMpR1 * kSeg * 4 + 256 * 8 + kMpBFrag + 32;
 
-template <int DT>
+// SP: frequency-sparse plan: only the a.np pairs listed in a.plist run.
+template <int DT, bool SP = false>
 __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
     using O = Op<DT>;
     constexpr int L = kMpL, R1 = kMpR1, SEG = kSeg;
@@ -354,7 +417,7 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const int R0 = a.R0;
     const uint32_t M = uint32_t(R0) * L;
-    const long rows = long(a.B) * a.H, pairs = R0 / 2, items = rows * pairs;
+    const long rows = long(a.B) * a.H, np = SP ? a.np : R0 / 2, items = rows * np;
     if (threadIdx.x == 0) {
         s_fail = 0;
         mbar_init(bar, 1);
@@ -372,8 +435,8 @@ __global__ void __launch_bounds__(512, 1) mp_pass_b(const MPArgs a) {
         // items channel-major with b fastest: the B rows of one channel use the
         // same k_f sub-rows at about the same time, so k_f is read from HBM once
         const long b = item % a.B, hp = item / a.B;
-        const int p = int(hp % pairs);
-        const long h = hp / pairs, row = b * a.H + h;
+        const int p = SP ? int(__ldg(a.plist + hp % np)) : int(hp % np);
+        const long h = hp / np, row = b * a.H + h;
         const int k0s[2] = {p == 0 ? 0 : p, p == 0 ? R0 / 2 : R0 - p};
         uint32_t* Trow = a.T + row * long(M);
         if (threadIdx.x == 0) {

@@ -21,6 +21,14 @@ struct fftconv_plan_s {
     bool mp2 = false;  // sub-rows of 4096 with the outer factor R0 = RA * 64 in two levels (N >= 2^20)
     bool tc64 = false;               // N = 4096: order-2 64 x 64 product on tcgen05
     const uint32_t* fmat = nullptr;  // the 64 x 64 DFT matrix rows (device), N = 4096 and mpL = 4096
+    // frequency-sparse plan: a band per factor (every band >= M_j/2 + 1 on a
+    // dense plan); on the multi-pass path the pass-B pairs that run and the
+    // dead sub-rows of passes A and C (device tables inside dev)
+    bool sparse = false;
+    int32_t band[8] = {};
+    int pairs_run = 0;                          // = R0 / 2 when nothing is skipped
+    const uint16_t* plist = nullptr;            // [pairs_run]; null: every pair runs
+    const unsigned long long* zbits = nullptr;  // [RA or 1][2] bit k0: sub-row k0 is dead; null: none
     int num_sms = 0;
     void* workspace = nullptr;
     size_t workspace_bytes = 0;
@@ -38,6 +46,13 @@ cudaError_t launch_mp_l16k(const fftconv_plan_s* p, const MPArgs& args, int64_t 
 cudaError_t launch_mp_l4k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st);
 cudaError_t launch_mp_l4k_2level(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
                                  cudaStream_t st);
+// The same for frequency-sparse plans (p->zbits and p->plist set).
+cudaError_t launch_mp_l16k_sparse(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
+                                  cudaStream_t st);
+cudaError_t launch_mp_l4k_sparse(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
+                                 cudaStream_t st);
+cudaError_t launch_mp_l4k_2level_sparse(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
+                                        cudaStream_t st);
 
 // Dynamic shared memory opt-in and resident blocks per SM of a kernel (once).
 template <typename K>

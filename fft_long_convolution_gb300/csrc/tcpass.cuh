@@ -44,6 +44,8 @@ struct TcBArgs {
     int* err;
     int RA;                 // 0: sub-row k0 at position k0; else (two-level outer factor R0 = RA * 64)
                             // at position (k0 mod RA) * 64 + k0 / RA
+    int np;                 // pairs that run (frequency-sparse plans skip pairs whose bins are all zero)
+    const uint16_t* plist;  // [np] pair indices; null: all R0 / 2 pairs
 };
 
 struct TcB {
@@ -74,7 +76,8 @@ struct TcB {
 static_assert(TcB::SMEM <= 232448, "shared memory");
 static_assert(TcB::BBUF >= 16 * TcB::SBO1, "B1 fits");
 
-template <int DT>
+// SP: frequency-sparse plan: only the a.np pairs listed in a.plist run.
+template <int DT, bool SP = false>
 __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a) {
     using O = Op<DT>;
     using C = TcB;
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
     // items (row b*H + h, pair p): b fastest, then p, then h (the B rows of a
     // pair use the same k_f back to back); contiguous ranges per pipeline
     const int pairs = a.R0 >> 1;
-    const int items = a.B * a.H * pairs;  // the host guarantees < 2^30
+    const int items = a.B * a.H * (SP ? a.np : pairs);  // the host guarantees < 2^30
     const int V = int(gridDim.x) * 2, v = int(blockIdx.x) * 2 + g;
     const int i0 = int(int64_t(v) * items / V), i1 = int(int64_t(v + 1) * items / V);
     const size_t M = size_t(a.R0) * C::L;
@@ -105,7 +108,18 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
     };
     auto pos = [&](int k0) -> size_t { return a.RA ? size_t(k0 % a.RA) * 64 + size_t(k0 / a.RA) : size_t(k0); };
     auto decode = [&](int it) -> Item {
-        const int b = it % a.B, hp = it / a.B, p = hp % pairs, h = hp / pairs;
+        int b, p, h;
+        if constexpr (SP) {
+            b = it % a.B;
+            const int hp = it / a.B;
+            p = int(__ldg(a.plist + hp % a.np));
+            h = hp / a.np;
+        } else {
+            b = it % a.B;
+            const int hp = it / a.B;
+            p = hp % pairs;
+            h = hp / pairs;
+        }
         uint32_t* Trow = a.T + (size_t(b) * a.H + h) * M;
         return {p, h, Trow + pos(p) * C::L, Trow + pos(p ? a.R0 - p : pairs) * C::L};
     };

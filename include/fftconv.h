@@ -107,6 +107,57 @@ fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype, int order,
 fftconv_status_t fftconv_plan_create(fftconv_plan_t *out, int64_t N, fftconv_dtype_t dtype,
                                      int order);
 
+/*
+ * Frequency-sparse plan (FlashFFTConv page, "Architectural Extensions:
+ * Partial and Frequency-Sparse Convolutions", frequency-sparse part: parts
+ * of k_f set to zero in a pattern that follows the decomposition, so whole
+ * blocks of work can be skipped).  As fftconv_plan_create, plus one band per
+ * factor: band[0..nband-1], nband = the plan's order (query it first when
+ * order = 0), outer factor first, each band >= 0.
+ *
+ * Pattern: the frequency index r = f mod N of spectrum bin f (0 <= f <= N of
+ * the 2N-point spectrum of the real kernel) is written in mixed radix over
+ * the factors, r = r_1 + M_1 r_2 + M_1 M_2 r_3 + ...; bin f is kept when
+ * min(r_j, M_j - r_j) < band[j] for every j and set to zero otherwise (band
+ * M_j/2 + 1 or more keeps axis j whole; band 0 drops every bin).  The forward
+ * of such a plan computes
+ *   y = first N outputs of IDFT_2N(DFT_2N(u0) . DFT_2N(k0) . m)
+ * with m the 0/1 pattern on bins 0..N, mirrored to 2N - f (gated forms as
+ * usual).  fftconv_kernel_fft and fftconv_kernel_fft_adjoint of the plan
+ * zero the dropped bins of k_f; k_f is valid only for a plan with the same N,
+ * dtype, order and band.
+ *
+ * Work skipped (multi-pass path): sub-row k0 of the inner transforms holds
+ * the bins whose leading digits form k0; a pair of sub-rows (k0, R0 - k0)
+ * whose bins are all dropped is not transformed, the first pass does not
+ * write it and the last pass reads zeros in its place.  The fused paths
+ * (N <= 16384) apply the pattern through k_f only.
+ *
+ * fftconv_backward_dk and the partial and circular forwards return
+ * UNSUPPORTED for a sparse plan.  Returns OK, INVALID (band NULL, nband not
+ * the order, a negative band), UNSUPPORTED, ALLOC or CUDA.
+ */
+fftconv_status_t fftconv_plan_create_sparse(fftconv_plan_t *out, int64_t N, fftconv_dtype_t dtype,
+                                            int order, const int32_t *band, int nband);
+
+/*
+ * Without touching the GPU: the pairs of sub-rows that a sparse plan with
+ * these arguments would transform (*pairs_run) out of *pairs_total on the
+ * multi-pass path (both 0 on the fused path).  Arguments as
+ * fftconv_plan_create_sparse.  Returns OK, INVALID or UNSUPPORTED.
+ */
+fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtype, int order, const int32_t *band,
+                                      int nband, int32_t *pairs_run, int32_t *pairs_total);
+
+/*
+ * The plan's bands (band[0..order-1]; band[order..7] = 0; a dense plan
+ * reports M_j/2 + 1 for every axis) and, on the multi-pass path, the pairs of
+ * sub-rows the inner pass transforms (*pairs_run) out of *pairs_total (both 0
+ * on the fused path).  Any output pointer may be NULL.  Returns OK or INVALID.
+ */
+fftconv_status_t fftconv_plan_get_band(fftconv_plan_t plan, int32_t *band, int32_t *pairs_run,
+                                       int32_t *pairs_total);
+
 /* Release a plan and its device tables (not the caller's buffers).  NULL is OK. */
 fftconv_status_t fftconv_plan_destroy(fftconv_plan_t plan);
 
