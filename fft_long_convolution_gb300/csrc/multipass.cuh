@@ -123,6 +123,12 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
     uint64_t* bar = reinterpret_cast<uint64_t*>(sw + (GATED ? HALF * SEG : 0));
     __shared__ int s_fail;
     __shared__ unsigned long long s_z[2];
+    // the DFT fragments of the outer factor, staged once per CTA in shared
+    // memory where that keeps the resident CTAs (else read through L1)
+    constexpr bool FS = MT * KS * 32 * 16 <= (GATED ? 8192 : 32768);
+    __shared__ uint4 s_frag[FS ? MT * KS * 32 : 1];
+    if (FS)
+        for (int i = threadIdx.x; i < MT * KS * 32; i += blockDim.x) s_frag[i] = frag[i];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const long rows = long(a.B) * a.H, tiles = L / TILE, items = rows * tiles;
     if (threadIdx.x == 0) {
@@ -195,14 +201,14 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
                     if (MT > 1) ts[j][e] = twiddle_pow2((8 * o) & (M - 1), M);
                 }
             }
-            #pragma unroll
+            #pragma unroll 2
             for (int m = 0; m < MT; ++m) {
                 float acc[NT][4];
                 #pragma unroll
                 for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
-                    const uint4 af = frag[(m * KS + s) * 32 + lane];
+                    const uint4 af = FS ? s_frag[(m * KS + s) * 32 + lane] : frag[(m * KS + s) * 32 + lane];
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         if (K8) {
@@ -264,6 +270,13 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
     uint32_t* swo = st + R0 * SEG;                      // gated: w_out [HALF][SEG]
     uint64_t* bar = reinterpret_cast<uint64_t*>(swo + (GATED ? HALF * SEG : 0));
     __shared__ int s_fail;
+    // the DFT fragments staged once per CTA in shared memory where that keeps
+    // the resident CTAs (the in-place stage and R0 <= 32), else read through L1
+    constexpr bool FS = (TOT || R0 <= 32) && MT * KS * 32 * 16 <= 32768;
+    constexpr int UNR = FS ? 2 : MT;  // full unroll keeps the L1 fragment loads ahead
+    __shared__ uint4 s_frag[FS ? MT * KS * 32 : 1];
+    if (FS)
+        for (int i = threadIdx.x; i < MT * KS * 32; i += blockDim.x) s_frag[i] = frag[i];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const long rows = long(a.B) * a.H, tiles = L / TILE, items = rows * tiles;
     if (threadIdx.x == 0) {
@@ -352,14 +365,14 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                     }
                 }
             }
-            #pragma unroll
+            #pragma unroll UNR
             for (int m = 0; m < MT; ++m) {
                 float acc[NT][4];
                 #pragma unroll
                 for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
-                    const uint4 af = frag[(m * KS + s) * 32 + lane];
+                    const uint4 af = FS ? s_frag[(m * KS + s) * 32 + lane] : frag[(m * KS + s) * 32 + lane];
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
                         if (K8) {
