@@ -516,7 +516,7 @@ def main():
         kern_s = (sum(kernel_ms) / len(kernel_ms)) * 1e-3
         achieved = alg["bytes"] / kern_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(w.name),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(w.name if band is None else f"{w.name}[band={','.join(map(str, band))}]"),
                 "peak_source": peaks["source"] + " hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": alg["bytes"],
                 "tensor_frac": alg["flops"] / kern_s / 1e12 / peaks["bf16_tflops"],
