@@ -160,12 +160,16 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
         }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
         uint32_t* Trow = a.T + row * long(M);
-        uint32_t lm = 0;  // SP: bit m set when this thread's output k0 = 8m + g exists and is read later
+        // SP: bit m of lm set when this thread's output k0 = 8m + g exists and
+        // is read later; bit m of lt (the same in every thread) when some
+        // output of the tile 8m .. 8m + 7 is, else the tile is not computed
+        uint32_t lm = 0, lt = 0;
         if constexpr (SP) {
             #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                const int k0 = 8 * m + g;
+                const int k0 = 8 * m + g, kc = 8 * m;
                 if (k0 < R0 && !((s_z[k0 >> 6] >> (k0 & 63)) & 1ull)) lm |= 1u << m;
+                if (((s_z[kc >> 6] >> (kc & 63)) & 0xffull) != 0xffull) lt |= 1u << m;
             }
         }
         // NT column groups of 8 per iteration share each DFT fragment load; the
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
                 for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
+                    if (SP && !((lt >> m) & 1u)) break;  // no output of this tile is stored
                     const uint4 af = FS ? s_frag[(m * KS + s) * 32 + lane] : frag[(m * KS + s) * 32 + lane];
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
@@ -253,7 +258,8 @@ __host__ __device__ constexpr int mp_pass_c_warps() { return R0 >= 128 ? 16 : 8;
 // W_M^(n' t) * W_M^(8 n')^s (and * W_M^(4 n')) for k0 = 8s + t (+ 4).
 // TOT: an inner outer stage of a two-level outer factor: all R0 outputs,
 // neither conjugated nor gated, written back over the staged tile of T.
-// SP: frequency-sparse plan: dead sub-rows (a.zbits) are zeros, not loaded.
+// SP: frequency-sparse plan: dead sub-rows (a.zbits) are not loaded and count
+// as zeros; chunks of eight dead sub-rows are skipped.
 template <int DT, int R0, bool GATED, int L, bool TWID, bool TOT = false, bool SP = false>
 __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT) ? 3 : (R0 <= 64 ? 2 : 1))
     mp_pass_c(const MPArgs a) {
@@ -279,6 +285,24 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
         for (int i = threadIdx.x; i < MT * KS * 32; i += blockDim.x) s_frag[i] = frag[i];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     const long rows = long(a.B) * a.H, tiles = L / TILE, items = rows * tiles;
+    // SP, last pass: one set of dead sub-rows for the whole launch; their
+    // staged segments are cleared once and never copied into.  SP, in-place
+    // stage: the set depends on the row's group, so dead inputs are masked
+    // per load instead.
+    constexpr bool CLR = SP && !TOT, ROWP = SP && TOT;
+    uint32_t lc_fixed = 0;  // CLR: bit s set when the chunk 8s .. 8s + 7 holds a live sub-row
+    if constexpr (CLR) {
+        const unsigned long long z0 = a.zbits ? __ldg(a.zbits) : 0ull, z1 = a.zbits ? __ldg(a.zbits + 1) : 0ull;
+        for (int k0 = 0; k0 < R0; ++k0)
+            if (zbit(z0, z1, k0))
+                for (int c = threadIdx.x; c < TILE / 4; c += blockDim.x)
+                    reinterpret_cast<uint4*>(st + k0 * SEG)[c] = make_uint4(0u, 0u, 0u, 0u);
+        #pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            const int kc = 8 * s;
+            if ((((kc < 64 ? z0 >> kc : z1 >> (kc - 64))) & 0xffull) != 0xffull) lc_fixed |= 1u << s;
+        }
+    }
     if (threadIdx.x == 0) {
         s_fail = 0;
         mbar_init(bar, 1);
@@ -286,8 +310,7 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
     }
     __syncthreads();
     uint32_t par = 0;
-    __shared__ unsigned long long s_z[2], s_zs[2];  // SP: dead sub-rows of this item; staged ones holding zeros
-    if (SP && threadIdx.x == 0) s_zs[0] = s_zs[1] = 0ull;
+    __shared__ unsigned long long s_z[2];  // ROWP: dead sub-rows of this item
     for (long item = blockIdx.x; item < items; item += gridDim.x, par ^= 1) {
         const long row = item / tiles;
         const int o_base = int(item % tiles) * TILE;
@@ -296,7 +319,7 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                 mbar_expect_tx(bar, (R0 + (GATED ? HALF : 0)) * TILE * 4u);
                 for (int k0 = 0; k0 < R0; ++k0)
                     bulk_g2s(st + k0 * SEG, a.T + row * M + long(k0) * L + o_base, TILE * 4, bar);
-            } else {  // dead sub-rows are zeros, not loaded
+            } else {  // dead sub-rows are not loaded; their inputs are taken as zeros
                 const unsigned long long z0 = a.zbits ? __ldg(a.zbits + 2 * (row % a.zmod)) : 0ull;
                 const unsigned long long z1 = a.zbits ? __ldg(a.zbits + 2 * (row % a.zmod) + 1) : 0ull;
                 s_z[0] = z0;
@@ -311,22 +334,19 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                 for (int n0 = 0; n0 < HALF; ++n0)
                     bulk_g2s(swo + n0 * SEG, a.w_out + row * M + 2 * (long(L) * n0 + o_base), TILE * 4, bar);
         }
-        if constexpr (SP) {  // newly dead sub-rows: clear their staged segments
-            __syncthreads();
-            const unsigned long long n0 = s_z[0] & ~s_zs[0], n1 = s_z[1] & ~s_zs[1];
-            if (n0 | n1) {
-                for (int k0 = 0; k0 < R0; ++k0)
-                    if (zbit(n0, n1, k0))
-                        for (int c = threadIdx.x; c < TILE / 4; c += blockDim.x)
-                            reinterpret_cast<uint4*>(st + k0 * SEG)[c] = make_uint4(0u, 0u, 0u, 0u);
-                // the cleared segments may be bulk-copy targets of a later item
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-        }
         if (!cta_wait(bar, par, &s_fail, a.err)) return;
-        if (SP && threadIdx.x == 0) {  // every live sub-row was overwritten by this item's copies
-            s_zs[0] = s_z[0];
-            s_zs[1] = s_z[1];
+        // ROWP: bit s of la / lb: this thread's input row 8s + t / 8s + 4 + t
+        // is live; bit s of lc (the same in every thread): some row of the chunk
+        // 8s .. 8s + 7 is live, else the chunk's twiddles and products are skipped
+        uint32_t la = 0, lb = 0, lc = lc_fixed;
+        if constexpr (ROWP) {
+            #pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                const int ka = 8 * s + t, kb = 8 * s + 4 + t, kc = 8 * s;
+                if (!((s_z[ka >> 6] >> (ka & 63)) & 1ull)) la |= 1u << s;
+                if (!((s_z[kb >> 6] >> (kb & 63)) & 1ull)) lb |= 1u << s;
+                if (((s_z[kc >> 6] >> (kc & 63)) & 0xffull) != 0xffull) lc |= 1u << s;
+            }
         }
         // NT column groups of 8 per iteration share each DFT fragment load
         constexpr int NT = KS <= 8 ? 2 : 1, NW = mp_pass_c_warps<R0>();
@@ -339,8 +359,10 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
                     const int ka = 8 * s + t, kb = 8 * s + 4 + t;
-                    bf[j][s][0] = ka < R0 ? st[ka * SEG + 8 * nt + g] : 0u;
-                    bf[j][s][1] = (!K8 && kb < R0) ? st[kb * SEG + 8 * nt + g] : 0u;
+                    const bool va = ka < R0 && (!ROWP || ((la >> s) & 1u));
+                    const bool vb = !K8 && kb < R0 && (!ROWP || ((lb >> s) & 1u));
+                    bf[j][s][0] = va ? st[ka * SEG + 8 * nt + g] : 0u;
+                    bf[j][s][1] = vb ? st[kb * SEG + 8 * nt + g] : 0u;
                 }
                 if constexpr (TWID && K8) {  // one input k0 = t per thread
                     const uint32_t np = uint32_t(o_base + 8 * nt + g);
@@ -357,10 +379,12 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                     const cpx w8 = twiddle_pow2((8 * np) & mask, uint32_t(M));
                     #pragma unroll
                     for (int s = 0; s < KS; ++s) {
-                        const cpx xa = cmul(O::unpack(bf[j][s][0]), wa);
-                        const cpx xb = cmul(O::unpack(bf[j][s][1]), cmul(wa, w4));
-                        bf[j][s][0] = O::pack(xa.r, xa.i);
-                        bf[j][s][1] = O::pack(xb.r, xb.i);
+                        if (!SP || ((lc >> s) & 1u)) {
+                            const cpx xa = cmul(O::unpack(bf[j][s][0]), wa);
+                            const cpx xb = cmul(O::unpack(bf[j][s][1]), cmul(wa, w4));
+                            bf[j][s][0] = O::pack(xa.r, xa.i);
+                            bf[j][s][1] = O::pack(xb.r, xb.i);
+                        }
                         if (s + 1 < KS) wa = cmul(wa, w8);
                     }
                 }
@@ -372,6 +396,7 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                 for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
                 #pragma unroll
                 for (int s = 0; s < KS; ++s) {
+                    if (SP && !K8 && !((lc >> s) & 1u)) continue;  // all eight inputs are zero
                     const uint4 af = FS ? s_frag[(m * KS + s) * 32 + lane] : frag[(m * KS + s) * 32 + lane];
                     #pragma unroll
                     for (int j = 0; j < NT; ++j) {
