@@ -70,6 +70,7 @@ def _load():
         lib.oracle_circular_conv.argtypes = [_dp, _dp, _dp, i64]
         lib.oracle_masked_causal_conv.argtypes = [_dp, _dp, _dp, _dp, i64]
         lib.oracle_direct_masked_causal_conv.argtypes = [_dp, _dp, _dp, _dp, i64]
+        lib.oracle_masked_causal_corr.argtypes = [_dp, _dp, _dp, _dp, i64]
         _lib = lib
     return _lib
 
@@ -331,3 +332,34 @@ def masked_causal_conv_batch(u: np.ndarray, k: np.ndarray, mask: np.ndarray, w_i
 
     _split(run, len(sel), threads)
     return out
+
+
+def masked_causal_corr(a: np.ndarray, b: np.ndarray, mask: np.ndarray) -> np.ndarray:
+    """One row of the masked causal correlation (the adjoint in u of the
+    frequency-sparse convolution with kernel b)."""
+    a, b, mask = _f64(a), _f64(b), _f64(mask)
+    if mask.size != a.size + 1:
+        raise ValueError("mask needs N + 1 entries")
+    out = np.empty_like(a)
+    if _load().oracle_masked_causal_corr(_ptr(a), _ptr(b), _ptr(mask), _ptr(out), a.size):
+        raise ValueError("N must be a power of two")
+    return out
+
+
+def masked_input_grad_batch(dy: np.ndarray, k: np.ndarray, mask: np.ndarray, w_in: Optional[np.ndarray] = None,
+                            w_out: Optional[np.ndarray] = None, threads: int = 1) -> np.ndarray:
+    """Input gradient of y = w_out . masked_conv(u . w_in, k) for dy [B, H, N]:
+    du = w_in . masked_corr(w_out . dy, k) per row (gates optional)."""
+    dy, k = _f64(dy), _f64(k)
+    B, H, N = dy.shape
+    g = dy * _f64(w_out) if w_out is not None else dy
+    gf = g.reshape(B * H, N)
+    out = np.empty((B * H, N))
+
+    def run(i0, i1):
+        for r in range(i0, i1):
+            out[r] = masked_causal_corr(gf[r], k[r % H], mask)
+
+    _split(run, B * H, threads)
+    out = out.reshape(B, H, N)
+    return out * _f64(w_in) if w_in is not None else out

@@ -429,3 +429,35 @@ int oracle_direct_masked_causal_conv(const double *u, const double *k, const dou
     free(pr); free(pi);
     return 0;
 }
+
+/*
+ * Adjoint in u of the frequency-sparse convolution: the masked causal
+ * correlation
+ *   out = first N outputs of IDFT_2N( DFT_2N(a0) . conj(DFT_2N(b0)) . m ),
+ * m mirrored as in oracle_masked_causal_conv.  With a = dy and b = k it is
+ * the input gradient of y = masked causal conv(u, k) (the adjoint of a
+ * product with a real, conjugate-symmetric weight is the product with the
+ * conjugate spectrum and the same weight).  N a power of two.
+ */
+int oracle_masked_causal_corr(const double *a, const double *b, const double *mask, double *out, int64_t N)
+{
+    if (!is_pow2(N)) return -1;
+    int64_t L2 = 2 * N;
+    double *ar = calloc((size_t)L2, sizeof(double)), *ai = calloc((size_t)L2, sizeof(double));
+    double *br = calloc((size_t)L2, sizeof(double)), *bi = calloc((size_t)L2, sizeof(double));
+    if (!ar || !ai || !br || !bi) { free(ar); free(ai); free(br); free(bi); return -1; }
+    memcpy(ar, a, (size_t)N * sizeof(double));
+    memcpy(br, b, (size_t)N * sizeof(double));
+    oracle_fft(ar, ai, L2, -1);
+    oracle_fft(br, bi, L2, -1);
+    for (int64_t f = 0; f < L2; ++f) {
+        double wgt = f <= N ? mask[f] : mask[L2 - f];
+        double cr = (ar[f] * br[f] + ai[f] * bi[f]) * wgt;
+        double ci = (ai[f] * br[f] - ar[f] * bi[f]) * wgt;
+        ar[f] = cr; ai[f] = ci;
+    }
+    oracle_fft(ar, ai, L2, 1);
+    memcpy(out, ar, (size_t)N * sizeof(double));
+    free(ar); free(ai); free(br); free(bi);
+    return 0;
+}

@@ -225,3 +225,80 @@ def test_band_pins_catch_planted_mistakes():
         ns = {"np": np}
         exec(src.replace(old, new), ns)
         assert not fixtures_pass(ns["band_mask"]), f"planted mistake not caught: {name}"
+
+
+# ---------------------------------------------------------------- adjoint (input gradient)
+
+@pytest.mark.parametrize("N,factors,band", [(64, [8, 8], [2, 3]), (256, [4, 8, 8], [1, 3, 2]), (1024, [32, 32], [9, 17])])
+def test_masked_corr_is_the_adjoint(N, factors, band):
+    # <dy, A_m u> = <A_m^T dy, u>, with A_m the masked convolution (pinned above)
+    rng = np.random.default_rng(N)
+    m = oracle.band_mask(N, factors, band)
+    for _ in range(3):
+        u, dy, k = rng.standard_normal(N), rng.standard_normal(N), rng.standard_normal(N)
+        lhs = float(dy @ oracle.masked_causal_conv(u, k, m))
+        rhs = float(u @ oracle.masked_causal_corr(dy, k, m))
+        assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(lhs), float(np.abs(dy).sum() * np.abs(u).sum()) * 1e-3)
+
+
+def test_masked_corr_all_ones_is_the_correlation():
+    rng = np.random.default_rng(2)
+    N = 512
+    a, b = rng.standard_normal(N), rng.standard_normal(N)
+    got = oracle.masked_causal_corr(a, b, np.ones(N + 1))
+    ref = oracle.causal_corr(a, b)
+    assert np.allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+    for i in (0, 1, N // 2, N - 1):  # the definition, not a transform
+        assert abs(got[i] - oracle.direct_causal_corr_at(a, b, i)) <= 1e-11 * np.abs(ref).max()
+
+
+def test_masked_input_grad_gates():
+    B, H, N = 2, 3, 64
+    rng = np.random.default_rng(4)
+    dy, wi, wo = (rng.standard_normal((B, H, N)) for _ in range(3))
+    k = rng.standard_normal((H, N))
+    m = oracle.band_mask(N, [8, 8], [3, 2])
+    du = oracle.masked_input_grad_batch(dy, k, m, wi, wo, threads=2)
+    for b in range(B):
+        for h in range(H):
+            ref = wi[b, h] * oracle.masked_causal_corr(wo[b, h] * dy[b, h], k[h], m)
+            assert np.allclose(du[b, h], ref, rtol=0, atol=1e-12 * max(1.0, np.abs(ref).max()))
+
+
+CORR_MUTANTS = {
+    "correlation weight not mirrored": ("double wgt = f <= N ? mask[f] : mask[L2 - f];",
+                                        "double wgt = f <= N ? mask[f] : 1.0;"),
+    "correlation without the conjugate": ("double ci = (ai[f] * br[f] - ar[f] * bi[f]) * wgt;",
+                                          "double ci = (ai[f] * br[f] + ar[f] * bi[f]) * wgt;"),
+    "weight on the real part only": ("double ci = (ai[f] * br[f] - ar[f] * bi[f]) * wgt;",
+                                     "double ci = (ai[f] * br[f] - ar[f] * bi[f]);"),
+}
+
+
+def _corr_pins_pass(lib) -> bool:
+    P = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    rng = np.random.default_rng(8)
+    N = 64
+    m = oracle.band_mask(N, [8, 8], [2, 3])
+    ok = True
+    for _ in range(2):
+        u, dy, k = rng.standard_normal(N), rng.standard_normal(N), rng.standard_normal(N)
+        y, du = np.zeros(N), np.zeros(N)
+        lib.oracle_masked_causal_conv(P(u), P(k), P(m), P(y), ctypes.c_int64(N))
+        lib.oracle_masked_causal_corr(P(dy), P(k), P(m), P(du), ctypes.c_int64(N))
+        ok &= abs(float(dy @ y) - float(u @ du)) <= 1e-10 * max(1.0, abs(float(dy @ y)))
+    return bool(ok)
+
+
+def test_corr_pins_catch_planted_mistakes(tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "fftconv_oracle.c")).read()
+    base = tmp_path / "base.c"
+    base.write_text(src)
+    subprocess.check_call(["gcc", "-O1", "-fPIC", "-shared", str(base), "-o", str(base) + ".so", "-lm"])
+    assert _corr_pins_pass(ctypes.CDLL(str(base) + ".so"))
+    for name, (old, new) in CORR_MUTANTS.items():
+        assert src.count(old) == 1, name
+        path = tmp_path / f"m_{abs(hash(name))}.c"
+        path.write_text(src.replace(old, new))
+        subprocess.check_call(["gcc", "-O1", "-fPIC", "-shared", str(path), "-o", str(path) + ".so", "-lm"])
+        assert not _corr_pins_pass(ctypes.CDLL(str(path) + ".so")), f"planted mistake not caught: {name}"
