@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import workloads as W
-from _util import TOL, rel_l2, run_gpu, torch_dtype
+from _util import TOL, rel_l2, run_gpu, to_dev, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -138,4 +138,35 @@ def test_full_size_gene_sampled():
         rel = rel_l2(got[r], ref[i])
         print(f"gene-2m row {r}: pairs {bd['pairs_run']}/{bd['pairs_total']} rel-L2={rel:.3e}")
         assert rel <= TOL["bf16"]
+    assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("N,dtype,gated,B,H,band", [
+    (4096, "bf16", True, 2, 3, [9, 20]),
+    (16384, "fp16", False, 1, 2, [20, 9, 9]),
+    (262144, "bf16", False, 1, 2, [16, 33, 33]),
+    (1048576, "bf16", False, 1, 1, [2, 16, 33, 33]),
+])
+def test_sparse_input_grad(N, dtype, gated, B, H, band):
+    """du of the frequency-sparse convolution: a forward with the adjoint k_f
+    of the same sparse plan (skipped pairs included) against the oracle's
+    masked correlation."""
+    w = W.Workload("t", B, H, N, dtype, gated, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=41)
+    dy = W.make_inputs(W.Workload("t", B, H, N, dtype, False, "normal", "decay", ""), seed=1041)["u"]
+    plan = F.Plan(N, torch_dtype(dtype), band=band)
+    mask = oracle.band_mask(N, plan.info["factors"], band)
+    kfa = plan.kernel_fft_adjoint(to_dev(ins["k"]))
+    if gated:
+        du = plan.backward_du(to_dev(dy), kfa, to_dev(ins["w_in"]), to_dev(ins["w_out"]))
+        ref = oracle.masked_input_grad_batch(dy.f64, ins["k"].f64, mask, ins["w_in"].f64, ins["w_out"].f64,
+                                             threads=8)
+    else:
+        du = plan.backward_du(to_dev(dy), kfa)
+        ref = oracle.masked_input_grad_batch(dy.f64, ins["k"].f64, mask, threads=8)
+    torch.cuda.synchronize()
+    got = du.float().cpu().numpy().astype(np.float64)
+    rel = rel_l2(got, ref)
+    print(f"sparse du N={N} {dtype} gated={gated} band={band} rel-L2={rel:.3e}")
+    assert rel <= TOL[dtype]
     assert plan.device_status() == 0
