@@ -174,8 +174,22 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
         }
         // NT column groups of 8 per iteration share each DFT fragment load; the
         // twiddle of output (k0 = 8m + g, o) is W_M^(o g) * W_M^(8 o)^m, a
-        // product chain over the output tiles m
+        // product chain over the output tiles m.  CHAIN (one output tile): the
+        // columns advance by 64 NT per iteration, so W_M^(o g) is carried from
+        // one iteration to the next by W_M^(64 NT g) instead of recomputed
         constexpr int NT = 2;
+        constexpr bool CHAIN = MT == 1;
+        cpx cb[NT][2], cstep;
+        if constexpr (CHAIN) {
+            #pragma unroll
+            for (int j = 0; j < NT; ++j)
+                #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t o = uint32_t(o_base + 8 * (warp + 8 * j) + 2 * t + e);
+                    cb[j][e] = twiddle_pow2((o * uint32_t(g)) & (M - 1), M);
+                }
+            cstep = twiddle_pow2((64u * NT * uint32_t(g)) & (M - 1), M);
+        }
         #pragma unroll 1
         for (int i = 0; i < TILE / 64 / NT; ++i) {
             uint32_t bf[NT][KS][2];
@@ -200,9 +214,14 @@ __global__ void __launch_bounds__(256, (R0 <= 64 && !FULL) ? 3 : 2) mp_pass_a(co
                 }
                 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const uint32_t o = uint32_t(o_base + 8 * nt + 2 * t + e);
-                    tw[j][e] = twiddle_pow2((o * uint32_t(g)) & (M - 1), M);
-                    if (MT > 1) ts[j][e] = twiddle_pow2((8 * o) & (M - 1), M);
+                    if constexpr (CHAIN) {
+                        tw[j][e] = cb[j][e];
+                        cb[j][e] = cmul(cb[j][e], cstep);
+                    } else {
+                        const uint32_t o = uint32_t(o_base + 8 * nt + 2 * t + e);
+                        tw[j][e] = twiddle_pow2((o * uint32_t(g)) & (M - 1), M);
+                        if (MT > 1) ts[j][e] = twiddle_pow2((8 * o) & (M - 1), M);
+                    }
                 }
             }
             #pragma unroll 2
@@ -348,8 +367,24 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                 if (((s_z[kc >> 6] >> (kc & 63)) & 0xffull) != 0xffull) lc |= 1u << s;
             }
         }
-        // NT column groups of 8 per iteration share each DFT fragment load
+        // NT column groups of 8 per iteration share each DFT fragment load.
+        // CHAIN (R0 <= 8): the columns advance by 8 NW NT per iteration, so the
+        // input twiddles W_M^(n' t) and W_M^(4 n') are carried from one
+        // iteration to the next by constant factors instead of recomputed
         constexpr int NT = KS <= 8 ? 2 : 1, NW = mp_pass_c_warps<R0>();
+        constexpr bool CHAIN = TWID && R0 <= 8;
+        constexpr uint32_t CSTEP = 8u * NW * NT;
+        cpx ca[NT], c4[NT], sa, s4;
+        if constexpr (CHAIN) {
+            #pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const uint32_t np = uint32_t(o_base + 8 * (warp + NW * j) + g);
+                ca[j] = twiddle_pow2((np * uint32_t(t)) & (uint32_t(M) - 1), uint32_t(M));
+                c4[j] = twiddle_pow2((4 * np) & (uint32_t(M) - 1), uint32_t(M));
+            }
+            sa = twiddle_pow2((CSTEP * uint32_t(t)) & (uint32_t(M) - 1), uint32_t(M));
+            s4 = twiddle_pow2((4 * CSTEP) & (uint32_t(M) - 1), uint32_t(M));
+        }
         #pragma unroll 1
         for (int i = 0; i < TILE / 8 / NW / NT; ++i) {
             uint32_t bf[NT][KS][2];
@@ -366,7 +401,13 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                 }
                 if constexpr (TWID && K8) {  // one input k0 = t per thread
                     const uint32_t np = uint32_t(o_base + 8 * nt + g);
-                    const cpx w = twiddle_pow2((np * uint32_t(t)) & (uint32_t(M) - 1), uint32_t(M));
+                    cpx w;
+                    if constexpr (CHAIN) {
+                        w = ca[j];
+                        ca[j] = cmul(ca[j], sa);
+                    } else {
+                        w = twiddle_pow2((np * uint32_t(t)) & (uint32_t(M) - 1), uint32_t(M));
+                    }
                     const cpx xa = cmul(O::unpack(bf[j][0][0]), w);
                     bf[j][0][0] = O::pack(xa.r, xa.i);
                 }
@@ -374,9 +415,17 @@ __global__ void __launch_bounds__(32 * mp_pass_c_warps<R0>(), (R0 <= 64 && !TOT)
                     static_assert(R0 % 8 == 0, "twiddled pass C needs R0 = 4 or a multiple of 8");
                     const uint32_t np = uint32_t(o_base + 8 * nt + g);
                     const uint32_t mask = uint32_t(M) - 1;
-                    cpx wa = twiddle_pow2((np * uint32_t(t)) & mask, uint32_t(M));
-                    const cpx w4 = twiddle_pow2((4 * np) & mask, uint32_t(M));
-                    const cpx w8 = twiddle_pow2((8 * np) & mask, uint32_t(M));
+                    cpx wa, w4;
+                    if constexpr (CHAIN) {
+                        wa = ca[j];
+                        w4 = c4[j];
+                        ca[j] = cmul(ca[j], sa);
+                        c4[j] = cmul(c4[j], s4);
+                    } else {
+                        wa = twiddle_pow2((np * uint32_t(t)) & mask, uint32_t(M));
+                        w4 = twiddle_pow2((4 * np) & mask, uint32_t(M));
+                    }
+                    const cpx w8 = KS > 1 ? twiddle_pow2((8 * np) & mask, uint32_t(M)) : cpx{1.f, 0.f};
                     #pragma unroll
                     for (int s = 0; s < KS; ++s) {
                         if (!SP || ((lc >> s) & 1u)) {
