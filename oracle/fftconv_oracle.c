@@ -24,11 +24,20 @@
  * exact angle at every use.  Nothing is blocked, fused or reordered beyond
  * that definition.
  *
+ * Further functions, each with its definition at its head: the causal
+ * correlation and the two gradients of the convolution (input and kernel),
+ * the partial convolution (kernel cut to T taps), the circular convolution,
+ * and the frequency-sparse forms (the masked convolution, its DFT-sum twin
+ * and the masked correlation).
+ *
  * Pins (tests that run without a GPU): brute-force DFT and direct
  * convolution on small sizes, the delta / shifted-delta kernels, u = delta,
  * constant u (prefix sums), linearity, commutativity, Parseval, single-tone
  * transforms, numpy's FFT as an independent library, and hand-worked
- * fixtures.  No function here is "parity unpinned".
+ * fixtures; adjoint identities for the correlations and gradients;
+ * windowed and modular brute-force sums for the partial and circular forms;
+ * single-bin closed forms and the all-ones weight for the masked forms; and
+ * planted mistakes for every group.  No function here is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
