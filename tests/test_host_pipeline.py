@@ -86,3 +86,23 @@ def test_host_argument_errors():
     assert call(u.data_ptr(), None, None, kf.data_ptr(), y.data_ptr(), 0, H, None, 0, None) == 0
     assert call(u.data_ptr(), None, None, kf.data_ptr(), y.data_ptr(), B, H, scratch.data_ptr(), need, None) == 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("N,dtype,B,H,band", [
+    (262144, "bf16", 3, 2, [16, 33, 33]),       # one-level sparse passes, chunks of batch entries
+    (1048576, "bf16", 1, 3, [2, 16, 33, 33]),   # two-level sparse passes, chunks of channels
+])
+def test_host_sparse_plan_matches_device(N, dtype, B, H, band):
+    """A frequency-sparse plan through the chunked host pipeline: each chunk
+    restarts the row index, which must not move the skipped sub-rows."""
+    w = W.Workload("t", B, H, N, dtype, False, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=23)
+    tdt = torch_dtype(dtype)
+    plan = F.Plan(N, tdt, band=band)
+    assert 0 < plan.band()["pairs_run"] < plan.band()["pairs_total"]
+    kf = plan.kernel_fft(to_dev(ins["k"]))
+    y_dev = plan.forward(to_dev(ins["u"]), kf)
+    y_host = plan.forward_host(_host(ins["u"], tdt), kf)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+    assert plan.device_status() == 0
