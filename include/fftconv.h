@@ -109,9 +109,9 @@ fftconv_status_t fftconv_plan_create(fftconv_plan_t *out, int64_t N, fftconv_dty
 
 /*
  * Frequency-sparse plan (FlashFFTConv page, "Architectural Extensions:
- * Partial and Frequency-Sparse Convolutions", frequency-sparse part: parts
- * of k_f set to zero in a pattern that follows the decomposition, so whole
- * blocks of work can be skipped).  As fftconv_plan_create, plus one band per
+ * Partial and Frequency-Sparse Convolutions", frequency-sparse part: a
+ * structured subset of the bins of k_f is zeroed, chosen along the
+ * decomposition so that whole blocks of work drop out).  As fftconv_plan_create, plus one band per
  * factor: band[0..nband-1], nband = the plan's order (query it first when
  * order = 0), outer factor first, each band >= 0.
  *

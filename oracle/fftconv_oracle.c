@@ -369,7 +369,7 @@ int oracle_circular_conv(const double *u, const double *k, double *y, int64_t N)
 /*
  * Frequency-sparse causal convolution (FlashFFTConv page, "Architectural
  * Extensions: Partial and Frequency-Sparse Convolutions", the
- * frequency-sparse part): part of the kernel's spectrum is set to zero
+ * frequency-sparse part): the kernel's spectrum is zeroed on some bins
  * before the product.  mask[f], f = 0..N, weighs bin f of the 2N-point
  * spectrum of the real kernel; bin 2N - f (f = 1..N-1) takes the same
  * weight, so the weighted spectrum keeps the conjugate symmetry of a real
