@@ -36,7 +36,7 @@ import workloads as W  # noqa: E402
 
 METRIC = ("long-conv B·H·N outputs/sec on 1 GB300; achieved fraction of "
           "HBM/tensor roofline")
-DEFAULT_WORKLOAD = "hyena-gated-4k"
+DEFAULT_WORKLOAD = "m2bert-16k"
 L2_BYTES = 129 * 1000 * 1000
 
 
