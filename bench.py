@@ -274,6 +274,8 @@ def path_of(plan_info: dict, pairs_run: Optional[int] = None) -> dict:
         return {"kernel": f"mp_pass_a + {b} + mp_pass_c (the whole step)", "launches_per_step": 2 + nb}
     if plan_info["order"] == 2:
         return {"kernel": "tc64_conv_kernel", "launches_per_step": 1}
+    if plan_info["factors"][1] == 64:  # R0 x 64 x 64 on the tensor cores
+        return {"kernel": "ftc_conv_kernel", "launches_per_step": 1}
     return {"kernel": "fused_conv_kernel", "launches_per_step": 1}
 
 

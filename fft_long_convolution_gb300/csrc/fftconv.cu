@@ -12,6 +12,7 @@
 
 #include "../../include/fftconv.h"
 #include "plan.h"
+#include "ftc.cuh"
 #include "tcconv.cuh"
 #include "tcpass.cuh"
 
@@ -60,6 +61,28 @@ uint32_t pack2(double lo, double hi, int dtype) {
 
 bool is_pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
 
+// Row counts the kernels index with 32-bit integers: B, H and B*H each at
+// most 2^30, tested without forming a product that could overflow.
+constexpr int64_t kMaxRows = int64_t(1) << 30;
+bool too_many_rows(int64_t B, int64_t H) {
+    return B > kMaxRows || H > kMaxRows || (B > 0 && H > kMaxRows / B);
+}
+
+}  // namespace
+
+// A plan's tables live on the device that was current when it was made; a
+// call made with another device current is refused (FFTCONV_ERR_INVALID).
+static bool wrong_device(const fftconv_plan_s* p) {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return d != p->device;
+}
+
+namespace {
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -83,6 +106,15 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
         q.order = 2;
         q.factors[0] = 64;
         q.factors[1] = 64;
+        q.workspace_bytes_per_row = 0;
+    } else if (N == 8192 || N == 16384) {
+        // fused on the fifth-generation tensor cores: M = R0 * 64 * 64, the
+        // outer factor R0 = 2 or 4 in shared memory
+        q.path = FFTCONV_PATH_FUSED;
+        q.order = 3;
+        q.factors[0] = int32_t(N / 4096);
+        q.factors[1] = 64;
+        q.factors[2] = 64;
         q.workspace_bytes_per_row = 0;
     } else if (N <= 16384) {
         // fused: M = R1 * 16 * 16
@@ -126,7 +158,7 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
     // 64 x 64 paths, whose k_f follows the kernels' column layouts)
     if (N == 4096)
         q.kf_bytes_per_channel = int64_t(Tc64::KFB);
-    else if (q.path == FFTCONV_PATH_MULTIPASS && q.order == 3)
+    else if (q.order == 3 && q.factors[1] == 64)  // pairs of 4096-point sub-rows (fused or multi-pass)
         q.kf_bytes_per_channel = int64_t(q.factors[0] / 2) * TcB::KFP * 16;
     else if (q.path == FFTCONV_PATH_MULTIPASS && q.factors[3] == 64)  // two-level outer factor
         q.kf_bytes_per_channel = int64_t(q.factors[0] * 64 / 2) * TcB::KFP * 16;
@@ -319,16 +351,10 @@ cudaError_t launch_fused_t(const fftconv_plan_s* p, const void* u, const void* w
                            const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
     using C = FusedCfg<R1, G>;
     auto fn = fused_conv_kernel<DT, R1, G>;
-    static int blocks_per_sm = 0;  // per instantiation, set once per process
-    if (blocks_per_sm == 0) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(C::SMEM_BYTES));
-        if (e != cudaSuccess) return e;
-        int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, C::THREADS, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        blocks_per_sm = nb > 0 ? nb : 1;
-    }
+    static PerDevice cache;  // per instantiation and device
+    int blocks_per_sm = 0;
+    cudaError_t e = prep_kernel(fn, C::SMEM_BYTES, C::THREADS, cache, &blocks_per_sm);
+    if (e != cudaSuccess) return e;
     if (C::TSMEM && p->tb.outer_bytes > C::TAB_BYTES) return cudaErrorInvalidValue;
     if (C::FSMEM && p->tb.off_twf > C::TAB_BYTES) return cudaErrorInvalidValue;
     const int64_t groups = (B * H + C::RP - 1) / C::RP;
@@ -346,12 +372,10 @@ template <int DT, bool G>
 cudaError_t launch_tc64_t(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
                           const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
     auto fn = tc64_conv_kernel<DT, G>;
-    static bool ready = false;  // per instantiation, set once per process
-    if (!ready) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Tc64::SMEM));
-        if (e != cudaSuccess) return e;
-        ready = true;
-    }
+    static PerDevice cache;  // per instantiation and device
+    int per_sm = 0;
+    cudaError_t e = prep_kernel(fn, Tc64::SMEM, Tc64::THREADS, cache, &per_sm);
+    if (e != cudaSuccess) return e;
     // one CTA per SM (its tensor-memory allocation takes all 512 columns);
     // work items are pairs of rows of one channel, two pipelines per CTA
     const int64_t items = (B + 1) / 2 * H;
@@ -364,16 +388,38 @@ cudaError_t launch_tc64_t(const fftconv_plan_s* p, const void* u, const void* wi
     return cudaGetLastError();
 }
 
+// N = R0 * 4096 (8192, 16384): the fused tensor-core kernel (ftc.cuh), one
+// CTA per SM (all 512 tensor-memory columns), rows split over its two
+// pipelines.
+template <int DT, int R0, bool G>
+cudaError_t launch_ftc_t(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
+                         const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
+    using C = Ftc<R0, G>;
+    auto fn = ftc_conv_kernel<DT, R0, G>;
+    static PerDevice cache;  // per instantiation and device
+    int per_sm = 0;
+    cudaError_t e = prep_kernel(fn, C::SMEM, C::THREADS, cache, &per_sm);
+    if (e != cudaSuccess) return e;
+    const int64_t rows = B * H, need = (rows + 1) / 2;
+    const int64_t grid = need < p->num_sms ? need : p->num_sms;
+    FtcArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
+                 static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
+                 p->fmat, int(B), int(H), p->dev_err};
+    fn<<<dim3(unsigned(grid)), dim3(C::THREADS), C::SMEM, st>>>(args);
+    return cudaGetLastError();
+}
+
 template <int DT, bool G>
 cudaError_t launch_fused_r(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
                            const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
     if (p->tc64) return launch_tc64_t<DT, G>(p, u, wi, wo, kf, y, B, H, st);
+    switch (p->ftc) {
+        case 2: return launch_ftc_t<DT, 2, G>(p, u, wi, wo, kf, y, B, H, st);
+        case 4: return launch_ftc_t<DT, 4, G>(p, u, wi, wo, kf, y, B, H, st);
+    }
     switch (p->R1) {
         case 4: return launch_fused_t<DT, 4, G>(p, u, wi, wo, kf, y, B, H, st);
         case 8: return launch_fused_t<DT, 8, G>(p, u, wi, wo, kf, y, B, H, st);
-        case 16: return launch_fused_t<DT, 16, G>(p, u, wi, wo, kf, y, B, H, st);
-        case 32: return launch_fused_t<DT, 32, G>(p, u, wi, wo, kf, y, B, H, st);
-        case 64: return launch_fused_t<DT, 64, G>(p, u, wi, wo, kf, y, B, H, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -487,11 +533,12 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     p->R0 = multi ? info.factors[0] : 1;
     p->R1 = multi ? kMpR1 : info.factors[0];
     p->tc64 = N == 4096;
+    p->ftc = (N == 8192 || N == 16384) ? int(N / 4096) : 0;
     p->mp2 = multi && info.order == 4 && info.factors[3] == 64;
     if (p->mp2) p->R0 = info.factors[0] * 64;  // the sub-row count of pass B
     p->mpL = multi ? ((info.order == 3 || p->mp2) ? kMpLtc : kMpL) : 0;
-    const bool need_fmat = p->tc64 || p->mpL == kMpLtc;
-    HostTables T = p->tc64 ? HostTables{} : build_fused_tables(p->R1, dtype);
+    const bool need_fmat = p->tc64 || p->ftc || p->mpL == kMpLtc;
+    HostTables T = (p->tc64 || p->ftc) ? HostTables{} : build_fused_tables(p->R1, dtype);
     std::vector<uint32_t> fmat;
     if (need_fmat) fmat = build_tc64_fmat(dtype);
     HostTables T0;
@@ -545,6 +592,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
         delete p;
         return FFTCONV_ERR_CUDA;
     }
+    p->device = dev;
     uint8_t* d = static_cast<uint8_t*>(p->dev);
     p->dev_err = reinterpret_cast<int*>(d + o_err);
     if (need_fmat) p->fmat = reinterpret_cast<const uint32_t*>(d + o_fmat);
@@ -959,7 +1007,7 @@ namespace {
 
 fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f, int64_t H,
                                  fftconv_stream_t stream, bool adjoint) {
-    if (!plan || H < 0) return FFTCONV_ERR_INVALID;
+    if (!plan || H < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (H == 0) return FFTCONV_OK;
     if (!k || !k_f) return FFTCONV_ERR_INVALID;
     if (misaligned(k) || misaligned(k_f)) return FFTCONV_ERR_ALIGN;
@@ -988,9 +1036,11 @@ fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f,
     if (plan->tc64)
         kfft_finalize_tc64<<<grid_for(H * 9 * 4 * 2 * 32), 256, 0, st>>>(a, static_cast<uint4*>(k_f), H,
                                                                            plan->info.dtype);
-    else if (plan->mpL == kMpLtc)
-        kfft_finalize_tcmp<<<grid_for(H * (plan->R0 / 2) * TcB::KFP), 256, 0, st>>>(
-            a, static_cast<uint4*>(k_f), H, plan->R0, plan->info.dtype);
+    else if (plan->mpL == kMpLtc || plan->ftc) {
+        const int R0 = plan->ftc ? plan->ftc : plan->R0;
+        kfft_finalize_tcmp<<<grid_for(H * (R0 / 2) * TcB::KFP), 256, 0, st>>>(a, static_cast<uint4*>(k_f), H, R0,
+                                                                             plan->info.dtype);
+    }
     else
         kfft_finalize<<<grid_for(H * plan->R0 * plan->R1 * 128), 256, 0, st>>>(
             a, static_cast<uint4*>(k_f), H, plan->R0, plan->R1, plan->info.dtype);
@@ -1006,12 +1056,12 @@ fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f,
 static fftconv_status_t forward_impl(fftconv_plan_t plan, const void* u, const void* w_in,
                                      const void* w_out, const void* k_f, void* y, int64_t B, int64_t H,
                                      fftconv_stream_t stream, bool gated) {
-    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (!plan || B < 0 || H < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (B == 0 || H == 0) return FFTCONV_OK;
     if (!u || !k_f || !y || (gated && (!w_in || !w_out))) return FFTCONV_ERR_INVALID;
     if (misaligned(u) || misaligned(k_f) || misaligned(y) || (gated && (misaligned(w_in) || misaligned(w_out))))
         return FFTCONV_ERR_ALIGN;
-    if (B * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    if (too_many_rows(B, H)) return FFTCONV_ERR_UNSUPPORTED;
     const size_t nb = size_t(B) * size_t(H) * size_t(plan->info.N) * 2;
     const size_t kb = fftconv_kf_bytes(plan, H);
     if (overlap(y, nb, u, nb) || overlap(y, nb, k_f, kb) ||
@@ -1048,7 +1098,7 @@ extern "C" fftconv_status_t fftconv_forward_gated(fftconv_plan_t plan, const voi
 }
 
 extern "C" fftconv_status_t fftconv_device_status(fftconv_plan_t plan, fftconv_stream_t stream, int* out) {
-    if (!plan || !out) return FFTCONV_ERR_INVALID;
+    if (!plan || !out || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int v = 0;
     if (cudaMemcpyAsync(&v, plan->dev_err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -1087,7 +1137,7 @@ __global__ void selftest_wait_kernel(int* err, int sleep) {
 }  // namespace
 
 extern "C" fftconv_status_t fftconv_selftest_wait(fftconv_plan_t plan, int sleep, fftconv_stream_t stream) {
-    if (!plan) return FFTCONV_ERR_INVALID;
+    if (!plan || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(plan->dev_err, sleep);
     return cudaGetLastError() == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
 }
@@ -1290,7 +1340,7 @@ extern "C" size_t fftconv_backward_dk_scratch_bytes(fftconv_plan_t plan, int64_t
 extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void* u, const void* dy, const void* w_in,
                                                 const void* w_out, float* dk, int64_t B, int64_t H, void* scratch,
                                                 size_t scratch_bytes, fftconv_stream_t stream) {
-    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (!plan || B < 0 || H < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (plan->sparse) return FFTCONV_ERR_UNSUPPORTED;  // the kernel gradient is not band-limited here
     if (H == 0) return FFTCONV_OK;
     if (!dk || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
@@ -1301,6 +1351,7 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
         return cudaMemsetAsync(dk, 0, size_t(H) * size_t(N) * 4, st) == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
     }
     if (!u || !dy) return FFTCONV_ERR_INVALID;
+    if (too_many_rows(B, H)) return FFTCONV_ERR_UNSUPPORTED;
     if (misaligned(u) || misaligned(dy) || (w_in && (misaligned(w_in) || misaligned(w_out)))) return FFTCONV_ERR_ALIGN;
     const size_t nb = size_t(B) * size_t(H) * size_t(N) * 2, kb = size_t(H) * size_t(N) * 4;
     if (overlap(dk, kb, u, nb) || overlap(dk, kb, dy, nb) || (w_in && (overlap(dk, kb, w_in, nb) || overlap(dk, kb, w_out, nb))))
@@ -1308,16 +1359,18 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
     const size_t need = fftconv_backward_dk_scratch_bytes(plan, B, H);
     if (L <= kDkMaxL) {
         const size_t smem = size_t(2) * L * sizeof(float2);
-        static bool ready[2] = {false, false};
+        static PerDevice ready[2];  // per dtype and device
         auto fn = plan->info.dtype == FFTCONV_F16 ? dk_channel_smem<0> : dk_channel_smem<1>;
         const int di = plan->info.dtype == FFTCONV_F16 ? 0 : 1;
-        if (!ready[di]) {
+        int* rd = ready[di].slot();
+        if (!rd) return FFTCONV_ERR_CUDA;
+        if (!*rd) {
             if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * kDkMaxL * sizeof(float2))) !=
                 cudaSuccess) {
                 cudaGetLastError();
                 return FFTCONV_ERR_CUDA;
             }
-            ready[di] = true;
+            *rd = 1;
         }
         const int64_t grid = H < 65535 ? H : 65535;
         fn<<<unsigned(grid), kDkThreads, smem, st>>>(static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy),
@@ -1446,7 +1499,7 @@ namespace {
 fftconv_status_t windowed_forward(fftconv_plan_t plan, const void* u, const void* w_in, const void* w_out,
                                   const void* k_f, void* y, int64_t B, int64_t H, int64_t N, void* scratch,
                                   size_t scratch_bytes, fftconv_stream_t stream, bool wrap) {
-    if (!plan || B < 0 || H < 0 || N < 0) return FFTCONV_ERR_INVALID;
+    if (!plan || B < 0 || H < 0 || N < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (plan->sparse) return FFTCONV_ERR_UNSUPPORTED;  // windows of a band-limited kernel are not defined here
     if (B == 0 || H == 0 || N == 0) return FFTCONV_OK;
     if (!u || !k_f || !y || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
@@ -1456,7 +1509,7 @@ fftconv_status_t windowed_forward(fftconv_plan_t plan, const void* u, const void
     if (misaligned(u) || misaligned(k_f) || misaligned(y) || (gated && (misaligned(w_in) || misaligned(w_out))))
         return FFTCONV_ERR_ALIGN;
     const PartialLayout lay = partial_layout(plan, B, H, N, gated);
-    if (B * lay.nwin * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    if (too_many_rows(B, lay.nwin) || too_many_rows(B * lay.nwin, H)) return FFTCONV_ERR_UNSUPPORTED;
     const size_t nb = size_t(B) * size_t(H) * size_t(N) * 2;
     if (overlap(y, nb, u, nb) || (gated && (overlap(y, nb, w_in, nb) || overlap(y, nb, w_out, nb))))
         return FFTCONV_ERR_INVALID;
@@ -1551,11 +1604,11 @@ void* static_scratch_for_current_device() {
 
 extern "C" fftconv_status_t fftconv_forward_noalloc(fftconv_plan_t plan, const void* u, const void* k_f,
                                                     void* y, int64_t B, int64_t H, fftconv_stream_t stream) {
-    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (!plan || B < 0 || H < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (B == 0 || H == 0) return FFTCONV_OK;
     if (!u || !k_f || !y) return FFTCONV_ERR_INVALID;
     if (misaligned(u) || misaligned(k_f) || misaligned(y)) return FFTCONV_ERR_ALIGN;
-    if (B * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    if (too_many_rows(B, H)) return FFTCONV_ERR_UNSUPPORTED;
     const size_t nb = size_t(B) * size_t(H) * size_t(plan->info.N) * 2;
     const size_t kb = fftconv_kf_bytes(plan, H);
     if (overlap(y, nb, u, nb) || overlap(y, nb, k_f, kb)) return FFTCONV_ERR_INVALID;
@@ -1637,12 +1690,12 @@ extern "C" fftconv_status_t fftconv_forward_host(fftconv_plan_t plan, const void
                                                  const void* w_out, const void* k_f, void* y, int64_t B,
                                                  int64_t H, void* scratch, size_t scratch_bytes,
                                                  fftconv_stream_t stream) {
-    if (!plan || B < 0 || H < 0) return FFTCONV_ERR_INVALID;
+    if (!plan || B < 0 || H < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (B == 0 || H == 0) return FFTCONV_OK;
     if (!u || !k_f || !y || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
     const bool gated = w_in != nullptr;
     if (misaligned(k_f)) return FFTCONV_ERR_ALIGN;
-    if (B * H > (int64_t(1) << 31) / 2) return FFTCONV_ERR_UNSUPPORTED;
+    if (too_many_rows(B, H)) return FFTCONV_ERR_UNSUPPORTED;
     const size_t nb = size_t(B) * size_t(H) * size_t(plan->info.N) * 2;
     if (overlap(y, nb, u, nb) || (gated && (overlap(y, nb, w_in, nb) || overlap(y, nb, w_out, nb))))
         return FFTCONV_ERR_INVALID;

@@ -11,11 +11,12 @@ template <int DT, int R0, bool G, bool SP>
 cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
     constexpr int HALF = R0 / 2, L = kMpL;
     const size_t smem_a = mp_pass_a_smem<R0, G>(), smem_c = mp_pass_c_smem<R0, G>();
-    static int na = 0, nb = 0, nc = 0;
+    static PerDevice ca, cb, cc;
+    int na = 0, nb = 0, nc = 0;
     cudaError_t e;
-    if ((e = prep_kernel(mp_pass_a<DT, R0, G, L, false, SP>, smem_a, 256, &na)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_b<DT, SP>, kMpBSmem, 512, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, false, false, SP>, smem_c, 32 * mp_pass_c_warps<R0>(), &nc)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_a<DT, R0, G, L, false, SP>, smem_a, 256, ca, &na)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_b<DT, SP>, kMpBSmem, 512, cb, &nb)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, false, false, SP>, smem_c, 32 * mp_pass_c_warps<R0>(), cc, &nc)) != cudaSuccess) return e;
     const int64_t items_ac = rows * (L / mp_tile<R0>()), items_b = rows * p->pairs_run;
     auto grid = [&](int64_t items, int per_sm) {
         int64_t gsz = int64_t(p->num_sms) * per_sm;

@@ -13,11 +13,12 @@ template <int DT, int R0, bool G, bool SP>
 cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
     constexpr int HALF = R0 / 2, L = kMpLtc;
     const size_t smem_a = mp_pass_a_smem<R0, G>(), smem_c = mp_pass_c_smem<R0, G>();
-    static int na = 0, nb = 0, nc = 0;
+    static PerDevice ca, cb, cc;
+    int na = 0, nb = 0, nc = 0;
     cudaError_t e;
-    if ((e = prep_kernel(mp_pass_a<DT, R0, G, L, false, SP>, smem_a, 256, &na)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_b_tc<DT, SP>, TcB::SMEM, TcB::THREADS, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true, false, SP>, smem_c, 32 * mp_pass_c_warps<R0>(), &nc)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_a<DT, R0, G, L, false, SP>, smem_a, 256, ca, &na)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_b_tc<DT, SP>, TcB::SMEM, TcB::THREADS, cb, &nb)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true, false, SP>, smem_c, 32 * mp_pass_c_warps<R0>(), cc, &nc)) != cudaSuccess) return e;
     const int64_t items_ac = rows * (L / mp_tile<R0>());
     auto grid = [&](int64_t items, int per_sm) {
         int64_t gsz = int64_t(p->num_sms) * per_sm;
@@ -56,15 +57,16 @@ cudaError_t launch_2l_t(const fftconv_plan_s* p, const MPArgs& args, int64_t row
     constexpr int L = kMpLtc, L1 = 64 * L, R0 = RA * 64;  // N = RA * L1
     const size_t smem_a1 = mp_pass_a_smem<RA, G>(), smem_c1 = mp_pass_c_smem<RA, G>();
     const size_t smem_a2 = mp_pass_a_smem<64, false, true>(), smem_c2 = mp_pass_c_smem<64, false>();
-    static int na1 = 0, na2 = 0, nb = 0, nc2 = 0, nc1 = 0;
+    static PerDevice ca1, ca2, cb, cc2, cc1;
+    int na1 = 0, na2 = 0, nb = 0, nc2 = 0, nc1 = 0;
     cudaError_t e;
-    if ((e = prep_kernel(mp_pass_a<DT, RA, G, L1>, smem_a1, 256, &na1)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_a<DT, 64, false, L, true, SP>, smem_a2, 256, &na2)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_b_tc<DT, SP>, TcB::SMEM, TcB::THREADS, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, 64, false, L, true, true, SP>, smem_c2, 32 * mp_pass_c_warps<64>(), &nc2)) !=
+    if ((e = prep_kernel(mp_pass_a<DT, RA, G, L1>, smem_a1, 256, ca1, &na1)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_a<DT, 64, false, L, true, SP>, smem_a2, 256, ca2, &na2)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_b_tc<DT, SP>, TcB::SMEM, TcB::THREADS, cb, &nb)) != cudaSuccess) return e;
+    if ((e = prep_kernel(mp_pass_c<DT, 64, false, L, true, true, SP>, smem_c2, 32 * mp_pass_c_warps<64>(), cc2, &nc2)) !=
         cudaSuccess)
         return e;
-    if ((e = prep_kernel(mp_pass_c<DT, RA, G, L1, true>, smem_c1, 32 * mp_pass_c_warps<RA>(), &nc1)) != cudaSuccess)
+    if ((e = prep_kernel(mp_pass_c<DT, RA, G, L1, true>, smem_c1, 32 * mp_pass_c_warps<RA>(), cc1, &nc1)) != cudaSuccess)
         return e;
     auto grid = [&](int64_t items, int per_sm) {
         int64_t gsz = int64_t(p->num_sms) * per_sm;

@@ -35,7 +35,7 @@ def test_version_and_status_strings():
     assert F.status_string(99) == "unknown status"
 
 
-@pytest.mark.parametrize("N,R1", [(1024, 4), (2048, 8), (8192, 32), (16384, 64)])
+@pytest.mark.parametrize("N,R1", [(1024, 4), (2048, 8)])
 def test_query_fused_factorization(N, R1):
     for dt in (F.F16, F.BF16):
         q = F.query(N, dt)
@@ -43,6 +43,19 @@ def test_query_fused_factorization(N, R1):
         assert q["factors"] == [R1, 16, 16]
         assert q["factors"][0] * 16 * 16 == N == q["M"]
         assert q["kf_bytes_per_channel"] == 8 * N
+        assert q["workspace_bytes_per_row"] == 0
+
+
+@pytest.mark.parametrize("N", [8192, 16384])
+def test_query_fused_tensor_core_factorization(N):
+    """N = 8192 and 16384 run fused as R0 x 64 x 64 (R0 = 2, 4) on the
+    fifth-generation tensor cores; k_f holds one pass-B block (17 chunks of
+    4 warps x 2 halves x 32 lanes x 16 bytes) per pair of sub-rows."""
+    for dt in (F.F16, F.BF16):
+        q = F.query(N, dt)
+        assert q["path"] == F.PATH_FUSED and q["order"] == 3
+        assert q["factors"] == [N // 4096, 64, 64] and q["M"] == N
+        assert q["kf_bytes_per_channel"] == (N // 8192) * 17 * 4 * 2 * 32 * 16
         assert q["workspace_bytes_per_row"] == 0
 
 

@@ -22,7 +22,7 @@ def _need_gpu():
 @pytest.mark.parametrize("C,dtype,gated,B,H", [
     (512, "fp16", False, 2, 3),       # plan 1024 (fused)
     (2048, "bf16", True, 3, 2),       # plan 4096 (tensor-memory kernel)
-    (8192, "fp16", False, 1, 2),      # plan 16384 (fused, 64 x 16 x 16)
+    (8192, "fp16", False, 1, 2),      # plan 16384 (fused, 4 x 64 x 64 on the tensor cores)
     (65536, "bf16", False, 1, 2),     # plan 131072 (multi-pass)
 ])
 def test_circular_matches_oracle(C, dtype, gated, B, H):

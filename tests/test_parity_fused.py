@@ -44,7 +44,7 @@ def test_fused_matches_oracle(N, dtype, gated):
     assert plan.device_status() == 0
 
 
-@pytest.mark.parametrize("N", [1024, 4096, 16384])
+@pytest.mark.parametrize("N", [1024, 4096, 8192, 16384])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_delta_kernels(N, dtype):
     """k = delta_s gives y[t] = u[t-s] (t >= s): pins causal truncation.
@@ -151,5 +151,23 @@ def test_tc64_many_items_every_row(dtype, gated):
     ref = oracle_rows(ins, gated, threads=8)
     worst = max(rel_l2(got[b, h], ref[b, h]) for b in range(w.B) for h in range(w.H))
     print(f"N=4096 {dtype} gated={gated} rows={w.rows} worst row rel-L2={worst:.3e}")
+    assert worst <= TOL[dtype]
+    assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("N,dtype,gated", [(16384, "fp16", False), (16384, "bf16", True),
+                                           (8192, "bf16", False), (8192, "fp16", True)])
+def test_ftc_many_rows_every_row(N, dtype, gated):
+    """N = 8192 / 16384 on the fused tensor-core kernel with several rows
+    per pipeline (the next row's staging overlaps the current row, pair
+    (1, 3) hands its outputs to pair (0, 2)); every row checked."""
+    w = W.Workload("t", 5, 130, N, dtype, gated, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=17)
+    plan = _plan(N, dtype)
+    y, _ = run_gpu(plan, ins, gated)
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle_rows(ins, gated, threads=8)
+    worst = max(rel_l2(got[b, h], ref[b, h]) for b in range(w.B) for h in range(w.H))
+    print(f"N={N} {dtype} gated={gated} rows={w.rows} worst row rel-L2={worst:.3e}")
     assert worst <= TOL[dtype]
     assert plan.device_status() == 0
