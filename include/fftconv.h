@@ -239,6 +239,9 @@ fftconv_status_t fftconv_forward_gated(fftconv_plan_t plan, const void *u, const
  *   returns FFTCONV_ERR_WORKSPACE and launches nothing.
  * - The first call on a device looks up the array's address for the current
  *   device; make that first call before any stream capture on the device.
+ *   The address is kept for the life of the process, so a device reset
+ *   (cudaDeviceReset) after that first call is not supported: the array would
+ *   live at a new address that the library does not look up again.
  * - Every call shares the one array.  Calls that can overlap on the GPU (on
  *   different streams or from different host threads) race and corrupt each
  *   other's results: serialise them.  Nothing in the array has to start at
