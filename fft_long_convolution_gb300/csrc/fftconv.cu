@@ -107,9 +107,9 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
         q.factors[0] = 64;
         q.factors[1] = 64;
         q.workspace_bytes_per_row = 0;
-    } else if (N == 8192 || N == 16384) {
+    } else if (N == 8192 || N == 16384 || (N == 32768 && order != 4)) {
         // fused on the fifth-generation tensor cores: M = R0 * 64 * 64, the
-        // outer factor R0 = 2 or 4 in shared memory
+        // outer factor R0 = 2, 4 or 8 in shared memory
         q.path = FFTCONV_PATH_FUSED;
         q.order = 3;
         q.factors[0] = int32_t(N / 4096);
@@ -337,6 +337,36 @@ std::vector<uint32_t> build_tc64_fmat(int dtype) {
     return v;
 }
 
+// Starting twiddles of the fused R0 x 64 x 64 kernel's threads (ftc.cuh):
+// input phase W_M^(k0 n') / sqrt(R0) at n' = 1024 (t / 64) + t % 64, [k0][t];
+// S4 post W_M^(k0 n') at n' = 64 kappa_b + 32 hf + 2q + e (thread t = 128 hf
+// + 32 w + 4 r + q, kappa_0 = 8w + r, kappa_1 = 63 - kappa_0), [k0][b][t] x
+// (re e0, re e1, im e0, im e1).  Built in double, rounded to float.
+void ftc_twiddle_tables(int R0, std::vector<float>& tin, std::vector<float>& tout) {
+    const int64_t M = int64_t(R0) * 4096;
+    const double sc = 1.0 / std::sqrt(double(R0));
+    tin.assign(size_t(R0) * 256 * 2, 0.f);
+    tout.assign(size_t(R0) * 2 * 256 * 4, 0.f);
+    for (int k0 = 0; k0 < R0; ++k0)
+        for (int t = 0; t < 256; ++t) {
+            const int64_t n = 1024 * (t >> 6) + (t & 63);
+            const cd w = W(M, int64_t(k0) * n);
+            tin[(size_t(k0) * 256 + t) * 2] = float(w.r * sc);
+            tin[(size_t(k0) * 256 + t) * 2 + 1] = float(w.i * sc);
+            const int hf = t >> 7, wq = (t >> 5) & 3, r = (t & 31) >> 2, q = t & 3;
+            for (int b = 0; b < 2; ++b) {
+                const int kap = b ? 63 - (8 * wq + r) : 8 * wq + r;
+                const int64_t n0p = 64 * kap + 32 * hf + 2 * q;
+                float* o = &tout[((size_t(k0) * 2 + b) * 256 + t) * 4];
+                for (int e = 0; e < 2; ++e) {
+                    const cd v = W(M, int64_t(k0) * (n0p + e));
+                    o[e] = float(v.r);
+                    o[2 + e] = float(v.i);
+                }
+            }
+        }
+}
+
 template <typename T>
 size_t append(std::vector<uint8_t>& blob, const std::vector<T>& v) {
     size_t off = (blob.size() + 255) & ~size_t(255);
@@ -388,9 +418,8 @@ cudaError_t launch_tc64_t(const fftconv_plan_s* p, const void* u, const void* wi
     return cudaGetLastError();
 }
 
-// N = R0 * 4096 (8192, 16384): the fused tensor-core kernel (ftc.cuh), one
-// CTA per SM (all 512 tensor-memory columns), rows split over its two
-// pipelines.
+// N = R0 * 4096 (8192, 16384, 32768): the fused tensor-core kernel
+// (ftc.cuh), one CTA per SM (all 512 tensor-memory columns).
 template <int DT, int R0, bool G>
 cudaError_t launch_ftc_t(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
                          const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
@@ -400,11 +429,12 @@ cudaError_t launch_ftc_t(const fftconv_plan_s* p, const void* u, const void* wi,
     int per_sm = 0;
     cudaError_t e = prep_kernel(fn, C::SMEM, C::THREADS, cache, &per_sm);
     if (e != cudaSuccess) return e;
-    const int64_t rows = B * H, need = (rows + 1) / 2;
+    // rows split over the two pipelines of a CTA; for R0 = 8 both work on each row
+    const int64_t rows = B * H, need = C::SPLIT ? rows : (rows + 1) / 2;
     const int64_t grid = need < p->num_sms ? need : p->num_sms;
     FtcArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
                  static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
-                 p->fmat, int(B), int(H), p->dev_err};
+                 p->fmat, p->ftw_in, p->ftw_out, int(B), int(H), p->dev_err};
     fn<<<dim3(unsigned(grid)), dim3(C::THREADS), C::SMEM, st>>>(args);
     return cudaGetLastError();
 }
@@ -416,6 +446,7 @@ cudaError_t launch_fused_r(const fftconv_plan_s* p, const void* u, const void* w
     switch (p->ftc) {
         case 2: return launch_ftc_t<DT, 2, G>(p, u, wi, wo, kf, y, B, H, st);
         case 4: return launch_ftc_t<DT, 4, G>(p, u, wi, wo, kf, y, B, H, st);
+        case 8: return launch_ftc_t<DT, 8, G>(p, u, wi, wo, kf, y, B, H, st);
     }
     switch (p->R1) {
         case 4: return launch_fused_t<DT, 4, G>(p, u, wi, wo, kf, y, B, H, st);
@@ -533,7 +564,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     p->R0 = multi ? info.factors[0] : 1;
     p->R1 = multi ? kMpR1 : info.factors[0];
     p->tc64 = N == 4096;
-    p->ftc = (N == 8192 || N == 16384) ? int(N / 4096) : 0;
+    p->ftc = (info.path == FFTCONV_PATH_FUSED && N >= 8192) ? int(N / 4096) : 0;
     p->mp2 = multi && info.order == 4 && info.factors[3] == 64;
     if (p->mp2) p->R0 = info.factors[0] * 64;  // the sub-row count of pass B
     p->mpL = multi ? ((info.order == 3 || p->mp2) ? kMpLtc : kMpL) : 0;
@@ -554,6 +585,9 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     const size_t o_twf = append(blob, T.twf), o_twi = append(blob, T.twi);
     const size_t outer_end = o_twi + T.twi.size() * sizeof(float);
     const size_t o_fmat = need_fmat ? append(blob, fmat) : 0;
+    std::vector<float> ftin, ftout;
+    if (p->ftc) ftc_twiddle_tables(p->ftc, ftin, ftout);
+    const size_t o_ftin = p->ftc ? append(blob, ftin) : 0, o_ftout = p->ftc ? append(blob, ftout) : 0;
     size_t o_ofa = 0, o_oic = 0, o_ofull = 0;
     if (multi) {
         o_ofa = append(blob, T0.of);
@@ -596,6 +630,10 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     uint8_t* d = static_cast<uint8_t*>(p->dev);
     p->dev_err = reinterpret_cast<int*>(d + o_err);
     if (need_fmat) p->fmat = reinterpret_cast<const uint32_t*>(d + o_fmat);
+    if (p->ftc) {
+        p->ftw_in = reinterpret_cast<const float2*>(d + o_ftin);
+        p->ftw_out = reinterpret_cast<const float4*>(d + o_ftout);
+    }
     p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);
     p->tb.rf = reinterpret_cast<const uint4*>(d + o_rf);
     p->tb.tw = reinterpret_cast<const float4*>(d + o_tw);

@@ -1,6 +1,6 @@
 // Fused causal long convolution for N = M = R0 * 4096 (R0 = 2: N = 8192,
-// R0 = 4: N = 16384) in one kernel on the fifth-generation tensor cores
-// (tcgen05): the whole row stays on the SM.
+// R0 = 4: N = 16384, R0 = 8: N = 32768, i.e. 2N <= 64K) in one kernel on the
+// fifth-generation tensor cores (tcgen05): the whole row stays on the SM.
 //
 // Monarch factorization (FlashFFTConv page, section 3.4, "The Monarch FFT
 // Decomposition" and "Higher-order decompositions"), decimation in
@@ -25,16 +25,25 @@
 // to its two contributions S = V1 + V3 and D = -i (V1 - V3) (V_k0 =
 // W_M^(n' k0) T_k0), kept per thread in shared memory in 16-bit, and pair
 // (0, 2) adds them: y_z[n'] = (T0 + V2 + S) / 2, y_z[4096 + n'] =
-// (T0 - V2 + D) / 2, conjugated.
+// (T0 - V2 + D) / 2, conjugated.  R0 = 8 accumulates the four pairs'
+// contributions c_p[n0] = W_8^(n0 kA) V_kA + W_8^(n0 kB) V_kB to the four
+// output blocks n0 < 4 in a shared 16-bit accumulator, in the order pair
+// (1, 7), (2, 6), (3, 5), (0, 4); the last one writes y.
 //
-// Each CTA runs two independent pipelines of eight warps (as tcpass.cuh);
-// a pipeline owns a contiguous range of rows taken channel-major (the B
-// rows of a channel use the same k_f back to back through L2).  The row of
-// u (and, for R0 = 2, w_in) is staged by a bulk copy (TMA engine), issued
-// as soon as the previous row's last input phase has read its staging.
-// Gated R0 = 4 reads w_in through L2 in the row's first input phase and
-// writes the gated row back into the staging for the second pair (each
-// position of the staging is read and written by one thread only).
+// Each CTA runs two pipelines of eight warps (as tcpass.cuh).  For R0 = 2
+// and 4 they are independent: a pipeline owns a contiguous range of rows
+// taken channel-major (the B rows of a channel use the same k_f back to back
+// through L2), and the row of u (and, for R0 = 2, w_in) is staged by a bulk
+// copy (TMA engine) as soon as the previous row's last input phase has read
+// its staging.  Gated R0 = 4 reads w_in through L2 in the row's first input
+// phase and writes the gated row back into the staging for the second pair
+// (each position of the staging is read and written by one thread only).
+// For R0 = 8 a row (64 KB staged, 64 KB of accumulator) only fits once per
+// SM, so both pipelines work on the same rows: pipeline 0 takes pairs
+// (1, 7) and (3, 5), pipeline 1 pairs (2, 6) and (0, 4).  Two mbarriers pass
+// the accumulator between them in the order above, a third one tells
+// pipeline 1 that both have read the staged row, after which it stages the
+// next; gated R0 = 8 reads w_in through L2 in every input phase.
 #pragma once
 #include "tcpass.cuh"
 
@@ -47,14 +56,21 @@ struct FtcArgs {
     const uint4* kf;        // [h][pair][chunk 17][warp 4][half 2][lane 32] uint4 (the pass-B layout)
     uint16_t* y;
     const uint32_t* fmat;   // the three 64 x 64 DFT matrices of tcconv.cuh
+    // per-thread starting twiddles, built with the plan (ftc_twiddle_tables):
+    // input phase  W_M^(k0 n') / sqrt(R0) at n' = 1024 (t / 64) + t % 64, [k0][t 256]
+    // S4 post      W_M^(k0 n') at n' = 64 kappa_b + 32 hf + 2q + e, [k0][b][t 256] as
+    //              (re e0, re e1, im e0, im e1)
+    const float2* twin;
+    const float4* twout;
     int B, H;
     int* err;
 };
 
 template <int R0, bool GATED>
 struct Ftc {
-    static_assert(R0 == 2 || R0 == 4, "fused tensor-core path: N = 8192 or 16384");
+    static_assert(R0 == 2 || R0 == 4 || R0 == 8, "fused tensor-core path: N = 8192, 16384 or 32768");
     static constexpr int L = 4096, M = R0 * L, NP = R0 / 2;  // sub-row length, row length, pairs per row
+    static constexpr bool SPLIT = R0 == 8;                   // both pipelines on one row
     static constexpr int THREADS = 512;                      // two pipelines of 256
     static constexpr uint32_t LBO1 = TcB::LBO1, SBO1 = TcB::SBO1;
     static constexpr uint32_t LBO2 = TcB::LBO2, SBO2 = TcB::SBO2;
@@ -64,26 +80,24 @@ struct Ftc {
     static constexpr uint32_t ZB = uint32_t(M / 2) * 4;              // a row of u: M/2 complex words
     static constexpr uint32_t WIB = (GATED && R0 == 2) ? ZB : 0;     // staged w_in
     static constexpr uint32_t TOB = R0 == 4 ? 8u * 256u * 16u : 0;   // S, D of pair (1, 3): [8][tg] uint4
+    static constexpr uint32_t ACCB = SPLIT ? 32u * 256u * 8u : 0;    // R0 = 8: [b 2][jj 4][n0 4][tg] uint2
+    // per pipeline: the B buffer, and (unless SPLIT) the staging and the handed-over outputs
     static constexpr uint32_t OFF_B = 0, OFF_Z = BBUF, OFF_WI = OFF_Z + ZB, OFF_TO = OFF_WI + WIB;
-    static constexpr uint32_t PIPE = OFF_TO + TOB;
+    static constexpr uint32_t PIPE = SPLIT ? BBUF : OFF_TO + TOB;
+    static constexpr uint32_t OFF_ZS = 2 * PIPE, OFF_ACC = OFF_ZS + (SPLIT ? ZB : 0);  // SPLIT: shared
     // twiddles W_L^(kappa o) of S1 / S3 post per thread, [b 2][jj 4][tg 256]:
     // float32 where that fits, else two 16-bit pairs (binary16)
-    static constexpr bool TW16 = 2 * PIPE + 8u * 256u * 16u + 1024u > 232448u;
+    static constexpr uint32_t SHARED_END = OFF_ACC + ACCB;
+    static constexpr bool TW16 = SHARED_END + 8u * 256u * 16u + 1024u > 232448u;
     static constexpr uint32_t TWB = TW16 ? 8u * 256u * 8u : 8u * 256u * 16u;
-    static constexpr uint32_t OFF_TW = 2 * PIPE, OFF_W64 = OFF_TW + TWB;
+    static constexpr uint32_t OFF_TW = SHARED_END, OFF_W64 = OFF_TW + TWB;
     static constexpr uint32_t OFF_STEP = OFF_W64 + 512;              // W_M^(64 k0), W_M^(8 k0) per k0: float4
+    // barriers: per pipeline (contraction, staging); SPLIT: staging read by both,
+    // accumulator handed to pipeline 1, accumulator handed to pipeline 0
     static constexpr uint32_t OFF_BAR = OFF_STEP + R0 * 16;
-    static constexpr uint32_t SMEM = OFF_BAR + 4 * 8;
+    static constexpr uint32_t SMEM = OFF_BAR + 8 * 8;
     static constexpr uint32_t TMEM_COLS = 512;
 };
-
-// c^k for a small exponent (k < 8).
-__device__ __forceinline__ cpx cpow_small(cpx c, int k) {
-    cpx p = {1.f, 0.f};
-    #pragma unroll 1
-    for (int i = 0; i < k; ++i) p = cmul(p, c);
-    return p;
-}
 
 template <int DT, int R0, bool GATED>
 __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
@@ -98,12 +112,17 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
     const int hf = tg >> 7, w = (tg >> 5) & 3, lane = tg & 31, r = lane >> 2, q = lane & 3;
     uint8_t* pb = smem + g * C::PIPE;
     uint8_t* bbuf = pb + C::OFF_B;
-    uint32_t* zs = reinterpret_cast<uint32_t*>(pb + C::OFF_Z);
+    uint32_t* zs = reinterpret_cast<uint32_t*>(C::SPLIT ? smem + C::OFF_ZS : pb + C::OFF_Z);
+    uint2* accs = reinterpret_cast<uint2*>(smem + C::OFF_ACC) + tg;  // R0 = 8: [(b 4 + jj) 4 + n0] x 256 threads
     const uint32_t* wis = reinterpret_cast<const uint32_t*>(pb + C::OFF_WI);
     uint4* tout = reinterpret_cast<uint4*>(pb + C::OFF_TO) + tg;  // [b 2][jj 4] x 256 threads
     const float4* w64 = reinterpret_cast<const float4*>(smem + C::OFF_W64);
     const float4* steps = reinterpret_cast<const float4*>(smem + C::OFF_STEP);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * g;  // mma, in
+    uint64_t* zfree = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 4;      // R0 = 8 (count 2)
+    uint64_t* accbar = zfree + 1;                                              // R0 = 8: [to pipeline 1, to 0]
+    // R0 = 8: both pipelines stage from one barrier (pipeline 0's slot)
+    uint64_t* zbar = C::SPLIT ? reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 1 : &bars[1];
 
     // twiddle (wr0, wr1, wi0, wi1) of this thread's chunk bj = 4 b + jj
     auto twl = [&](int bj) -> float4 {
@@ -116,11 +135,20 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         }
     };
 
-    // rows of this pipeline: a contiguous range in channel-major order (row
-    // index h*B + b, memory row b*H + h); items: the row's pairs, NP - 1 .. 0
+    // rows of this pipeline (R0 = 8: of this CTA): a contiguous range in
+    // channel-major order (row index h*B + b, memory row b*H + h).  Items:
+    // the row's pairs, NP - 1 .. 0 (R0 = 8: pipeline 0 pairs 1, 3, pipeline
+    // 1 pairs 2, 0).
     const int rows = a.B * a.H;  // the host guarantees B*H < 2^30
-    const int V = int(gridDim.x) * 2, v = int(blockIdx.x) * 2 + g;
-    const int i0 = int(int64_t(v) * rows / V) * NP, i1 = int(int64_t(v + 1) * rows / V) * NP;
+    const int V = C::SPLIT ? int(gridDim.x) : int(gridDim.x) * 2;
+    const int v = C::SPLIT ? int(blockIdx.x) : int(blockIdx.x) * 2 + g;
+    constexpr int IPR = C::SPLIT ? 2 : NP;  // items per row of one pipeline
+    const int i0 = int(int64_t(v) * rows / V) * IPR, i1 = int(int64_t(v + 1) * rows / V) * IPR;
+    auto item_row = [&](int it) -> int { return it / IPR; };
+    auto item_pair = [&](int it) -> int {
+        if constexpr (C::SPLIT) return g == 0 ? ((it & 1) ? 3 : 1) : ((it & 1) ? 0 : 2);
+        return NP - 1 - (it - (it / NP) * NP);
+    };
     auto chan = [&](int ri) -> int { return int(unsigned(ri) / unsigned(a.B)); };
     auto mrow = [&](int ri) -> size_t {
         const int h = chan(ri), b = ri - h * a.B;
@@ -132,7 +160,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
     auto stage_row = [&](int ri, uint8_t* pbp, uint64_t* bp) {
         const size_t off = mrow(ri) * M;
         mbar_expect_tx(&bp[1], C::ZB + C::WIB);
-        bulk_g2s(pbp + C::OFF_Z, a.u + off, C::ZB, &bp[1]);
+        bulk_g2s(C::SPLIT ? smem + C::OFF_ZS : pbp + C::OFF_Z, a.u + off, C::ZB, &bp[1]);
         if (GATED && R0 == 2) bulk_g2s(pbp + C::OFF_WI, a.w_in + off, C::ZB, &bp[1]);
         if (GATED && R0 == 4) bulk_prefetch_l2(a.w_in + off, C::ZB);
         if (GATED) bulk_prefetch_l2(a.w_out + off, C::ZB);
@@ -142,12 +170,17 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + i, 1);
         fence_mbar_init();
-        for (int gp = 0; gp < 2; ++gp) {  // the first row of both pipelines, overlapping the set-up
-            const int vp = int(blockIdx.x) * 2 + gp;
-            const int j0 = int(int64_t(vp) * rows / V) * NP, j1 = int(int64_t(vp + 1) * rows / V) * NP;
+        if (C::SPLIT) mbar_init(zfree, 2);
+        if (C::SPLIT) mbar_init(accbar, 256);
+        if (C::SPLIT) mbar_init(accbar + 1, 256);
+        fence_mbar_init();
+        for (int gp = 0; gp < (C::SPLIT ? 1 : 2); ++gp) {  // the first row of both pipelines, overlapping the set-up
+            const int vp = C::SPLIT ? int(blockIdx.x) : int(blockIdx.x) * 2 + gp;
+            const int j0 = int(int64_t(vp) * rows / V) * IPR, j1 = int(int64_t(vp + 1) * rows / V) * IPR;
             if (j0 < j1) {
-                stage_row(j0 / NP, smem + gp * C::PIPE, reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * gp);
-                bulk_prefetch_l2(kf_of(chan(j0 / NP), NP - 1), TcB::KFP * 16);
+                stage_row(j0 / IPR, smem + gp * C::PIPE, reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * gp);
+                for (int k = 0; k < (C::SPLIT ? 4 : 1); ++k)
+                    bulk_prefetch_l2(kf_of(chan(j0 / IPR), C::SPLIT ? k : NP - 1), TcB::KFP * 16);
             }
         }
     }
@@ -228,34 +261,76 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
 
     const uint32_t bsm = smem_u32(bbuf);
     constexpr uint32_t id128 = tc::idesc(DT, 128, 128), id144 = tc::idesc(DT, 128, 144);
-    const float scale = R0 == 2 ? 0.70710678118654752f : 0.5f;  // 1 / sqrt(R0)
+    const float scale = R0 == 2 ? 0.70710678118654752f : (R0 == 4 ? 0.5f : 0.35355339059327373f);  // 1 / sqrt(R0)
 
     bool mma_pending = false, in_pending = i0 < i1;  // the first row's copies were issued in the set-up
     uint32_t mmapar = 0, inpar = 0;
+    uint32_t zfpar = 0, accpar = 0;  // R0 = 8: the staging-read and accumulator hand-over phases
     const uint32_t bar_id = 1 + g;
     bool failed = false;
 
     for (int it = i0; it < i1; ++it) {
-        const int ri = it / NP, p = NP - 1 - (it - ri * NP);
+        const int ri = item_row(it), p = item_pair(it);
         const int h = chan(ri);
-        const bool sp = p == 0, first = p == NP - 1, last = p == 0;
+        const bool sp = p == 0;
+        // first / last: this pipeline's first and last input phase of the row;
+        // fin: the row's output is written here
+        const bool first = (it % IPR) == 0, last = (it % IPR) == IPR - 1, fin = p == 0;
         const int kA = p, kB = p ? R0 - p : R0 / 2;
         const size_t roff = mrow(ri) * M;  // element offset of the row
         const bool has_next = it + 1 < i1;
         if (tg == 32 && has_next) {  // the next item's k_f into L2 (read by the next fold)
-            const int rn = (it + 1) / NP, pn = NP - 1 - (it + 1 - rn * NP), hn = chan(rn);
+            const int rn = item_row(it + 1), pn = item_pair(it + 1), hn = chan(rn);
             if (pn != p || hn != h) bulk_prefetch_l2(kf_of(hn, pn), TcB::KFP * 16);
         }
 
         // ---------------- input: the outer stage for sub-rows kA, kB -> B1
+        const float2 tin_a = __ldg(a.twin + kA * 256 + tg), tin_b = __ldg(a.twin + kB * 256 + tg);
         bool bad = false;
-        if (first) bad = !mbar_wait_sleep(&bars[1], inpar, kWaitSleepLimit, kWaitHintNs);
+        if (first) bad = !mbar_wait_sleep(zbar, inpar, kWaitSleepLimit, kWaitHintNs);
+        constexpr int NZW = R0 == 8 ? 4 : (R0 == 4 ? 2 : 1);  // nonzero input blocks n0 < R0/2
         uint32_t zlo[16], zhi[16];
-        if (!bad) {
+        if (!bad && R0 == 8) {
+            // the radix-8 stage over the four nonzero blocks, with gating on the fly
+            const cpx wa = twiddle_pow2(uint32_t(kA), 8), wb = twiddle_pow2(uint32_t(kB), 8);  // W_8^k0
+            const float4 sa = steps[kA], sb = steps[kB];
+            float4 tw = make_float4(tin_a.x, tin_b.x, tin_a.y, tin_b.y);
+            const float4 st = make_float4(sa.x, sb.x, sa.y, sb.y);
+            const uint32_t* wr = GATED ? reinterpret_cast<const uint32_t*>(a.w_in + roff) : nullptr;
+            #pragma unroll 1
+            for (int gq = 0; gq < 4; ++gq) {  // inputs n1 = 16 grp + 4 gq + 0..3
+                uint32_t xa[4], xb[4];
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t n = in_n + 64 * uint32_t(4 * gq + e);
+                    cpx zz[4];
+                    #pragma unroll
+                    for (int n0 = 0; n0 < 4; ++n0) {
+                        uint32_t wd = zs[4096 * n0 + n];
+                        if (GATED) wd = O::mul2(wd, __ldg(wr + 4096 * n0 + n));
+                        zz[n0] = O::unpack(wd);
+                    }
+                    // sum_n0 W_8^(n0 k0) z_n0 by Horner's rule, for kA and kB
+                    cpx xA = zz[3], xB = zz[3];
+                    #pragma unroll
+                    for (int n0 = 2; n0 >= 0; --n0) {
+                        xA = cmul(xA, wa); xA.r += zz[n0].r; xA.i += zz[n0].i;
+                        xB = cmul(xB, wb); xB.r += zz[n0].r; xB.i += zz[n0].i;
+                    }
+                    const float4 x = cmul2_split(xA.r, xB.r, xA.i, xB.i, tw);
+                    xa[e] = O::pack(x.x, x.z);
+                    xb[e] = O::pack(x.y, x.w);
+                    tw = cmul2_split(tw.x, tw.y, tw.z, tw.w, st);
+                }
+                *reinterpret_cast<uint4*>(bbuf + in_dst + gq * C::LBO1) = make_uint4(xa[0], xa[1], xa[2], xa[3]);
+                *reinterpret_cast<uint4*>(bbuf + in_dst + 8 * C::SBO1 + gq * C::LBO1) =
+                    make_uint4(xb[0], xb[1], xb[2], xb[3]);
+            }
+        } else if (!bad) {
             #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 zlo[i] = zs[in_n + 64 * i];
-                zhi[i] = R0 == 4 ? zs[4096 + in_n + 64 * i] : 0u;
+                zhi[i] = NZW == 2 ? zs[4096 + in_n + 64 * i] : 0u;
             }
             if constexpr (GATED) {
                 if (R0 == 2) {
@@ -282,10 +357,8 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
             }
             // twiddles W_M^(k0 n') / sqrt(R0) along n' = in_n + 64 i, both sub-rows
             // as the two halves of packed pairs: (A, B)
-            const cpx cin = twiddle_pow2(in_n & (M - 1), M);
-            cpx ta = cpow_small(cin, kA), tb = cpow_small(cin, kB);
             const float4 sa = steps[kA], sb = steps[kB];
-            float4 tw = make_float4(ta.r * scale, tb.r * scale, ta.i * scale, tb.i * scale);
+            float4 tw = make_float4(tin_a.x, tin_b.x, tin_a.y, tin_b.y);
             const float4 st = make_float4(sa.x, sb.x, sa.y, sb.y);
             const bool odd = (p & 1) != 0;  // R0 = 4, pair (1, 3): W_4^(kA) = -i, W_4^(kB) = i
             #pragma unroll
@@ -326,7 +399,21 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         }
         mma_pending = true;
         if (last && has_next) {  // the staging is free: fetch the next row
-            if (tg == 64) stage_row(ri + 1, pb, bars);
+            if constexpr (C::SPLIT) {
+                // both pipelines have to be done with it; pipeline 1 stages the next row
+                if (tg == 64) {
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(zfree)) : "memory");
+                    if (g == 1) {
+                        if (mbar_wait_sleep(zfree, zfpar, kWaitSleepLimit, kWaitHintNs))
+                            stage_row(ri + 1, smem, reinterpret_cast<uint64_t*>(smem + C::OFF_BAR));
+                        else
+                            atomicExch(a.err, 7);  // the next row's staging wait then gives up too
+                    }
+                }
+                zfpar ^= 1;
+            } else {
+                if (tg == 64) stage_row(ri + 1, pb, bars);
+            }
             in_pending = true;
         }
 
@@ -519,8 +606,9 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         // gated, last pair: w_out at (b, jj, n0), read while the contraction
         // runs (R0 = 2; R0 = 4 reads it at the store, registers being short)
         constexpr bool WPRE = GATED && R0 == 2;
-        uint2 wov[2][4][NP];
-        if (WPRE && last) {
+        uint2 wov[2][4][NP > 2 ? 1 : NP];
+        if constexpr (WPRE) {
+          if (last) {
             #pragma unroll
             for (int b = 0; b < 2; ++b)
                 #pragma unroll
@@ -529,11 +617,86 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                     for (int n0 = 0; n0 < NP; ++n0)
                         wov[b][jj][n0] = __ldg(reinterpret_cast<const uint2*>(
                             a.w_out + roff + 2 * size_t(4096 * n0 + 64 * (b ? kapB : kapA) + 32 * hf + 2 * q + 8 * jj)));
+          }
+        }
+        // the starting twiddles of this thread's outputs, read while the contraction runs
+        float4 tstart[2][2];  // [sub-row A, B][b]
+        #pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tstart[0][b] = __ldg(a.twout + (kA * 2 + b) * 256 + tg);
+            tstart[1][b] = __ldg(a.twout + (kB * 2 + b) * 256 + tg);
         }
         bad = !mbar_wait_sleep(&bars[0], mmapar, kWaitSleepLimit, kWaitHintNs);
+        // R0 = 8: the accumulator's turn (pair 1 of the CTA's first row starts it)
+        const bool acc_wait = C::SPLIT && !(p == 1 && it == i0);
+        if (acc_wait) bad |= !mbar_wait_sleep(&accbar[g == 0 ? 1 : 0], accpar, kWaitSleepLimit, kWaitHintNs);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
-        if (!bad) {
+        if (acc_wait) accpar ^= 1;
+        if constexpr (C::SPLIT) {
+          if (!bad) {
+            uint32_t vr[2][2][16];
+            tc::ld16x256b_x4(tD + laneA + 32 * hf, vr[0][0]);
+            tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
+            tc::ld16x256b_x4(tD + laneA + 64 + 32 * hf, vr[1][0]);
+            tc::ld16x256b_x4(tD + laneB + 64 + 32 * hf, vr[1][1]);
+            // c[n0] = W_8^(n0 kA) V_A + W_8^(n0 kB) V_B, V = W_M^(k0 n') T, added
+            // to the accumulator of the four output blocks n0 < 4
+            const cpx wa = twiddle_pow2(uint32_t(kA), 8), wb = twiddle_pow2(uint32_t(kB), 8);
+            const float4 sB = steps[kB], sA = steps[kA];
+            const float4 stB = make_float4(sB.z, sB.z, sB.w, sB.w), stA = make_float4(sA.z, sA.z, sA.w, sA.w);
+            tc::wait_ld();
+            #pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const uint32_t n0p = uint32_t(64 * (b ? kapB : kapA) + 32 * hf + 2 * q);
+                float4 twA = tstart[0][b], twB = tstart[1][b];
+                #pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const uint32_t* va = vr[0][b] + 4 * jj;
+                    const uint32_t* vb = vr[1][b] + 4 * jj;
+                    const float4 vA = cmul2_split(__uint_as_float(va[0]), __uint_as_float(va[1]), __uint_as_float(va[2]),
+                                                  __uint_as_float(va[3]), twA);
+                    const float4 vB = cmul2_split(__uint_as_float(vb[0]), __uint_as_float(vb[1]), __uint_as_float(vb[2]),
+                                                  __uint_as_float(vb[3]), twB);
+                    if (jj + 1 < 4) {
+                        twA = cmul2_split(twA.x, twA.y, twA.z, twA.w, stA);
+                        twB = cmul2_split(twB.x, twB.y, twB.z, twB.w, stB);
+                    }
+                    cpx al = {1.f, 0.f}, be = {1.f, 0.f};  // W_8^(n0 kA), W_8^(n0 kB)
+                    #pragma unroll
+                    for (int n0 = 0; n0 < 4; ++n0) {
+                        const float4 x = cmul2_split(vA.x, vA.y, vA.z, vA.w, make_float4(al.r, al.r, al.i, al.i));
+                        const float4 yv = cmul2_split(vB.x, vB.y, vB.z, vB.w, make_float4(be.r, be.r, be.i, be.i));
+                        float4 cc = make_float4(x.x + yv.x, x.y + yv.y, x.z + yv.z, x.w + yv.w);
+                        uint2* ap = accs + ((4 * b + jj) * 4 + n0) * 256;
+                        if (p != 1) {  // pairs 2, 3, 0 add to the accumulator
+                            const uint2 old = *ap;
+                            const cpx o0 = O::unpack(old.x), o1 = O::unpack(old.y);
+                            cc.x += o0.r; cc.y += o1.r; cc.z += o0.i; cc.w += o1.i;
+                        }
+                        if (!fin) {
+                            *ap = make_uint2(O::pack(cc.x, cc.z), O::pack(cc.y, cc.w));
+                        } else {
+                            // y_z = conj(sum / sqrt(8)): y[2n] = Re, y[2n+1] = -Im
+                            const size_t yo = roff + 2 * size_t(n0p + 8 * jj + 4096 * n0);
+                            float r0 = scale * cc.x, r1 = scale * cc.y, im0 = -scale * cc.z, im1 = -scale * cc.w;
+                            if (GATED) {
+                                const uint2 wv = __ldg(reinterpret_cast<const uint2*>(a.w_out + yo));
+                                const cpx w0 = O::unpack(wv.x), w1 = O::unpack(wv.y);
+                                r0 *= w0.r; im0 *= w0.i; r1 *= w1.r; im1 *= w1.i;
+                            }
+                            *reinterpret_cast<uint2*>(a.y + yo) = make_uint2(O::pack(r0, im0), O::pack(r1, im1));
+                        }
+                        al = cmul(al, wa);
+                        be = cmul(be, wb);
+                    }
+                }
+            }
+            // the accumulator to the other pipeline (release of this thread's writes)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&accbar[g == 0 ? 0 : 1]))
+                         : "memory");
+          }
+        } else if (!bad) {
             uint32_t vr[2][2][16];
             tc::ld16x256b_x4(tD + laneA + 32 * hf, vr[0][0]);
             tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
@@ -547,10 +710,8 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
             #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 const uint32_t n0p = uint32_t(64 * (b ? kapB : kapA) + 32 * hf + 2 * q);
-                const cpx c0 = twiddle_pow2(n0p & (M - 1), M), c1 = twiddle_pow2((n0p + 1) & (M - 1), M);
-                const cpx b0 = cpow_small(c0, kB), b1 = cpow_small(c1, kB);
-                float4 twB = make_float4(b0.r, b1.r, b0.i, b1.i);
-                float4 twA = make_float4(c0.r, c1.r, c0.i, c1.i);  // k0 = kA = 1 on pair (1, 3)
+                float4 twB = tstart[1][b];
+                float4 twA = tstart[0][b];  // k0 = kA = 1 on pair (1, 3)
                 const uint32_t* va = vr[0][b];
                 const uint32_t* vb = vr[1][b];
                 #pragma unroll
@@ -612,7 +773,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         // record the timeout, then wait (bounded) for this pipeline's work in flight
         atomicExch(a.err, 7);
         if (mma_pending) mbar_wait_bounded(&bars[0], mmapar, kWaitLimit);
-        if (in_pending) mbar_wait_bounded(&bars[1], inpar, kWaitLimit);
+        if (in_pending) mbar_wait_bounded(zbar, inpar, kWaitLimit);
     }
     tc::fence_before();
     __syncthreads();

@@ -20,7 +20,9 @@ struct fftconv_plan_s {
     int mpL = 0;    // multi-pass sub-row length: 16384 (warp-level pass B) or 4096 (tensor-core pass B)
     bool mp2 = false;  // sub-rows of 4096 with the outer factor R0 = RA * 64 in two levels (N >= 2^20)
     bool tc64 = false;               // N = 4096: order-2 64 x 64 product on tcgen05
-    int ftc = 0;                     // N = 8192 / 16384: the fused R0 x 64 x 64 kernel on tcgen05 (R0 = 2 / 4)
+    int ftc = 0;                     // N = 8192 / 16384 / 32768: the fused R0 x 64 x 64 kernel on tcgen05
+    const float2* ftw_in = nullptr;  // its per-thread starting twiddles (device, inside dev)
+    const float4* ftw_out = nullptr;
     const uint32_t* fmat = nullptr;  // the 64 x 64 DFT matrix rows (device), N = 4096 and mpL = 4096
     // frequency-sparse plan: a band per factor (every band >= M_j/2 + 1 on a
     // dense plan); on the multi-pass path the pass-B pairs that run and the

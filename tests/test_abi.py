@@ -46,11 +46,12 @@ def test_query_fused_factorization(N, R1):
         assert q["workspace_bytes_per_row"] == 0
 
 
-@pytest.mark.parametrize("N", [8192, 16384])
+@pytest.mark.parametrize("N", [8192, 16384, 32768])
 def test_query_fused_tensor_core_factorization(N):
-    """N = 8192 and 16384 run fused as R0 x 64 x 64 (R0 = 2, 4) on the
-    fifth-generation tensor cores; k_f holds one pass-B block (17 chunks of
-    4 warps x 2 halves x 32 lanes x 16 bytes) per pair of sub-rows."""
+    """N = 8192, 16384 and 32768 (2N <= 64K) run fused as R0 x 64 x 64 (R0 =
+    2, 4, 8) on the fifth-generation tensor cores; k_f holds one pass-B block
+    (17 chunks of 4 warps x 2 halves x 32 lanes x 16 bytes) per pair of
+    sub-rows."""
     for dt in (F.F16, F.BF16):
         q = F.query(N, dt)
         assert q["path"] == F.PATH_FUSED and q["order"] == 3
@@ -71,9 +72,9 @@ def test_query_fused_order2_4096():
         assert q["workspace_bytes_per_row"] == 0
 
 
-@pytest.mark.parametrize("N,R0", [(32768, 8), (262144, 64), (524288, 128)])
+@pytest.mark.parametrize("N,R0", [(65536, 16), (262144, 64), (524288, 128)])
 def test_query_multipass_order3_factorization(N, R0):
-    """Sub-rows of 64 x 64 on the tensor cores: the default up to N = 512K."""
+    """Sub-rows of 64 x 64 on the tensor cores: the default from N = 65536 up to 512K."""
     q = F.query(N, F.BF16)
     assert q["path"] == F.PATH_MULTIPASS and q["order"] == 3
     assert q["factors"] == [R0, 64, 64]

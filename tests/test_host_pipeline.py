@@ -29,7 +29,8 @@ def _host(r, tdt, pinned=True):
     (1024, "fp16", False, 2, 8, 0),       # fused, two chunks of one batch entry
     (4096, "bf16", True, 7, 20, 0),       # tensor-memory kernel, seven chunks: buffer sets reused
     (16384, "fp16", False, 9, 5, 0),      # fused, chunks of two batch entries and a short last one
-    (32768, "bf16", False, 1, 12, 0),     # multi-pass 64 x 64, B = 1: chunks of channels (k_f offsets)
+    (65536, "bf16", False, 1, 12, 0),     # multi-pass 64 x 64, B = 1: chunks of channels (k_f offsets)
+    (32768, "bf16", False, 1, 12, 0),     # fused 8 x 64 x 64, B = 1: chunks of channels (k_f offsets)
     (65536, "fp16", True, 3, 2, 4),       # multi-pass 64 x 16 x 16
 ])
 def test_host_matches_device(N, dtype, gated, B, H, order):

@@ -10,7 +10,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 F = pytest.importorskip("fft_long_convolution_gb300")
 
-FUSED_N = [1024, 2048, 4096, 8192, 16384]
+FUSED_N = [1024, 2048, 4096, 8192, 16384, 32768]
 
 
 def _plan(N, dtype):
@@ -44,7 +44,7 @@ def test_fused_matches_oracle(N, dtype, gated):
     assert plan.device_status() == 0
 
 
-@pytest.mark.parametrize("N", [1024, 4096, 8192, 16384])
+@pytest.mark.parametrize("N", [1024, 4096, 8192, 16384, 32768])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_delta_kernels(N, dtype):
     """k = delta_s gives y[t] = u[t-s] (t >= s): pins causal truncation.
@@ -156,11 +156,13 @@ def test_tc64_many_items_every_row(dtype, gated):
 
 
 @pytest.mark.parametrize("N,dtype,gated", [(16384, "fp16", False), (16384, "bf16", True),
-                                           (8192, "bf16", False), (8192, "fp16", True)])
+                                           (8192, "bf16", False), (8192, "fp16", True),
+                                           (32768, "bf16", False), (32768, "fp16", True)])
 def test_ftc_many_rows_every_row(N, dtype, gated):
-    """N = 8192 / 16384 on the fused tensor-core kernel with several rows
-    per pipeline (the next row's staging overlaps the current row, pair
-    (1, 3) hands its outputs to pair (0, 2)); every row checked."""
+    """N = 8192 / 16384 / 32768 on the fused tensor-core kernel with several
+    rows per pipeline (the next row's staging overlaps the current row; pair
+    (1, 3) hands its outputs to pair (0, 2); for 32768 the two pipelines pass
+    the accumulator and the staging between them); every row checked."""
     w = W.Workload("t", 5, 130, N, dtype, gated, "normal", "decay", "")
     ins = W.make_inputs(w, seed=17)
     plan = _plan(N, dtype)

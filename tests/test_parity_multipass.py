@@ -20,8 +20,8 @@ def _need_gpu():
 
 
 @pytest.mark.parametrize("N,dtype,gated,B,H", [
-    (32768, "fp16", False, 2, 3),
-    (32768, "bf16", True, 1, 3),
+    (65536, "fp16", False, 2, 3),
+    (65536, "bf16", True, 1, 3),
     (65536, "bf16", False, 1, 2),
     (131072, "fp16", False, 1, 2),
     (262144, "bf16", True, 1, 2),
@@ -87,7 +87,7 @@ def test_multipass_delta_kernels(dtype):
 
 
 def test_multipass_needs_workspace():
-    N = 32768
+    N = 65536
     plan = F.Plan(N, torch.bfloat16)
     assert plan.workspace_bytes(2, 3) == 2 * 3 * N * 4
     u = torch.zeros(2, 3, N, dtype=torch.bfloat16, device="cuda")
@@ -130,7 +130,7 @@ def test_workload_full_size_sampled(name, nrows):
 
 
 @pytest.mark.parametrize("N,dtype,gated,B,H", [
-    (32768, "bf16", False, 3, 100),
+    (65536, "bf16", False, 3, 40),
     (65536, "fp16", True, 2, 40),
 ])
 def test_multipass_many_items_every_row(N, dtype, gated, B, H):

@@ -55,6 +55,7 @@ def _check(N, dtype, gated, B, H, band, order=0, seed=21, u_kind="normal", k_kin
     (4096, "bf16", True, 2, 3, [9, 20]),
     (4096, "fp16", False, 1, 2, [33, 3]),
     (16384, "fp16", False, 1, 3, [20, 9, 9]),
+    (32768, "bf16", False, 1, 2, [3, 20, 20]),
 ])
 def test_fused_sparse(N, dtype, gated, B, H, band):
     bd = _check(N, dtype, gated, B, H, band)
@@ -62,7 +63,7 @@ def test_fused_sparse(N, dtype, gated, B, H, band):
 
 
 @pytest.mark.parametrize("N,dtype,gated,B,H,band", [
-    (32768, "fp16", False, 2, 3, [3, 33, 33]),        # outer digits 0, +-1, +-2 kept
+    (65536, "fp16", False, 2, 3, [3, 33, 33]),        # outer digits 0, +-1, +-2 kept
     (65536, "bf16", True, 1, 3, [5, 20, 33]),
     (262144, "bf16", False, 1, 2, [16, 33, 33]),      # half of the pairs skipped
     (262144, "fp16", True, 1, 2, [9, 20, 7]),         # all three axes cut

@@ -22,7 +22,7 @@ def _pairs_run_brute(N, factors, band):
 
 
 CASES = [
-    (32768, 0, [3, 33, 33]),
+    (65536, 0, [3, 33, 33]),
     (65536, 0, [4, 33, 33]),
     (262144, 0, [16, 33, 33]),
     (262144, 0, [9, 20, 7]),
@@ -50,7 +50,7 @@ def test_pairs_run_matches_brute_force(N, order, band):
 
 
 def test_full_band_runs_every_pair():
-    for N in (32768, 262144, 2097152):
+    for N in (65536, 262144, 2097152):
         info = F.query(N, F.BF16)
         full = [Mj // 2 + 1 for Mj in info["factors"]]
         got = F.sparse_query(N, F.BF16, full)
