@@ -287,10 +287,12 @@ def path_of(plan_info: dict, pairs_run: Optional[int] = None) -> dict:
     if plan_info["path"] == 1:
         nb = 0 if pairs_run == 0 else 1
         if plan_info["order"] == 4 and plan_info["factors"][3] == 64:  # outer factor in two HBM levels
-            return {"kernel": "mp_pass_a x2 + mp_pass_b_tc + mp_pass_c x2 (the whole step)",
+            return {"kernel": "otc_pass (A) x2 + mp_pass_b_tc + otc_pass (C) x2 (the whole step)",
                     "launches_per_step": 4 + nb}
-        b = "mp_pass_b_tc" if plan_info["order"] == 3 else "mp_pass_b"
-        return {"kernel": f"mp_pass_a + {b} + mp_pass_c (the whole step)", "launches_per_step": 2 + nb}
+        if plan_info["order"] == 3:
+            return {"kernel": "otc_pass (A) + mp_pass_b_tc + otc_pass (C) (the whole step)",
+                    "launches_per_step": 2 + nb}
+        return {"kernel": "mp_pass_a + mp_pass_b + mp_pass_c (the whole step)", "launches_per_step": 2 + nb}
     if plan_info["order"] == 2:
         return {"kernel": "tc64_conv_kernel", "launches_per_step": 1}
     if plan_info["factors"][1] == 64:  # R0 x 64 x 64 on the tensor cores

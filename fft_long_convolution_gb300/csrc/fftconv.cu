@@ -367,6 +367,64 @@ void ftc_twiddle_tables(int R0, std::vector<float>& tin, std::vector<float>& tou
         }
 }
 
+// The real-embedded DFT matrix of an outer pass on the tensor cores
+// (otc.cuh), F[o][n] = W_R^(o n) / sqrt(R) for the pass's outputs o and
+// inputs n (pass A: o = k0, n = n0 < NIN; pass C: o = n0 < NOUT, n = k0), as
+// the B operand of Otc<R, MODE>: row 2 o + part (0 real, 1 imaginary part of
+// output o), K index 2 n + pin (0 real, 1 imaginary part of input n),
+// K-major without swizzle; padding rows and K indices zero.
+template <int R, int MODE>
+std::vector<uint16_t> build_otc_fmat(int dtype) {
+    using C = Otc<R, MODE>;
+    std::vector<uint16_t> v(C::BBYTES / 2, 0);
+    const double sc = 1.0 / std::sqrt(double(R));
+    for (int o = 0; o < C::NOUT; ++o)
+        for (int part = 0; part < 2; ++part) {
+            const int row = 2 * o + part;
+            for (int n = 0; n < C::NIN; ++n) {
+                cd w = W(R, int64_t(o) * n);
+                w = {w.r * sc, w.i * sc};
+                for (int pin = 0; pin < 2; ++pin) {
+                    const int k = 2 * n + pin;
+                    const size_t off = size_t(row / 8) * C::SBO + size_t(k / 8) * C::LBO + size_t(row % 8) * 16 +
+                                       size_t(k % 8) * 2;
+                    v[off / 2] = to_bits(embed(w, part, pin), dtype);
+                }
+            }
+        }
+    return v;
+}
+
+// The outer-pass matrices a multi-pass plan with 4096-point sub-rows uses:
+// pass A and pass C over the outermost factor (R0, or RA of a two-level
+// factor) and, for two levels, the in-place 64-point stages.
+struct OtcTables {
+    std::vector<uint16_t> fa, fc, fa2, fc2;
+};
+
+template <int R>
+void otc_outer(OtcTables& t, int dtype) {
+    t.fa = build_otc_fmat<R, 0>(dtype);
+    t.fc = build_otc_fmat<R, 3>(dtype);
+}
+
+OtcTables build_otc_tables(int R, bool two_level, int dtype) {
+    OtcTables t;
+    switch (R) {
+        case 4: otc_outer<4>(t, dtype); break;
+        case 8: otc_outer<8>(t, dtype); break;
+        case 16: otc_outer<16>(t, dtype); break;
+        case 32: otc_outer<32>(t, dtype); break;
+        case 64: otc_outer<64>(t, dtype); break;
+        case 128: otc_outer<128>(t, dtype); break;
+    }
+    if (two_level) {
+        t.fa2 = build_otc_fmat<64, 1>(dtype);
+        t.fc2 = build_otc_fmat<64, 2>(dtype);
+    }
+    return t;
+}
+
 template <typename T>
 size_t append(std::vector<uint8_t>& blob, const std::vector<T>& v) {
     size_t off = (blob.size() + 255) & ~size_t(255);
@@ -588,6 +646,11 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     std::vector<float> ftin, ftout;
     if (p->ftc) ftc_twiddle_tables(p->ftc, ftin, ftout);
     const size_t o_ftin = p->ftc ? append(blob, ftin) : 0, o_ftout = p->ftc ? append(blob, ftout) : 0;
+    const bool otc = p->mpL == kMpLtc;
+    OtcTables ot;
+    if (otc) ot = build_otc_tables(p->mp2 ? info.factors[0] : p->R0, p->mp2, dtype);
+    const size_t o_tfa = otc ? append(blob, ot.fa) : 0, o_tfc = otc ? append(blob, ot.fc) : 0;
+    const size_t o_tfa2 = (otc && p->mp2) ? append(blob, ot.fa2) : 0, o_tfc2 = (otc && p->mp2) ? append(blob, ot.fc2) : 0;
     size_t o_ofa = 0, o_oic = 0, o_ofull = 0;
     if (multi) {
         o_ofa = append(blob, T0.of);
@@ -633,6 +696,14 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     if (p->ftc) {
         p->ftw_in = reinterpret_cast<const float2*>(d + o_ftin);
         p->ftw_out = reinterpret_cast<const float4*>(d + o_ftout);
+    }
+    if (otc) {
+        p->otc_fa = d + o_tfa;
+        p->otc_fc = d + o_tfc;
+        if (p->mp2) {
+            p->otc_fa2 = d + o_tfa2;
+            p->otc_fc2 = d + o_tfc2;
+        }
     }
     p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);
     p->tb.rf = reinterpret_cast<const uint4*>(d + o_rf);

@@ -163,6 +163,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
+// Bounded waits of the tensor-core kernels: polls that may each suspend for
+// up to 2 us (at most about 2 s in total before the kernel reports a timeout).
+constexpr uint32_t kWaitSleepLimit = 1u << 20, kWaitHintNs = 2000;
+
 // Same, but each poll may suspend the thread for up to `hint_ns` nanoseconds
 // until the phase completes, so waiting warps do not compete for issue slots.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t limit, uint32_t hint_ns) {
@@ -194,6 +198,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Three-dimensional tiled copy global -> shared through the TMA engine (the
+// box of the tensor map at coordinates x, y, z, innermost first), completing
+// on `bar` with its byte count.  x times the element size must be a multiple
+// of 16 bytes; the destination is 128-byte aligned.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -30,6 +30,12 @@ cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, 
     if (items_b >= (int64_t(1) << 30)) return cudaErrorInvalidValue;  // pass B counts items in int
     const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);
     TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, 0, p->pairs_run, p->plist};
+    if constexpr (!SP) {  // dense: the outer passes on the tensor cores
+        if ((e = launch_otc<DT, R0, 0, G, L>(p, args, rows, p->otc_fa, st)) != cudaSuccess) return e;
+        if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return launch_otc<DT, R0, 3, G, L>(p, args, rows, p->otc_fc, st);
+    }
     mp_pass_a<DT, R0, G, L, false, SP><<<grid(items_ac, na), 256, smem_a, st>>>(args);
     if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
     mp_pass_c<DT, R0, G, L, true, false, SP><<<grid(items_ac, nc), 32 * mp_pass_c_warps<R0>(), smem_c, st>>>(args);
@@ -38,8 +44,7 @@ cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, 
 
 template <int DT, bool G, bool SP>
 cudaError_t launch_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    switch (p->R0) {
-        case 8: return launch_t<DT, 8, G, SP>(p, args, rows, st);
+    switch (p->R0) {  // N = 32768 (R0 = 8) runs fused
         case 16: return launch_t<DT, 16, G, SP>(p, args, rows, st);
         case 32: return launch_t<DT, 32, G, SP>(p, args, rows, st);
         case 64: return launch_t<DT, 64, G, SP>(p, args, rows, st);
@@ -83,6 +88,14 @@ cudaError_t launch_2l_t(const fftconv_plan_s* p, const MPArgs& args, int64_t row
     inner.w_in = inner.w_out = nullptr;
     inner.zmod = RA;      // inner row r holds sub-rows k0 = (r mod RA) + RA j, j < 64
     TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, RA, p->pairs_run, p->plist};
+    if constexpr (!SP) {  // dense: the four outer passes on the tensor cores
+        if ((e = launch_otc<DT, RA, 0, G, L1>(p, outer, rows, p->otc_fa, st)) != cudaSuccess) return e;
+        if ((e = launch_otc<DT, 64, 1, false, L>(p, inner, rows * RA, p->otc_fa2, st)) != cudaSuccess) return e;
+        if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_otc<DT, 64, 2, false, L>(p, inner, rows * RA, p->otc_fc2, st)) != cudaSuccess) return e;
+        return launch_otc<DT, RA, 3, G, L1>(p, outer, rows, p->otc_fc, st);
+    }
     mp_pass_a<DT, RA, G, L1><<<grid(items1, na1), 256, smem_a1, st>>>(outer);
     mp_pass_a<DT, 64, false, L, true, SP><<<grid(items2, na2), 256, smem_a2, st>>>(inner);
     if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);

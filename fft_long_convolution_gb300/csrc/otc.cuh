@@ -1,0 +1,294 @@
+// Outer passes of the multi-pass path on the fifth-generation tensor cores
+// (tcgen05): pass A (forward outer stage, from u or in place on T) and pass
+// C (inverse outer stage, in place on T or to y).
+//
+// FlashFFTConv page, section 3.4 "Kernel Fusion and Recomputation
+// Strategies": the outermost Monarch factor goes through HBM.  With the
+// row of length M = R * L viewed as R sub-rows of L columns (n = L n0 + n',
+// k = k0 + R kappa):
+//   pass A  T[k0][n'] = W_M^(n' k0) sum_{n0 < NIN} x[n0][n'] W_R^(n0 k0) / sqrt(R)
+//           MODE 0: x = z (the packed row of u, times w_in), NIN = R/2 (the
+//           implicit zero padding); MODE 1: x = T itself, NIN = R (an inner
+//           stage of a two-level outer factor), written back in place
+//   pass C  out[n0][n'] = sum_{k0} W_R^(n0 k0) W_M^(n' k0) T[k0][n'] / sqrt(R)
+//           MODE 2: all R outputs, in place; MODE 3: n0 < R/2 only (the
+//           causal truncation), y_z = conj(out) (times w_out)
+//
+// One CTA of 128 threads walks tiles of 128 columns of one row; thread t
+// owns column t of the tile.  A tile's input rows are staged by one tiled
+// copy of the TMA engine (a box of 128 columns x all input rows of a
+// three-dimensional tensor map: columns, input rows, rows) in a ring of NST
+// buffers issued NST tiles ahead.  Each thread
+// moves its column into the K-major A operand of the contraction (M = the
+// 128 columns, K = the real-embedded inputs), multiplying by w_in (MODE 0)
+// or by W_M^(n' k0) (MODE 2, 3: a product chain along k0); one thread issues
+// D = X F on the tensor cores (F: the real-embedded DFT matrix as the B
+// operand, N = the outputs, real and imaginary part adjacent, padded to a
+// multiple of 16; both operands in shared memory; D float32 in tensor
+// memory, double-buffered so that the contraction of a tile runs during the
+// epilogue of the one before).  In the epilogue tensor-memory lane t is
+// column t: the thread reads all outputs of its column, applies the output
+// twiddle W_M^(n' k0) (pass A, a chain along k0) or the conjugation and
+// gate (MODE 3), and every output row is written as 128-byte runs per warp.
+#pragma once
+#include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime)
+
+#include "multipass.cuh"
+#include "tc.cuh"
+
+namespace fftconv {
+
+template <int R, int MODE>
+struct Otc {
+    static_assert(R >= 4 && R <= 128 && MODE >= 0 && MODE <= 3, "outer pass shape");
+    static constexpr bool FWD = MODE <= 1;
+    static constexpr int NIN = MODE == 0 ? R / 2 : R;            // input rows
+    static constexpr int NOUT = MODE == 3 ? R / 2 : R;           // outputs kept
+    static constexpr int TC = 128, THREADS = 128;                // columns per tile = threads = the MMA's M
+    static constexpr int KP = 2 * NIN < 16 ? 16 : 2 * NIN;       // K of the contraction (real), padded
+    static constexpr int NP = (2 * NOUT + 15) / 16 * 16;         // N (output re/im), padded
+    static constexpr int NG = KP / 8;                            // groups of four complex inputs (16 bytes)
+    // operand layouts (K-major, no swizzle): element (row, k) at
+    // (row/8) SBO + (k/8) LBO + (row%8) 16 + (k%8) 2 bytes
+    static constexpr uint32_t LBO = 128, SBO = (KP / 8) * 128;
+    static constexpr uint32_t ABYTES = (TC / 8) * SBO;             // the data tile
+    static constexpr uint32_t BBYTES = uint32_t(NP / 8) * SBO;     // the DFT matrix
+    static constexpr int SEG = TC;                               // staged row segment (words)
+    static constexpr uint32_t STAGE_WORDS = uint32_t(NIN) * SEG;
+    static constexpr int NST = NIN <= 16 ? 4 : (NIN <= 32 ? 2 : 1);  // staged tiles in flight
+    static constexpr uint32_t DCOLS = NP;                            // tensor-memory columns per accumulator
+    static constexpr uint32_t TMEM_COLS = 2 * DCOLS < 32 ? 32 : 2 * DCOLS;  // double-buffered (allocation >= 32)
+};
+
+template <int R, int MODE, bool GATED>
+constexpr size_t otc_smem() {
+    using C = Otc<R, MODE>;
+    return size_t(C::ABYTES) + size_t(C::BBYTES) + size_t(C::NST) * C::STAGE_WORDS * 4 * ((GATED && MODE == 0) ? 2 : 1) +
+           size_t(C::TC) * 8 + size_t(C::NST + 3) * 8 + 64;
+}
+
+// tin: the input rows (MODE 0: u as 32-bit words, [rows][R/2][L]; else T,
+// [rows][R][L]); tgate: w_in in u's shape (gated MODE 0).
+template <int DT, int R, int MODE, bool GATED, int L>
+__global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* __restrict__ fmat,
+                                                const __grid_constant__ CUtensorMap tin,
+                                                const __grid_constant__ CUtensorMap tgate) {
+    using O = Op<DT>;
+    using C = Otc<R, MODE>;
+    static_assert(!(GATED && (MODE == 1 || MODE == 2)), "the inner stages have no gates");
+    constexpr uint32_t M = uint32_t(R) * L;  // the twiddle modulus (the row length of this pass)
+    constexpr int TILES = L / C::TC;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint32_t s_tmem;
+    // W_M^(o_base) of a tile, by local tile index mod 3: tile i's value is read
+    // in its own reformat and epilogue (the next iteration), and rewritten
+    // by tile i + 3 only after every thread has passed tile i + 1's barrier
+    __shared__ float2 s_pt[3];
+
+    uint8_t* sa = smem;                                          // data tile (A operand)
+    uint8_t* sf = sa + C::ABYTES;                                // DFT matrix (B operand)
+    uint32_t* st = reinterpret_cast<uint32_t*>(sf + C::BBYTES);  // [NST][NIN][SEG]
+    uint32_t* sw = st + C::NST * C::STAGE_WORDS;                 // gated pass A: w_in, same shape
+    float2* qtab = reinterpret_cast<float2*>(sw + ((GATED && MODE == 0) ? C::NST * C::STAGE_WORDS : 0));  // W_M^c, c < TC
+    uint64_t* full = reinterpret_cast<uint64_t*>(qtab + C::TC);  // [NST] staged tile arrived
+    uint64_t* mbar = full + C::NST;                              // [2] contraction done, per accumulator
+    uint64_t* fbar = mbar + 2;                                   // DFT matrix arrived
+
+    const int t = threadIdx.x, wq = t >> 5;
+    const long rows = long(a.B) * a.H;
+    const long items = rows * TILES;
+    const long first_item = blockIdx.x, stride = gridDim.x;
+
+    auto stage = [&](long item, int s) {  // the tile's input rows into staging slot s
+        const int row = int(item / TILES);
+        const int o_base = int(item % TILES) * C::TC;
+        mbar_expect_tx(&full[s], C::STAGE_WORDS * 4u * ((GATED && MODE == 0) ? 2u : 1u));
+        tma_load_3d(st + s * C::STAGE_WORDS, &tin, o_base, 0, row, &full[s]);
+        if (GATED && MODE == 0) tma_load_3d(sw + s * C::STAGE_WORDS, &tgate, o_base, 0, row, &full[s]);
+    };
+
+    // ---------------- set-up
+    // thread 0's record of what is in flight: staging slots with copies
+    // issued and not yet consumed, and the contractions per accumulator
+    uint32_t issued = 0, mma_pending = 0;
+    if (t == 0) {
+        for (int s = 0; s < C::NST + 3; ++s) mbar_init(full + s, 1);
+        fence_mbar_init();
+        mbar_expect_tx(fbar, C::BBYTES);
+        bulk_g2s(sf, fmat, C::BBYTES, fbar);
+        for (int s = 0; s < C::NST; ++s)
+            if (first_item + s * stride < items) {
+                stage(first_item + s * stride, s);
+                issued |= 1u << s;
+            }
+    }
+    if (wq == 0) tc::alloc(&s_tmem, C::TMEM_COLS);
+    for (uint32_t i = t; i < C::ABYTES / 16; i += blockDim.x)  // K padding stays zero
+        reinterpret_cast<uint4*>(sa)[i] = make_uint4(0, 0, 0, 0);
+    {
+        const cpx v = twiddle_pow2(uint32_t(t) & (M - 1), M);
+        qtab[t] = make_float2(v.r, v.i);
+    }
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = s_tmem;
+    bool failed = __syncthreads_or(!mbar_wait_bounded(fbar, 0, kWaitLimit));
+    const float2 qt = qtab[t];
+    // this thread's row of the A operand (column t of the tile)
+    uint8_t* arow = sa + (t >> 3) * C::SBO + (t & 7) * 16;
+
+    // the epilogue of a tile (accumulator slot d): all outputs of column t
+    auto epilogue = [&](long pitem, int d, int ps) {
+        const long row = pitem / TILES;
+        const int o_base = int(pitem % TILES) * C::TC;
+        const int n1 = o_base + t;  // this thread's column
+        const float2 pt = s_pt[ps];
+        const cpx w1 = cmul({pt.x, pt.y}, {qt.x, qt.y});  // W_M^(n1)
+        cpx tw = {1.f, 0.f};                                // W_M^(n1 k0), k0 = 0, 1, ...
+        constexpr int CH = C::NP < 32 ? C::NP : 32;         // accumulator columns per load
+        #pragma unroll 1
+        for (int c0 = 0; c0 < 2 * C::NOUT; c0 += CH) {
+            uint32_t vv[32];
+            const uint32_t taddr = tmem + (uint32_t(32 * wq) << 16) + d * C::DCOLS + c0;
+            if constexpr (CH == 16)
+                tc::ld32x32b_x16(taddr, vv);
+            else
+                tc::ld32x32b_x32(taddr, vv);
+            tc::wait_ld();
+            #pragma unroll
+            for (int j = 0; j < CH / 2; ++j) {
+                const int o = c0 / 2 + j;
+                if (o >= C::NOUT) break;
+                cpx x = {__uint_as_float(vv[2 * j]), __uint_as_float(vv[2 * j + 1])};
+                if constexpr (C::FWD) {
+                    x = cmul(x, tw);
+                    tw = cmul(tw, w1);
+                }
+                if constexpr (MODE <= 2) {
+                    a.T[row * long(M) + long(L) * o + n1] = O::pack(x.r, x.i);
+                } else {
+                    // y_z = conj(out): y[2n] = Re, y[2n+1] = -Im
+                    const long e = row * long(M) + 2 * (long(L) * o + n1);
+                    float re = x.r, im = -x.i;
+                    if (GATED) {
+                        const cpx g = O::unpack(__ldg(reinterpret_cast<const uint32_t*>(a.w_out + e)));
+                        re *= g.r;
+                        im *= g.i;
+                    }
+                    *reinterpret_cast<uint32_t*>(a.y + e) = O::pack(re, im);
+                }
+            }
+        }
+    };
+
+    uint32_t par[C::NST] = {}, mpar[2] = {0, 0};
+    long li = 0;     // local tile index
+    long prev = -1;  // the tile whose epilogue is pending
+    for (long item = first_item; item < items && !failed; item += stride, ++li) {
+        const int s = int(li % C::NST), d = int(li & 1), ps = int(li % 3);
+        const int o_base = int(item % TILES) * C::TC;
+        if (t == 0) {
+            const cpx v = twiddle_pow2(uint32_t(o_base) & (M - 1), M);
+            s_pt[ps] = make_float2(v.r, v.i);
+        }
+        bool bad = !mbar_wait_sleep(&full[s], par[s], kWaitSleepLimit, kWaitHintNs);
+        if (!bad) {
+            par[s] ^= 1;
+            issued &= ~(1u << s);
+        }
+        // the contraction of the tile before must be done reading the A operand
+        if (prev >= 0) {
+            const bool ok = mbar_wait_sleep(&mbar[d ^ 1], mpar[d ^ 1], kWaitSleepLimit, kWaitHintNs);
+            bad |= !ok;
+            if (ok) {
+                mpar[d ^ 1] ^= 1;
+                mma_pending &= ~(1u << (d ^ 1));
+            }
+        }
+        tc::fence_after();
+        if (__syncthreads_or(bad)) { failed = true; break; }
+
+        // ---------------- column t of the staged rows -> row t of the A operand
+        {
+            const uint32_t* sts = st + s * C::STAGE_WORDS + t;
+            const uint32_t* sws = sw + s * C::STAGE_WORDS + t;
+            cpx tw = {1.f, 0.f}, w1 = {1.f, 0.f};  // pass C: W_M^(n' k0) along k0
+            if constexpr (!C::FWD) {
+                const float2 pt = s_pt[ps];
+                w1 = cmul({pt.x, pt.y}, {qt.x, qt.y});
+            }
+            #pragma unroll 4
+            for (int g = 0; g < C::NG; ++g) {
+                uint32_t v[4];
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int n0 = 4 * g + i;
+                    uint32_t x = 0u;
+                    if (n0 < C::NIN) {
+                        x = sts[n0 * C::SEG];
+                        if (GATED && MODE == 0) x = O::mul2(x, sws[n0 * C::SEG]);
+                        if constexpr (!C::FWD) {
+                            const cpx xv = cmul(O::unpack(x), tw);
+                            x = O::pack(xv.r, xv.i);
+                            tw = cmul(tw, w1);
+                        }
+                    }
+                    v[i] = x;
+                }
+                *reinterpret_cast<uint4*>(arow + g * C::LBO) = make_uint4(v[0], v[1], v[2], v[3]);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::fence_before();
+        __syncthreads();
+        if (t == 0) {
+            // the staging slot is free: the tile NST ahead
+            const long nxt = item + long(C::NST) * stride;
+            if (nxt < items) {
+                stage(nxt, s);
+                issued |= 1u << s;
+            }
+            tc::fence_after();
+            const uint32_t sam = smem_u32(sa), sfm = smem_u32(sf);
+            constexpr uint32_t id = tc::idesc(DT, 128, C::NP);
+            #pragma unroll
+            for (int ks = 0; ks < C::KP / 16; ++ks)
+                tc::mma_ss(tmem + d * C::DCOLS, tc::sdesc(sam + 2 * ks * C::LBO, C::LBO, C::SBO),
+                           tc::sdesc(sfm + 2 * ks * C::LBO, C::LBO, C::SBO), id, ks > 0);
+            tc::commit(&mbar[d]);
+            mma_pending |= 1u << d;
+        }
+
+        // ---------------- the previous tile's epilogue, while this contraction runs
+        if (prev >= 0) epilogue(prev, d ^ 1, int((li + 2) % 3));
+        prev = item;
+    }
+    // the last tile's epilogue
+    if (!failed && prev >= 0) {
+        const int d = int((li - 1) & 1);
+        const bool ok = mbar_wait_sleep(&mbar[d], mpar[d], kWaitSleepLimit, kWaitHintNs);
+        if (ok) {
+            mpar[d] ^= 1;
+            mma_pending &= ~(1u << d);
+        }
+        tc::fence_after();
+        failed = __syncthreads_or(!ok);
+        if (!failed) epilogue(prev, d, int((li - 1) % 3));
+    }
+    if (failed && t == 0) {
+        // record the timeout, then wait (bounded) for the copies and the contractions in flight
+        atomicExch(a.err, 7);
+        for (int s = 0; s < C::NST; ++s)
+            if ((issued >> s) & 1u) mbar_wait_bounded(&full[s], par[s], kWaitLimit);
+        for (int d = 0; d < 2; ++d)
+            if ((mma_pending >> d) & 1u) mbar_wait_bounded(&mbar[d], mpar[d], kWaitLimit);
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (wq == 0) tc::dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace fftconv

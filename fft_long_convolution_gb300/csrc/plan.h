@@ -5,9 +5,11 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstring>
 
 #include "../../include/fftconv.h"
 #include "multipass.cuh"
+#include "otc.cuh"
 
 struct fftconv_plan_s {
     fftconv_plan_info_t info;
@@ -23,6 +25,13 @@ struct fftconv_plan_s {
     int ftc = 0;                     // N = 8192 / 16384 / 32768: the fused R0 x 64 x 64 kernel on tcgen05
     const float2* ftw_in = nullptr;  // its per-thread starting twiddles (device, inside dev)
     const float4* ftw_out = nullptr;
+    // multi-pass outer passes on the tensor cores (otc.cuh): the DFT matrices of
+    // pass A and pass C (the outermost factor) and of the in-place 64-point
+    // stages of a two-level outer factor (device, inside dev)
+    const uint8_t* otc_fa = nullptr;
+    const uint8_t* otc_fc = nullptr;
+    const uint8_t* otc_fa2 = nullptr;
+    const uint8_t* otc_fc2 = nullptr;
     const uint32_t* fmat = nullptr;  // the 64 x 64 DFT matrix rows (device), N = 4096 and mpL = 4096
     // frequency-sparse plan: a band per factor (every band >= M_j/2 + 1 on a
     // dense plan); on the multi-pass path the pass-B pairs that run and the
@@ -87,6 +96,81 @@ cudaError_t prep_kernel(K fn, size_t smem, int threads, PerDevice& cache, int* p
     }
     *per_sm = *s;
     return cudaSuccess;
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime (once per process;
+// null if the driver does not provide it).
+using TensorMapEncoder = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+inline TensorMapEncoder tensor_map_encoder() {
+    static TensorMapEncoder fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return TensorMapEncoder(nullptr);
+        }
+        return reinterpret_cast<TensorMapEncoder>(ptr);
+    }();
+    return fn;
+}
+
+// A tensor map over rows of `nin` sub-rows of L 32-bit words (row stride
+// row_bytes), read as boxes of 128 words x nin sub-rows x 1 row.
+inline bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t L, uint64_t nin, uint64_t rows,
+                            uint64_t row_bytes) {
+    TensorMapEncoder enc = tensor_map_encoder();
+    if (!enc || !base) return false;
+    const cuuint64_t dims[3] = {L, nin, rows};
+    const cuuint64_t strides[2] = {4 * L, row_bytes};
+    const cuuint32_t box[3] = {128, cuuint32_t(nin), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One outer pass on the tensor cores: rows x (L / 128) column tiles over the
+// resident CTAs of the SM (their tensor-memory columns included).
+template <int DT, int R, int MODE, bool G, int L>
+cudaError_t launch_otc(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, const uint8_t* fmat,
+                       cudaStream_t st) {
+    using C = Otc<R, MODE>;
+    auto fn = otc_pass<DT, R, MODE, G, L>;
+    // no more CTAs per SM than its 512 tensor-memory columns hold: the shared
+    // memory request is raised until the SM's 228 KB (1 KB reserved per CTA)
+    // fit no more of them
+    constexpr int tmem_cap = int(512 / C::TMEM_COLS);
+    constexpr size_t smem_need = otc_smem<R, MODE, G>();
+    constexpr size_t smem_floor = size_t(233472 / (tmem_cap + 1)) - 1024 + 16;
+    constexpr size_t smem = smem_need > smem_floor ? smem_need : smem_floor;
+    static_assert(smem <= 232448, "shared memory");
+    static PerDevice cache;  // per instantiation and device
+    int per_sm = 0;
+    cudaError_t e = prep_kernel(fn, smem, C::THREADS, cache, &per_sm);
+    if (e != cudaSuccess) return e;
+    // resident CTAs from the shared-memory and tensor-memory budgets
+    per_sm = int(233472 / (smem + 1024));
+    if (per_sm > tmem_cap) per_sm = tmem_cap;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t items = rows * (L / C::TC);
+    int64_t grid = int64_t(p->num_sms) * per_sm;
+    if (grid > items) grid = items;
+    if (grid < 1) return cudaSuccess;
+    // the input rows: u (MODE 0: R/2 sub-rows of a row of R L / 2 words) or T
+    // (R sub-rows of a row of R L words); w_in in u's shape
+    CUtensorMap tin, tgate;
+    std::memset(&tgate, 0, sizeof(tgate));
+    const bool ok = MODE == 0 ? encode_rows_map(&tin, args.u, L, R / 2, uint64_t(rows), uint64_t(2) * R * L)
+                              : encode_rows_map(&tin, args.T, L, R, uint64_t(rows), uint64_t(4) * R * L);
+    if (!ok) return cudaErrorInvalidValue;
+    if (G && MODE == 0 && !encode_rows_map(&tgate, args.w_in, L, R / 2, uint64_t(rows), uint64_t(2) * R * L))
+        return cudaErrorInvalidValue;
+    fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, fmat, tin, tgate);
+    return cudaGetLastError();
 }
 
 }  // namespace fftconv

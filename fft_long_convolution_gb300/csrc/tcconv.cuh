@@ -53,9 +53,6 @@
 
 namespace fftconv {
 
-// Bounded waits of this kernel: polls that may each suspend for up to 2 us
-// (at most about 2 s in total before the kernel reports a timeout).
-constexpr uint32_t kWaitSleepLimit = 1u << 20, kWaitHintNs = 2000;
 
 struct Tc64Args {
     const uint16_t* u;
