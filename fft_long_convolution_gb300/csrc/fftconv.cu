@@ -100,12 +100,15 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
     q.N = N;
     q.M = N;
     q.dtype = dtype;
-    if (N == 4096) {
-        // fused on the fifth-generation tensor cores: M = 64 * 64
+    if (N == 4096 || (N < 4096 && (order == 0 || order == 2))) {
+        // fused on the fifth-generation tensor cores: M = 64 * 64; N = 1024 and
+        // 2048 as rows zero-padded to 4096 (a causal convolution's first N
+        // outputs are those of the padded rows)
         q.path = FFTCONV_PATH_FUSED;
         q.order = 2;
         q.factors[0] = 64;
         q.factors[1] = 64;
+        q.M = 4096;
         q.workspace_bytes_per_row = 0;
     } else if (N == 8192 || N == 16384 || (N == 32768 && order != 4)) {
         // fused on the fifth-generation tensor cores: M = R0 * 64 * 64, the
@@ -156,7 +159,7 @@ extern "C" fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype,
     if (order != 0 && order != q.order) return FFTCONV_ERR_UNSUPPORTED;
     // two 16-bit complex coefficients per bin (plus zero padding bins on the
     // 64 x 64 paths, whose k_f follows the kernels' column layouts)
-    if (N == 4096)
+    if (q.order == 2)
         q.kf_bytes_per_channel = int64_t(Tc64::KFB);
     else if (q.order == 3 && q.factors[1] == 64)  // pairs of 4096-point sub-rows (fused or multi-pass)
         q.kf_bytes_per_channel = int64_t(q.factors[0] / 2) * TcB::KFP * 16;
@@ -471,7 +474,7 @@ cudaError_t launch_tc64_t(const fftconv_plan_s* p, const void* u, const void* wi
     const int64_t grid = need < p->num_sms ? need : p->num_sms;
     Tc64Args args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
                   static_cast<const uint16_t*>(wo), static_cast<const uint8_t*>(kf), static_cast<uint16_t*>(y),
-                  p->fmat, int(B), int(H), p->dev_err};
+                  p->fmat, int(B), int(H), p->dev_err, int(p->info.N)};
     fn<<<dim3(unsigned(grid)), dim3(Tc64::THREADS), Tc64::SMEM, st>>>(args);
     return cudaGetLastError();
 }
@@ -601,6 +604,9 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
                                   const int32_t* band, int nband) {
     if (!out) return FFTCONV_ERR_INVALID;
     *out = nullptr;
+    // a band pattern is defined over the digits of an N-point transform: rows
+    // shorter than 4096 keep their own factorization R1 x 16 x 16 then
+    if (band && order == 0 && N < 4096) order = 3;
     fftconv_plan_info_t info;
     fftconv_status_t st = fftconv_plan_query(N, dtype, order, &info);
     if (st != FFTCONV_OK) return st;
@@ -621,7 +627,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     const bool multi = info.path == FFTCONV_PATH_MULTIPASS;
     p->R0 = multi ? info.factors[0] : 1;
     p->R1 = multi ? kMpR1 : info.factors[0];
-    p->tc64 = N == 4096;
+    p->tc64 = info.order == 2;  // 4096 = 64 x 64 (N = 1024, 2048 zero-padded to it)
     p->ftc = (info.path == FFTCONV_PATH_FUSED && N >= 8192) ? int(N / 4096) : 0;
     p->mp2 = multi && info.order == 4 && info.factors[3] == 64;
     if (p->mp2) p->R0 = info.factors[0] * 64;  // the sub-row count of pass B
@@ -746,6 +752,7 @@ extern "C" fftconv_status_t fftconv_plan_create_sparse(fftconv_plan_t* out, int6
 
 extern "C" fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtype, int order, const int32_t* band,
                                                  int nband, int32_t* pairs_run, int32_t* pairs_total) {
+    if (order == 0 && N < 4096) order = 3;  // as fftconv_plan_create_sparse
     fftconv_plan_info_t info;
     fftconv_status_t st = fftconv_plan_query(N, dtype, order, &info);
     if (st != FFTCONV_OK) return st;
@@ -821,14 +828,17 @@ extern "C" fftconv_status_t fftconv_set_workspace(fftconv_plan_t plan, void* dev
 
 namespace {
 
-__global__ void kfft_init(const float* __restrict__ k, float2* __restrict__ buf, int64_t H, int64_t N) {
+// buf[h][n] = k[h][n] for n < Nk, 0 up to 2N (Nk <= N: a kernel shorter than
+// the transform, as for rows zero-padded to the transform length)
+__global__ void kfft_init(const float* __restrict__ k, float2* __restrict__ buf, int64_t H, int64_t N,
+                          int64_t Nk) {
     const int64_t L = 2 * N;
     int lgL = 0;
     while ((int64_t(1) << lgL) < L) ++lgL;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * L;
          i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t h = i >> lgL, n = i & (L - 1);
-        buf[i] = make_float2(n < N ? k[h * N + n] : 0.f, 0.f);
+        buf[i] = make_float2(n < Nk ? k[h * Nk + n] : 0.f, 0.f);
     }
 }
 
@@ -1120,8 +1130,9 @@ fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f,
     if (H == 0) return FFTCONV_OK;
     if (!k || !k_f) return FFTCONV_ERR_INVALID;
     if (misaligned(k) || misaligned(k_f)) return FFTCONV_ERR_ALIGN;
-    const int64_t N = plan->info.N, L = 2 * N;
-    if (overlap(k, size_t(H * N) * 4, k_f, fftconv_kf_bytes(plan, H))) return FFTCONV_ERR_INVALID;
+    // the transform length (4096 for rows of 1024 / 2048 zero-padded to it) and the kernel's length
+    const int64_t N = plan->info.M, Nk = plan->info.N, L = 2 * N;
+    if (overlap(k, size_t(H * Nk) * 4, k_f, fftconv_kf_bytes(plan, H))) return FFTCONV_ERR_INVALID;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     float2* buf = nullptr;
     const size_t bytes = size_t(H) * size_t(L) * sizeof(float2);
@@ -1131,7 +1142,7 @@ fftconv_status_t kernel_fft_impl(fftconv_plan_t plan, const float* k, void* k_f,
     }
     float2* a = buf;
     float2* b = buf + H * L;
-    kfft_init<<<grid_for(H * L), 256, 0, st>>>(k, a, H, N);
+    kfft_init<<<grid_for(H * L), 256, 0, st>>>(k, a, H, N, Nk);
     a = fft_rows(a, b, H, L, st);
     if (adjoint) kfft_conj<<<grid_for(H * L), 256, 0, st>>>(a, H * L);
     if (plan->sparse) {

@@ -37,6 +37,11 @@
 // whose transform is Z[64 (k2 + 1)].  Columns 66..71 are padding; the second
 // row's slots follow at 72.
 //
+// Rows shorter than 4096 (Nu = 1024, 2048) run as the same transform of the
+// row zero-padded to 4096 (the staging beyond the copied Nu / 2 words stays
+// zero), and only the outputs n < Nu / 2 are stored: a causal convolution's
+// first Nu outputs do not depend on anything beyond position Nu.
+//
 // Work item = two rows of the same channel (b = 2p, 2p + 1): every
 // contraction covers both rows (N = 128, 144 for S2), which halves the number
 // of tensor-core instructions per row (each one costs about the same up to
@@ -53,7 +58,6 @@
 
 namespace fftconv {
 
-
 struct Tc64Args {
     const uint16_t* u;
     const uint16_t* w_in;
@@ -63,6 +67,8 @@ struct Tc64Args {
     const uint32_t* fmat;   // [3][lane 128][64 words]: F64/8 with permuted rows; columns natural, P3, P4
     int B, H;
     int* err;
+    int Nu;                 // row length of u, w_in, w_out and y: 4096, or 1024 / 2048 (the row zero-padded
+                            // to 4096: the causal convolution's first Nu outputs are those of the padded rows)
 };
 
 struct Tc64 {
@@ -151,13 +157,14 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
             uint64_t* bp = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 3 * gp;
             const int h0 = int(unsigned(j0) / unsigned(P)), b0 = 2 * (j0 - h0 * P);
             const bool okB0 = b0 + 1 < a.B;
-            const size_t bA = (size_t(b0) * a.H + h0) * C::M, bB = (size_t(okB0 ? b0 + 1 : 0) * a.H + h0) * C::M;
-            mbar_expect_tx(&bp[2], C::STG * (okB0 ? 2u : 1u) * (GATED ? 2u : 1u));
-            bulk_g2s(pbp + C::OFF_ST, a.u + bA, C::STG, &bp[2]);
-            if (okB0) bulk_g2s(pbp + C::OFF_ST + C::STG, a.u + bB, C::STG, &bp[2]);
+            const uint32_t stg = uint32_t(a.Nu) * 2u;  // bytes of a row
+            const size_t bA = (size_t(b0) * a.H + h0) * a.Nu, bB = (size_t(okB0 ? b0 + 1 : 0) * a.H + h0) * a.Nu;
+            mbar_expect_tx(&bp[2], stg * (okB0 ? 2u : 1u) * (GATED ? 2u : 1u));
+            bulk_g2s(pbp + C::OFF_ST, a.u + bA, stg, &bp[2]);
+            if (okB0) bulk_g2s(pbp + C::OFF_ST + C::STG, a.u + bB, stg, &bp[2]);
             if (GATED) {
-                bulk_g2s(pbp + C::OFF_ST + 2 * C::STG, a.w_in + bA, C::STG, &bp[2]);
-                if (okB0) bulk_g2s(pbp + C::OFF_ST + 3 * C::STG, a.w_in + bB, C::STG, &bp[2]);
+                bulk_g2s(pbp + C::OFF_ST + 2 * C::STG, a.w_in + bA, stg, &bp[2]);
+                if (okB0) bulk_g2s(pbp + C::OFF_ST + 3 * C::STG, a.w_in + bB, stg, &bp[2]);
             }
             mbar_expect_tx(&bp[0], C::KFB);
             bulk_g2s(pbp + C::OFF_KF, a.kf + size_t(h0) * C::KFB, C::KFB, &bp[0]);
@@ -174,6 +181,14 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     for (uint32_t i = threadIdx.x; i < 2 * C::BBUF / 16; i += blockDim.x) {  // padding columns start finite
         const uint32_t pi = i / (C::BBUF / 16), off = (i % (C::BBUF / 16)) * 16;
         *reinterpret_cast<uint4*>(smem + pi * C::PIPE + off) = make_uint4(0, 0, 0, 0);
+    }
+    if (a.Nu < C::M) {  // the zero padding beyond a short row: the staging tails that no copy writes
+        const uint32_t head = uint32_t(a.Nu) * 2u, tail = (C::STG - head) / 16;
+        for (uint32_t i = threadIdx.x; i < 8 * tail; i += blockDim.x) {
+            const uint32_t slot = i / tail, off = head + (i % tail) * 16;  // 2 pipelines x 4 staged rows
+            *reinterpret_cast<uint4*>(smem + (slot >> 2) * C::PIPE + C::OFF_ST + (slot & 3) * C::STG + off) =
+                make_uint4(0, 0, 0, 0);
+        }
     }
     tc::fence_proxy_async();
     tc::fence_before();
@@ -259,13 +274,14 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
     // u and w_in of both rows into the staging buffers (one bulk copy each)
     auto stage_item = [&](int it) {
         bool okA, okB;
-        const size_t bA = size_t(row_of(it, 0, okA)) * C::M, bB = size_t(row_of(it, 1, okB)) * C::M;
-        mbar_expect_tx(&bars[2], C::STG * (okB ? 2u : 1u) * (GATED ? 2u : 1u));
-        bulk_g2s(pb + C::OFF_ST, a.u + bA, C::STG, &bars[2]);
-        if (okB) bulk_g2s(pb + C::OFF_ST + C::STG, a.u + bB, C::STG, &bars[2]);
+        const uint32_t stg = uint32_t(a.Nu) * 2u;  // bytes of a row
+        const size_t bA = size_t(row_of(it, 0, okA)) * a.Nu, bB = size_t(row_of(it, 1, okB)) * a.Nu;
+        mbar_expect_tx(&bars[2], stg * (okB ? 2u : 1u) * (GATED ? 2u : 1u));
+        bulk_g2s(pb + C::OFF_ST, a.u + bA, stg, &bars[2]);
+        if (okB) bulk_g2s(pb + C::OFF_ST + C::STG, a.u + bB, stg, &bars[2]);
         if (GATED) {
-            bulk_g2s(pb + C::OFF_ST + 2 * C::STG, a.w_in + bA, C::STG, &bars[2]);
-            if (okB) bulk_g2s(pb + C::OFF_ST + 3 * C::STG, a.w_in + bB, C::STG, &bars[2]);
+            bulk_g2s(pb + C::OFF_ST + 2 * C::STG, a.w_in + bA, stg, &bars[2]);
+            if (okB) bulk_g2s(pb + C::OFF_ST + 3 * C::STG, a.w_in + bB, stg, &bars[2]);
         }
     };
     auto issue_kf = [&](int h) {
@@ -289,8 +305,8 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
         bool okA, okB;
         const int rowA = row_of(it, 0, okA), rowB = row_of(it, 1, okB);
         if (GATED && tg == 32) {  // w_out of this item into L2 (read in S4 post)
-            bulk_prefetch_l2(a.w_out + size_t(rowA) * C::M, C::STG);
-            if (okB) bulk_prefetch_l2(a.w_out + size_t(rowB) * C::M, C::STG);
+            bulk_prefetch_l2(a.w_out + size_t(rowA) * a.Nu, uint32_t(a.Nu) * 2u);
+            if (okB) bulk_prefetch_l2(a.w_out + size_t(rowB) * a.Nu, uint32_t(a.Nu) * 2u);
         }
 
         // ---------------- input: z (times w_in) of row hf -> B1
@@ -513,15 +529,17 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
 
         // ---------------- S4 post: conjugate, gate, store y (outputs n1 < 32)
         const size_t yin = 2 * size_t(64 * kapA + 32 * hf + 2 * q);  // element offset inside a row
+        // outputs n = yin / 2 + 8 jj (+1) exist for n < Nu / 2
+        auto kept = [&](int jj) { return 64 * kapA + 32 * hf + 8 * jj + 2 * q + 1 < (a.Nu >> 1); };
         uint2 wov[2][4];
         if (GATED) {  // w_out of this thread's outputs, read while the contraction runs
             #pragma unroll
             for (int R = 0; R < 2; ++R)
                 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
-                    wov[R][jj] = (R ? okB : okA)
+                    wov[R][jj] = ((R ? okB : okA) && kept(jj))
                                      ? __ldg(reinterpret_cast<const uint2*>(
-                                           a.w_out + size_t(R ? rowB : rowA) * C::M + yin + 16 * jj))
+                                           a.w_out + size_t(R ? rowB : rowA) * a.Nu + yin + 16 * jj))
                                      : make_uint2(0, 0);
         }
         bad = !mbar_wait_sleep(&bars[1], mmapar, kWaitSleepLimit, kWaitHintNs);
@@ -534,7 +552,7 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
                 tc::ld16x256b_x4(tD + laneA + 64 * R + 32 * hf, vv);
                 tc::wait_ld();
                 if (R ? okB : okA) {
-                    uint16_t* yr = a.y + size_t(R ? rowB : rowA) * C::M + yin;
+                    uint16_t* yr = a.y + size_t(R ? rowB : rowA) * a.Nu + yin;
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
                         float r0 = __uint_as_float(vv[4 * jj]), r1 = __uint_as_float(vv[4 * jj + 1]);
@@ -543,7 +561,8 @@ __global__ void __launch_bounds__(Tc64::THREADS, 1) tc64_conv_kernel(const Tc64A
                             const cpx w0 = O::unpack(wov[R][jj].x), w1 = O::unpack(wov[R][jj].y);
                             r0 *= w0.r; i0 *= w0.i; r1 *= w1.r; i1 *= w1.i;
                         }
-                        *reinterpret_cast<uint2*>(yr + 16 * jj) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
+                        if (kept(jj))
+                            *reinterpret_cast<uint2*>(yr + 16 * jj) = make_uint2(O::pack(r0, i0), O::pack(r1, i1));
                     }
                 }
             }

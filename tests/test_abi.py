@@ -37,8 +37,9 @@ def test_version_and_status_strings():
 
 @pytest.mark.parametrize("N,R1", [(1024, 4), (2048, 8)])
 def test_query_fused_factorization(N, R1):
+    """Order 3 keeps the warp-level R1 x 16 x 16 kernel for N = 1024, 2048."""
     for dt in (F.F16, F.BF16):
-        q = F.query(N, dt)
+        q = F.query(N, dt, order=3)
         assert q["path"] == F.PATH_FUSED and q["order"] == 3
         assert q["factors"] == [R1, 16, 16]
         assert q["factors"][0] * 16 * 16 == N == q["M"]
@@ -58,6 +59,20 @@ def test_query_fused_tensor_core_factorization(N):
         assert q["factors"] == [N // 4096, 64, 64] and q["M"] == N
         assert q["kf_bytes_per_channel"] == (N // 8192) * 17 * 4 * 2 * 32 * 16
         assert q["workspace_bytes_per_row"] == 0
+
+
+@pytest.mark.parametrize("N", [1024, 2048])
+def test_query_short_rows_padded_to_4096(N):
+    """By default N = 1024 and 2048 run on the 64 x 64 tensor-core kernel as
+    rows zero-padded to 4096 (transform length M = 4096, 36 KB of k_f per
+    channel); a frequency-sparse pattern keeps R1 x 16 x 16."""
+    for dt in (F.F16, F.BF16):
+        q = F.query(N, dt)
+        assert q["path"] == F.PATH_FUSED and q["order"] == 2
+        assert q["factors"] == [64, 64] and q["M"] == 4096 and q["N"] == N
+        assert q["kf_bytes_per_channel"] == 9 * 4 * 2 * 32 * 16
+        assert F.query(N, dt, order=2) == q
+    assert F.sparse_query(N, F.BF16, [1, 1, 1]) == {"pairs_run": 0, "pairs_total": 0}
 
 
 def test_query_fused_order2_4096():

@@ -173,3 +173,43 @@ def test_ftc_many_rows_every_row(N, dtype, gated):
     print(f"N={N} {dtype} gated={gated} rows={w.rows} worst row rel-L2={worst:.3e}")
     assert worst <= TOL[dtype]
     assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("N", [1024, 2048])
+@pytest.mark.parametrize("dtype,gated", [("fp16", False), ("bf16", True)])
+def test_short_rows_order3_warp_level_kernel(N, dtype, gated):
+    """N = 1024 / 2048 with order 3: the warp-level R1 x 16 x 16 kernel
+    (the default pads these rows to 4096 on the tensor cores)."""
+    w = W.Workload("t", 3, 5, N, dtype, gated, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=19)
+    plan = F.Plan(N, torch_dtype(dtype), order=3)
+    assert plan.info["order"] == 3 and plan.info["factors"][1] == 16
+    y, _ = run_gpu(plan, ins, gated)
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle_rows(ins, gated)
+    assert rel_l2(got, ref) <= TOL[dtype]
+    assert plan.device_status() == 0
+
+
+@pytest.mark.parametrize("N,B,H", [(1024, 7, 37), (2048, 3, 50)])
+def test_short_rows_padded_every_row(N, B, H):
+    """N = 1024 / 2048 on the 4096-point tensor-core kernel (rows zero-padded
+    in shared memory, only outputs t < N stored): several row pairs per
+    pipeline, an odd batch, every row checked, and nothing written beyond the
+    rows."""
+    w = W.Workload("t", B, H, N, "bf16", True, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=23)
+    plan = _plan(N, "bf16")
+    assert plan.info["order"] == 2 and plan.info["M"] == 4096
+    kf = plan.kernel_fft(to_dev(ins["k"]))
+    u, wi, wo = to_dev(ins["u"]), to_dev(ins["w_in"]), to_dev(ins["w_out"])
+    guard = torch.full((B * H * N + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = guard[: B * H * N].view(B, H, N)
+    plan.forward_gated(u, wi, wo, kf, y=y)
+    torch.cuda.synchronize()
+    assert torch.all(guard[B * H * N:] == 7.0)
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = oracle_rows(ins, True, threads=8)
+    worst = max(rel_l2(got[b, h], ref[b, h]) for b in range(B) for h in range(H))
+    assert worst <= TOL["bf16"], worst
+    assert plan.device_status() == 0

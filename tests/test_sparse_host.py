@@ -61,7 +61,7 @@ def test_full_band_runs_every_pair():
 
 def test_fused_lengths_report_no_pairs():
     for N in (1024, 4096, 16384):
-        info = F.query(N, F.F16)
+        info = F.query(N, F.F16, order=3 if N < 4096 else 0)  # sparse patterns at 1K keep R1 x 16 x 16
         got = F.sparse_query(N, F.BF16, [1] * info["order"])
         assert got == {"pairs_run": 0, "pairs_total": 0}
 
