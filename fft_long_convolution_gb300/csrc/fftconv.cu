@@ -495,7 +495,8 @@ cudaError_t launch_ftc_t(const fftconv_plan_s* p, const void* u, const void* wi,
     const int64_t grid = need < p->num_sms ? need : p->num_sms;
     FtcArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
                  static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
-                 p->fmat, p->ftw_in, p->ftw_out, int(B), int(H), p->dev_err};
+                 p->fmat, p->ftw_in, p->ftw_out, int(B), int(H), p->dev_err,
+                 (R0 == 4 && p->pairs_run == 1) ? 1 : 0};
     fn<<<dim3(unsigned(grid)), dim3(C::THREADS), C::SMEM, st>>>(args);
     return cudaGetLastError();
 }
@@ -600,6 +601,18 @@ SparseTables sparse_tables(const fftconv_plan_info_t& info, const int32_t* band,
     return t;
 }
 
+// The fused tensor-core kernel at N = 16384 (outer factor R0 = 4) runs its
+// row as the sub-row pairs (1, 3) and (0, 2); pair (1, 3) is skipped when
+// both of its sub-rows are dead, pair (0, 2) always runs (it writes the row).
+// Returns the pairs that run out of R0 / 2 (R0 = 2 and 8: all of them).
+int ftc_pairs_run(const fftconv_plan_info_t& info, const int32_t* band, bool sparse) {
+    const int R0 = info.factors[0];
+    if (!sparse || R0 != 4) return R0 / 2;
+    const SparseTables t = sparse_tables(info, band, R0, false);
+    const bool pair1 = std::find(t.plist.begin(), t.plist.end(), uint16_t(1)) != t.plist.end();
+    return pair1 ? 2 : 1;
+}
+
 fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype, int order,
                                   const int32_t* band, int nband) {
     if (!out) return FFTCONV_ERR_INVALID;
@@ -665,7 +678,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     }
     SparseTables sp;
     size_t o_plist = 0, o_zbits = 0;
-    p->pairs_run = multi ? p->R0 / 2 : 0;
+    p->pairs_run = multi ? p->R0 / 2 : (p->ftc ? ftc_pairs_run(info, p->band, p->sparse) : 0);
     if (multi && p->sparse) {
         sp = sparse_tables(info, p->band, p->R0, p->mp2);
         if (sp.any_skipped) {
@@ -771,6 +784,9 @@ extern "C" fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtyp
         const int R0 = two_level ? info.factors[0] * 64 : info.factors[0];
         total = run = R0 / 2;
         if (sparse) run = int(sparse_tables(info, b, R0, two_level).plist.size());
+    } else if (info.order == 3 && info.factors[1] == 64) {  // the fused tensor-core kernel
+        total = info.factors[0] / 2;
+        run = ftc_pairs_run(info, b, sparse);
     }
     if (pairs_run) *pairs_run = run;
     if (pairs_total) *pairs_total = total;
@@ -783,8 +799,9 @@ extern "C" fftconv_status_t fftconv_plan_get_band(fftconv_plan_t plan, int32_t* 
     if (band)
         for (int j = 0; j < 8; ++j) band[j] = j < plan->info.order ? plan->band[j] : 0;
     const bool multi = plan->info.path == FFTCONV_PATH_MULTIPASS;
-    if (pairs_run) *pairs_run = multi ? plan->pairs_run : 0;
-    if (pairs_total) *pairs_total = multi ? plan->R0 / 2 : 0;
+    const int total = multi ? plan->R0 / 2 : (plan->ftc ? plan->ftc / 2 : 0);
+    if (pairs_run) *pairs_run = (multi || plan->ftc) ? plan->pairs_run : 0;
+    if (pairs_total) *pairs_total = total;
     return FFTCONV_OK;
 }
 

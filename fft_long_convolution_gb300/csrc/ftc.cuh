@@ -64,6 +64,7 @@ struct FtcArgs {
     const float4* twout;
     int B, H;
     int* err;
+    int skip1;  // R0 = 4, frequency-sparse plan: pair (1, 3) holds no kept bin and is not run
 };
 
 template <int R0, bool GATED>
@@ -142,12 +143,12 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
     const int rows = a.B * a.H;  // the host guarantees B*H < 2^30
     const int V = C::SPLIT ? int(gridDim.x) : int(gridDim.x) * 2;
     const int v = C::SPLIT ? int(blockIdx.x) : int(blockIdx.x) * 2 + g;
-    constexpr int IPR = C::SPLIT ? 2 : NP;  // items per row of one pipeline
+    const int IPR = C::SPLIT ? 2 : NP - a.skip1;  // items per row of one pipeline
     const int i0 = int(int64_t(v) * rows / V) * IPR, i1 = int(int64_t(v + 1) * rows / V) * IPR;
     auto item_row = [&](int it) -> int { return it / IPR; };
     auto item_pair = [&](int it) -> int {
         if constexpr (C::SPLIT) return g == 0 ? ((it & 1) ? 3 : 1) : ((it & 1) ? 0 : 2);
-        return NP - 1 - (it - (it / NP) * NP);
+        return IPR - 1 - (it - (it / IPR) * IPR);
     };
     auto chan = [&](int ri) -> int { return int(unsigned(ri) / unsigned(a.B)); };
     auto mrow = [&](int ri) -> size_t {
@@ -737,7 +738,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                             out[0] = make_float4(scale * (tA.x + vB.x), scale * (tA.y + vB.y), scale * (tA.z + vB.z),
                                                  scale * (tA.w + vB.w));
                         } else {
-                            const uint4 sd = tout[(4 * b + jj) * 256];
+                            const uint4 sd = a.skip1 ? make_uint4(0, 0, 0, 0) : tout[(4 * b + jj) * 256];
                             const cpx s0 = O::unpack(sd.x), s1 = O::unpack(sd.y);
                             const cpx d0 = O::unpack(sd.z), d1 = O::unpack(sd.w);
                             out[0] = make_float4(scale * (tA.x + vB.x + s0.r), scale * (tA.y + vB.y + s1.r),

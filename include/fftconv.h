@@ -130,8 +130,11 @@ fftconv_status_t fftconv_plan_create(fftconv_plan_t *out, int64_t N, fftconv_dty
  * Work skipped (multi-pass path): sub-row k0 of the inner transforms holds
  * the bins whose leading digits form k0; a pair of sub-rows (k0, R0 - k0)
  * whose bins are all dropped is not transformed, the first pass does not
- * write it and the last pass reads zeros in its place.  The fused paths
- * (N <= 16384) apply the pattern through k_f only.
+ * write it and the last pass reads zeros in its place.  The fused
+ * tensor-core kernel (N = 8192 .. 32768, outer factor R0 = N / 4096) works
+ * on the same pairs inside one CTA: at R0 = 4 the pair (1, 3) is not run
+ * when all its bins are dropped; R0 = 2 and 8 run every pair.  The other
+ * fused paths apply the pattern through k_f only.
  *
  * fftconv_backward_dk and the partial and circular forwards return
  * UNSUPPORTED for a sparse plan.  Returns OK, INVALID (band NULL, nband not
@@ -143,7 +146,8 @@ fftconv_status_t fftconv_plan_create_sparse(fftconv_plan_t *out, int64_t N, fftc
 /*
  * Without touching the GPU: the pairs of sub-rows that a sparse plan with
  * these arguments would transform (*pairs_run) out of *pairs_total on the
- * multi-pass path (both 0 on the fused path).  Arguments as
+ * multi-pass path and in the fused tensor-core kernel (N = 8192 .. 32768;
+ * both 0 on the other fused paths).  Arguments as
  * fftconv_plan_create_sparse.  Returns OK, INVALID or UNSUPPORTED.
  */
 fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtype, int order, const int32_t *band,
@@ -151,9 +155,8 @@ fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtype, int orde
 
 /*
  * The plan's bands (band[0..order-1]; band[order..7] = 0; a dense plan
- * reports M_j/2 + 1 for every axis) and, on the multi-pass path, the pairs of
- * sub-rows the inner pass transforms (*pairs_run) out of *pairs_total (both 0
- * on the fused path).  Any output pointer may be NULL.  Returns OK or INVALID.
+ * reports M_j/2 + 1 for every axis) and the pairs of sub-rows that run
+ * (*pairs_run) out of *pairs_total, as fftconv_sparse_query reports them.  Any output pointer may be NULL.  Returns OK or INVALID.
  */
 fftconv_status_t fftconv_plan_get_band(fftconv_plan_t plan, int32_t *band, int32_t *pairs_run,
                                        int32_t *pairs_total);

@@ -55,11 +55,20 @@ def _check(N, dtype, gated, B, H, band, order=0, seed=21, u_kind="normal", k_kin
     (4096, "bf16", True, 2, 3, [9, 20]),
     (4096, "fp16", False, 1, 2, [33, 3]),
     (16384, "fp16", False, 1, 3, [20, 9, 9]),
+    (16384, "bf16", False, 2, 3, [1, 33, 33]),       # outer digit 0 only: pair (1, 3) not run
+    (16384, "fp16", True, 1, 3, [1, 20, 9]),         # and the inner axes cut
+    (16384, "bf16", True, 2, 2, [2, 12, 33]),        # digits 0, +-1 kept: both pairs run
+    (8192, "fp16", False, 1, 2, [1, 33, 20]),
     (32768, "bf16", False, 1, 2, [3, 20, 20]),
 ])
 def test_fused_sparse(N, dtype, gated, B, H, band):
     bd = _check(N, dtype, gated, B, H, band)
-    assert bd["pairs_total"] == 0
+    if N >= 8192:  # the fused tensor-core kernel: pairs of sub-rows (k0, R0 - k0)
+        R0 = N // 4096
+        assert bd["pairs_total"] == R0 // 2
+        assert bd["pairs_run"] == (1 if (R0 == 4 and band[0] <= 1) else R0 // 2)
+    else:
+        assert bd["pairs_total"] == 0
 
 
 @pytest.mark.parametrize("N,dtype,gated,B,H,band", [

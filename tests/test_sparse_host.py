@@ -59,11 +59,21 @@ def test_full_band_runs_every_pair():
         assert got["pairs_run"] == got["pairs_total"]
 
 
-def test_fused_lengths_report_no_pairs():
-    for N in (1024, 4096, 16384):
+def test_fused_lengths_report_pairs_of_the_tensor_core_kernel():
+    """The warp-level and 64 x 64 fused kernels report no pairs; the fused
+    tensor-core kernel (N = 8192 .. 32768) reports R0 / 2 pairs of sub-rows
+    (R0 = N / 4096) and, at R0 = 4, skips pair (1, 3) when the outer band
+    keeps digit 0 alone."""
+    for N in (1024, 4096):
         info = F.query(N, F.F16, order=3 if N < 4096 else 0)  # sparse patterns at 1K keep R1 x 16 x 16
         got = F.sparse_query(N, F.BF16, [1] * info["order"])
         assert got == {"pairs_run": 0, "pairs_total": 0}
+    assert F.sparse_query(8192, F.BF16, [1, 1, 1]) == {"pairs_run": 1, "pairs_total": 1}
+    assert F.sparse_query(16384, F.BF16, [1, 1, 1]) == {"pairs_run": 1, "pairs_total": 2}
+    assert F.sparse_query(16384, F.BF16, [1, 33, 33]) == {"pairs_run": 1, "pairs_total": 2}
+    assert F.sparse_query(16384, F.BF16, [2, 1, 1]) == {"pairs_run": 2, "pairs_total": 2}
+    assert F.sparse_query(16384, F.BF16, [3, 0, 33]) == {"pairs_run": 1, "pairs_total": 2}  # inner axis empty
+    assert F.sparse_query(32768, F.BF16, [1, 1, 1]) == {"pairs_run": 4, "pairs_total": 4}
 
 
 @pytest.mark.parametrize("band", [[16, 33], [16, 33, 33, 33], [-1, 33, 33]])
