@@ -12,6 +12,7 @@
 
 #include "../../include/fftconv.h"
 #include "plan.h"
+#include "dkgrad.cuh"
 #include "ftc.cuh"
 #include "tcconv.cuh"
 #include "tcpass.cuh"
@@ -1466,12 +1467,54 @@ __global__ void __launch_bounds__(kDkThreads, 1) dk_channel_smem(const uint16_t*
     }
 }
 
+// 2N in (8192, 65536]: the four-step form of dkgrad.cuh, L = L1 x 2048
+constexpr int64_t kDk4MaxL = 65536;
+
+template <int DT, int L1, bool G>
+cudaError_t launch_dk4_t(const void* u, const void* dy, const void* w_in, const void* w_out, float* dk, int64_t B,
+                         int64_t H, float2* R, cudaStream_t st) {
+    const size_t smem = (size_t(6) * kDkL2 + kDkTwEntries) * sizeof(float2);
+    static PerDevice ready;  // per instantiation and device
+    auto fn = dk_rows<DT, L1, G>;
+    int* rd = ready.slot();
+    if (!rd) return cudaErrorInvalidDevice;
+    if (!*rd) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        *rd = 1;
+    }
+    const int64_t items = H * (L1 / 2);
+    fn<<<unsigned(items < 65535 * 16 ? items : 65535 * 16), kDkRowThreads, smem, st>>>(
+        static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(w_in),
+        static_cast<const uint16_t*>(w_out), R, B, H);
+    dk_cols_inv<L1><<<grid_for(H * kDkL2), 256, 0, st>>>(R, dk, H);
+    return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dk4(const void* u, const void* dy, const void* w_in, const void* w_out, float* dk, int64_t B,
+                       int64_t H, int64_t L, void* scratch, cudaStream_t st) {
+    float2* R = static_cast<float2*>(scratch);
+    const bool g = w_in != nullptr;
+    switch (L / kDkL2) {
+        case 8: return g ? launch_dk4_t<DT, 8, true>(u, dy, w_in, w_out, dk, B, H, R, st)
+                         : launch_dk4_t<DT, 8, false>(u, dy, w_in, w_out, dk, B, H, R, st);
+        case 16: return g ? launch_dk4_t<DT, 16, true>(u, dy, w_in, w_out, dk, B, H, R, st)
+                          : launch_dk4_t<DT, 16, false>(u, dy, w_in, w_out, dk, B, H, R, st);
+        case 32: return g ? launch_dk4_t<DT, 32, true>(u, dy, w_in, w_out, dk, B, H, R, st)
+                          : launch_dk4_t<DT, 32, false>(u, dy, w_in, w_out, dk, B, H, R, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 extern "C" size_t fftconv_backward_dk_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H) {
     if (!plan || B <= 0 || H <= 0) return 0;
-    if (2 * plan->info.N <= kDkMaxL) return 0;  // whole channels in shared memory
-    return 2 * size_t(B) * size_t(H) * size_t(2 * plan->info.N) * sizeof(float2);
+    const int64_t L = 2 * plan->info.N;
+    if (L <= kDkMaxL) return 0;  // whole channels in shared memory
+    if (L <= kDk4MaxL) return size_t(H) * size_t(L) * sizeof(float2);
+    return 2 * size_t(B) * size_t(H) * size_t(L) * sizeof(float2);
 }
 
 extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void* u, const void* dy, const void* w_in,
@@ -1517,6 +1560,12 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
     }
     if (!scratch || scratch_bytes < need) return FFTCONV_ERR_WORKSPACE;
     if (misaligned(scratch)) return FFTCONV_ERR_ALIGN;
+    if (L <= kDk4MaxL) {
+        const cudaError_t e = plan->info.dtype == FFTCONV_F16
+                                  ? launch_dk4<0>(u, dy, w_in, w_out, dk, B, H, L, scratch, st)
+                                  : launch_dk4<1>(u, dy, w_in, w_out, dk, B, H, L, scratch, st);
+        return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+    }
     const int64_t rows = B * H;
     float2* a = static_cast<float2*>(scratch);
     float2* b = a + rows * L;

@@ -60,8 +60,11 @@ def test_input_grad_matches_oracle(N, dtype, gated, B, H, order):
     (1024, "fp16", False, 3, 2),      # shared-memory channels
     (4096, "bf16", True, 4, 3),
     (4096, "fp16", False, 1, 5),
-    (8192, "fp16", True, 2, 2),       # spectra through HBM
-    (32768, "bf16", False, 2, 2),
+    (8192, "fp16", True, 2, 2),       # four-step, L = 8 x 2048
+    (16384, "fp16", True, 3, 2),      # four-step, L = 16 x 2048
+    (16384, "bf16", False, 1, 3),
+    (32768, "bf16", False, 2, 2),     # four-step, L = 32 x 2048
+    (65536, "fp16", False, 1, 2),     # row transforms through HBM
 ])
 def test_kernel_grad_matches_oracle(N, dtype, gated, B, H):
     ins, dy = _inputs(B, H, N, dtype, gated, seed=32)
@@ -109,6 +112,6 @@ def test_kernel_grad_edge_cases():
     u = torch.zeros(1, 2, 8192, dtype=torch.float16, device="cuda")
     dk8 = torch.empty(2, 8192, device="cuda")
     need = L.fftconv_backward_dk_scratch_bytes(big._h, 1, 2)
-    assert need == 2 * 2 * 16384 * 8
+    assert need == 2 * 16384 * 8  # four-step form: the per-channel inverse intermediate
     assert L.fftconv_backward_dk(big._h, u.data_ptr(), u.data_ptr(), None, None, dk8.data_ptr(), 1, 2, None, 0,
                                  None) == 4
