@@ -38,68 +38,120 @@ __device__ __forceinline__ float2 dk_cmul(float2 a, float2 b) {
     return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
 }
 
-// Twiddles of the radix-4 passes of dk_fft2048x2: W_4Ns^kk for kk < Ns, pass
-// p (Ns = 2 * 4^p) at offset 2 (4^p - 1) / 3, i.e. 0, 2, 10, 42, 170.
+// Twiddles of the radix-4 passes of the 2048-point transforms: W_4Ns^kk for
+// kk < Ns, pass p (Ns = 2 * 4^p) at offset 2 (4^p - 1) / 3, i.e. 0, 2, 10,
+// 42, 170.
 constexpr int kDkTwEntries = 2 + 8 + 32 + 128 + 512;
 __device__ __forceinline__ int dk_tw_off(int p) { return (2 * ((1 << (2 * p)) - 1)) / 3; }
 
-// Two 2048-point DFTs (exponent sign -1) of the sequences at a[0..2048) and
-// a[2048..4096), Stockham: one radix-2 pass a -> b, then five radix-4 passes
-// of span Ns = 2, 8, 32, 128, 512 alternating b -> a -> b ..., so the result
-// lands back in a.  512 threads: thread t runs butterfly t of both sequences
-// with the twiddle W_4Ns^(t mod Ns) from the table tw.
-__device__ __forceinline__ void dk_fft2048x2(float2* a, float2* b, const float2* tw) {
-    constexpr int L2 = kDkL2, Q = L2 / 4;
+// The two sub-rows of a pair travel together: entry n of a transform buffer
+// is one float4 (Re A, Re B, Im A, Im B), so every butterfly and twiddle of
+// the transform works on both sub-rows with packed f32x2 arithmetic.
+struct DkPair {
+    unsigned long long re, im;  // (A, B) real parts, (A, B) imaginary parts
+};
+
+__device__ __forceinline__ unsigned long long dk_pk(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 dk_upk(unsigned long long r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ unsigned long long dk_add2(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long dk_sub2(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long dk_mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long dk_fma2(unsigned long long a, unsigned long long b,
+                                                      unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ DkPair dk_ld(const float4* p) {
+    const float4 v = *p;
+    return {dk_pk(v.x, v.y), dk_pk(v.z, v.w)};
+}
+__device__ __forceinline__ void dk_st(float4* p, DkPair v) {
+    const float2 r = dk_upk(v.re), i = dk_upk(v.im);
+    *p = make_float4(r.x, r.y, i.x, i.y);
+}
+__device__ __forceinline__ DkPair dk_padd(DkPair a, DkPair b) { return {dk_add2(a.re, b.re), dk_add2(a.im, b.im)}; }
+__device__ __forceinline__ DkPair dk_psub(DkPair a, DkPair b) { return {dk_sub2(a.re, b.re), dk_sub2(a.im, b.im)}; }
+// both sub-rows times the same twiddle c + i s
+__device__ __forceinline__ DkPair dk_pmul(DkPair v, float c, float s) {
+    const unsigned long long C = dk_pk(c, c), S = dk_pk(s, s), Sn = dk_pk(-s, -s);
+    return {dk_fma2(v.im, Sn, dk_mul2(v.re, C)), dk_fma2(v.re, S, dk_mul2(v.im, C))};
+}
+
+// Entry e of a transform buffer sits at slot e ^ ((e >> 2) & 7) (a bijection
+// within each block of 32 entries): the strided stores of the first passes
+// then spread over the banks (about 7 % above conflict-free over one row,
+// against 43 % without it, counted per quarter-warp of 16-byte accesses).
+__device__ __forceinline__ int dk_sw(int e) { return e ^ ((e >> 2) & 7); }
+
+// The radix-4 passes (span Ns = 2, 8, 32, 128, 512) of two 2048-point DFTs
+// (exponent sign -1, Stockham, self-sorting) whose radix-2 pass has been
+// done into b: b -> a -> b -> a -> b -> a, the result in a.  512 threads:
+// thread t runs butterfly t with the twiddle W_4Ns^(t mod Ns) of the table.
+__device__ __forceinline__ void dk_fft_r4(float4* a, float4* b, const float2* tw) {
+    constexpr int Q = kDkL2 / 4;
     const int t = threadIdx.x;
-    #pragma unroll
-    for (int s = 0; s < 2; ++s) {  // radix 2: 1024 butterflies per sequence, two per thread
-        #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int j = t + kDkRowThreads * hh;
-            const float2 c0 = a[s * L2 + j], c1 = a[s * L2 + j + L2 / 2];
-            b[s * L2 + 2 * j] = make_float2(c0.x + c1.x, c0.y + c1.y);
-            b[s * L2 + 2 * j + 1] = make_float2(c0.x - c1.x, c0.y - c1.y);
-        }
-    }
-    __syncthreads();
     #pragma unroll
     for (int p = 0; p < 5; ++p) {
         const int lgNs = 1 + 2 * p, Ns = 1 << lgNs;
-        const float2* x0 = (p & 1) ? a : b;
-        float2* y0 = (p & 1) ? b : a;
+        const float4* x = (p & 1) ? a : b;
+        float4* y0 = (p & 1) ? b : a;
         const int kk = t & (Ns - 1), jj = t >> lgNs;
         const float2 w1 = tw[dk_tw_off(p) + kk];
         const float c1 = w1.x, s1 = w1.y;
         const float c2 = c1 * c1 - s1 * s1, s2 = 2.f * c1 * s1;
         const float c3 = c2 * c1 - s2 * s1, s3 = c2 * s1 + s2 * c1;
-        #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            const float2* x = x0 + s * L2;
-            float2 v0 = x[t], v1 = x[t + Q], v2 = x[t + 2 * Q], v3 = x[t + 3 * Q];
-            v1 = make_float2(v1.x * c1 - v1.y * s1, v1.x * s1 + v1.y * c1);
-            v2 = make_float2(v2.x * c2 - v2.y * s2, v2.x * s2 + v2.y * c2);
-            v3 = make_float2(v3.x * c3 - v3.y * s3, v3.x * s3 + v3.y * c3);
-            const float2 a0 = make_float2(v0.x + v2.x, v0.y + v2.y), a1 = make_float2(v0.x - v2.x, v0.y - v2.y);
-            const float2 a2 = make_float2(v1.x + v3.x, v1.y + v3.y);
-            const float2 a3 = make_float2(v1.y - v3.y, v3.x - v1.x);  // -i (v1 - v3)
-            float2* y = y0 + s * L2 + kk + (jj << (lgNs + 2));
-            y[0] = make_float2(a0.x + a2.x, a0.y + a2.y);
-            y[Ns] = make_float2(a1.x + a3.x, a1.y + a3.y);
-            y[2 * Ns] = make_float2(a0.x - a2.x, a0.y - a2.y);
-            y[3 * Ns] = make_float2(a1.x - a3.x, a1.y - a3.y);
-        }
+        const DkPair v0 = dk_ld(x + dk_sw(t));
+        const DkPair v1 = dk_pmul(dk_ld(x + dk_sw(t + Q)), c1, s1);
+        const DkPair v2 = dk_pmul(dk_ld(x + dk_sw(t + 2 * Q)), c2, s2);
+        const DkPair v3 = dk_pmul(dk_ld(x + dk_sw(t + 3 * Q)), c3, s3);
+        const DkPair a0 = dk_padd(v0, v2), a1 = dk_psub(v0, v2), a2 = dk_padd(v1, v3);
+        const DkPair a3 = {dk_sub2(v1.im, v3.im), dk_sub2(v3.re, v1.re)};  // -i (v1 - v3)
+        const int o = kk + (jj << (lgNs + 2));
+        dk_st(y0 + dk_sw(o), dk_padd(a0, a2));
+        dk_st(y0 + dk_sw(o + Ns), dk_padd(a1, a3));
+        dk_st(y0 + dk_sw(o + 2 * Ns), dk_psub(a0, a2));
+        dk_st(y0 + dk_sw(o + 3 * Ns), dk_psub(a1, a3));
         __syncthreads();
     }
+}
+
+// G[f] conj X[f] from Z[f] = (ar, ai) and Z[-f] = (cr, ci)
+__device__ __forceinline__ float2 dk_cross(float ar, float ai, float cr, float ci) {
+    const float gr = 0.5f * (ar + cr), gi = 0.5f * (ai - ci);   // G = (Z[f] + conj Z[-f]) / 2
+    const float xr = 0.5f * (ai + ci), xi = -0.5f * (ar - cr);  // X = (Z[f] - conj Z[-f]) / (2i)
+    return make_float2(gr * xr + gi * xi, gi * xr - gr * xi);
 }
 
 // One CTA per (channel h, pair of sub-rows p), looping over the batch.  The
 // CTAs of a channel run side by side (items are numbered channel-major), so
 // each row of u and dy comes from DRAM about once and from L2 L1/2 times.
-// Thread t computes the column sums of columns n2 = 4t .. 4t + 3 (8-byte
-// loads of four 16-bit inputs, a few rows n1 in flight at once) and owns
-// entries t + 512 e of the pair's 2 x 2048 bins in the batch sum.  Shared
-// memory: two transform buffers and the batch sum S, 2 x 2048 entries each,
-// and the transform's twiddles (101.5 KB, two CTAs per SM).
+// Thread t computes the column sums of columns 2t, 2t + 1, 2t + 1024 and
+// 2t + 1025 (4-byte loads of two 16-bit inputs, a few rows n1 in flight at
+// once), which are the inputs of the transform's radix-2 butterflies 2t and
+// 2t + 1: that pass runs in registers.  It owns bins t + 512 e of the batch
+// sum.  Shared memory: two transform buffers of 2048 float4, the batch sum S
+// of both sub-rows and the radix-4 twiddles (101.5 KB, two CTAs per SM).
 template <int DT, int L1, bool G>
 __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __restrict__ u,
                                                             const uint16_t* __restrict__ dy,
@@ -107,16 +159,16 @@ __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __re
                                                             const uint16_t* __restrict__ w_out,
                                                             float2* __restrict__ R, int64_t B, int64_t H) {
     using O = Op<DT>;
-    constexpr int L2 = kDkL2, T = kDkRowThreads, COLS = L2 / T, E = 2 * COLS;
-    constexpr int NH = L1 / 2, CH = G ? 2 : 4;  // input rows n1; rows loaded per round
-    static_assert(COLS == 4 && NH % CH == 0, "four columns per thread");
+    constexpr int L2 = kDkL2, T = kDkRowThreads, NE = L2 / T;  // 4 bins per thread per sub-row
+    constexpr int NH = L1 / 2, CH = G ? 2 : 4;                 // input rows n1; rows loaded per round
+    static_assert(NE == 4 && NH % CH == 0, "2048-point sub-rows, 512 threads");
     constexpr int64_t N = int64_t(L2) * NH;
     constexpr uint32_t L = uint32_t(L1) * uint32_t(L2);
-    extern __shared__ __align__(16) float2 dsm[];
-    float2* buf0 = dsm;
-    float2* buf1 = dsm + 2 * L2;
-    float2* acc = dsm + 4 * L2;  // S, entry q = sub-row * L2 + k2
-    float2* ftw = dsm + 6 * L2;  // radix-4 twiddles of the transforms
+    extern __shared__ __align__(16) float4 dsm4[];
+    float4* bufA = dsm4;
+    float4* bufB = dsm4 + L2;
+    float2* acc = reinterpret_cast<float2*>(dsm4 + 2 * L2);  // S[sub-row][k2]
+    float2* ftw = acc + 2 * L2;                              // radix-4 twiddles
     const int t = threadIdx.x;
     for (int i = t; i < kDkTwEntries; i += T) {
         int p = 0;
@@ -132,124 +184,143 @@ __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __re
         const int64_t h = it / NH;
         const int p = int(it - h * NH);
         const int kA = p, kB = p ? L1 - p : NH;
-        // W_L^(n2 k1) of this thread's columns n2 = 4t + c, both sub-rows
-        float2 ctw[COLS][2];
+        // W_L^(n2 k1) of this thread's columns n2 = 2t + 1024 gc + c, both sub-rows
+        float2 ctw[4][2];
         #pragma unroll
-        for (int c = 0; c < COLS; ++c) {
-            const uint32_t n2 = uint32_t(4 * t + c);
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t n2 = uint32_t(2 * t + 1024 * (c >> 1) + (c & 1));
             ctw[c][0] = dk_twiddle(n2 * uint32_t(kA), L);
             ctw[c][1] = dk_twiddle(n2 * uint32_t(kB), L);
         }
         const float2 wst = dk_twiddle(uint32_t(kA), uint32_t(L1));  // W_L1^kA
         #pragma unroll
-        for (int e = 0; e < E; ++e) acc[t + T * e] = make_float2(0.f, 0.f);
+        for (int e = 0; e < 2 * NE; ++e) acc[t + T * e] = make_float2(0.f, 0.f);
         for (int64_t b = 0; b < B; ++b) {
-            const int64_t roff = (b * H + h) * N + 4 * t;
+            const int64_t roff = (b * H + h) * N + 2 * t;
             // A_k1[n2] = W_L^(n2 k1) sum_{n1 < L1/2} z[L2 n1 + n2] W_L1^(n1 k1), with
             // W_L1^(n1 kB) = conj W_L1^(n1 kA) (kB = L1 - kA) or, on pair 0,
             // W_L1^0 = 1 and W_L1^(n1 L1/2) = (-1)^n1
-            float2 sa[COLS], sb[COLS];
+            // accumulators as f32x2 pairs over the columns (2t, 2t + 1) of group gc
+            unsigned long long are[2], aim[2], bre[2], bim[2];  // sub-row A / B, real / imaginary
             #pragma unroll
-            for (int c = 0; c < COLS; ++c) sa[c] = sb[c] = make_float2(0.f, 0.f);
+            for (int gc = 0; gc < 2; ++gc) are[gc] = aim[gc] = bre[gc] = bim[gc] = 0ull;
             float2 w = make_float2(1.f, 0.f);
             #pragma unroll
             for (int n0 = 0; n0 < NH; n0 += CH) {
-                uint2 vg[CH], vx[CH], vo[G ? CH : 1], vi[G ? CH : 1];
+                uint32_t vg[CH][2], vx[CH][2], vo[G ? CH : 1][2], vi[G ? CH : 1][2];
                 #pragma unroll
-                for (int m = 0; m < CH; ++m) {
-                    const int64_t j = roff + int64_t(L2) * (n0 + m);
-                    vg[m] = __ldg(reinterpret_cast<const uint2*>(dy + j));
-                    vx[m] = __ldg(reinterpret_cast<const uint2*>(u + j));
-                    if constexpr (G) {
-                        vo[m] = __ldg(reinterpret_cast<const uint2*>(w_out + j));
-                        vi[m] = __ldg(reinterpret_cast<const uint2*>(w_in + j));
+                for (int m = 0; m < CH; ++m)
+                    #pragma unroll
+                    for (int gc = 0; gc < 2; ++gc) {
+                        const int64_t j = roff + int64_t(L2) * (n0 + m) + 1024 * gc;
+                        vg[m][gc] = __ldg(reinterpret_cast<const uint32_t*>(dy + j));
+                        vx[m][gc] = __ldg(reinterpret_cast<const uint32_t*>(u + j));
+                        if constexpr (G) {
+                            vo[m][gc] = __ldg(reinterpret_cast<const uint32_t*>(w_out + j));
+                            vi[m][gc] = __ldg(reinterpret_cast<const uint32_t*>(w_in + j));
+                        }
                     }
-                }
                 #pragma unroll
                 for (int m = 0; m < CH; ++m) {
                     const int n1 = n0 + m;
-                    const cpx g01 = O::unpack(vg[m].x), g23 = O::unpack(vg[m].y);
-                    const cpx x01 = O::unpack(vx[m].x), x23 = O::unpack(vx[m].y);
-                    float gg[4] = {g01.r, g01.i, g23.r, g23.i}, xx[4] = {x01.r, x01.i, x23.r, x23.i};
-                    if constexpr (G) {
-                        const cpx o01 = O::unpack(vo[m].x), o23 = O::unpack(vo[m].y);
-                        const cpx i01 = O::unpack(vi[m].x), i23 = O::unpack(vi[m].y);
-                        gg[0] *= o01.r; gg[1] *= o01.i; gg[2] *= o23.r; gg[3] *= o23.i;
-                        xx[0] *= i01.r; xx[1] *= i01.i; xx[2] *= i23.r; xx[3] *= i23.i;
-                    }
+                    const unsigned long long WX = dk_pk(w.x, w.x), WY = dk_pk(w.y, w.y), WYn = dk_pk(-w.y, -w.y);
                     #pragma unroll
-                    for (int c = 0; c < COLS; ++c) {
-                        const float g = gg[c], x = xx[c];
+                    for (int gc = 0; gc < 2; ++gc) {
+                        cpx g2 = O::unpack(vg[m][gc]), x2 = O::unpack(vx[m][gc]);
+                        if constexpr (G) {
+                            const cpx o2 = O::unpack(vo[m][gc]), i2 = O::unpack(vi[m][gc]);
+                            g2.r *= o2.r; g2.i *= o2.i;
+                            x2.r *= i2.r; x2.i *= i2.i;
+                        }
+                        const unsigned long long g = dk_pk(g2.r, g2.i), x = dk_pk(x2.r, x2.i);
                         if (p == 0) {
-                            const float sg = (n1 & 1) ? -1.f : 1.f;
-                            sa[c].x += g;
-                            sa[c].y += x;
-                            sb[c].x += sg * g;
-                            sb[c].y += sg * x;
+                            are[gc] = dk_add2(are[gc], g);
+                            aim[gc] = dk_add2(aim[gc], x);
+                            bre[gc] = (n1 & 1) ? dk_sub2(bre[gc], g) : dk_add2(bre[gc], g);
+                            bim[gc] = (n1 & 1) ? dk_sub2(bim[gc], x) : dk_add2(bim[gc], x);
                         } else {
-                            const float P1 = g * w.x, P2 = x * w.y, P3 = g * w.y, P4 = x * w.x;
-                            sa[c].x += P1 - P2;  // z W
-                            sa[c].y += P3 + P4;
-                            sb[c].x += P1 + P2;  // z conj W
-                            sb[c].y += P4 - P3;
+                            are[gc] = dk_fma2(x, WYn, dk_fma2(g, WX, are[gc]));  // z W
+                            aim[gc] = dk_fma2(x, WX, dk_fma2(g, WY, aim[gc]));
+                            bre[gc] = dk_fma2(x, WY, dk_fma2(g, WX, bre[gc]));   // z conj W
+                            bim[gc] = dk_fma2(g, WYn, dk_fma2(x, WX, bim[gc]));
                         }
                     }
                     w = dk_cmul(w, wst);
                 }
             }
+            float2 sa[4], sb[4];  // column c = 2 gc + e
             #pragma unroll
-            for (int c = 0; c < COLS; c += 2) {
-                const float2 a0 = dk_cmul(sa[c], ctw[c][0]), a1 = dk_cmul(sa[c + 1], ctw[c + 1][0]);
-                const float2 b0 = dk_cmul(sb[c], ctw[c][1]), b1 = dk_cmul(sb[c + 1], ctw[c + 1][1]);
-                *reinterpret_cast<float4*>(buf0 + 4 * t + c) = make_float4(a0.x, a0.y, a1.x, a1.y);
-                *reinterpret_cast<float4*>(buf0 + L2 + 4 * t + c) = make_float4(b0.x, b0.y, b1.x, b1.y);
+            for (int gc = 0; gc < 2; ++gc) {
+                const float2 ar = dk_upk(are[gc]), ai = dk_upk(aim[gc]), br = dk_upk(bre[gc]), bi = dk_upk(bim[gc]);
+                sa[2 * gc] = make_float2(ar.x, ai.x);
+                sa[2 * gc + 1] = make_float2(ar.y, ai.y);
+                sb[2 * gc] = make_float2(br.x, bi.x);
+                sb[2 * gc + 1] = make_float2(br.y, bi.y);
+            }
+            // the radix-2 pass: butterfly j = 2t + e takes columns j and j + 1024
+            #pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float2 a0 = dk_cmul(sa[e], ctw[e][0]), b0 = dk_cmul(sb[e], ctw[e][1]);
+                const float2 a1 = dk_cmul(sa[2 + e], ctw[2 + e][0]), b1 = dk_cmul(sb[2 + e], ctw[2 + e][1]);
+                const int j = 2 * t + e;
+                bufB[dk_sw(2 * j)] = make_float4(a0.x + a1.x, b0.x + b1.x, a0.y + a1.y, b0.y + b1.y);
+                bufB[dk_sw(2 * j + 1)] = make_float4(a0.x - a1.x, b0.x - b1.x, a0.y - a1.y, b0.y - b1.y);
             }
             __syncthreads();
-            dk_fft2048x2(buf0, buf1, ftw);
-            // S += G conj X on this thread's entries; for k1 > 0 on sub-row A only,
+            dk_fft_r4(bufA, bufB, ftw);
+            // S += G conj X on this thread's bins; for k1 > 0 on sub-row A only,
             // since S[-f] = conj S[f] gives sub-row B's bins at the end
             #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int s = e / COLS, q = t + T * e, k2 = q - s * L2;  // sub-row s (T * COLS = L2)
-                if (s == 1 && p != 0) break;
-                int pq;  // the partner entry -f
-                if (p == 0)
-                    pq = s == 0 ? ((L2 - k2) & (L2 - 1)) : L2 + (L2 - 1 - k2);
-                else
-                    pq = (s == 0 ? L2 : 0) + (L2 - 1 - k2);
-                const float2 a = buf0[q], cc = buf0[pq];  // Z[f], Z[-f]
-                const float gr = 0.5f * (a.x + cc.x), gi = 0.5f * (a.y - cc.y);   // G
-                const float xr = 0.5f * (a.y + cc.y), xi = -0.5f * (a.x - cc.x);  // X
-                float2 v = acc[q];
-                v.x += gr * xr + gi * xi;  // G conj X
-                v.y += gi * xr - gr * xi;
-                acc[q] = v;
+            for (int e = 0; e < NE; ++e) {
+                const int k2 = t + T * e;
+                const float4 z = bufA[dk_sw(k2)];
+                const float4 zb = bufA[dk_sw(L2 - 1 - k2)];  // partner of sub-row A (k1 > 0) or of sub-row B (pair 0)
+                float2 sA;
+                if (p == 0) {
+                    const float4 za = bufA[dk_sw((L2 - k2) & (L2 - 1))];
+                    sA = dk_cross(z.x, z.z, za.x, za.z);
+                    const float2 sB = dk_cross(z.y, z.w, zb.y, zb.w);
+                    float2 v = acc[L2 + k2];
+                    acc[L2 + k2] = make_float2(v.x + sB.x, v.y + sB.y);
+                } else {
+                    sA = dk_cross(z.x, z.z, zb.y, zb.w);
+                }
+                float2 v = acc[k2];
+                acc[k2] = make_float2(v.x + sA.x, v.y + sA.y);
             }
-            __syncthreads();  // buf0 is refilled by the next row
+            __syncthreads();  // the buffers are refilled by the next row
         }
-        // conj S, transformed along k2; the twiddle W_L^(k1 n2) -> R[h][k1][n2]
-        if (p == 0) {
-            #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const float2 v = acc[t + T * e];
-                buf0[t + T * e] = make_float2(v.x, -v.y);
+        // conj S (both sub-rows; conj S_B[k2] = S_A[L2 - 1 - k2] for k1 > 0),
+        // transformed along k2; the twiddle W_L^(k1 n2) -> R[h][k1][n2]
+        #pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int k2 = t + T * e;
+            const float2 sA = acc[k2];
+            float2 cB;  // conj S_B[k2]
+            if (p == 0) {
+                const float2 v = acc[L2 + k2];
+                cB = make_float2(v.x, -v.y);
+            } else {
+                cB = acc[L2 - 1 - k2];
             }
-        } else {  // conj S_B[L2 - 1 - k2] = S_A[k2]
-            #pragma unroll
-            for (int e = 0; e < COLS; ++e) {
-                const int q = t + T * e;
-                const float2 v = acc[q];
-                buf0[q] = make_float2(v.x, -v.y);
-                buf0[2 * L2 - 1 - q] = v;
-            }
+            bufA[dk_sw(k2)] = make_float4(sA.x, cB.x, -sA.y, cB.y);
         }
         __syncthreads();
-        dk_fft2048x2(buf0, buf1, ftw);
         #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int s = e / COLS, q = t + T * e, n2 = q - s * L2;
-            const int k1 = s ? kB : kA;
-            R[(h * L1 + k1) * L2 + n2] = dk_cmul(buf0[q], dk_twiddle(uint32_t(k1) * uint32_t(n2), L));
+        for (int e = 0; e < 2; ++e) {  // radix-2 pass: butterflies t and t + 512
+            const int j = t + T * e;
+            const float4 c0 = bufA[dk_sw(j)], c1 = bufA[dk_sw(j + L2 / 2)];
+            bufB[dk_sw(2 * j)] = make_float4(c0.x + c1.x, c0.y + c1.y, c0.z + c1.z, c0.w + c1.w);
+            bufB[dk_sw(2 * j + 1)] = make_float4(c0.x - c1.x, c0.y - c1.y, c0.z - c1.z, c0.w - c1.w);
+        }
+        __syncthreads();
+        dk_fft_r4(bufA, bufB, ftw);
+        #pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int n2 = t + T * e;
+            const float4 v = bufA[dk_sw(n2)];
+            R[(h * L1 + kA) * L2 + n2] = dk_cmul(make_float2(v.x, v.z), dk_twiddle(uint32_t(kA) * uint32_t(n2), L));
+            R[(h * L1 + kB) * L2 + n2] = dk_cmul(make_float2(v.y, v.w), dk_twiddle(uint32_t(kB) * uint32_t(n2), L));
         }
         __syncthreads();  // the buffers are reused by the next item
     }

@@ -1473,7 +1473,7 @@ constexpr int64_t kDk4MaxL = 65536;
 template <int DT, int L1, bool G>
 cudaError_t launch_dk4_t(const void* u, const void* dy, const void* w_in, const void* w_out, float* dk, int64_t B,
                          int64_t H, float2* R, cudaStream_t st) {
-    const size_t smem = (size_t(6) * kDkL2 + kDkTwEntries) * sizeof(float2);
+    const size_t smem = size_t(2) * kDkL2 * sizeof(float4) + (size_t(2) * kDkL2 + kDkTwEntries) * sizeof(float2);
     static PerDevice ready;  // per instantiation and device
     auto fn = dk_rows<DT, L1, G>;
     int* rd = ready.slot();
