@@ -414,6 +414,90 @@ def run_backward(args, w: W.Workload):
         torch.distributed.destroy_process_group()
 
 
+def run_circular(args, w: W.Workload):
+    """The circular convolution of length C = the workload's N, B, H and
+    dtype: the native circular plan (C/2 complex points, every outer row in
+    and out) against the windowed form on a causal plan of length 2C (outputs
+    [C, 2C) of the causal convolution of [u, u] with [k, 0]).  One line with
+    the native time as the value and the windowed time beside it."""
+    import torch
+    import fft_long_convolution_gb300 as F
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    F.build_library()
+    ins = W.make_inputs(w, seed=rank)
+    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+
+    def dev_t(r):
+        if r.dtype == "fp32":
+            return torch.from_numpy(r.bits).to(dev)
+        return torch.from_numpy(r.bits.view(np.int16)).view(tdt).to(dev)
+
+    C = w.N
+    k = dev_t(ins["k"])  # C taps
+    u = dev_t(ins["u"])
+    wi = dev_t(ins["w_in"]) if w.gated else None
+    wo = dev_t(ins["w_out"]) if w.gated else None
+    y = torch.empty_like(u)
+    stream = torch.cuda.current_stream()
+    native = F.Plan(C, tdt, circular=True)
+    kf_n = native.kernel_fft(k)
+    win = F.Plan(2 * C, tdt)
+    kf_w = win.kernel_fft_partial(k)
+
+    def step_native():
+        if w.gated:
+            native.forward_gated(u, wi, wo, kf_n, y=y, stream=stream)
+        else:
+            native.forward(u, kf_n, y=y, stream=stream)
+
+    def step_windowed():
+        win.forward_circular(u, kf_w, wi, wo, y=y, stream=stream)
+
+    def timed(step, steps):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    steps = max(1, min(args.steps, 200))
+    ms_w = timed(step_windowed, steps)
+    clocks = ClockSampler(local)
+    ms = timed(step_native, steps)
+    clk = clocks.stop()
+    assert native.device_status() == 0 and win.device_status() == 0
+    ms = max_over_ranks(ms, world, dev)
+    if rank == 0:
+        peaks = measured_peaks()
+        nbytes = w.rows * C * 2 * (2 + (2 if w.gated else 0)) + native.kf_bytes(w.H)
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        fac = native.info["factors"]
+        out = {"metric": METRIC + " (circular convolution)", "value": job_value(w.outputs, world, ms),
+               "unit": "outputs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
+               "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": {"fp16": "f16", "bf16": "bf16"}[w.dtype], "data": "synthetic",
+               "config": dict(config_of(w), circular_length=C, factors=fac),
+               "windowed_2C_ms_per_step": ms_w,
+               "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                            "algorithmic_bytes_per_launch": nbytes,
+                            "kernel": "otc_pass (A, all rows) + mp_pass_b_tc + otc_pass (C, all rows)"},
+               "gpu_launches": steps * 3, "clocks": clk}
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,8 +508,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--band", default=None,
                     help="frequency-sparse forward: one band per plan factor, comma separated (e.g. 16,33,33)")
-    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
-                    help="backward: input and kernel gradients (du + dk) per step")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "circular"],
+                    help="backward: input and kernel gradients (du + dk) per step; circular: the circular "
+                         "convolution of length N (native plan, with the windowed 2N form timed beside it)")
     ap.add_argument("--batch", type=int, default=None,
                     help="run the workload with this batch size instead of its own (small cases for profiler "
                          "captures; the benchmark is quoted on the workload's own size)")
@@ -438,6 +523,9 @@ def main():
         return
     if args.which == "backward":
         run_backward(args, w)
+        return
+    if args.which == "circular":
+        run_circular(args, w)
         return
 
     import torch

@@ -24,7 +24,8 @@ EXPORTED = ["fftconv_plan_query", "fftconv_plan_create", "fftconv_plan_destroy",
             "fftconv_backward_du_gated", "fftconv_backward_dk_scratch_bytes", "fftconv_backward_dk",
             "fftconv_partial_scratch_bytes", "fftconv_forward_partial", "fftconv_circular_scratch_bytes",
             "fftconv_forward_circular", "fftconv_selftest_wait", "fftconv_plan_create_sparse",
-            "fftconv_plan_get_band", "fftconv_sparse_query",
+            "fftconv_plan_get_band", "fftconv_sparse_query", "fftconv_circular_query",
+            "fftconv_plan_create_circular",
             "fftconv_device_status", "fftconv_status_string", "fftconv_version"]
 
 
@@ -66,6 +67,8 @@ def lib(auto_build: bool = True):
         L.fftconv_sparse_query.argtypes = [i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
                                            ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
                                            ctypes.POINTER(ctypes.c_int32)]
+        L.fftconv_circular_query.argtypes = [i64, ctypes.c_int, ctypes.POINTER(PlanInfo)]
+        L.fftconv_plan_create_circular.argtypes = [ctypes.POINTER(vp), i64, ctypes.c_int]
         L.fftconv_plan_get_band.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                             ctypes.POINTER(ctypes.c_int32)]
         L.fftconv_plan_destroy.argtypes = [vp]
@@ -114,6 +117,13 @@ def query(N: int, dtype: int, order: int = 0) -> dict:
     return info.as_dict()
 
 
+def circular_query(C: int, dtype: int) -> dict:
+    """The plan a circular convolution of length C would use (no GPU)."""
+    info = PlanInfo()
+    _check(lib().fftconv_circular_query(C, dtype, ctypes.byref(info)), "fftconv_circular_query")
+    return info.as_dict()
+
+
 def sparse_query(N: int, dtype: int, band, order: int = 0) -> dict:
     """Pairs of sub-rows a frequency-sparse plan would transform (no GPU)."""
     arr = (ctypes.c_int32 * max(1, len(band)))(*[int(b) for b in band])
@@ -145,14 +155,21 @@ def _stream(stream) -> Optional[int]:
 class Plan:
     """A plan for one sequence length N and dtype (torch.float16 / bfloat16)."""
 
-    def __init__(self, N: int, dtype, order: int = 0, band=None):
+    def __init__(self, N: int, dtype, order: int = 0, band=None, circular: bool = False):
         """band: one int per factor (outer first) for a frequency-sparse plan;
-        None for the dense convolution."""
+        None for the dense convolution.  circular: a plan for the circular
+        convolution of length N (rows of N samples, k of N taps)."""
         self.N = int(N)
         self.torch_dtype = dtype
         self.dtype = _dtype_code(dtype)
+        self.circular = bool(circular)
         h = ctypes.c_void_p()
-        if band is None:
+        if circular:
+            if band is not None or order != 0:
+                raise ValueError("a circular plan takes no band and no order")
+            _check(lib().fftconv_plan_create_circular(ctypes.byref(h), self.N, self.dtype),
+                   "fftconv_plan_create_circular")
+        elif band is None:
             _check(lib().fftconv_plan_create(ctypes.byref(h), self.N, self.dtype, order), "fftconv_plan_create")
         else:
             arr = (ctypes.c_int32 * max(1, len(band)))(*[int(b) for b in band])

@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libfftconv_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["fftconv.cu", "mp_l16k.cu", "mp_l4k.cu", "mp_l16k_sparse.cu", "mp_l4k_sparse.cu"]  # compiled in parallel, then linked
+SOURCES = ["fftconv.cu", "mp_l16k.cu", "mp_l4k.cu", "mp_l16k_sparse.cu", "mp_l4k_sparse.cu", "mp_circ.cu"]  # compiled in parallel, then linked
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 _lock = threading.Lock()
 

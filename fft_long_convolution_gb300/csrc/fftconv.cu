@@ -377,9 +377,9 @@ void ftc_twiddle_tables(int R0, std::vector<float>& tin, std::vector<float>& tou
 // the B operand of Otc<R, MODE>: row 2 o + part (0 real, 1 imaginary part of
 // output o), K index 2 n + pin (0 real, 1 imaginary part of input n),
 // K-major without swizzle; padding rows and K indices zero.
-template <int R, int MODE>
+template <int R, int MODE, bool FULL = false>
 std::vector<uint16_t> build_otc_fmat(int dtype) {
-    using C = Otc<R, MODE>;
+    using C = Otc<R, MODE, FULL>;
     std::vector<uint16_t> v(C::BBYTES / 2, 0);
     const double sc = 1.0 / std::sqrt(double(R));
     for (int o = 0; o < C::NOUT; ++o)
@@ -412,8 +412,25 @@ void otc_outer(OtcTables& t, int dtype) {
     t.fc = build_otc_fmat<R, 3>(dtype);
 }
 
-OtcTables build_otc_tables(int R, bool two_level, int dtype) {
+template <int R>
+void otc_outer_full(OtcTables& t, int dtype) {
+    t.fa = build_otc_fmat<R, 0, true>(dtype);
+    t.fc = build_otc_fmat<R, 3, true>(dtype);
+}
+
+OtcTables build_otc_tables(int R, bool two_level, int dtype, bool full = false) {
     OtcTables t;
+    if (full) {  // circular plans: every input and output row of the outer factor
+        switch (R) {
+            case 2: otc_outer_full<2>(t, dtype); break;
+            case 4: otc_outer_full<4>(t, dtype); break;
+            case 8: otc_outer_full<8>(t, dtype); break;
+            case 16: otc_outer_full<16>(t, dtype); break;
+            case 32: otc_outer_full<32>(t, dtype); break;
+            case 64: otc_outer_full<64>(t, dtype); break;
+        }
+        return t;
+    }
     switch (R) {
         case 4: otc_outer<4>(t, dtype); break;
         case 8: otc_outer<8>(t, dtype); break;
@@ -536,6 +553,7 @@ cudaError_t launch_multipass(const fftconv_plan_s* p, const void* u, const void*
                 static_cast<uint32_t*>(T), int(B), int(H), p->R0, p->mp, p->dev_err,
                 p->zbits, 1, p->pairs_run, p->plist};
     const bool gated = wi != nullptr;
+    if (p->circular) return launch_mp_l4k_circular(p, args, B * H, gated, st);
     if (p->zbits) {  // frequency-sparse plan with pairs of sub-rows to skip
         if (p->mp2) return launch_mp_l4k_2level_sparse(p, args, B * H, gated, st);
         return p->mpL == kMpLtc ? launch_mp_l4k_sparse(p, args, B * H, gated, st)
@@ -615,14 +633,14 @@ int ftc_pairs_run(const fftconv_plan_info_t& info, const int32_t* band, bool spa
 }
 
 fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_t dtype, int order,
-                                  const int32_t* band, int nband) {
+                                  const int32_t* band, int nband, bool circular = false) {
     if (!out) return FFTCONV_ERR_INVALID;
     *out = nullptr;
     // a band pattern is defined over the digits of an N-point transform: rows
     // shorter than 4096 keep their own factorization R1 x 16 x 16 then
     if (band && order == 0 && N < 4096) order = 3;
     fftconv_plan_info_t info;
-    fftconv_status_t st = fftconv_plan_query(N, dtype, order, &info);
+    fftconv_status_t st = circular ? fftconv_circular_query(N, dtype, &info) : fftconv_plan_query(N, dtype, order, &info);
     if (st != FFTCONV_OK) return st;
     if (band) {
         if (nband != info.order) return FFTCONV_ERR_INVALID;
@@ -632,6 +650,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     fftconv_plan_s* p = new (std::nothrow) fftconv_plan_s();
     if (!p) return FFTCONV_ERR_ALLOC;
     p->info = info;
+    p->circular = circular;
     for (int j = 0; j < info.order; ++j) {
         const int32_t full = info.factors[j] / 2 + 1;  // keeps every digit value
         p->band[j] = band ? std::min(band[j], full) : full;
@@ -652,7 +671,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     if (need_fmat) fmat = build_tc64_fmat(dtype);
     HostTables T0;
     std::vector<uint32_t> ofull;
-    if (multi) {
+    if (multi && !circular) {  // the warp-level outer passes (frequency-sparse and order-4 plans)
         T0 = build_fused_tables(p->mp2 ? info.factors[0] : p->R0, dtype);  // fragments of the outermost factor
         ofull = build_full_frags(kMpR1, dtype);
     }
@@ -668,11 +687,11 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     const size_t o_ftin = p->ftc ? append(blob, ftin) : 0, o_ftout = p->ftc ? append(blob, ftout) : 0;
     const bool otc = p->mpL == kMpLtc;
     OtcTables ot;
-    if (otc) ot = build_otc_tables(p->mp2 ? info.factors[0] : p->R0, p->mp2, dtype);
+    if (otc) ot = build_otc_tables(p->mp2 ? info.factors[0] : p->R0, p->mp2, dtype, circular);
     const size_t o_tfa = otc ? append(blob, ot.fa) : 0, o_tfc = otc ? append(blob, ot.fc) : 0;
     const size_t o_tfa2 = (otc && p->mp2) ? append(blob, ot.fa2) : 0, o_tfc2 = (otc && p->mp2) ? append(blob, ot.fc2) : 0;
     size_t o_ofa = 0, o_oic = 0, o_ofull = 0;
-    if (multi) {
+    if (multi && !circular) {
         o_ofa = append(blob, T0.of);
         o_oic = append(blob, T0.oi);
         o_ofull = append(blob, ofull);
@@ -733,7 +752,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     p->tb.off_oi = uint32_t(o_oi - o_of);
     p->tb.off_twf = uint32_t(o_twf - o_of);
     p->tb.off_twi = uint32_t(o_twi - o_of);
-    if (multi) {
+    if (multi && !circular) {
         p->mp.lf = p->tb.lf;
         p->mp.rf = p->tb.rf;
         p->mp.tw = p->tb.tw;
@@ -762,6 +781,32 @@ extern "C" fftconv_status_t fftconv_plan_create_sparse(fftconv_plan_t* out, int6
                                                        int order, const int32_t* band, int nband) {
     if (!band) return FFTCONV_ERR_INVALID;
     return plan_create_impl(out, N, dtype, order, band, nband);
+}
+
+extern "C" fftconv_status_t fftconv_circular_query(int64_t C, fftconv_dtype_t dtype, fftconv_plan_info_t* info) {
+    if (!info) return FFTCONV_ERR_INVALID;
+    if (dtype != FFTCONV_F16 && dtype != FFTCONV_BF16) return FFTCONV_ERR_UNSUPPORTED;
+    // M = C / 2 = R0 * 4096 with R0 = 2 .. 64: the multi-pass factorization
+    // R0 x 64 x 64 with the outer passes over every row
+    if (!is_pow2(C) || C < 16384 || C > (int64_t(1) << 19)) return FFTCONV_ERR_UNSUPPORTED;
+    fftconv_plan_info_t q;
+    std::memset(&q, 0, sizeof(q));
+    q.N = C;
+    q.M = C / 2;
+    q.order = 3;
+    q.factors[0] = int32_t(C / 8192);
+    q.factors[1] = 64;
+    q.factors[2] = 64;
+    q.path = FFTCONV_PATH_MULTIPASS;
+    q.dtype = dtype;
+    q.kf_bytes_per_channel = int64_t(q.factors[0] / 2) * TcB::KFP * 16;
+    q.workspace_bytes_per_row = 4 * q.M;  // 16-bit complex intermediate
+    *info = q;
+    return FFTCONV_OK;
+}
+
+extern "C" fftconv_status_t fftconv_plan_create_circular(fftconv_plan_t* out, int64_t C, fftconv_dtype_t dtype) {
+    return plan_create_impl(out, C, dtype, 0, nullptr, 0, true);
 }
 
 extern "C" fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtype, int order, const int32_t* band,
@@ -1522,6 +1567,7 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
                                                 size_t scratch_bytes, fftconv_stream_t stream) {
     if (!plan || B < 0 || H < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (plan->sparse) return FFTCONV_ERR_UNSUPPORTED;  // the kernel gradient is not band-limited here
+    if (plan->circular) return FFTCONV_ERR_UNSUPPORTED;  // the batch sum assumes causal (zero-padded) rows
     if (H == 0) return FFTCONV_OK;
     if (!dk || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
     const int64_t N = plan->info.N, L = 2 * N;
@@ -1687,6 +1733,7 @@ fftconv_status_t windowed_forward(fftconv_plan_t plan, const void* u, const void
                                   size_t scratch_bytes, fftconv_stream_t stream, bool wrap) {
     if (!plan || B < 0 || H < 0 || N < 0 || wrong_device(plan)) return FFTCONV_ERR_INVALID;
     if (plan->sparse) return FFTCONV_ERR_UNSUPPORTED;  // windows of a band-limited kernel are not defined here
+    if (plan->circular) return FFTCONV_ERR_UNSUPPORTED;  // windows are causal convolutions
     if (B == 0 || H == 0 || N == 0) return FFTCONV_OK;
     if (!u || !k_f || !y || (w_in == nullptr) != (w_out == nullptr)) return FFTCONV_ERR_INVALID;
     const bool gated = w_in != nullptr;

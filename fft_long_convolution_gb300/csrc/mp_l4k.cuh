@@ -120,6 +120,44 @@ cudaError_t launch_l4k_2level(const fftconv_plan_s* p, const MPArgs& args, int64
     return gated ? launch_2l_r<1, true, SP>(p, args, rows, st) : launch_2l_r<1, false, SP>(p, args, rows, st);
 }
 
+// Circular convolution of length 2 M, M = R0 * 4096: pass A over all R0 rows
+// of z, pass B unchanged, pass C writing all R0 output rows.
+template <int DT, int R0, bool G>
+cudaError_t launch_circ_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
+    constexpr int L = kMpLtc;
+    static PerDevice cb;
+    int nb = 0;
+    cudaError_t e;
+    if ((e = prep_kernel(mp_pass_b_tc<DT, false>, TcB::SMEM, TcB::THREADS, cb, &nb)) != cudaSuccess) return e;
+    const int64_t items_b = rows * (R0 / 2), need_b = (items_b + 1) / 2;
+    if (items_b >= (int64_t(1) << 30)) return cudaErrorInvalidValue;  // pass B counts items in int
+    const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);
+    TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, 0, R0 / 2, nullptr};
+    if ((e = launch_otc<DT, R0, 0, G, L, true>(p, args, rows, p->otc_fa, st)) != cudaSuccess) return e;
+    mp_pass_b_tc<DT, false><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_otc<DT, R0, 3, G, L, true>(p, args, rows, p->otc_fc, st);
+}
+
+template <int DT, bool G>
+cudaError_t launch_circ_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
+    switch (p->R0) {
+        case 2: return launch_circ_t<DT, 2, G>(p, args, rows, st);
+        case 4: return launch_circ_t<DT, 4, G>(p, args, rows, st);
+        case 8: return launch_circ_t<DT, 8, G>(p, args, rows, st);
+        case 16: return launch_circ_t<DT, 16, G>(p, args, rows, st);
+        case 32: return launch_circ_t<DT, 32, G>(p, args, rows, st);
+        case 64: return launch_circ_t<DT, 64, G>(p, args, rows, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+inline cudaError_t launch_circ(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st) {
+    if (p->info.dtype == FFTCONV_F16)
+        return gated ? launch_circ_r<0, true>(p, args, rows, st) : launch_circ_r<0, false>(p, args, rows, st);
+    return gated ? launch_circ_r<1, true>(p, args, rows, st) : launch_circ_r<1, false>(p, args, rows, st);
+}
+
 template <bool SP>
 cudaError_t launch_l4k(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated, cudaStream_t st) {
     if (p->info.dtype == FFTCONV_F16)

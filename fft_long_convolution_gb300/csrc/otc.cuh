@@ -13,6 +13,9 @@
 //   pass C  out[n0][n'] = sum_{k0} W_R^(n0 k0) W_M^(n' k0) T[k0][n'] / sqrt(R)
 //           MODE 2: all R outputs, in place; MODE 3: n0 < R/2 only (the
 //           causal truncation), y_z = conj(out) (times w_out)
+// FULL (circular convolution of length 2M): MODE 0 reads all R input rows
+// of z (no zero half) and MODE 3 writes all R output rows; u and y rows hold
+// 2M samples instead of M.
 //
 // One CTA of 128 threads walks tiles of 128 columns of one row; thread t
 // owns column t of the tile.  A tile's input rows are staged by one tiled
@@ -38,12 +41,12 @@
 
 namespace fftconv {
 
-template <int R, int MODE>
+template <int R, int MODE, bool FULL = false>
 struct Otc {
-    static_assert(R >= 4 && R <= 128 && MODE >= 0 && MODE <= 3, "outer pass shape");
+    static_assert(R >= (FULL ? 2 : 4) && R <= 128 && MODE >= 0 && MODE <= 3, "outer pass shape");
     static constexpr bool FWD = MODE <= 1;
-    static constexpr int NIN = MODE == 0 ? R / 2 : R;            // input rows
-    static constexpr int NOUT = MODE == 3 ? R / 2 : R;           // outputs kept
+    static constexpr int NIN = (MODE == 0 && !FULL) ? R / 2 : R;   // input rows
+    static constexpr int NOUT = (MODE == 3 && !FULL) ? R / 2 : R;  // outputs kept
     static constexpr int TC = 128, THREADS = 128;                // columns per tile = threads = the MMA's M
     static constexpr int KP = 2 * NIN < 16 ? 16 : 2 * NIN;       // K of the contraction (real), padded
     static constexpr int NP = (2 * NOUT + 15) / 16 * 16;         // N (output re/im), padded
@@ -60,21 +63,21 @@ struct Otc {
     static constexpr uint32_t TMEM_COLS = 2 * DCOLS < 32 ? 32 : 2 * DCOLS;  // double-buffered (allocation >= 32)
 };
 
-template <int R, int MODE, bool GATED>
+template <int R, int MODE, bool GATED, bool FULL = false>
 constexpr size_t otc_smem() {
-    using C = Otc<R, MODE>;
+    using C = Otc<R, MODE, FULL>;
     return size_t(C::ABYTES) + size_t(C::BBYTES) + size_t(C::NST) * C::STAGE_WORDS * 4 * ((GATED && MODE == 0) ? 2 : 1) +
            size_t(C::TC) * 8 + size_t(C::NST + 3) * 8 + 64;
 }
 
-// tin: the input rows (MODE 0: u as 32-bit words, [rows][R/2][L]; else T,
-// [rows][R][L]); tgate: w_in in u's shape (gated MODE 0).
-template <int DT, int R, int MODE, bool GATED, int L>
+// tin: the input rows (MODE 0: u as 32-bit words, [rows][R/2][L], FULL
+// [rows][R][L]; else T, [rows][R][L]); tgate: w_in in u's shape (gated MODE 0).
+template <int DT, int R, int MODE, bool GATED, int L, bool FULL = false>
 __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* __restrict__ fmat,
                                                 const __grid_constant__ CUtensorMap tin,
                                                 const __grid_constant__ CUtensorMap tgate) {
     using O = Op<DT>;
-    using C = Otc<R, MODE>;
+    using C = Otc<R, MODE, FULL>;
     static_assert(!(GATED && (MODE == 1 || MODE == 2)), "the inner stages have no gates");
     constexpr uint32_t M = uint32_t(R) * L;  // the twiddle modulus (the row length of this pass)
     constexpr int TILES = L / C::TC;
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
                     a.T[row * long(M) + long(L) * o + n1] = O::pack(x.r, x.i);
                 } else {
                     // y_z = conj(out): y[2n] = Re, y[2n+1] = -Im
-                    const long e = row * long(M) + 2 * (long(L) * o + n1);
+                    const long e = row * long(FULL ? 2 * M : M) + 2 * (long(L) * o + n1);
                     float re = x.r, im = -x.i;
                     if (GATED) {
                         const cpx g = O::unpack(__ldg(reinterpret_cast<const uint32_t*>(a.w_out + e)));

@@ -42,6 +42,7 @@ struct fftconv_plan_s {
     const uint16_t* plist = nullptr;            // [pairs_run]; null: every pair runs
     const unsigned long long* zbits = nullptr;  // [RA or 1][2] bit k0: sub-row k0 is dead; null: none
     int num_sms = 0;
+    bool circular = false;  // circular convolution of length 2 M (every input and output row of the outer passes)
     int device = 0;  // the device the plan's tables live on (current at creation)
     void* workspace = nullptr;
     size_t workspace_bytes = 0;
@@ -66,6 +67,10 @@ cudaError_t launch_mp_l4k_sparse(const fftconv_plan_s* p, const MPArgs& args, in
                                  cudaStream_t st);
 cudaError_t launch_mp_l4k_2level_sparse(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
                                         cudaStream_t st);
+// Circular convolution of length 2 M (p->circular): the outer passes over all
+// R0 input and output rows, R0 = 2 .. 128.
+cudaError_t launch_mp_l4k_circular(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, bool gated,
+                                   cudaStream_t st);
 
 // A value per device: kernel attribute opt-ins belong to the context of the
 // device that is current when they are made, so launch preparations are kept
@@ -134,17 +139,18 @@ inline bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t L, uint64
 }
 
 // One outer pass on the tensor cores: rows x (L / 128) column tiles over the
-// resident CTAs of the SM (their tensor-memory columns included).
-template <int DT, int R, int MODE, bool G, int L>
+// resident CTAs of the SM (their tensor-memory columns included).  FULL: the
+// circular form (rows of u and y of 2 R L samples, every input and output row).
+template <int DT, int R, int MODE, bool G, int L, bool FULL = false>
 cudaError_t launch_otc(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, const uint8_t* fmat,
                        cudaStream_t st) {
-    using C = Otc<R, MODE>;
-    auto fn = otc_pass<DT, R, MODE, G, L>;
+    using C = Otc<R, MODE, FULL>;
+    auto fn = otc_pass<DT, R, MODE, G, L, FULL>;
     // no more CTAs per SM than its 512 tensor-memory columns hold: the shared
     // memory request is raised until the SM's 228 KB (1 KB reserved per CTA)
     // fit no more of them
     constexpr int tmem_cap = int(512 / C::TMEM_COLS);
-    constexpr size_t smem_need = otc_smem<R, MODE, G>();
+    constexpr size_t smem_need = otc_smem<R, MODE, G, FULL>();
     constexpr size_t smem_floor = size_t(233472 / (tmem_cap + 1)) - 1024 + 16;
     constexpr size_t smem = smem_need > smem_floor ? smem_need : smem_floor;
     static_assert(smem <= 232448, "shared memory");
@@ -160,14 +166,16 @@ cudaError_t launch_otc(const fftconv_plan_s* p, const MPArgs& args, int64_t rows
     int64_t grid = int64_t(p->num_sms) * per_sm;
     if (grid > items) grid = items;
     if (grid < 1) return cudaSuccess;
-    // the input rows: u (MODE 0: R/2 sub-rows of a row of R L / 2 words) or T
-    // (R sub-rows of a row of R L words); w_in in u's shape
+    // the input rows: u (MODE 0: R/2 sub-rows of a row of R L / 2 words; FULL:
+    // R sub-rows of R L words) or T (R sub-rows of a row of R L words); w_in in
+    // u's shape
     CUtensorMap tin, tgate;
     std::memset(&tgate, 0, sizeof(tgate));
-    const bool ok = MODE == 0 ? encode_rows_map(&tin, args.u, L, R / 2, uint64_t(rows), uint64_t(2) * R * L)
+    constexpr uint64_t uin = FULL ? R : R / 2, urow = uint64_t(FULL ? 4 : 2) * R * L;
+    const bool ok = MODE == 0 ? encode_rows_map(&tin, args.u, L, uin, uint64_t(rows), urow)
                               : encode_rows_map(&tin, args.T, L, R, uint64_t(rows), uint64_t(4) * R * L);
     if (!ok) return cudaErrorInvalidValue;
-    if (G && MODE == 0 && !encode_rows_map(&tgate, args.w_in, L, R / 2, uint64_t(rows), uint64_t(2) * R * L))
+    if (G && MODE == 0 && !encode_rows_map(&tgate, args.w_in, L, uin, uint64_t(rows), urow))
         return cudaErrorInvalidValue;
     fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, fmat, tin, tgate);
     return cudaGetLastError();

@@ -156,7 +156,8 @@ fftconv_status_t fftconv_sparse_query(int64_t N, fftconv_dtype_t dtype, int orde
 /*
  * The plan's bands (band[0..order-1]; band[order..7] = 0; a dense plan
  * reports M_j/2 + 1 for every axis) and the pairs of sub-rows that run
- * (*pairs_run) out of *pairs_total, as fftconv_sparse_query reports them.  Any output pointer may be NULL.  Returns OK or INVALID.
+ * (*pairs_run) out of *pairs_total, as fftconv_sparse_query reports them.
+ * Any output pointer may be NULL.  Returns OK or INVALID.
  */
 fftconv_status_t fftconv_plan_get_band(fftconv_plan_t plan, int32_t *band, int32_t *pairs_run,
                                        int32_t *pairs_total);
@@ -369,6 +370,33 @@ size_t fftconv_circular_scratch_bytes(fftconv_plan_t plan, int64_t B, int64_t H,
 fftconv_status_t fftconv_forward_circular(fftconv_plan_t plan, const void *u, const void *w_in,
                                           const void *w_out, const void *k_f, void *y, int64_t B, int64_t H,
                                           void *scratch, size_t scratch_bytes, fftconv_stream_t stream);
+
+/*
+ * Native circular convolution of length C (FlashFFTConv page, section 5,
+ * "Convolution Micro-Benchmarks": the non-causal FFT convolution, the
+ * convolution theorem on C points without zero padding or truncation):
+ *   y[b,h,t] = sum_{j=0}^{C-1} u[b,h,j] k[h,(t-j) mod C]   (gated: w_out . conv(u . w_in, k))
+ * A circular plan transforms C real samples as M = C/2 complex points
+ * (z[n] = u[2n] + i u[2n+1]), factored R0 x 64 x 64 with R0 = C/8192: the
+ * first outer pass reads all R0 rows of z (no zero half) and the last one
+ * writes all R0 output rows; the 4096-point sub-rows, the fold with the
+ * kernel spectrum and the workspace are those of the multi-pass path.
+ * - fftconv_circular_query: host only; C a power of two, 16384 <= C <= 2^19;
+ *   info->N = C (samples per row), info->M = C/2.  Returns OK, INVALID
+ *   (info NULL) or UNSUPPORTED.
+ * - fftconv_plan_create_circular: the plan (device tables on the current
+ *   device).  On it, fftconv_kernel_fft and fftconv_kernel_fft_adjoint read
+ *   k as [H][C] (all C taps of the circular kernel) and write k_f of
+ *   fftconv_kf_bytes(plan, H) bytes; fftconv_forward and fftconv_forward_gated
+ *   take u, w_in, w_out, y as device [B][H][C] and need a workspace of
+ *   fftconv_workspace_bytes(plan, B, H) (= B H 2C) bytes
+ *   (fftconv_set_workspace); fftconv_backward_du(_gated) with the adjoint
+ *   k_f gives the input gradient (the circular correlation).  The partial,
+ *   windowed-circular and kernel-gradient calls return UNSUPPORTED.
+ *   Returns OK, INVALID, UNSUPPORTED, ALLOC or CUDA.
+ */
+fftconv_status_t fftconv_circular_query(int64_t C, fftconv_dtype_t dtype, fftconv_plan_info_t *info);
+fftconv_status_t fftconv_plan_create_circular(fftconv_plan_t *out, int64_t C, fftconv_dtype_t dtype);
 
 /*
  * Read and clear the plan's device error word (waits for `stream`).

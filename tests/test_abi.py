@@ -168,3 +168,26 @@ def test_product_path_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "oracle/" not in text and "liboracle" not in text, f
+
+
+@pytest.mark.parametrize("C", [16384, 32768, 65536, 131072, 262144, 524288])
+def test_circular_query_factorization(C):
+    """A circular plan of length C transforms M = C/2 points as R0 x 64 x 64
+    (R0 = C / 8192) on the multi-pass path; its rows hold C samples."""
+    for dt in (F.F16, F.BF16):
+        q = F.circular_query(C, dt)
+        R0 = C // 8192
+        assert q["N"] == C and q["M"] == C // 2
+        assert q["path"] == F.PATH_MULTIPASS and q["order"] == 3 and q["factors"] == [R0, 64, 64]
+        assert q["workspace_bytes_per_row"] == 2 * C
+        # the k_f of the causal plan with the same transform (pairs of 4096-point sub-rows)
+        if C // 2 >= 65536:
+            assert q["kf_bytes_per_channel"] == F.query(C // 2, dt)["kf_bytes_per_channel"]
+        assert q["kf_bytes_per_channel"] == (R0 // 2) * 17 * 4 * 2 * 32 * 16
+
+
+@pytest.mark.parametrize("C", [1024, 8192, 12288, 1 << 20, 0, -16384])
+def test_circular_query_rejects_unsupported_lengths(C):
+    with pytest.raises(F.FFTConvError) as e:
+        F.circular_query(C, F.F16)
+    assert e.value.status == 2
