@@ -511,6 +511,8 @@ def main():
     ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward", "circular"],
                     help="backward: input and kernel gradients (du + dk) per step; circular: the circular "
                          "convolution of length N (native plan, with the windowed 2N form timed beside it)")
+    ap.add_argument("--order", type=int, default=0,
+                    help="the plan's factorization order (0: the default per length; see fftconv_plan_query)")
     ap.add_argument("--batch", type=int, default=None,
                     help="run the workload with this batch size instead of its own (small cases for profiler "
                          "captures; the benchmark is quoted on the workload's own size)")
@@ -548,7 +550,7 @@ def main():
         return torch.from_numpy(r.bits.view(np.int16)).view(tdt).to(dev)
 
     band = parse_band(args.band)
-    plan = F.Plan(w.N, tdt, band=band)
+    plan = F.Plan(w.N, tdt, order=args.order, band=band)
     bd = plan.band()
     path = path_of(plan.info, bd["pairs_run"] if band is not None else None)
     k = dev_t(ins["k"])
@@ -649,7 +651,8 @@ def main():
             "warmup": max(args.warmup, 3), "ms_per_step": step_ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": {"fp16": "f16", "bf16": "bf16"}[w.dtype],
             "data": "synthetic (seeded SplitMix64 / Box-Muller, see workloads/)",
-            "config": config_of(w, band, plan.info["factors"]), "roofline": roof,
+            "config": dict(config_of(w, band, plan.info["factors"]), factors=plan.info["factors"],
+                           order=plan.info["order"]), "roofline": roof,
             "gpu_launches": args.steps * path["launches_per_step"],
             "e2e": {"value": e2e_value, "unit": "outputs/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
