@@ -551,7 +551,7 @@ cudaError_t launch_multipass(const fftconv_plan_s* p, const void* u, const void*
     MPArgs args{static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(wi),
                 static_cast<const uint16_t*>(wo), static_cast<const uint4*>(kf), static_cast<uint16_t*>(y),
                 static_cast<uint32_t*>(T), int(B), int(H), p->R0, p->mp, p->dev_err,
-                p->zbits, 1, p->pairs_run, p->plist};
+                p->zbits, 1, p->pairs_run, p->plist, p->zcbits};
     const bool gated = wi != nullptr;
     if (p->circular) return launch_mp_l4k_circular(p, args, B * H, gated, st);
     if (p->zbits) {  // frequency-sparse plan with pairs of sub-rows to skip
@@ -577,6 +577,7 @@ namespace {
 struct SparseTables {
     std::vector<uint16_t> plist;
     std::vector<unsigned long long> zbits;
+    unsigned long long zero[2] = {0ull, 0ull};  // bit k0 (one level): every bin of sub-row k0 is dropped
     bool any_skipped = false;
 };
 
@@ -600,6 +601,9 @@ SparseTables sparse_tables(const fftconv_plan_info_t& info, const int32_t* band,
         zero_sub[size_t(k0)] = z;
     }
     SparseTables t;
+    if (!two_level)
+        for (int k0 = 0; k0 < R0; ++k0)
+            if (zero_sub[size_t(k0)]) t.zero[k0 >> 6] |= 1ull << (k0 & 63);
     std::vector<char> dead(size_t(R0), 0);
     for (int pr = 0; pr < R0 / 2; ++pr) {
         const int a = pr, b = pr ? R0 - pr : R0 / 2;
@@ -697,7 +701,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
         o_ofull = append(blob, ofull);
     }
     SparseTables sp;
-    size_t o_plist = 0, o_zbits = 0;
+    size_t o_plist = 0, o_zbits = 0, o_zc = 0;
     p->pairs_run = multi ? p->R0 / 2 : (p->ftc ? ftc_pairs_run(info, p->band, p->sparse) : 0);
     if (multi && p->sparse) {
         sp = sparse_tables(info, p->band, p->R0, p->mp2);
@@ -706,6 +710,11 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
             if (sp.plist.empty()) sp.plist.push_back(0);  // nothing runs; keep the table non-empty
             o_plist = append(blob, sp.plist);
             o_zbits = append(blob, sp.zbits);
+            if (!p->mp2) {  // the last pass reads zeros for every sub-row whose bins are all dropped
+                p->zhost[0] = sp.zero[0];
+                p->zhost[1] = sp.zero[1];
+                o_zc = append(blob, std::vector<unsigned long long>{sp.zero[0], sp.zero[1]});
+            }
         }
     }
     blob.resize((blob.size() + 255) & ~size_t(255));
@@ -765,6 +774,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     if (sp.any_skipped) {
         p->plist = reinterpret_cast<const uint16_t*>(d + o_plist);
         p->zbits = reinterpret_cast<const unsigned long long*>(d + o_zbits);
+        if (o_zc) p->zcbits = reinterpret_cast<const unsigned long long*>(d + o_zc);
     }
     *out = p;
     return FFTCONV_OK;

@@ -11,35 +11,23 @@ namespace {
 
 template <int DT, int R0, bool G, bool SP>
 cudaError_t launch_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    constexpr int HALF = R0 / 2, L = kMpLtc;
-    const size_t smem_a = mp_pass_a_smem<R0, G>(), smem_c = mp_pass_c_smem<R0, G>();
-    static PerDevice ca, cb, cc;
-    int na = 0, nb = 0, nc = 0;
+    constexpr int L = kMpLtc;
+    static PerDevice cb;
+    int nb = 0;
     cudaError_t e;
-    if ((e = prep_kernel(mp_pass_a<DT, R0, G, L, false, SP>, smem_a, 256, ca, &na)) != cudaSuccess) return e;
     if ((e = prep_kernel(mp_pass_b_tc<DT, SP>, TcB::SMEM, TcB::THREADS, cb, &nb)) != cudaSuccess) return e;
-    if ((e = prep_kernel(mp_pass_c<DT, R0, G, L, true, false, SP>, smem_c, 32 * mp_pass_c_warps<R0>(), cc, &nc)) != cudaSuccess) return e;
-    const int64_t items_ac = rows * (L / mp_tile<R0>());
-    auto grid = [&](int64_t items, int per_sm) {
-        int64_t gsz = int64_t(p->num_sms) * per_sm;
-        return unsigned(gsz < items ? gsz : items);
-    };
     // pass B: one CTA per SM (its tensor-memory allocation takes all 512
     // columns), two item pipelines per CTA
     const int64_t items_b = rows * p->pairs_run, need_b = (items_b + 1) / 2;
     if (items_b >= (int64_t(1) << 30)) return cudaErrorInvalidValue;  // pass B counts items in int
     const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);
     TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, 0, p->pairs_run, p->plist};
-    if constexpr (!SP) {  // dense: the outer passes on the tensor cores
-        if ((e = launch_otc<DT, R0, 0, G, L>(p, args, rows, p->otc_fa, st)) != cudaSuccess) return e;
-        if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        return launch_otc<DT, R0, 3, G, L>(p, args, rows, p->otc_fc, st);
-    }
-    mp_pass_a<DT, R0, G, L, false, SP><<<grid(items_ac, na), 256, smem_a, st>>>(args);
+    // the outer passes on the tensor cores; frequency-sparse plans (SP) skip
+    // the dead sub-rows there (not stored by pass A, not loaded by pass C)
+    if ((e = launch_otc<DT, R0, 0, G, L, false, SP>(p, args, rows, p->otc_fa, st)) != cudaSuccess) return e;
     if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
-    mp_pass_c<DT, R0, G, L, true, false, SP><<<grid(items_ac, nc), 32 * mp_pass_c_warps<R0>(), smem_c, st>>>(args);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_otc<DT, R0, 3, G, L, false, SP>(p, args, rows, p->otc_fc, st);
 }
 
 template <int DT, bool G, bool SP>

@@ -59,6 +59,9 @@ struct MPArgs {
     int zmod = 1;
     int np = 0;                                 // pass-B pairs that run (R0 / 2 when plist is null)
     const uint16_t* plist = nullptr;
+    // one-level frequency-sparse plans: sub-rows whose bins are all dropped
+    // (bit k0 of [2]); the tensor-core last pass reads them as zeros
+    const unsigned long long* zcbits = nullptr;
 };
 
 // Bit k0 (< 128) of a dead-sub-row pair of words.

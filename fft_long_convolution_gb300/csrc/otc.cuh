@@ -16,6 +16,12 @@
 // FULL (circular convolution of length 2M): MODE 0 reads all R input rows
 // of z (no zero half) and MODE 3 writes all R output rows; u and y rows hold
 // 2M samples instead of M.
+// SP (frequency-sparse plans, one-level outer factor): sub-rows k0 whose
+// pass-B pair is skipped (bit k0 of a.zbits[0..1]) are not stored by MODE 0;
+// MODE 3 reads as zeros every sub-row whose bins are all dropped (bit k0 of
+// a.zcbits[0..1]: pass B leaves exact zeros there, or nothing for a skipped
+// pair) and copies only the runs of the others (otc_live_runs) when there
+// are at most two of them.
 //
 // One CTA of 128 threads walks tiles of 128 columns of one row; thread t
 // owns column t of the tile.  A tile's input rows are staged by one tiled
@@ -63,6 +69,37 @@ struct Otc {
     static constexpr uint32_t TMEM_COLS = 2 * DCOLS < 32 ? 32 : 2 * DCOLS;  // double-buffered (allocation >= 32)
 };
 
+// The live sub-rows of a frequency-sparse plan as at most two runs of
+// consecutive rows, each copied as one box of `box` rows starting at
+// start[i] (start[i] + box <= R; a box may cover dead rows, which are read
+// as zeros).  n = 0: more than two runs, or boxes that would overlap: copy
+// all R rows.  The host encodes the tensor map's box height with the same
+// function.
+struct OtcRuns {
+    int n, box, start[2];
+};
+__host__ __device__ inline OtcRuns otc_live_runs(unsigned long long z0, unsigned long long z1, int R) {
+    OtcRuns r{0, 0, {0, 0}};
+    int len[2] = {0, 0}, runs = 0;
+    bool prev = false;
+    for (int k = 0; k < R; ++k) {
+        const bool live = ((k < 64 ? z0 >> k : z1 >> (k - 64)) & 1ull) == 0;
+        if (live && !prev) {
+            if (runs == 2) return OtcRuns{0, R, {0, 0}};
+            r.start[runs++] = k;
+        }
+        if (live) ++len[runs - 1];
+        prev = live;
+    }
+    if (runs == 0) return OtcRuns{0, 0, {0, 0}};  // nothing live: nothing to copy
+    r.n = runs;
+    r.box = len[0] > len[1] ? len[0] : len[1];
+    for (int i = 0; i < runs; ++i)
+        if (r.start[i] + r.box > R) r.start[i] = R - r.box;
+    if (runs == 2 && r.start[0] + r.box > r.start[1]) return OtcRuns{0, R, {0, 0}};
+    return r;
+}
+
 template <int R, int MODE, bool GATED, bool FULL = false>
 constexpr size_t otc_smem() {
     using C = Otc<R, MODE, FULL>;
@@ -72,12 +109,13 @@ constexpr size_t otc_smem() {
 
 // tin: the input rows (MODE 0: u as 32-bit words, [rows][R/2][L], FULL
 // [rows][R][L]; else T, [rows][R][L]); tgate: w_in in u's shape (gated MODE 0).
-template <int DT, int R, int MODE, bool GATED, int L, bool FULL = false>
+template <int DT, int R, int MODE, bool GATED, int L, bool FULL = false, bool SP = false>
 __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* __restrict__ fmat,
                                                 const __grid_constant__ CUtensorMap tin,
                                                 const __grid_constant__ CUtensorMap tgate) {
     using O = Op<DT>;
     using C = Otc<R, MODE, FULL>;
+    static_assert(!SP || ((MODE == 0 || MODE == 3) && !FULL), "sparse outer passes: one level, causal");
     static_assert(!(GATED && (MODE == 1 || MODE == 2)), "the inner stages have no gates");
     constexpr uint32_t M = uint32_t(R) * L;  // the twiddle modulus (the row length of this pass)
     constexpr int TILES = L / C::TC;
@@ -98,6 +136,27 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
     uint64_t* fbar = mbar + 2;                                   // DFT matrix arrived
 
     const int t = threadIdx.x, wq = t >> 5;
+    // SP: the dead sub-rows (every row of the plan shares them)
+    const unsigned long long* zb = MODE == 3 ? a.zcbits : a.zbits;
+    const unsigned long long z0 = (SP && zb) ? __ldg(zb) : 0ull;
+    const unsigned long long z1 = (SP && zb) ? __ldg(zb + 1) : 0ull;
+    uint32_t live_bytes = C::STAGE_WORDS * 4u;  // bytes one tile's staging receives
+    OtcRuns runs{0, C::NIN, {0, 0}};
+    uint32_t gmask = ~0u;  // SP pass C: groups of four input rows with a live row (the others stay zero in A)
+    unsigned long long omask = ~0ull;  // SP pass A: chunks of outputs (CH/2 sub-rows) with a live sub-row
+    if constexpr (SP && MODE == 0) {
+        constexpr int OPC = (C::NP < 32 ? C::NP : 32) / 2;  // outputs per epilogue chunk
+        omask = 0ull;
+        for (int o = 0; o < C::NOUT; ++o)
+            if (!zbit(z0, z1, o)) omask |= 1ull << (o / OPC);
+    }
+    if constexpr (SP && MODE == 3) {
+        runs = otc_live_runs(z0, z1, C::NIN);
+        live_bytes = uint32_t(runs.n ? runs.n * runs.box : runs.box) * C::SEG * 4u;
+        gmask = 0u;
+        for (int n0 = 0; n0 < C::NIN; ++n0)
+            if (!zbit(z0, z1, n0)) gmask |= 1u << (n0 >> 2);
+    }
     const long rows = long(a.B) * a.H;
     const long items = rows * TILES;
     const long first_item = blockIdx.x, stride = gridDim.x;
@@ -105,8 +164,15 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
     auto stage = [&](long item, int s) {  // the tile's input rows into staging slot s
         const int row = int(item / TILES);
         const int o_base = int(item % TILES) * C::TC;
-        mbar_expect_tx(&full[s], C::STAGE_WORDS * 4u * ((GATED && MODE == 0) ? 2u : 1u));
-        tma_load_3d(st + s * C::STAGE_WORDS, &tin, o_base, 0, row, &full[s]);
+        mbar_expect_tx(&full[s], live_bytes * ((GATED && MODE == 0) ? 2u : 1u));
+        if constexpr (SP && MODE == 3) {  // the runs of live rows (or all rows; none if nothing is live)
+            if (runs.n == 0 && runs.box > 0) tma_load_3d(st + s * C::STAGE_WORDS, &tin, o_base, 0, row, &full[s]);
+            for (int i = 0; i < runs.n; ++i)
+                tma_load_3d(st + s * C::STAGE_WORDS + runs.start[i] * C::SEG, &tin, o_base, runs.start[i], row,
+                            &full[s]);
+        } else {
+            tma_load_3d(st + s * C::STAGE_WORDS, &tin, o_base, 0, row, &full[s]);
+        }
         if (GATED && MODE == 0) tma_load_3d(sw + s * C::STAGE_WORDS, &tgate, o_base, 0, row, &full[s]);
     };
 
@@ -151,8 +217,18 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
         const cpx w1 = cmul({pt.x, pt.y}, {qt.x, qt.y});  // W_M^(n1)
         cpx tw = {1.f, 0.f};                                // W_M^(n1 k0), k0 = 0, 1, ...
         constexpr int CH = C::NP < 32 ? C::NP : 32;         // accumulator columns per load
+        cpx wch = {1.f, 0.f};                               // SP pass A: W_M^(n1 CH/2), one chunk of outputs
+        if constexpr (SP && MODE == 0) {
+            wch = w1;
+            #pragma unroll
+            for (int e = 1; e < CH / 2; e <<= 1) wch = cmul(wch, wch);
+        }
         #pragma unroll 1
         for (int c0 = 0; c0 < 2 * C::NOUT; c0 += CH) {
+            if (SP && MODE == 0 && !((omask >> (c0 / CH)) & 1ull)) {  // a chunk of dead outputs: not stored
+                tw = cmul(tw, wch);
+                continue;
+            }
             uint32_t vv[32];
             const uint32_t taddr = tmem + (uint32_t(32 * wq) << 16) + d * C::DCOLS + c0;
             if constexpr (CH == 16)
@@ -170,6 +246,7 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
                     tw = cmul(tw, w1);
                 }
                 if constexpr (MODE <= 2) {
+                    if (SP && zbit(z0, z1, o)) continue;  // a skipped pair's sub-row: never read
                     a.T[row * long(M) + long(L) * o + n1] = O::pack(x.r, x.i);
                 } else {
                     // y_z = conj(out): y[2n] = Re, y[2n+1] = -Im
@@ -217,26 +294,35 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
         {
             const uint32_t* sts = st + s * C::STAGE_WORDS + t;
             const uint32_t* sws = sw + s * C::STAGE_WORDS + t;
-            cpx tw = {1.f, 0.f}, w1 = {1.f, 0.f};  // pass C: W_M^(n' k0) along k0
+            cpx tw = {1.f, 0.f}, w1 = {1.f, 0.f}, w4 = {1.f, 0.f};  // pass C: W_M^(n' k0) along k0
             if constexpr (!C::FWD) {
                 const float2 pt = s_pt[ps];
                 w1 = cmul({pt.x, pt.y}, {qt.x, qt.y});
+                if constexpr (SP) w4 = cmul(cmul(w1, w1), cmul(w1, w1));
             }
+            static_assert(C::NG <= 32, "group mask");
             #pragma unroll 4
             for (int g = 0; g < C::NG; ++g) {
+                if (SP && MODE == 3 && !((gmask >> g) & 1u)) {  // four dead rows: A keeps its zeros
+                    if constexpr (!C::FWD) tw = cmul(tw, w4);
+                    continue;
+                }
                 uint32_t v[4];
                 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int n0 = 4 * g + i;
                     uint32_t x = 0u;
                     if (n0 < C::NIN) {
-                        x = sts[n0 * C::SEG];
-                        if (GATED && MODE == 0) x = O::mul2(x, sws[n0 * C::SEG]);
-                        if constexpr (!C::FWD) {
-                            const cpx xv = cmul(O::unpack(x), tw);
-                            x = O::pack(xv.r, xv.i);
-                            tw = cmul(tw, w1);
+                        // SP, pass C: a skipped pair's sub-row was never written and reads as zero
+                        if (!(SP && MODE == 3 && zbit(z0, z1, n0))) {
+                            x = sts[n0 * C::SEG];
+                            if (GATED && MODE == 0) x = O::mul2(x, sws[n0 * C::SEG]);
+                            if constexpr (!C::FWD) {
+                                const cpx xv = cmul(O::unpack(x), tw);
+                                x = O::pack(xv.r, xv.i);
+                            }
                         }
+                        if constexpr (!C::FWD) tw = cmul(tw, w1);
                     }
                     v[i] = x;
                 }

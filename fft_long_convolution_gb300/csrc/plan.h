@@ -41,6 +41,11 @@ struct fftconv_plan_s {
     int pairs_run = 0;                          // = R0 / 2 when nothing is skipped
     const uint16_t* plist = nullptr;            // [pairs_run]; null: every pair runs
     const unsigned long long* zbits = nullptr;  // [RA or 1][2] bit k0: sub-row k0 is dead; null: none
+    // one-level plans: the sub-rows whose bins are all dropped (a superset of
+    // the skipped pairs' sub-rows, whose pass-B output is exactly zero), read
+    // as zeros by the last pass: device copy and host copy
+    const unsigned long long* zcbits = nullptr;
+    unsigned long long zhost[2] = {0ull, 0ull};
     int num_sms = 0;
     bool circular = false;  // circular convolution of length 2 M (every input and output row of the outer passes)
     int device = 0;  // the device the plan's tables live on (current at creation)
@@ -124,14 +129,15 @@ inline TensorMapEncoder tensor_map_encoder() {
 }
 
 // A tensor map over rows of `nin` sub-rows of L 32-bit words (row stride
-// row_bytes), read as boxes of 128 words x nin sub-rows x 1 row.
+// row_bytes), read as boxes of 128 words x box_rows sub-rows (default: all
+// nin) x 1 row.
 inline bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t L, uint64_t nin, uint64_t rows,
-                            uint64_t row_bytes) {
+                            uint64_t row_bytes, uint32_t box_rows = 0) {
     TensorMapEncoder enc = tensor_map_encoder();
     if (!enc || !base) return false;
     const cuuint64_t dims[3] = {L, nin, rows};
     const cuuint64_t strides[2] = {4 * L, row_bytes};
-    const cuuint32_t box[3] = {128, cuuint32_t(nin), 1};
+    const cuuint32_t box[3] = {128, box_rows ? box_rows : cuuint32_t(nin), 1};
     const cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -141,11 +147,11 @@ inline bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t L, uint64
 // One outer pass on the tensor cores: rows x (L / 128) column tiles over the
 // resident CTAs of the SM (their tensor-memory columns included).  FULL: the
 // circular form (rows of u and y of 2 R L samples, every input and output row).
-template <int DT, int R, int MODE, bool G, int L, bool FULL = false>
+template <int DT, int R, int MODE, bool G, int L, bool FULL = false, bool SP = false>
 cudaError_t launch_otc(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, const uint8_t* fmat,
                        cudaStream_t st) {
     using C = Otc<R, MODE, FULL>;
-    auto fn = otc_pass<DT, R, MODE, G, L, FULL>;
+    auto fn = otc_pass<DT, R, MODE, G, L, FULL, SP>;
     // no more CTAs per SM than its 512 tensor-memory columns hold: the shared
     // memory request is raised until the SM's 228 KB (1 KB reserved per CTA)
     // fit no more of them
@@ -172,8 +178,14 @@ cudaError_t launch_otc(const fftconv_plan_s* p, const MPArgs& args, int64_t rows
     CUtensorMap tin, tgate;
     std::memset(&tgate, 0, sizeof(tgate));
     constexpr uint64_t uin = FULL ? R : R / 2, urow = uint64_t(FULL ? 4 : 2) * R * L;
+    // SP pass C copies the runs of live sub-rows (boxes of the longest run's height)
+    uint32_t box = 0;
+    if (SP && MODE == 3) {
+        const OtcRuns r = otc_live_runs(p->zhost[0], p->zhost[1], R);
+        box = uint32_t(r.box > 0 ? r.box : R);
+    }
     const bool ok = MODE == 0 ? encode_rows_map(&tin, args.u, L, uin, uint64_t(rows), urow)
-                              : encode_rows_map(&tin, args.T, L, R, uint64_t(rows), uint64_t(4) * R * L);
+                              : encode_rows_map(&tin, args.T, L, R, uint64_t(rows), uint64_t(4) * R * L, box);
     if (!ok) return cudaErrorInvalidValue;
     if (G && MODE == 0 && !encode_rows_map(&tgate, args.w_in, L, uin, uint64_t(rows), urow))
         return cudaErrorInvalidValue;
