@@ -64,7 +64,10 @@ struct Otc {
     static constexpr uint32_t BBYTES = uint32_t(NP / 8) * SBO;     // the DFT matrix
     static constexpr int SEG = TC;                               // staged row segment (words)
     static constexpr uint32_t STAGE_WORDS = uint32_t(NIN) * SEG;
-    static constexpr int NST = NIN <= 16 ? 4 : (NIN <= 32 ? 2 : 1);  // staged tiles in flight
+    // staged tiles in flight; the last pass at R = 64 keeps two stages of
+    // 32 KB (its DFT matrix has only NOUT = 32 outputs, so two CTAs per SM
+    // still fit, as its tensor memory allows)
+    static constexpr int NST = NIN <= 16 ? 4 : (NIN <= 32 ? 2 : ((MODE == 3 && !FULL && R == 64) ? 2 : 1));
     static constexpr uint32_t DCOLS = NP;                            // tensor-memory columns per accumulator
     static constexpr uint32_t TMEM_COLS = 2 * DCOLS < 32 ? 32 : 2 * DCOLS;  // double-buffered (allocation >= 32)
 };
@@ -104,7 +107,7 @@ template <int R, int MODE, bool GATED, bool FULL = false>
 constexpr size_t otc_smem() {
     using C = Otc<R, MODE, FULL>;
     return size_t(C::ABYTES) + size_t(C::BBYTES) + size_t(C::NST) * C::STAGE_WORDS * 4 * ((GATED && MODE == 0) ? 2 : 1) +
-           size_t(C::TC) * 8 + size_t(C::NST + 3) * 8 + 64;
+           size_t(C::NST + 3) * 8 + 3 * 8 + 8;
 }
 
 // tin: the input rows (MODE 0: u as 32-bit words, [rows][R/2][L], FULL
@@ -119,21 +122,23 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
     static_assert(!(GATED && (MODE == 1 || MODE == 2)), "the inner stages have no gates");
     constexpr uint32_t M = uint32_t(R) * L;  // the twiddle modulus (the row length of this pass)
     constexpr int TILES = L / C::TC;
+    // all shared state is dynamic (no static shared memory, so the dynamic
+    // region starts at the CTA's base without an alignment gap and two CTAs
+    // of the R = 64 last pass fit an SM)
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint32_t s_tmem;
-    // W_M^(o_base) of a tile, by local tile index mod 3: tile i's value is read
-    // in its own reformat and epilogue (the next iteration), and rewritten
-    // by tile i + 3 only after every thread has passed tile i + 1's barrier
-    __shared__ float2 s_pt[3];
 
     uint8_t* sa = smem;                                          // data tile (A operand)
     uint8_t* sf = sa + C::ABYTES;                                // DFT matrix (B operand)
     uint32_t* st = reinterpret_cast<uint32_t*>(sf + C::BBYTES);  // [NST][NIN][SEG]
     uint32_t* sw = st + C::NST * C::STAGE_WORDS;                 // gated pass A: w_in, same shape
-    float2* qtab = reinterpret_cast<float2*>(sw + ((GATED && MODE == 0) ? C::NST * C::STAGE_WORDS : 0));  // W_M^c, c < TC
-    uint64_t* full = reinterpret_cast<uint64_t*>(qtab + C::TC);  // [NST] staged tile arrived
+    uint64_t* full = reinterpret_cast<uint64_t*>(sw + ((GATED && MODE == 0) ? C::NST * C::STAGE_WORDS : 0));  // [NST] staged tile arrived
     uint64_t* mbar = full + C::NST;                              // [2] contraction done, per accumulator
     uint64_t* fbar = mbar + 2;                                   // DFT matrix arrived
+    // W_M^(o_base) of a tile, by local tile index mod 3: tile i's value is read
+    // in its own reformat and epilogue (the next iteration), and rewritten
+    // by tile i + 3 only after every thread has passed tile i + 1's barrier
+    float2* s_pt = reinterpret_cast<float2*>(fbar + 1);
+    uint32_t& s_tmem = *reinterpret_cast<uint32_t*>(s_pt + 3);
 
     const int t = threadIdx.x, wq = t >> 5;
     // SP: the dead sub-rows (every row of the plan shares them)
@@ -194,17 +199,17 @@ __global__ void __launch_bounds__(128) otc_pass(const MPArgs a, const uint8_t* _
     if (wq == 0) tc::alloc(&s_tmem, C::TMEM_COLS);
     for (uint32_t i = t; i < C::ABYTES / 16; i += blockDim.x)  // K padding stays zero
         reinterpret_cast<uint4*>(sa)[i] = make_uint4(0, 0, 0, 0);
-    {
-        const cpx v = twiddle_pow2(uint32_t(t) & (M - 1), M);
-        qtab[t] = make_float2(v.r, v.i);
-    }
     tc::fence_proxy_async();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = s_tmem;
     bool failed = __syncthreads_or(!mbar_wait_bounded(fbar, 0, kWaitLimit));
-    const float2 qt = qtab[t];
+    float2 qt;  // W_M^t, this thread's column within a tile
+    {
+        const cpx v = twiddle_pow2(uint32_t(t) & (M - 1), M);
+        qt = make_float2(v.r, v.i);
+    }
     // this thread's row of the A operand (column t of the tile)
     uint8_t* arow = sa + (t >> 3) * C::SBO + (t & 7) * 16;
 
