@@ -467,6 +467,15 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                 }
             }
         }
+        // the fold's k_f of chunks 0..3, read from L2 while the vote, S2 and its
+        // wait run (chunks 4..7 follow during the fold's first half)
+        const uint4* kft = kf_of(h, p) + (sp ? 9 : 8) * hf * 256 + w * 64 + lane;
+        uint4 kv[2][4][2];
+        #pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            kv[0][jj][0] = __ldg(kft + jj * 256);
+            kv[0][jj][1] = __ldg(kft + jj * 256 + 32);
+        }
         tc::fence_proxy_async();
         tc::fence_before();
         if (tc::bar_vote(bar_id, 256, bad)) { failed = true; break; }
@@ -482,13 +491,6 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         mma_pending = true;
 
         // ---------------- fold of this warpgroup's sub-row with the kernel spectrum -> B3
-        const uint4* kft = kf_of(h, p) + (sp ? 9 : 8) * hf * 256 + w * 64 + lane;
-        uint4 kv[2][4][2];
-        #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {  // chunks 0..3, read while the contraction runs
-            kv[0][jj][0] = __ldg(kft + jj * 256);
-            kv[0][jj][1] = __ldg(kft + jj * 256 + 32);
-        }
         bad = !mbar_wait_sleep(&bars[0], mmapar, kWaitSleepLimit, kWaitHintNs);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();

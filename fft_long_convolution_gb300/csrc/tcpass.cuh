@@ -309,6 +309,15 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
                 }
             }
         }
+        // the fold's k_f of chunks 0..3 ([c][w][half][lane], this warpgroup's
+        // first chunk), read from L2 while the vote, S2 and its wait run
+        const uint4* kft = a.kf + (size_t(x.h) * pairs + x.p) * C::KFP + (sp ? 9 : 8) * hf * 256 + w * 64 + lane;
+        uint4 kv[2][4][2];
+        #pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            kv[0][jj][0] = __ldg(kft + jj * 256);
+            kv[0][jj][1] = __ldg(kft + jj * 256 + 32);
+        }
         tc::fence_proxy_async();
         tc::fence_before();
         if (tc::bar_vote(bar_id, 256, bad)) { failed = true; break; }
@@ -324,14 +333,6 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
         mma_pending = true;
 
         // ---------------- fold of this warpgroup's columns with the kernel spectrum -> B3
-        // chunk c of the item's k_f: [c][w][half][lane]; this warpgroup's first chunk
-        const uint4* kft = a.kf + (size_t(x.h) * pairs + x.p) * C::KFP + (sp ? 9 : 8) * hf * 256 + w * 64 + lane;
-        uint4 kv[2][4][2];
-        #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {  // chunks 0..3, read while the contraction runs
-            kv[0][jj][0] = __ldg(kft + jj * 256);
-            kv[0][jj][1] = __ldg(kft + jj * 256 + 32);
-        }
         bad = !mbar_wait_sleep(&bars[0], mmapar, kWaitSleepLimit, kWaitHintNs);
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();

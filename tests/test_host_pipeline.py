@@ -52,6 +52,28 @@ def test_host_matches_device(N, dtype, gated, B, H, order):
     assert plan.device_status() == 0
 
 
+@pytest.mark.parametrize("C,dtype,gated,B,H", [
+    (32768, "fp16", True, 3, 4),      # circular plan, chunks of batch entries
+    (65536, "bf16", False, 1, 6),     # circular plan, B = 1: chunks of channels
+])
+def test_host_matches_device_circular(C, dtype, gated, B, H):
+    """The host-buffer call on a circular plan (rows of C samples)."""
+    w = W.Workload("t", B, H, C, dtype, gated, "normal", "decay", "")
+    ins = W.make_inputs(w, seed=23)
+    tdt = torch_dtype(dtype)
+    plan = F.Plan(C, tdt, circular=True)
+    kf = plan.kernel_fft(to_dev(ins["k"]))
+    if gated:
+        y_dev = plan.forward_gated(to_dev(ins["u"]), to_dev(ins["w_in"]), to_dev(ins["w_out"]), kf)
+        y_host = plan.forward_host(_host(ins["u"], tdt), kf, _host(ins["w_in"], tdt), _host(ins["w_out"], tdt))
+    else:
+        y_dev = plan.forward(to_dev(ins["u"]), kf)
+        y_host = plan.forward_host(_host(ins["u"], tdt), kf)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+    assert plan.device_status() == 0
+
+
 def test_host_pageable_memory_and_oracle():
     """Pageable host memory serialises the copies but gives the same rows."""
     w = W.Workload("t", 4, 6, 4096, "bf16", False, "normal", "decay", "")

@@ -62,6 +62,21 @@ def test_noalloc_matches_forward_bitwise_on_two_calls(N, dtype):
     assert plan.device_status() == 0
 
 
+def test_noalloc_circular_plan_matches_forward_bitwise():
+    """A circular plan's rows (C samples, the multi-pass intermediate of C/2
+    complex points) through the fixed array."""
+    C, B, H = 65536, 2, 3
+    ins = _inputs(C, "bf16", B, H, seed=24)
+    plan = F.Plan(C, torch.bfloat16, circular=True)
+    kf = plan.kernel_fft(to_dev(ins["k"]))
+    u = to_dev(ins["u"])
+    ref = plan.forward(u, kf)
+    torch.cuda.synchronize()
+    y = _noalloc(plan, u, kf, B, H)
+    assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+    assert plan.device_status() == 0
+
+
 def test_noalloc_rejects_calls_beyond_the_scratch_size():
     N = 2097152
     plan = F.Plan(N, torch.bfloat16)
