@@ -152,16 +152,21 @@ __device__ __forceinline__ float2 dk_cross(float ar, float ai, float cr, float c
 // 2t + 1: that pass runs in registers.  It owns bins t + 512 e of the batch
 // sum.  Shared memory: two transform buffers of 2048 float4, the batch sum S
 // of both sub-rows and the radix-4 twiddles (101.5 KB, two CTAs per SM).
-template <int DT, int L1, bool G>
+//
+// FA (2N = 128K .. 1M): the column transforms come precomputed and twiddled
+// from dk_colfft_fwd in A[row][k1][n2] (float32), so the CTA loads its two
+// sub-rows instead of forming column sums (u, dy and the gates are unused).
+template <int DT, int L1, bool G, bool FA = false>
 __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __restrict__ u,
                                                             const uint16_t* __restrict__ dy,
                                                             const uint16_t* __restrict__ w_in,
                                                             const uint16_t* __restrict__ w_out,
-                                                            float2* __restrict__ R, int64_t B, int64_t H) {
+                                                            float2* __restrict__ R, int64_t B, int64_t H,
+                                                            const float2* __restrict__ A) {
     using O = Op<DT>;
     constexpr int L2 = kDkL2, T = kDkRowThreads, NE = L2 / T;  // 4 bins per thread per sub-row
     constexpr int NH = L1 / 2, CH = G ? 2 : 4;                 // input rows n1; rows loaded per round
-    static_assert(NE == 4 && NH % CH == 0, "2048-point sub-rows, 512 threads");
+    static_assert(NE == 4 && (FA || NH % CH == 0), "2048-point sub-rows, 512 threads");
     constexpr int64_t N = int64_t(L2) * NH;
     constexpr uint32_t L = uint32_t(L1) * uint32_t(L2);
     extern __shared__ __align__(16) float4 dsm4[];
@@ -185,17 +190,32 @@ __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __re
         const int p = int(it - h * NH);
         const int kA = p, kB = p ? L1 - p : NH;
         // W_L^(n2 k1) of this thread's columns n2 = 2t + 1024 gc + c, both sub-rows
+        // (FA: already applied to A)
         float2 ctw[4][2];
         #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const uint32_t n2 = uint32_t(2 * t + 1024 * (c >> 1) + (c & 1));
-            ctw[c][0] = dk_twiddle(n2 * uint32_t(kA), L);
-            ctw[c][1] = dk_twiddle(n2 * uint32_t(kB), L);
+            ctw[c][0] = FA ? make_float2(1.f, 0.f) : dk_twiddle(n2 * uint32_t(kA), L);
+            ctw[c][1] = FA ? make_float2(1.f, 0.f) : dk_twiddle(n2 * uint32_t(kB), L);
         }
         const float2 wst = dk_twiddle(uint32_t(kA), uint32_t(L1));  // W_L1^kA
         #pragma unroll
         for (int e = 0; e < 2 * NE; ++e) acc[t + T * e] = make_float2(0.f, 0.f);
         for (int64_t b = 0; b < B; ++b) {
+          float2 sa[4], sb[4];  // column c = 2 gc + e of this thread, sub-rows A and B
+          if constexpr (FA) {
+            const float2* ra = A + ((b * H + h) * L1 + kA) * int64_t(L2) + 2 * t;
+            const float2* rb = A + ((b * H + h) * L1 + kB) * int64_t(L2) + 2 * t;
+            #pragma unroll
+            for (int gc = 0; gc < 2; ++gc) {
+                const float4 va = __ldg(reinterpret_cast<const float4*>(ra + 1024 * gc));
+                const float4 vb = __ldg(reinterpret_cast<const float4*>(rb + 1024 * gc));
+                sa[2 * gc] = make_float2(va.x, va.y);
+                sa[2 * gc + 1] = make_float2(va.z, va.w);
+                sb[2 * gc] = make_float2(vb.x, vb.y);
+                sb[2 * gc + 1] = make_float2(vb.z, vb.w);
+            }
+          } else {
             const int64_t roff = (b * H + h) * N + 2 * t;
             // A_k1[n2] = W_L^(n2 k1) sum_{n1 < L1/2} z[L2 n1 + n2] W_L1^(n1 k1), with
             // W_L1^(n1 kB) = conj W_L1^(n1 kA) (kB = L1 - kA) or, on pair 0,
@@ -248,7 +268,6 @@ __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __re
                     w = dk_cmul(w, wst);
                 }
             }
-            float2 sa[4], sb[4];  // column c = 2 gc + e
             #pragma unroll
             for (int gc = 0; gc < 2; ++gc) {
                 const float2 ar = dk_upk(are[gc]), ai = dk_upk(aim[gc]), br = dk_upk(bre[gc]), bi = dk_upk(bim[gc]);
@@ -257,6 +276,7 @@ __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __re
                 sb[2 * gc] = make_float2(br.x, bi.x);
                 sb[2 * gc + 1] = make_float2(br.y, bi.y);
             }
+          }
             // the radix-2 pass: butterfly j = 2t + e takes columns j and j + 1024
             #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -323,6 +343,127 @@ __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __re
             R[(h * L1 + kB) * L2 + n2] = dk_cmul(make_float2(v.y, v.w), dk_twiddle(uint32_t(kB) * uint32_t(n2), L));
         }
         __syncthreads();  // the buffers are reused by the next item
+    }
+}
+
+// 2N = 128K .. 1M: the column passes of the four-step form run as batched
+// L1-point transforms in shared memory, L1 = L / 2048 = 64 .. 512, on tiles
+// of kDkColTC consecutive columns (element (n1, c) at n1 * TC + c); Stockham
+// radix-4 passes (one radix-2 pass first for odd log2 L1) between two
+// buffers.  Returns the buffer holding the result.
+constexpr int kDkColTC = 16, kDkColThreads = 256;
+
+__device__ float2* dk_colfft(float2* a, float2* b, int lgL1) {
+    constexpr int TC = kDkColTC;
+    const int L1 = 1 << lgL1;
+    int lgNs = 0;
+    if (lgL1 & 1) {
+        for (int j = threadIdx.x; j < (L1 / 2) * TC; j += blockDim.x) {
+            const int c = j % TC, jj = j / TC;
+            const float2 c0 = a[jj * TC + c], c1 = a[(jj + L1 / 2) * TC + c];
+            b[(2 * jj) * TC + c] = make_float2(c0.x + c1.x, c0.y + c1.y);
+            b[(2 * jj + 1) * TC + c] = make_float2(c0.x - c1.x, c0.y - c1.y);
+        }
+        __syncthreads();
+        float2* x = a; a = b; b = x;
+        lgNs = 1;
+    }
+    for (; lgNs < lgL1; lgNs += 2) {
+        const int Ns = 1 << lgNs, Q = L1 >> 2;
+        for (int j = threadIdx.x; j < Q * TC; j += blockDim.x) {
+            const int c = j % TC, jq = j / TC;
+            const int kk = jq & (Ns - 1), jh = jq >> lgNs;
+            float2 v0 = a[jq * TC + c], v1 = a[(jq + Q) * TC + c], v2 = a[(jq + 2 * Q) * TC + c],
+                   v3 = a[(jq + 3 * Q) * TC + c];
+            float s1, c1;  // W_{4 Ns}^kk
+            sincospif(-float(kk) / float(2 * Ns), &s1, &c1);
+            const float c2 = c1 * c1 - s1 * s1, s2 = 2.f * c1 * s1;
+            const float c3 = c2 * c1 - s2 * s1, s3 = c2 * s1 + s2 * c1;
+            v1 = make_float2(v1.x * c1 - v1.y * s1, v1.x * s1 + v1.y * c1);
+            v2 = make_float2(v2.x * c2 - v2.y * s2, v2.x * s2 + v2.y * c2);
+            v3 = make_float2(v3.x * c3 - v3.y * s3, v3.x * s3 + v3.y * c3);
+            const float2 a0 = make_float2(v0.x + v2.x, v0.y + v2.y), a1 = make_float2(v0.x - v2.x, v0.y - v2.y);
+            const float2 a2 = make_float2(v1.x + v3.x, v1.y + v3.y);
+            const float2 a3 = make_float2(v1.y - v3.y, v3.x - v1.x);  // -i (v1 - v3)
+            const int o = kk + (jh << (lgNs + 2));
+            b[o * TC + c] = make_float2(a0.x + a2.x, a0.y + a2.y);
+            b[(o + Ns) * TC + c] = make_float2(a1.x + a3.x, a1.y + a3.y);
+            b[(o + 2 * Ns) * TC + c] = make_float2(a0.x - a2.x, a0.y - a2.y);
+            b[(o + 3 * Ns) * TC + c] = make_float2(a1.x - a3.x, a1.y - a3.y);
+        }
+        __syncthreads();
+        float2* x = a; a = b; b = x;
+    }
+    return a;
+}
+
+// A[r][k1][n2] = W_L^(n2 k1) sum_{n1 < L1/2} z_r[L2 n1 + n2] W_L1^(n1 k1), one CTA
+// per tile of kDkColTC columns of a row; shared memory 2 L1 TC float2.
+template <int DT, bool G>
+__global__ void __launch_bounds__(kDkColThreads) dk_colfft_fwd(const uint16_t* __restrict__ u,
+                                                               const uint16_t* __restrict__ dy,
+                                                               const uint16_t* __restrict__ w_in,
+                                                               const uint16_t* __restrict__ w_out,
+                                                               float2* __restrict__ A, int64_t rows, int lgL1) {
+    using O = Op<DT>;
+    constexpr int L2 = kDkL2, TC = kDkColTC;
+    extern __shared__ __align__(16) float2 csm[];
+    const int L1 = 1 << lgL1;
+    const int64_t N = int64_t(L1 / 2) * L2;
+    const uint32_t L = uint32_t(L1) * uint32_t(L2);
+    const int64_t tiles = rows * (L2 / TC);
+    for (int64_t it = blockIdx.x; it < tiles; it += gridDim.x) {
+        const int64_t r = it / (L2 / TC);
+        const int c0 = int(it - r * (L2 / TC)) * TC;
+        for (int i = threadIdx.x; i < L1 * TC; i += blockDim.x) {
+            const int n1 = i / TC, c = i % TC;
+            float2 v = make_float2(0.f, 0.f);
+            if (n1 < L1 / 2) {  // the upper half of z is zero
+                const int64_t j = r * N + int64_t(L2) * n1 + c0 + c;
+                float g = O::unpack(uint32_t(dy[j])).r, x = O::unpack(uint32_t(u[j])).r;
+                if (G) {
+                    g *= O::unpack(uint32_t(w_out[j])).r;
+                    x *= O::unpack(uint32_t(w_in[j])).r;
+                }
+                v = make_float2(g, x);
+            }
+            csm[i] = v;
+        }
+        __syncthreads();
+        const float2* z = dk_colfft(csm, csm + L1 * TC, lgL1);
+        for (int i = threadIdx.x; i < L1 * TC; i += blockDim.x) {
+            const int k1 = i / TC, c = i % TC;
+            const uint32_t n2 = uint32_t(c0 + c);
+            A[(r * L1 + k1) * int64_t(L2) + n2] = dk_cmul(z[i], dk_twiddle(n2 * uint32_t(k1), L));
+        }
+        __syncthreads();  // the buffers are refilled by the next tile
+    }
+}
+
+// dk[h][n2 + L2 n1] = Re(sum_k1 R[h][k1][n2] W_L1^(k1 n1)) / L for n1 < L1/2,
+// one CTA per tile of kDkColTC columns of a channel.
+__global__ void __launch_bounds__(kDkColThreads) dk_colfft_inv(const float2* __restrict__ R, float* __restrict__ dk,
+                                                               int64_t H, int lgL1) {
+    constexpr int L2 = kDkL2, TC = kDkColTC;
+    extern __shared__ __align__(16) float2 csm[];
+    const int L1 = 1 << lgL1;
+    const int64_t N = int64_t(L1 / 2) * L2;
+    const float sc = 1.f / (float(L1) * float(L2));
+    const int64_t tiles = H * (L2 / TC);
+    for (int64_t it = blockIdx.x; it < tiles; it += gridDim.x) {
+        const int64_t h = it / (L2 / TC);
+        const int c0 = int(it - h * (L2 / TC)) * TC;
+        for (int i = threadIdx.x; i < L1 * TC; i += blockDim.x) {
+            const int k1 = i / TC, c = i % TC;
+            csm[i] = R[(h * L1 + k1) * int64_t(L2) + c0 + c];
+        }
+        __syncthreads();
+        const float2* y = dk_colfft(csm, csm + L1 * TC, lgL1);
+        for (int i = threadIdx.x; i < (L1 / 2) * TC; i += blockDim.x) {
+            const int n1 = i / TC, c = i % TC;
+            dk[h * N + int64_t(L2) * n1 + c0 + c] = y[i].x * sc;
+        }
+        __syncthreads();
     }
 }
 

@@ -1541,8 +1541,67 @@ cudaError_t launch_dk4_t(const void* u, const void* dy, const void* w_in, const 
     const int64_t items = H * (L1 / 2);
     fn<<<unsigned(items < 65535 * 16 ? items : 65535 * 16), kDkRowThreads, smem, st>>>(
         static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(w_in),
-        static_cast<const uint16_t*>(w_out), R, B, H);
+        static_cast<const uint16_t*>(w_out), R, B, H, nullptr);
     dk_cols_inv<L1><<<grid_for(H * kDkL2), 256, 0, st>>>(R, dk, H);
+    return cudaGetLastError();
+}
+
+// 2N in (64K, 1M]: the four-step form with the column transforms through HBM
+// (A: rows x L float2, then R: H x L float2), L = L1 x 2048, L1 = 64 .. 512
+constexpr int64_t kDk4FaMaxL = int64_t(1) << 20;
+
+template <int L1>
+cudaError_t launch_dk4_rows_fa(const float2* A, float2* R, int64_t B, int64_t H, cudaStream_t st) {
+    const size_t smem = size_t(2) * kDkL2 * sizeof(float4) + (size_t(2) * kDkL2 + kDkTwEntries) * sizeof(float2);
+    static PerDevice ready;
+    auto fn = dk_rows<0, L1, false, true>;
+    int* rd = ready.slot();
+    if (!rd) return cudaErrorInvalidDevice;
+    if (!*rd) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        *rd = 1;
+    }
+    const int64_t items = H * (L1 / 2);
+    fn<<<unsigned(items < 65535 * 16 ? items : 65535 * 16), kDkRowThreads, smem, st>>>(nullptr, nullptr, nullptr,
+                                                                                          nullptr, R, B, H, A);
+    return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dk4_fa(const void* u, const void* dy, const void* w_in, const void* w_out, float* dk, int64_t B,
+                          int64_t H, int64_t L, void* scratch, cudaStream_t st) {
+    const int L1 = int(L / kDkL2), lgL1 = ilog2(L1);
+    const int64_t rows = B * H;
+    float2* A = static_cast<float2*>(scratch);
+    float2* R = A + rows * L;
+    const size_t csmem = size_t(2) * L1 * kDkColTC * sizeof(float2);
+    static PerDevice ready[2];  // per gating and device (the column kernels' shared-memory opt-in)
+    auto fwd = w_in ? dk_colfft_fwd<DT, true> : dk_colfft_fwd<DT, false>;
+    int* rd = ready[w_in ? 1 : 0].slot();
+    if (!rd) return cudaErrorInvalidDevice;
+    if (!*rd) {
+        cudaError_t e = cudaFuncSetAttribute(fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * 512 * kDkColTC * sizeof(float2)));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(dk_colfft_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * 512 * kDkColTC * sizeof(float2)));
+        if (e != cudaSuccess) return e;
+        *rd = 1;
+    }
+    const int64_t tiles_f = rows * (kDkL2 / kDkColTC), tiles_i = H * (kDkL2 / kDkColTC);
+    fwd<<<unsigned(tiles_f < 65535 * 16 ? tiles_f : 65535 * 16), kDkColThreads, csmem, st>>>(
+        static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(w_in),
+        static_cast<const uint16_t*>(w_out), A, rows, lgL1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    switch (L1) {
+        case 64: e = launch_dk4_rows_fa<64>(A, R, B, H, st); break;
+        case 128: e = launch_dk4_rows_fa<128>(A, R, B, H, st); break;
+        case 256: e = launch_dk4_rows_fa<256>(A, R, B, H, st); break;
+        case 512: e = launch_dk4_rows_fa<512>(A, R, B, H, st); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    dk_colfft_inv<<<unsigned(tiles_i < 65535 * 16 ? tiles_i : 65535 * 16), kDkColThreads, csmem, st>>>(R, dk, H, lgL1);
     return cudaGetLastError();
 }
 
@@ -1569,6 +1628,7 @@ extern "C" size_t fftconv_backward_dk_scratch_bytes(fftconv_plan_t plan, int64_t
     const int64_t L = 2 * plan->info.N;
     if (L <= kDkMaxL) return 0;  // whole channels in shared memory
     if (L <= kDk4MaxL) return size_t(H) * size_t(L) * sizeof(float2);
+    if (L <= kDk4FaMaxL) return (size_t(B) * size_t(H) + size_t(H)) * size_t(L) * sizeof(float2);
     return 2 * size_t(B) * size_t(H) * size_t(L) * sizeof(float2);
 }
 
@@ -1620,6 +1680,12 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
         const cudaError_t e = plan->info.dtype == FFTCONV_F16
                                   ? launch_dk4<0>(u, dy, w_in, w_out, dk, B, H, L, scratch, st)
                                   : launch_dk4<1>(u, dy, w_in, w_out, dk, B, H, L, scratch, st);
+        return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+    }
+    if (L <= kDk4FaMaxL) {
+        const cudaError_t e = plan->info.dtype == FFTCONV_F16
+                                  ? launch_dk4_fa<0>(u, dy, w_in, w_out, dk, B, H, L, scratch, st)
+                                  : launch_dk4_fa<1>(u, dy, w_in, w_out, dk, B, H, L, scratch, st);
         return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
     }
     const int64_t rows = B * H;

@@ -64,7 +64,11 @@ def test_input_grad_matches_oracle(N, dtype, gated, B, H, order):
     (16384, "fp16", True, 3, 2),      # four-step, L = 16 x 2048
     (16384, "bf16", False, 1, 3),
     (32768, "bf16", False, 2, 2),     # four-step, L = 32 x 2048
-    (65536, "fp16", False, 1, 2),     # row transforms through HBM
+    (65536, "fp16", False, 1, 2),     # four-step with the columns through HBM, L = 64 x 2048
+    (131072, "bf16", True, 2, 1),     # L = 128 x 2048
+    (262144, "fp16", False, 1, 2),    # L = 256 x 2048 (the path512 length)
+    (524288, "bf16", False, 1, 1),    # L = 512 x 2048
+    (1048576, "fp16", False, 1, 1),   # row transforms through HBM
 ])
 def test_kernel_grad_matches_oracle(N, dtype, gated, B, H):
     ins, dy = _inputs(B, H, N, dtype, gated, seed=32)
