@@ -393,12 +393,8 @@ def run_backward(args, w: W.Workload):
             dk_kernels, dk_launches = "dk_channel_smem", 1
         elif Ld <= 65536:  # four-step: batch-summed pairs of sub-rows, then the inverse columns
             dk_kernels, dk_launches = "dk_rows + dk_cols_inv", 2
-        elif Ld <= 1 << 20:  # four-step with the column transforms through HBM
+        else:  # four-step with the column transforms through HBM
             dk_kernels, dk_launches = "dk_colfft_fwd + dk_rows + dk_colfft_inv", 3
-        else:  # row transforms through HBM
-            lg = int(np.log2(Ld))
-            passes = (lg + 1) // 2
-            dk_kernels, dk_launches = "dk_pack + kfft_pass + dk_reduce + kfft_pass + dk_extract", 3 + 2 * passes
         launches = path_of(plan.info)["launches_per_step"] + dk_launches
         achieved = nbytes / (ms * 1e-3) / 1e9
         out = {"metric": METRIC + " (backward: du + dk)", "value": job_value(w.outputs, world, ms),

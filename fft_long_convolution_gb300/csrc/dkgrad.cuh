@@ -346,20 +346,22 @@ __global__ void __launch_bounds__(kDkRowThreads, 2) dk_rows(const uint16_t* __re
     }
 }
 
-// 2N = 128K .. 1M: the column passes of the four-step form run as batched
-// L1-point transforms in shared memory, L1 = L / 2048 = 64 .. 512, on tiles
-// of kDkColTC consecutive columns (element (n1, c) at n1 * TC + c); Stockham
-// radix-4 passes (one radix-2 pass first for odd log2 L1) between two
-// buffers.  Returns the buffer holding the result.
-constexpr int kDkColTC = 16, kDkColThreads = 256;
+// 2N = 128K .. 4M: the column passes of the four-step form run as batched
+// L1-point transforms in shared memory, L1 = L / 2048 = 64 .. 2048, on tiles
+// of TC = 2^lgTC consecutive columns (element (n1, c) at n1 * TC + c; TC = 16
+// up to L1 = 512, then 8 and 4, so that two buffers take at most 128 KB);
+// Stockham radix-4 passes (one radix-2 pass first for odd log2 L1) between
+// two buffers.  Returns the buffer holding the result.
+constexpr int kDkColThreads = 256;
+__host__ __device__ inline int dk_col_lgtc(int lgL1) { return lgL1 <= 9 ? 4 : (lgL1 == 10 ? 3 : 2); }
 
-__device__ float2* dk_colfft(float2* a, float2* b, int lgL1) {
-    constexpr int TC = kDkColTC;
+__device__ float2* dk_colfft(float2* a, float2* b, int lgL1, int lgTC) {
+    const int TC = 1 << lgTC;
     const int L1 = 1 << lgL1;
     int lgNs = 0;
     if (lgL1 & 1) {
         for (int j = threadIdx.x; j < (L1 / 2) * TC; j += blockDim.x) {
-            const int c = j % TC, jj = j / TC;
+            const int c = j & (TC - 1), jj = j >> lgTC;
             const float2 c0 = a[jj * TC + c], c1 = a[(jj + L1 / 2) * TC + c];
             b[(2 * jj) * TC + c] = make_float2(c0.x + c1.x, c0.y + c1.y);
             b[(2 * jj + 1) * TC + c] = make_float2(c0.x - c1.x, c0.y - c1.y);
@@ -371,7 +373,7 @@ __device__ float2* dk_colfft(float2* a, float2* b, int lgL1) {
     for (; lgNs < lgL1; lgNs += 2) {
         const int Ns = 1 << lgNs, Q = L1 >> 2;
         for (int j = threadIdx.x; j < Q * TC; j += blockDim.x) {
-            const int c = j % TC, jq = j / TC;
+            const int c = j & (TC - 1), jq = j >> lgTC;
             const int kk = jq & (Ns - 1), jh = jq >> lgNs;
             float2 v0 = a[jq * TC + c], v1 = a[(jq + Q) * TC + c], v2 = a[(jq + 2 * Q) * TC + c],
                    v3 = a[(jq + 3 * Q) * TC + c];
@@ -398,7 +400,7 @@ __device__ float2* dk_colfft(float2* a, float2* b, int lgL1) {
 }
 
 // A[r][k1][n2] = W_L^(n2 k1) sum_{n1 < L1/2} z_r[L2 n1 + n2] W_L1^(n1 k1), one CTA
-// per tile of kDkColTC columns of a row; shared memory 2 L1 TC float2.
+// per tile of TC columns of a row; shared memory 2 L1 TC float2.
 template <int DT, bool G>
 __global__ void __launch_bounds__(kDkColThreads) dk_colfft_fwd(const uint16_t* __restrict__ u,
                                                                const uint16_t* __restrict__ dy,
@@ -406,9 +408,9 @@ __global__ void __launch_bounds__(kDkColThreads) dk_colfft_fwd(const uint16_t* _
                                                                const uint16_t* __restrict__ w_out,
                                                                float2* __restrict__ A, int64_t rows, int lgL1) {
     using O = Op<DT>;
-    constexpr int L2 = kDkL2, TC = kDkColTC;
+    constexpr int L2 = kDkL2;
     extern __shared__ __align__(16) float2 csm[];
-    const int L1 = 1 << lgL1;
+    const int L1 = 1 << lgL1, lgTC = dk_col_lgtc(lgL1), TC = 1 << lgTC;
     const int64_t N = int64_t(L1 / 2) * L2;
     const uint32_t L = uint32_t(L1) * uint32_t(L2);
     const int64_t tiles = rows * (L2 / TC);
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kDkColThreads) dk_colfft_fwd(const uint16_t* _
         const int64_t r = it / (L2 / TC);
         const int c0 = int(it - r * (L2 / TC)) * TC;
         for (int i = threadIdx.x; i < L1 * TC; i += blockDim.x) {
-            const int n1 = i / TC, c = i % TC;
+            const int n1 = i >> lgTC, c = i & (TC - 1);
             float2 v = make_float2(0.f, 0.f);
             if (n1 < L1 / 2) {  // the upper half of z is zero
                 const int64_t j = r * N + int64_t(L2) * n1 + c0 + c;
@@ -430,9 +432,9 @@ __global__ void __launch_bounds__(kDkColThreads) dk_colfft_fwd(const uint16_t* _
             csm[i] = v;
         }
         __syncthreads();
-        const float2* z = dk_colfft(csm, csm + L1 * TC, lgL1);
+        const float2* z = dk_colfft(csm, csm + L1 * TC, lgL1, lgTC);
         for (int i = threadIdx.x; i < L1 * TC; i += blockDim.x) {
-            const int k1 = i / TC, c = i % TC;
+            const int k1 = i >> lgTC, c = i & (TC - 1);
             const uint32_t n2 = uint32_t(c0 + c);
             A[(r * L1 + k1) * int64_t(L2) + n2] = dk_cmul(z[i], dk_twiddle(n2 * uint32_t(k1), L));
         }
@@ -441,12 +443,12 @@ __global__ void __launch_bounds__(kDkColThreads) dk_colfft_fwd(const uint16_t* _
 }
 
 // dk[h][n2 + L2 n1] = Re(sum_k1 R[h][k1][n2] W_L1^(k1 n1)) / L for n1 < L1/2,
-// one CTA per tile of kDkColTC columns of a channel.
+// one CTA per tile of TC columns of a channel.
 __global__ void __launch_bounds__(kDkColThreads) dk_colfft_inv(const float2* __restrict__ R, float* __restrict__ dk,
                                                                int64_t H, int lgL1) {
-    constexpr int L2 = kDkL2, TC = kDkColTC;
+    constexpr int L2 = kDkL2;
     extern __shared__ __align__(16) float2 csm[];
-    const int L1 = 1 << lgL1;
+    const int L1 = 1 << lgL1, lgTC = dk_col_lgtc(lgL1), TC = 1 << lgTC;
     const int64_t N = int64_t(L1 / 2) * L2;
     const float sc = 1.f / (float(L1) * float(L2));
     const int64_t tiles = H * (L2 / TC);
@@ -454,13 +456,13 @@ __global__ void __launch_bounds__(kDkColThreads) dk_colfft_inv(const float2* __r
         const int64_t h = it / (L2 / TC);
         const int c0 = int(it - h * (L2 / TC)) * TC;
         for (int i = threadIdx.x; i < L1 * TC; i += blockDim.x) {
-            const int k1 = i / TC, c = i % TC;
+            const int k1 = i >> lgTC, c = i & (TC - 1);
             csm[i] = R[(h * L1 + k1) * int64_t(L2) + c0 + c];
         }
         __syncthreads();
-        const float2* y = dk_colfft(csm, csm + L1 * TC, lgL1);
+        const float2* y = dk_colfft(csm, csm + L1 * TC, lgL1, lgTC);
         for (int i = threadIdx.x; i < (L1 / 2) * TC; i += blockDim.x) {
-            const int n1 = i / TC, c = i % TC;
+            const int n1 = i >> lgTC, c = i & (TC - 1);
             dk[h * N + int64_t(L2) * n1 + c0 + c] = y[i].x * sc;
         }
         __syncthreads();

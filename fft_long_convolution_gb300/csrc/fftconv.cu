@@ -1359,65 +1359,6 @@ extern "C" fftconv_status_t fftconv_backward_du_gated(fftconv_plan_t plan, const
 
 namespace {
 
-// z[r][n] = g[n] + i x[n] (n < N), 0 above: g = dy (* w_out), x = u (* w_in)
-template <int DT>
-__global__ void dk_pack(const uint16_t* __restrict__ u, const uint16_t* __restrict__ dy,
-                        const uint16_t* __restrict__ w_in, const uint16_t* __restrict__ w_out,
-                        float2* __restrict__ z, int64_t rows, int64_t N) {
-    using O = Op<DT>;
-    const int64_t L = 2 * N;
-    int lgL = 0;
-    while ((int64_t(1) << lgL) < L) ++lgL;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < rows * L;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t r = i >> lgL, n = i & (L - 1);
-        float g = 0.f, x = 0.f;
-        if (n < N) {
-            const int64_t j = r * N + n;
-            g = O::unpack(uint32_t(dy[j])).r;
-            x = O::unpack(uint32_t(u[j])).r;
-            if (w_out) g *= O::unpack(uint32_t(w_out[j])).r;
-            if (w_in) x *= O::unpack(uint32_t(w_in[j])).r;
-        }
-        z[i] = make_float2(g, x);
-    }
-}
-
-// P~[h][f] = conj(sum_b G_b[f] conj X_b[f]) with G = (Z[f] + conj Z[-f]) / 2 and
-// X = (Z[f] - conj Z[-f]) / (2i), the spectra of the real rows g and x packed
-// as Z = DFT(g + i x); the conjugate lets a forward DFT compute the inverse.
-__global__ void dk_reduce(const float2* __restrict__ Z, float2* __restrict__ P, int64_t B, int64_t H, int64_t L) {
-    int lgL = 0;
-    while ((int64_t(1) << lgL) < L) ++lgL;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * L;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t h = i >> lgL, f = i & (L - 1), fm = (L - f) & (L - 1);
-        float pr = 0.f, pi = 0.f;
-        for (int64_t b = 0; b < B; ++b) {
-            const float2* Zr = Z + (b * H + h) * L;
-            const float2 a = Zr[f], c = Zr[fm];  // Z[f], Z[-f]
-            const float gr = 0.5f * (a.x + c.x), gi = 0.5f * (a.y - c.y);     // G = (Z[f] + conj Z[-f]) / 2
-            const float xr = 0.5f * (a.y + c.y), xi = -0.5f * (a.x - c.x);    // X = (Z[f] - conj Z[-f]) / (2i)
-            pr += gr * xr + gi * xi;  // G conj X
-            pi += gi * xr - gr * xi;
-        }
-        P[i] = make_float2(pr, -pi);
-    }
-}
-
-// dk[h][n] = Re(DFT(conj P)[n]) / L = Re(IDFT(P)[n]), n < N
-__global__ void dk_extract(const float2* __restrict__ Y, float* __restrict__ dk, int64_t H, int64_t N) {
-    const int64_t L = 2 * N;
-    const float s = 1.f / float(L);
-    int lgN = 0;
-    while ((int64_t(1) << lgN) < N) ++lgN;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < H * N;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t h = i >> lgN, n = i & (N - 1);
-        dk[i] = Y[h * L + n].x * s;
-    }
-}
-
 // The kernel gradient of whole channels for 2N <= 8192, in shared memory: one
 // CTA per channel transforms each batch row g + i x (Stockham radix-4 /
 // radix-2 passes between two shared buffers), adds the row's cross spectrum
@@ -1546,9 +1487,9 @@ cudaError_t launch_dk4_t(const void* u, const void* dy, const void* w_in, const 
     return cudaGetLastError();
 }
 
-// 2N in (64K, 1M]: the four-step form with the column transforms through HBM
-// (A: rows x L float2, then R: H x L float2), L = L1 x 2048, L1 = 64 .. 512
-constexpr int64_t kDk4FaMaxL = int64_t(1) << 20;
+// 2N in (64K, 4M]: the four-step form with the column transforms through HBM
+// (A: rows x L float2, then R: H x L float2), L = L1 x 2048, L1 = 64 .. 2048
+constexpr int64_t kDk4FaMaxL = int64_t(1) << 22;
 
 template <int L1>
 cudaError_t launch_dk4_rows_fa(const float2* A, float2* R, int64_t B, int64_t H, cudaStream_t st) {
@@ -1575,19 +1516,20 @@ cudaError_t launch_dk4_fa(const void* u, const void* dy, const void* w_in, const
     const int64_t rows = B * H;
     float2* A = static_cast<float2*>(scratch);
     float2* R = A + rows * L;
-    const size_t csmem = size_t(2) * L1 * kDkColTC * sizeof(float2);
+    const int lgTC = dk_col_lgtc(lgL1);
+    const size_t csmem = size_t(2) * L1 * (size_t(1) << lgTC) * sizeof(float2);  // at most 128 KB
     static PerDevice ready[2];  // per gating and device (the column kernels' shared-memory opt-in)
     auto fwd = w_in ? dk_colfft_fwd<DT, true> : dk_colfft_fwd<DT, false>;
     int* rd = ready[w_in ? 1 : 0].slot();
     if (!rd) return cudaErrorInvalidDevice;
     if (!*rd) {
-        cudaError_t e = cudaFuncSetAttribute(fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * 512 * kDkColTC * sizeof(float2)));
+        cudaError_t e = cudaFuncSetAttribute(fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(dk_colfft_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * 512 * kDkColTC * sizeof(float2)));
+        e = cudaFuncSetAttribute(dk_colfft_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
         if (e != cudaSuccess) return e;
         *rd = 1;
     }
-    const int64_t tiles_f = rows * (kDkL2 / kDkColTC), tiles_i = H * (kDkL2 / kDkColTC);
+    const int64_t tiles_f = rows * (kDkL2 >> lgTC), tiles_i = H * (kDkL2 >> lgTC);
     fwd<<<unsigned(tiles_f < 65535 * 16 ? tiles_f : 65535 * 16), kDkColThreads, csmem, st>>>(
         static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy), static_cast<const uint16_t*>(w_in),
         static_cast<const uint16_t*>(w_out), A, rows, lgL1);
@@ -1598,6 +1540,8 @@ cudaError_t launch_dk4_fa(const void* u, const void* dy, const void* w_in, const
         case 128: e = launch_dk4_rows_fa<128>(A, R, B, H, st); break;
         case 256: e = launch_dk4_rows_fa<256>(A, R, B, H, st); break;
         case 512: e = launch_dk4_rows_fa<512>(A, R, B, H, st); break;
+        case 1024: e = launch_dk4_rows_fa<1024>(A, R, B, H, st); break;
+        case 2048: e = launch_dk4_rows_fa<2048>(A, R, B, H, st); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
@@ -1628,8 +1572,7 @@ extern "C" size_t fftconv_backward_dk_scratch_bytes(fftconv_plan_t plan, int64_t
     const int64_t L = 2 * plan->info.N;
     if (L <= kDkMaxL) return 0;  // whole channels in shared memory
     if (L <= kDk4MaxL) return size_t(H) * size_t(L) * sizeof(float2);
-    if (L <= kDk4FaMaxL) return (size_t(B) * size_t(H) + size_t(H)) * size_t(L) * sizeof(float2);
-    return 2 * size_t(B) * size_t(H) * size_t(L) * sizeof(float2);
+    return (size_t(B) * size_t(H) + size_t(H)) * size_t(L) * sizeof(float2);  // L <= kDk4FaMaxL (N <= 2^21)
 }
 
 extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void* u, const void* dy, const void* w_in,
@@ -1682,29 +1625,11 @@ extern "C" fftconv_status_t fftconv_backward_dk(fftconv_plan_t plan, const void*
                                   : launch_dk4<1>(u, dy, w_in, w_out, dk, B, H, L, scratch, st);
         return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
     }
-    if (L <= kDk4FaMaxL) {
-        const cudaError_t e = plan->info.dtype == FFTCONV_F16
-                                  ? launch_dk4_fa<0>(u, dy, w_in, w_out, dk, B, H, L, scratch, st)
-                                  : launch_dk4_fa<1>(u, dy, w_in, w_out, dk, B, H, L, scratch, st);
-        return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
-    }
-    const int64_t rows = B * H;
-    float2* a = static_cast<float2*>(scratch);
-    float2* b = a + rows * L;
-    if (plan->info.dtype == FFTCONV_F16)
-        dk_pack<0><<<grid_for(rows * L), 256, 0, st>>>(static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy),
-                                                       static_cast<const uint16_t*>(w_in),
-                                                       static_cast<const uint16_t*>(w_out), a, rows, N);
-    else
-        dk_pack<1><<<grid_for(rows * L), 256, 0, st>>>(static_cast<const uint16_t*>(u), static_cast<const uint16_t*>(dy),
-                                                       static_cast<const uint16_t*>(w_in),
-                                                       static_cast<const uint16_t*>(w_out), a, rows, N);
-    float2* z = fft_rows(a, b, rows, L, st);  // Z = DFT(g + i x) of every row
-    float2* pb = z == a ? b : a;
-    dk_reduce<<<grid_for(H * L), 256, 0, st>>>(z, pb, B, H, L);
-    a = fft_rows(pb, z, H, L, st);  // DFT of conj P per channel
-    dk_extract<<<grid_for(H * N), 256, 0, st>>>(a, dk, H, N);
-    return cudaGetLastError() == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
+    // every plan length (2N <= 4M): the four-step form with the column transforms through HBM
+    const cudaError_t e = plan->info.dtype == FFTCONV_F16
+                              ? launch_dk4_fa<0>(u, dy, w_in, w_out, dk, B, H, L, scratch, st)
+                              : launch_dk4_fa<1>(u, dy, w_in, w_out, dk, B, H, L, scratch, st);
+    return e == cudaSuccess ? FFTCONV_OK : FFTCONV_ERR_CUDA;
 }
 
 // --------------------------------------------------------------- partial convolution

@@ -309,12 +309,15 @@ fftconv_status_t fftconv_forward_host(fftconv_plan_t plan, const void *u, const 
  *   workspace and errors as fftconv_forward(_gated).
  * fftconv_backward_dk: dk float32 [H][N] on the device; w_in / w_out both
  *   NULL or both given; scratch: device memory of at least
- *   fftconv_backward_dk_scratch_bytes(plan, B, H) bytes (16-byte aligned), the
- *   float32 spectra of all rows (two buffers of B*H*2N complex).  Computed in
- *   float32: one radix-2 transform of g + i x per row (g = w_out . dy,
- *   x = u . w_in), the per-channel sum over b of the cross spectra, one
- *   inverse transform per channel.  B = 0 writes zeros.  Returns OK, INVALID,
- *   ALIGN, WORKSPACE or CUDA.
+ *   fftconv_backward_dk_scratch_bytes(plan, B, H) bytes (16-byte aligned; 0
+ *   for 2N <= 8192, H*2N float32 complex values for 2N <= 65536, else
+ *   (B + 1)*H*2N).  Computed in float32: the 2N-point transform of g + i x
+ *   per row (g = w_out . dy, x = u . w_in), the per-channel sum over b of
+ *   the cross spectra G conj X, one inverse transform per channel; for
+ *   2N > 8192 as a four-step transform 2N = L1 x 2048 whose column
+ *   transforms go through the scratch when 2N > 65536.  B = 0 writes zeros.
+ *   Returns OK, INVALID, UNSUPPORTED (sparse or circular plan, too many
+ *   rows), ALIGN, WORKSPACE or CUDA.
  */
 fftconv_status_t fftconv_kernel_fft_adjoint(fftconv_plan_t plan, const float *k, void *k_f, int64_t H,
                                             fftconv_stream_t stream);

@@ -68,7 +68,8 @@ def test_input_grad_matches_oracle(N, dtype, gated, B, H, order):
     (131072, "bf16", True, 2, 1),     # L = 128 x 2048
     (262144, "fp16", False, 1, 2),    # L = 256 x 2048 (the path512 length)
     (524288, "bf16", False, 1, 1),    # L = 512 x 2048
-    (1048576, "fp16", False, 1, 1),   # row transforms through HBM
+    (1048576, "fp16", False, 1, 1),   # L = 1024 x 2048 (tiles of 8 columns)
+    (2097152, "bf16", True, 1, 1),    # L = 2048 x 2048 (tiles of 4 columns), the longest plan
 ])
 def test_kernel_grad_matches_oracle(N, dtype, gated, B, H):
     ins, dy = _inputs(B, H, N, dtype, gated, seed=32)
