@@ -265,36 +265,40 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
-            uint32_t vr[2][2][16];  // [sub-row][block]: sub-row 1's loads fly while sub-row 0 is processed
+            // [sub-row][block]: block b = 1's loads fly while block 0 of both
+            // sub-rows is processed; each twiddle serves both sub-rows
+            uint32_t vr[2][2][16];
             tc::ld16x256b_x4(tD + laneA + 32 * hf, vr[0][0]);
-            tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
-            tc::wait_ld();
             tc::ld16x256b_x4(tD + laneA + 64 + 32 * hf, vr[1][0]);
+            tc::wait_ld();
+            tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
             tc::ld16x256b_x4(tD + laneB + 64 + 32 * hf, vr[1][1]);
+            float4 x0[4];   // sub-row 0, k1 = 0 (block a): kept for the pre-twiddled copy
+            uint2 p32[4];   // sub-row 0, k1 = 32 (block b): kept for the duplicate
             #pragma unroll
-            for (int R = 0; R < 2; ++R) {
-                float4 x0[4];   // k1 = 0 (block a): kept for the pre-twiddled copy
-                uint2 p32[4];   // k1 = 32 (block b): kept for the duplicate
-                if (R == 1) tc::wait_ld();
+            for (int b = 0; b < 2; ++b) {
+                if (b == 1) tc::wait_ld();
+                const int kap = b ? kapB : kapA;
+                const int slot0 = sp ? tc64_slot(kap) : 2 * kap;                // sub-row 0 (R = 0)
+                const int slot1 = sp ? 72 + 2 * kapA + b : 2 * (63 - kap) + 1;  // sub-row 1 (R = 1)
+                uint8_t* dst0 = bbuf + rowoff(slot0) + kq2;
+                uint8_t* dst1 = bbuf + rowoff(slot1) + kq2;
                 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const uint32_t* vv = vr[R][b];
-                    const int kap = b ? kapB : kapA;
-                    const int slot = sp ? (R == 0 ? tc64_slot(kap) : 72 + 2 * kapA + b)
-                                        : (R == 0 ? 2 * kap : 2 * (63 - kap) + 1);
-                    uint8_t* dst = bbuf + rowoff(slot) + kq2;
-                    #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const float4 xv = cmul2_twiddle(__uint_as_float(vv[4 * jj]), __uint_as_float(vv[4 * jj + 1]),
-                                                      __uint_as_float(vv[4 * jj + 2]), __uint_as_float(vv[4 * jj + 3]),
-                                                      tws[(4 * b + jj) * 256]);
-                        const uint2 wd = make_uint2(O::pack(xv.x, xv.z), O::pack(xv.y, xv.w));
-                        *reinterpret_cast<uint2*>(dst + 2 * jj * C::LBO2) = wd;
-                        if (b == 0) x0[jj] = xv;
-                        else p32[jj] = wd;
-                    }
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float4 tw = tws[(4 * b + jj) * 256];
+                    const uint32_t* v0 = vr[0][b] + 4 * jj;
+                    const uint32_t* v1 = vr[1][b] + 4 * jj;
+                    const float4 xv = cmul2_twiddle(__uint_as_float(v0[0]), __uint_as_float(v0[1]),
+                                                    __uint_as_float(v0[2]), __uint_as_float(v0[3]), tw);
+                    const float4 xw = cmul2_twiddle(__uint_as_float(v1[0]), __uint_as_float(v1[1]),
+                                                    __uint_as_float(v1[2]), __uint_as_float(v1[3]), tw);
+                    const uint2 wd = make_uint2(O::pack(xv.x, xv.z), O::pack(xv.y, xv.w));
+                    *reinterpret_cast<uint2*>(dst0 + 2 * jj * C::LBO2) = wd;
+                    *reinterpret_cast<uint2*>(dst1 + 2 * jj * C::LBO2) = make_uint2(O::pack(xw.x, xw.z), O::pack(xw.y, xw.w));
+                    if (b == 0) x0[jj] = xv;
+                    else p32[jj] = wd;
                 }
-                if (sp && R == 0 && is_k0) {  // sub-problem 0 again, pre-twiddled by W_64^o (slot 1)
+                if (b == 0 && sp && is_k0) {  // sub-problem 0 again, pre-twiddled by W_64^o (slot 1)
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
                         const float4 y0 = cmul2_twiddle(x0[jj].x, x0[jj].y, x0[jj].z, x0[jj].w, w64[4 * (4 * hf + jj) + q]);
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
                             make_uint2(O::pack(y0.x, y0.z), O::pack(y0.y, y0.w));
                     }
                 }
-                if (sp && R == 0 && is_k32) {  // sub-problem 32 again (slot 65)
+                if (b == 1 && sp && is_k32) {  // sub-problem 32 again (slot 65)
                     #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
                         *reinterpret_cast<uint2*>(bbuf + 8 * C::SBO2 + 16 + kq2 + 2 * jj * C::LBO2) = p32[jj];
@@ -411,25 +415,27 @@ __global__ void __launch_bounds__(TcB::THREADS, 1) mp_pass_b_tc(const TcBArgs a)
         bad = __any_sync(0xffffffffu, bad);  // warp-uniform before the collective TMEM loads
         tc::fence_after();
         if (!bad) {
+            // as in S1 post: block 1's loads fly while block 0 of both sub-rows
+            // is processed, one twiddle per column pair serving both
             uint32_t vr[2][2][16];
             tc::ld16x256b_x4(tD + laneA + 32 * hf, vr[0][0]);
-            tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
-            tc::wait_ld();
             tc::ld16x256b_x4(tD + laneA + 64 + 32 * hf, vr[1][0]);
+            tc::wait_ld();
+            tc::ld16x256b_x4(tD + laneB + 32 * hf, vr[0][1]);
             tc::ld16x256b_x4(tD + laneB + 64 + 32 * hf, vr[1][1]);
             #pragma unroll
-            for (int R = 0; R < 2; ++R) {
-                if (R == 1) tc::wait_ld();
+            for (int b = 0; b < 2; ++b) {
+                if (b == 1) tc::wait_ld();
+                uint8_t* dst = bbuf + rowoff(b ? kapB : kapA) + kq4;
                 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const uint32_t* vv = vr[R][b];
-                    uint8_t* dst = bbuf + rowoff(b ? kapB : kapA) + 8 * R * C::SBO4 + kq4;
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float4 tw = tws[(4 * b + jj) * 256];
                     #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const float4 xv = cmul2_twiddle(__uint_as_float(vv[4 * jj]), __uint_as_float(vv[4 * jj + 1]),
-                                                      __uint_as_float(vv[4 * jj + 2]), __uint_as_float(vv[4 * jj + 3]),
-                                                      tws[(4 * b + jj) * 256]);
-                        *reinterpret_cast<uint2*>(dst + jj * C::LBO4) =
+                    for (int R = 0; R < 2; ++R) {
+                        const uint32_t* vv = vr[R][b] + 4 * jj;
+                        const float4 xv = cmul2_twiddle(__uint_as_float(vv[0]), __uint_as_float(vv[1]),
+                                                        __uint_as_float(vv[2]), __uint_as_float(vv[3]), tw);
+                        *reinterpret_cast<uint2*>(dst + 8 * R * C::SBO4 + jj * C::LBO4) =
                             make_uint2(O::pack(xv.x, xv.z), O::pack(xv.y, xv.w));
                     }
                 }
