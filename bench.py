@@ -287,7 +287,8 @@ def path_of(plan_info: dict, pairs_run: Optional[int] = None) -> dict:
     if plan_info["path"] == 1:
         nb = 0 if pairs_run == 0 else 1
         if plan_info["order"] == 4 and plan_info["factors"][3] == 64:  # outer factor in two HBM levels
-            return {"kernel": "otc_pass (A) x2 + mp_pass_b_tc + otc_pass (C) x2 (the whole step)",
+            return {"kernel": "mp_pass_a (RA) + otc_pass (64, in place) + mp_pass_b_tc + otc_pass (64, in place) "
+                              "+ mp_pass_c (RA) (the whole step)",
                     "launches_per_step": 4 + nb}
         if plan_info["order"] == 3:
             return {"kernel": "otc_pass (A) + mp_pass_b_tc + otc_pass (C) (the whole step)",

@@ -76,13 +76,19 @@ cudaError_t launch_2l_t(const fftconv_plan_s* p, const MPArgs& args, int64_t row
     inner.w_in = inner.w_out = nullptr;
     inner.zmod = RA;      // inner row r holds sub-rows k0 = (r mod RA) + RA j, j < 64
     TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, RA, p->pairs_run, p->plist};
-    if constexpr (!SP) {  // dense: the four outer passes on the tensor cores
-        if ((e = launch_otc<DT, RA, 0, G, L1>(p, outer, rows, p->otc_fa, st)) != cudaSuccess) return e;
+    if constexpr (!SP) {
+        // dense: the in-place 64-point passes on the tensor cores; the first
+        // and last passes over RA = 4 or 8 stay warp-level (mma.sync with
+        // chained column twiddles): their contraction has K = RA or 2 RA and
+        // the tensor-core tile machinery cost more than it saved (gene-2m
+        // 646 us with them on tcgen05, 618 us as here)
+        mp_pass_a<DT, RA, G, L1><<<grid(items1, na1), 256, smem_a1, st>>>(outer);
         if ((e = launch_otc<DT, 64, 1, false, L>(p, inner, rows * RA, p->otc_fa2, st)) != cudaSuccess) return e;
         if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = launch_otc<DT, 64, 2, false, L>(p, inner, rows * RA, p->otc_fc2, st)) != cudaSuccess) return e;
-        return launch_otc<DT, RA, 3, G, L1>(p, outer, rows, p->otc_fc, st);
+        mp_pass_c<DT, RA, G, L1, true><<<grid(items1, nc1), 32 * mp_pass_c_warps<RA>(), smem_c1, st>>>(outer);
+        return cudaGetLastError();
     }
     mp_pass_a<DT, RA, G, L1><<<grid(items1, na1), 256, smem_a1, st>>>(outer);
     mp_pass_a<DT, 64, false, L, true, SP><<<grid(items2, na2), 256, smem_a2, st>>>(inner);
