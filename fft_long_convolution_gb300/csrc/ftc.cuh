@@ -635,6 +635,15 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
             tstart[0][b] = __ldg(a.twout + (kA * 2 + b) * 256 + tg);
             tstart[1][b] = __ldg(a.twout + (kB * 2 + b) * 256 + tg);
         }
+        // R0 = 4, last pair: pair (1, 3)'s S and D of block 0, read while the
+        // contraction runs (block 1's are read in the loop; all eight would spill)
+        uint4 sdp[R0 == 4 ? 4 : 1];
+        if constexpr (R0 == 4 && !C::SPLIT) {
+            if (last) {
+                #pragma unroll
+                for (int c = 0; c < 4; ++c) sdp[c] = a.skip1 ? make_uint4(0, 0, 0, 0) : tout[c * 256];
+            }
+        }
         bad = !mbar_wait_sleep(&bars[0], mmapar, kWaitSleepLimit, kWaitHintNs);
         // R0 = 8: the accumulator's turn (pair 1 of the CTA's first row starts it)
         const bool acc_wait = C::SPLIT && !(p == 1 && it == i0);
@@ -746,7 +755,8 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                             out[0] = make_float4(scale * (tA.x + vB.x), scale * (tA.y + vB.y), scale * (tA.z + vB.z),
                                                  scale * (tA.w + vB.w));
                         } else {
-                            const uint4 sd = a.skip1 ? make_uint4(0, 0, 0, 0) : tout[(4 * b + jj) * 256];
+                            const uint4 sd = b == 0 ? sdp[R0 == 4 ? jj : 0]
+                                                    : (a.skip1 ? make_uint4(0, 0, 0, 0) : tout[(4 * b + jj) * 256]);
                             const cpx s0 = O::unpack(sd.x), s1 = O::unpack(sd.y);
                             const cpx d0 = O::unpack(sd.z), d1 = O::unpack(sd.w);
                             out[0] = make_float4(scale * (tA.x + vB.x + s0.r), scale * (tA.y + vB.y + s1.r),
