@@ -481,6 +481,9 @@ def run_circular(args, w: W.Workload):
         nbytes = w.rows * C * 2 * (2 + (2 if w.gated else 0)) + native.kf_bytes(w.H)
         achieved = nbytes / (ms * 1e-3) / 1e9
         fac = native.info["factors"]
+        fused = native.info["path"] == F.PATH_FUSED
+        kern = ("ftc_conv_kernel (circular rows, R0 = 2)" if fused
+                else "otc_pass (A, all rows) + mp_pass_b_tc + otc_pass (C, all rows)")
         out = {"metric": METRIC + " (circular convolution)", "value": job_value(w.outputs, world, ms),
                "unit": "outputs/s", "n_gpus": world, "steps": steps, "warmup": max(args.warmup, 3),
                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -490,8 +493,8 @@ def run_circular(args, w: W.Workload):
                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                             "algorithmic_bytes_per_launch": nbytes,
-                            "kernel": "otc_pass (A, all rows) + mp_pass_b_tc + otc_pass (C, all rows)"},
-               "gpu_launches": steps * 3, "clocks": clk}
+                            "kernel": kern},
+               "gpu_launches": steps * (1 if fused else 3), "clocks": clk}
         print(json.dumps(out))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -498,12 +498,13 @@ cudaError_t launch_tc64_t(const fftconv_plan_s* p, const void* u, const void* wi
 }
 
 // N = R0 * 4096 (8192, 16384, 32768): the fused tensor-core kernel
-// (ftc.cuh), one CTA per SM (all 512 tensor-memory columns).
-template <int DT, int R0, bool G>
+// (ftc.cuh), one CTA per SM (all 512 tensor-memory columns).  FULL: the
+// circular convolution of C = 16384 samples (R0 = 2, no zero half).
+template <int DT, int R0, bool G, bool FULL = false>
 cudaError_t launch_ftc_t(const fftconv_plan_s* p, const void* u, const void* wi, const void* wo,
                          const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
-    using C = Ftc<R0, G>;
-    auto fn = ftc_conv_kernel<DT, R0, G>;
+    using C = Ftc<R0, G, FULL>;
+    auto fn = ftc_conv_kernel<DT, R0, G, FULL>;
     static PerDevice cache;  // per instantiation and device
     int per_sm = 0;
     cudaError_t e = prep_kernel(fn, C::SMEM, C::THREADS, cache, &per_sm);
@@ -524,7 +525,9 @@ cudaError_t launch_fused_r(const fftconv_plan_s* p, const void* u, const void* w
                            const void* kf, void* y, int64_t B, int64_t H, cudaStream_t st) {
     if (p->tc64) return launch_tc64_t<DT, G>(p, u, wi, wo, kf, y, B, H, st);
     switch (p->ftc) {
-        case 2: return launch_ftc_t<DT, 2, G>(p, u, wi, wo, kf, y, B, H, st);
+        case 2:
+            return p->circular ? launch_ftc_t<DT, 2, G, true>(p, u, wi, wo, kf, y, B, H, st)
+                               : launch_ftc_t<DT, 2, G>(p, u, wi, wo, kf, y, B, H, st);
         case 4: return launch_ftc_t<DT, 4, G>(p, u, wi, wo, kf, y, B, H, st);
         case 8: return launch_ftc_t<DT, 8, G>(p, u, wi, wo, kf, y, B, H, st);
     }
@@ -665,7 +668,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     p->R0 = multi ? info.factors[0] : 1;
     p->R1 = multi ? kMpR1 : info.factors[0];
     p->tc64 = info.order == 2;  // 4096 = 64 x 64 (N = 1024, 2048 zero-padded to it)
-    p->ftc = (info.path == FFTCONV_PATH_FUSED && N >= 8192) ? int(N / 4096) : 0;
+    p->ftc = (info.path == FFTCONV_PATH_FUSED && info.order == 3 && info.factors[1] == 64) ? info.factors[0] : 0;
     p->mp2 = multi && info.order == 4 && info.factors[3] == 64;
     if (p->mp2) p->R0 = info.factors[0] * 64;  // the sub-row count of pass B
     p->mpL = multi ? ((info.order == 3 || p->mp2) ? kMpLtc : kMpL) : 0;
@@ -796,8 +799,9 @@ extern "C" fftconv_status_t fftconv_plan_create_sparse(fftconv_plan_t* out, int6
 extern "C" fftconv_status_t fftconv_circular_query(int64_t C, fftconv_dtype_t dtype, fftconv_plan_info_t* info) {
     if (!info) return FFTCONV_ERR_INVALID;
     if (dtype != FFTCONV_F16 && dtype != FFTCONV_BF16) return FFTCONV_ERR_UNSUPPORTED;
-    // M = C / 2 = R0 * 4096 with R0 = 2 .. 64: the multi-pass factorization
-    // R0 x 64 x 64 with the outer passes over every row
+    // M = C / 2 = R0 * 4096 with R0 = 2 .. 64, factored R0 x 64 x 64: C = 16384
+    // on the fused tensor-core kernel (both blocks of the row in shared
+    // memory), longer rows multi-pass with the outer passes over every row
     if (!is_pow2(C) || C < 16384 || C > (int64_t(1) << 19)) return FFTCONV_ERR_UNSUPPORTED;
     fftconv_plan_info_t q;
     std::memset(&q, 0, sizeof(q));
@@ -807,10 +811,10 @@ extern "C" fftconv_status_t fftconv_circular_query(int64_t C, fftconv_dtype_t dt
     q.factors[0] = int32_t(C / 8192);
     q.factors[1] = 64;
     q.factors[2] = 64;
-    q.path = FFTCONV_PATH_MULTIPASS;
+    q.path = C == 16384 ? FFTCONV_PATH_FUSED : FFTCONV_PATH_MULTIPASS;
     q.dtype = dtype;
     q.kf_bytes_per_channel = int64_t(q.factors[0] / 2) * TcB::KFP * 16;
-    q.workspace_bytes_per_row = 4 * q.M;  // 16-bit complex intermediate
+    q.workspace_bytes_per_row = C == 16384 ? 0 : 4 * q.M;  // 16-bit complex intermediate
     *info = q;
     return FFTCONV_OK;
 }

@@ -67,10 +67,15 @@ struct FtcArgs {
     int skip1;  // R0 = 4, frequency-sparse plan: pair (1, 3) holds no kept bin and is not run
 };
 
-template <int R0, bool GATED>
+// FULL: the circular convolution of length 2M (R0 = 2 only): the input
+// stage sums both blocks of z (no zero half), the output stage writes both
+// blocks, and rows of u and y hold 2M samples.
+template <int R0, bool GATED, bool FULL = false>
 struct Ftc {
     static_assert(R0 == 2 || R0 == 4 || R0 == 8, "fused tensor-core path: N = 8192, 16384 or 32768");
+    static_assert(!FULL || R0 == 2, "circular fused rows: R0 = 2");
     static constexpr int L = 4096, M = R0 * L, NP = R0 / 2;  // sub-row length, row length, pairs per row
+    static constexpr int NB = FULL ? R0 : R0 / 2;            // blocks of z in and of y_z out
     static constexpr bool SPLIT = R0 == 8;                   // both pipelines on one row
     static constexpr int THREADS = 512;                      // two pipelines of 256
     static constexpr uint32_t LBO1 = TcB::LBO1, SBO1 = TcB::SBO1;
@@ -78,8 +83,8 @@ struct Ftc {
     static constexpr uint32_t LBO3 = TcB::LBO3, SBO3 = TcB::SBO3;
     static constexpr uint32_t LBO4 = TcB::LBO4, SBO4 = TcB::SBO4;
     static constexpr uint32_t TRASH = TcB::TRASH, BBUF = TcB::BBUF;
-    static constexpr uint32_t ZB = uint32_t(M / 2) * 4;              // a row of u: M/2 complex words
-    static constexpr uint32_t WIB = (GATED && R0 == 2) ? ZB : 0;     // staged w_in
+    static constexpr uint32_t ZB = uint32_t(NB * L) * 4;             // a row of u: NB L complex words
+    static constexpr uint32_t WIB = (GATED && R0 == 2 && !FULL) ? ZB : 0;  // staged w_in
     static constexpr uint32_t TOB = R0 == 4 ? 8u * 256u * 16u : 0;   // S, D of pair (1, 3): [8][tg] uint4
     static constexpr uint32_t ACCB = SPLIT ? 32u * 256u * 8u : 0;    // R0 = 8: [b 2][jj 4][n0 4][tg] uint2
     // per pipeline: the B buffer, and (unless SPLIT) the staging and the handed-over outputs
@@ -100,11 +105,12 @@ struct Ftc {
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
-template <int DT, int R0, bool GATED>
+template <int DT, int R0, bool GATED, bool FULL = false>
 __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
     using O = Op<DT>;
-    using C = Ftc<R0, GATED>;
-    constexpr int NP = C::NP;
+    using C = Ftc<R0, GATED, FULL>;
+    constexpr int NP = C::NP, NB = C::NB;
+    constexpr size_t RS = size_t(FULL ? 2 : 1) * C::M;  // 16-bit samples per row of u and y
     constexpr uint32_t M = uint32_t(C::M);
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint32_t s_tmem;
@@ -159,11 +165,11 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
     // the row's u (and w_in) into the staging (one bulk copy each); the gates
     // that are read through L2 are prefetched there
     auto stage_row = [&](int ri, uint8_t* pbp, uint64_t* bp) {
-        const size_t off = mrow(ri) * M;
+        const size_t off = mrow(ri) * RS;
         mbar_expect_tx(&bp[1], C::ZB + C::WIB);
         bulk_g2s(C::SPLIT ? smem + C::OFF_ZS : pbp + C::OFF_Z, a.u + off, C::ZB, &bp[1]);
-        if (GATED && R0 == 2) bulk_g2s(pbp + C::OFF_WI, a.w_in + off, C::ZB, &bp[1]);
-        if (GATED && R0 == 4) bulk_prefetch_l2(a.w_in + off, C::ZB);
+        if (GATED && C::WIB) bulk_g2s(pbp + C::OFF_WI, a.w_in + off, C::ZB, &bp[1]);
+        if (GATED && (R0 == 4 || FULL)) bulk_prefetch_l2(a.w_in + off, C::ZB);
         if (GATED) bulk_prefetch_l2(a.w_out + off, C::ZB);
     };
 
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         // fin: the row's output is written here
         const bool first = (it % IPR) == 0, last = (it % IPR) == IPR - 1, fin = p == 0;
         const int kA = p, kB = p ? R0 - p : R0 / 2;
-        const size_t roff = mrow(ri) * M;  // element offset of the row
+        const size_t roff = mrow(ri) * RS;  // element offset of the row
         const bool has_next = it + 1 < i1;
         if (tg == 32 && has_next) {  // the next item's k_f into L2 (read by the next fold)
             const int rn = item_row(it + 1), pn = item_pair(it + 1), hn = chan(rn);
@@ -289,7 +295,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         const float2 tin_a = __ldg(a.twin + kA * 256 + tg), tin_b = __ldg(a.twin + kB * 256 + tg);
         bool bad = false;
         if (first) bad = !mbar_wait_sleep(zbar, inpar, kWaitSleepLimit, kWaitHintNs);
-        constexpr int NZW = R0 == 8 ? 4 : (R0 == 4 ? 2 : 1);  // nonzero input blocks n0 < R0/2
+        constexpr int NZW = NB;  // nonzero input blocks (n0 < R0/2; FULL: all)
         uint32_t zlo[16], zhi[16];
         if (!bad && R0 == 8) {
             // the radix-8 stage over the four nonzero blocks, with gating on the fly
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                 zhi[i] = NZW == 2 ? zs[4096 + in_n + 64 * i] : 0u;
             }
             if constexpr (GATED) {
-                if (R0 == 2) {
+                if (R0 == 2 && !FULL) {
                     #pragma unroll
                     for (int i = 0; i < 16; ++i) zlo[i] = O::mul2(zlo[i], wis[in_n + 64 * i]);
                 } else if (first) {
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                     const int i = 4 * gq + e;
                     const cpx l = O::unpack(zlo[i]);
                     cpx t = {0.f, 0.f};
-                    if (R0 == 4) {
+                    if (R0 == 4 || FULL) {  // the second nonzero block
                         const cpx hh = O::unpack(zhi[i]);
                         t = odd ? cpx{hh.i, -hh.r} : hh;
                     }
@@ -613,9 +619,10 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
         // ---------------- S4 post: the inverse outer stage.  This thread's
         // outputs n' = 64 kappa_b + 32 hf + 8 jj + 2q + e of both sub-rows.
         // gated, last pair: w_out at (b, jj, n0), read while the contraction
-        // runs (R0 = 2; R0 = 4 reads it at the store, registers being short)
-        constexpr bool WPRE = GATED && R0 == 2;
-        uint2 wov[2][4][NP > 2 ? 1 : NP];
+        // runs (R0 = 2; R0 = 4 and the circular rows read it at the store,
+        // registers being short)
+        constexpr bool WPRE = GATED && R0 == 2 && !FULL;
+        uint2 wov[2][4][WPRE ? NB : 1];
         if constexpr (WPRE) {
           if (last) {
             #pragma unroll
@@ -623,7 +630,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
                     #pragma unroll
-                    for (int n0 = 0; n0 < NP; ++n0)
+                    for (int n0 = 0; n0 < NB; ++n0)
                         wov[b][jj][n0] = __ldg(reinterpret_cast<const uint2*>(
                             a.w_out + roff + 2 * size_t(4096 * n0 + 64 * (b ? kapB : kapA) + 32 * hf + 2 * q + 8 * jj)));
           }
@@ -750,10 +757,13 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                                                               O::pack(D.x, D.z), O::pack(D.y, D.w));
                     } else {
                         // (re e0, re e1, im e0, im e1) of each output block n0
-                        float4 out[NP];
+                        float4 out[NB];
                         if constexpr (R0 == 2) {
                             out[0] = make_float4(scale * (tA.x + vB.x), scale * (tA.y + vB.y), scale * (tA.z + vB.z),
                                                  scale * (tA.w + vB.w));
+                            if constexpr (FULL)  // block 1: W_2^(1 * 1) = -1 on sub-row 1
+                                out[NB - 1] = make_float4(scale * (tA.x - vB.x), scale * (tA.y - vB.y),
+                                                          scale * (tA.z - vB.z), scale * (tA.w - vB.w));
                         } else {
                             const uint4 sd = b == 0 ? sdp[R0 == 4 ? jj : 0]
                                                     : (a.skip1 ? make_uint4(0, 0, 0, 0) : tout[(4 * b + jj) * 256]);
@@ -766,7 +776,7 @@ __global__ void __launch_bounds__(512, 1) ftc_conv_kernel(const FtcArgs a) {
                         }
                         uint16_t* yr = a.y + roff + 2 * size_t(n0p + 8 * jj);
                         #pragma unroll
-                        for (int n0 = 0; n0 < NP; ++n0) {
+                        for (int n0 = 0; n0 < NB; ++n0) {
                             // y_z = conj(out): y[2n] = Re, y[2n+1] = -Im
                             float r0 = out[n0].x, r1 = out[n0].y, im0 = -out[n0].z, im1 = -out[n0].w;
                             if (GATED) {

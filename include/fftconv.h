@@ -380,19 +380,22 @@ fftconv_status_t fftconv_forward_circular(fftconv_plan_t plan, const void *u, co
  * convolution theorem on C points without zero padding or truncation):
  *   y[b,h,t] = sum_{j=0}^{C-1} u[b,h,j] k[h,(t-j) mod C]   (gated: w_out . conv(u . w_in, k))
  * A circular plan transforms C real samples as M = C/2 complex points
- * (z[n] = u[2n] + i u[2n+1]), factored R0 x 64 x 64 with R0 = C/8192: the
- * first outer pass reads all R0 rows of z (no zero half) and the last one
- * writes all R0 output rows; the 4096-point sub-rows, the fold with the
+ * (z[n] = u[2n] + i u[2n+1]), factored R0 x 64 x 64 with R0 = C/8192.
+ * C = 16384 runs on the fused kernel (path FUSED, no workspace: both
+ * 4096-point blocks of a row in shared memory); longer rows run multi-pass:
+ * the first outer pass reads all R0 rows of z (no zero half) and the last
+ * one writes all R0 output rows; the 4096-point sub-rows, the fold with the
  * kernel spectrum and the workspace are those of the multi-pass path.
  * - fftconv_circular_query: host only; C a power of two, 16384 <= C <= 2^19;
- *   info->N = C (samples per row), info->M = C/2.  Returns OK, INVALID
- *   (info NULL) or UNSUPPORTED.
+ *   info->N = C (samples per row), info->M = C/2, info->path FUSED for
+ *   C = 16384, else MULTIPASS.  Returns OK, INVALID (info NULL) or
+ *   UNSUPPORTED.
  * - fftconv_plan_create_circular: the plan (device tables on the current
  *   device).  On it, fftconv_kernel_fft and fftconv_kernel_fft_adjoint read
  *   k as [H][C] (all C taps of the circular kernel) and write k_f of
  *   fftconv_kf_bytes(plan, H) bytes; fftconv_forward and fftconv_forward_gated
- *   take u, w_in, w_out, y as device [B][H][C] and need a workspace of
- *   fftconv_workspace_bytes(plan, B, H) (= B H 2C) bytes
+ *   take u, w_in, w_out, y as device [B][H][C] and, on a multi-pass plan,
+ *   a workspace of fftconv_workspace_bytes(plan, B, H) (= B H 2C) bytes
  *   (fftconv_set_workspace); fftconv_backward_du(_gated) with the adjoint
  *   k_f gives the input gradient (the circular correlation).  The partial,
  *   windowed-circular and kernel-gradient calls return UNSUPPORTED.

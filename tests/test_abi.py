@@ -173,13 +173,17 @@ def test_product_path_does_not_touch_the_oracle():
 @pytest.mark.parametrize("C", [16384, 32768, 65536, 131072, 262144, 524288])
 def test_circular_query_factorization(C):
     """A circular plan of length C transforms M = C/2 points as R0 x 64 x 64
-    (R0 = C / 8192) on the multi-pass path; its rows hold C samples."""
+    (R0 = C / 8192): C = 16384 on the fused kernel (no workspace), longer
+    rows on the multi-pass path; its rows hold C samples."""
     for dt in (F.F16, F.BF16):
         q = F.circular_query(C, dt)
         R0 = C // 8192
         assert q["N"] == C and q["M"] == C // 2
-        assert q["path"] == F.PATH_MULTIPASS and q["order"] == 3 and q["factors"] == [R0, 64, 64]
-        assert q["workspace_bytes_per_row"] == 2 * C
+        assert q["order"] == 3 and q["factors"] == [R0, 64, 64]
+        if C == 16384:
+            assert q["path"] == F.PATH_FUSED and q["workspace_bytes_per_row"] == 0
+        else:
+            assert q["path"] == F.PATH_MULTIPASS and q["workspace_bytes_per_row"] == 2 * C
         # the k_f of the causal plan with the same transform (pairs of 4096-point sub-rows)
         if C // 2 >= 65536:
             assert q["kf_bytes_per_channel"] == F.query(C // 2, dt)["kf_bytes_per_channel"]

@@ -53,6 +53,7 @@ def test_host_matches_device(N, dtype, gated, B, H, order):
 
 
 @pytest.mark.parametrize("C,dtype,gated,B,H", [
+    (16384, "bf16", True, 2, 5),      # circular plan on the fused kernel
     (32768, "fp16", True, 3, 4),      # circular plan, chunks of batch entries
     (65536, "bf16", False, 1, 6),     # circular plan, B = 1: chunks of channels
 ])

@@ -64,7 +64,10 @@ def test_circular_shift_wraps_on_device():
 
 
 @pytest.mark.parametrize("C,dtype,gated,B,H", [
-    (16384, "fp16", True, 2, 3),      # R0 = 2: one pair of sub-rows
+    (16384, "fp16", True, 2, 3),      # R0 = 2, fused: one pair of sub-rows
+    (16384, "bf16", False, 3, 1),     # fused, an odd row count (one pipeline idle at the end)
+    (16384, "fp16", False, 4, 101),   # fused, 404 rows: several rows per CTA
+    (16384, "bf16", True, 2, 161),    # fused gated, 322 rows
     (32768, "bf16", False, 1, 3),     # R0 = 4
     (65536, "bf16", True, 1, 2),      # R0 = 8
     (131072, "fp16", False, 2, 1),    # R0 = 16
@@ -95,10 +98,11 @@ def test_native_circular_matches_oracle(C, dtype, gated, B, H):
     assert plan.device_status() == 0
 
 
-def test_native_circular_shift_and_adjoint():
+@pytest.mark.parametrize("C", [16384, 32768])
+def test_native_circular_shift_and_adjoint(C):
     """k = delta_s rolls each row by s; the adjoint k_f gives the circular
     correlation, i.e. the convolution with the reversed kernel k[-m mod C]."""
-    C, H = 32768, 3
+    H = 3
     plan = F.Plan(C, torch.float16, circular=True)
     shifts = [1, 12345, C - 1]
     k = torch.zeros(H, C, device="cuda")

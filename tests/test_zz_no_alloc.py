@@ -62,10 +62,11 @@ def test_noalloc_matches_forward_bitwise_on_two_calls(N, dtype):
     assert plan.device_status() == 0
 
 
-def test_noalloc_circular_plan_matches_forward_bitwise():
-    """A circular plan's rows (C samples, the multi-pass intermediate of C/2
-    complex points) through the fixed array."""
-    C, B, H = 65536, 2, 3
+@pytest.mark.parametrize("C", [16384, 65536])
+def test_noalloc_circular_plan_matches_forward_bitwise(C):
+    """A circular plan's rows (C samples; the fused kernel at 16384, the
+    multi-pass intermediate of C/2 complex points above) through the fixed array."""
+    B, H = 2, 3
     ins = _inputs(C, "bf16", B, H, seed=24)
     plan = F.Plan(C, torch.bfloat16, circular=True)
     kf = plan.kernel_fft(to_dev(ins["k"]))
