@@ -281,15 +281,20 @@ def run_reference(args, w: W.Workload):
     }))
 
 
-def path_of(plan_info: dict, pairs_run: Optional[int] = None) -> dict:
+def path_of(plan_info: dict, pairs_run: Optional[int] = None, pairs_total: Optional[int] = None) -> dict:
     """The kernels one step launches for a plan (names as in the sources);
     pass B is not launched when a frequency-sparse plan skips every pair."""
     if plan_info["path"] == 1:
         nb = 0 if pairs_run == 0 else 1
+        skips = pairs_run is not None and pairs_total is not None and pairs_run < pairs_total
         if plan_info["order"] == 4 and plan_info["factors"][3] == 64:  # outer factor in two HBM levels
-            return {"kernel": "mp_pass_a (RA) + otc_pass (64, in place) + mp_pass_b_tc + otc_pass (64, in place) "
-                              "+ mp_pass_c (RA) (the whole step)",
-                    "launches_per_step": 4 + nb}
+            if skips:
+                return {"kernel": "mp_pass_a (RA) + mp_pass_a (64, in place) + mp_pass_b_tc + mp_pass_c (64, in "
+                                  "place) + mp_pass_c (RA) (the whole step, frequency-sparse)",
+                        "launches_per_step": 4 + nb}
+            return {"kernel": "otc2_pass (A: RA in registers, 64 on tcgen05) + mp_pass_b_tc + otc2_pass (C) "
+                              "(the whole step)",
+                    "launches_per_step": 2 + nb}
         if plan_info["order"] == 3:
             return {"kernel": "otc_pass (A) + mp_pass_b_tc + otc_pass (C) (the whole step)",
                     "launches_per_step": 2 + nb}
@@ -554,7 +559,8 @@ def main():
     band = parse_band(args.band)
     plan = F.Plan(w.N, tdt, order=args.order, band=band)
     bd = plan.band()
-    path = path_of(plan.info, bd["pairs_run"] if band is not None else None)
+    path = path_of(plan.info, bd["pairs_run"] if band is not None else None,
+                   bd["pairs_total"] if band is not None else None)
     k = dev_t(ins["k"])
     kf = plan.kernel_fft(k)
     # the kernel spectrum is computed once per set of weights (outside the

@@ -404,6 +404,7 @@ std::vector<uint16_t> build_otc_fmat(int dtype) {
 // factor) and, for two levels, the in-place 64-point stages.
 struct OtcTables {
     std::vector<uint16_t> fa, fc, fa2, fc2;
+    std::vector<float> tw2;  // two levels: W_(64 RA)^(n_b k_a) / sqrt(RA) as (re, im), [k_a][n_b]
 };
 
 template <int R>
@@ -442,6 +443,14 @@ OtcTables build_otc_tables(int R, bool two_level, int dtype, bool full = false) 
     if (two_level) {
         t.fa2 = build_otc_fmat<64, 1>(dtype);
         t.fc2 = build_otc_fmat<64, 2>(dtype);
+        const double sc = 1.0 / std::sqrt(double(R));
+        t.tw2.resize(size_t(R) * 64 * 2);
+        for (int ka = 0; ka < R; ++ka)
+            for (int nb = 0; nb < 64; ++nb) {
+                const cd w = W(64 * R, int64_t(nb) * ka);
+                t.tw2[(size_t(ka) * 64 + nb) * 2] = float(w.r * sc);
+                t.tw2[(size_t(ka) * 64 + nb) * 2 + 1] = float(w.i * sc);
+            }
     }
     return t;
 }
@@ -697,6 +706,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
     if (otc) ot = build_otc_tables(p->mp2 ? info.factors[0] : p->R0, p->mp2, dtype, circular);
     const size_t o_tfa = otc ? append(blob, ot.fa) : 0, o_tfc = otc ? append(blob, ot.fc) : 0;
     const size_t o_tfa2 = (otc && p->mp2) ? append(blob, ot.fa2) : 0, o_tfc2 = (otc && p->mp2) ? append(blob, ot.fc2) : 0;
+    const size_t o_ttw2 = (otc && p->mp2) ? append(blob, ot.tw2) : 0;
     size_t o_ofa = 0, o_oic = 0, o_ofull = 0;
     if (multi && !circular) {
         o_ofa = append(blob, T0.of);
@@ -754,6 +764,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
         if (p->mp2) {
             p->otc_fa2 = d + o_tfa2;
             p->otc_fc2 = d + o_tfc2;
+            p->otc_tw2 = reinterpret_cast<const float2*>(d + o_ttw2);
         }
     }
     p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);

@@ -10,6 +10,7 @@
 #include "../../include/fftconv.h"
 #include "multipass.cuh"
 #include "otc.cuh"
+#include "otc2.cuh"
 
 struct fftconv_plan_s {
     fftconv_plan_info_t info;
@@ -32,6 +33,7 @@ struct fftconv_plan_s {
     const uint8_t* otc_fc = nullptr;
     const uint8_t* otc_fa2 = nullptr;
     const uint8_t* otc_fc2 = nullptr;
+    const float2* otc_tw2 = nullptr;  // two levels: W_(64 RA)^(n_b k_a) / sqrt(RA), [RA][64]
     const uint32_t* fmat = nullptr;  // the 64 x 64 DFT matrix rows (device), N = 4096 and mpL = 4096
     // frequency-sparse plan: a band per factor (every band >= M_j/2 + 1 on a
     // dense plan); on the multi-pass path the pass-B pairs that run and the
@@ -129,15 +131,15 @@ inline TensorMapEncoder tensor_map_encoder() {
 }
 
 // A tensor map over rows of `nin` sub-rows of L 32-bit words (row stride
-// row_bytes), read as boxes of 128 words x box_rows sub-rows (default: all
-// nin) x 1 row.
+// row_bytes), read as boxes of box_cols words (default 128) x box_rows
+// sub-rows (default: all nin) x 1 row.
 inline bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t L, uint64_t nin, uint64_t rows,
-                            uint64_t row_bytes, uint32_t box_rows = 0) {
+                            uint64_t row_bytes, uint32_t box_rows = 0, uint32_t box_cols = 128) {
     TensorMapEncoder enc = tensor_map_encoder();
     if (!enc || !base) return false;
     const cuuint64_t dims[3] = {L, nin, rows};
     const cuuint64_t strides[2] = {4 * L, row_bytes};
-    const cuuint32_t box[3] = {128, box_rows ? box_rows : cuuint32_t(nin), 1};
+    const cuuint32_t box[3] = {box_cols, box_rows ? box_rows : cuuint32_t(nin), 1};
     const cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -190,6 +192,42 @@ cudaError_t launch_otc(const fftconv_plan_s* p, const MPArgs& args, int64_t rows
     if (G && MODE == 0 && !encode_rows_map(&tgate, args.w_in, L, uin, uint64_t(rows), urow))
         return cudaErrorInvalidValue;
     fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, fmat, tin, tgate);
+    return cudaGetLastError();
+}
+
+// The fused two-level outer pass (otc2.cuh): pass A (FWD, from u) or pass C
+// (to y) over rows x (4096 / TC) column tiles, as many CTAs per SM as shared
+// and tensor memory hold.
+template <int DT, int RA, bool FWD, bool G>
+cudaError_t launch_otc2(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
+    using C = Otc2<RA>;
+    using P = Otc2Pass<RA, FWD, G>;
+    auto fn = otc2_pass<DT, RA, FWD, G>;
+    constexpr size_t smem = P::SMEM;
+    static_assert(smem <= 232448, "shared memory");
+    static PerDevice cache;  // per instantiation and device
+    int per_sm = 0;
+    cudaError_t e = prep_kernel(fn, smem, C::THREADS, cache, &per_sm);
+    if (e != cudaSuccess) return e;
+    per_sm = int(233472 / (smem + 1024));
+    if (per_sm > 512 / C::TMEM_COLS) per_sm = 512 / C::TMEM_COLS;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t items = rows * C::TILES;
+    int64_t grid = int64_t(p->num_sms) * per_sm;
+    if (grid > items) grid = items;
+    if (grid < 1) return cudaSuccess;
+    if (!p->otc_fa2 || !p->otc_fc2 || !p->otc_tw2) return cudaErrorInvalidValue;
+    CUtensorMap tin, tgate;
+    std::memset(&tgate, 0, sizeof(tgate));
+    // pass A: u as RA/2 x 64 sub-rows of 4096 words per row (2 M bytes);
+    // pass C: T as RA x 64 sub-rows per row (4 M bytes)
+    const bool ok = FWD ? encode_rows_map(&tin, args.u, C::L, P::NIN, uint64_t(rows), uint64_t(2) * C::M, P::BOXR, C::TC)
+                        : encode_rows_map(&tin, args.T, C::L, P::NIN, uint64_t(rows), uint64_t(4) * C::M, P::BOXR, C::TC);
+    if (!ok) return cudaErrorInvalidValue;
+    if (G && FWD &&
+        !encode_rows_map(&tgate, args.w_in, C::L, P::NIN, uint64_t(rows), uint64_t(2) * C::M, P::BOXR, C::TC))
+        return cudaErrorInvalidValue;
+    fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, FWD ? p->otc_fa2 : p->otc_fc2, p->otc_tw2, tin, tgate);
     return cudaGetLastError();
 }
 

@@ -18,7 +18,7 @@ F = pytest.importorskip("fft_long_convolution_gb300")
     (16384, 0, 1),
     (262144, 0, 3),      # passes A, B (tcgen05), C
     (262144, 4, 3),      # passes A, B (warp level), C
-    (2097152, 0, 5),     # two-level outer factor: A, A (in place), B, C (in place), C
+    (2097152, 0, 3),     # two-level outer factor, dense: fused A (RA and 64), B, fused C
 ])
 def test_launches_per_step(N, order, launches):
     info = F.query(N, F.BF16, order)
@@ -28,6 +28,15 @@ def test_launches_per_step(N, order, launches):
         # a sparse plan that skips every pair launches no pass B
         assert bench.path_of(info, 0)["launches_per_step"] == launches - 1
         assert bench.path_of(info, 3)["launches_per_step"] == launches
+
+
+def test_launches_per_step_two_level_sparse():
+    """A frequency-sparse two-level plan that skips pairs keeps the four
+    warp-level outer passes: A, A (in place), B, C (in place), C."""
+    info = F.query(2097152, F.BF16, 0)
+    assert bench.path_of(info, 40, 256)["launches_per_step"] == 5
+    assert bench.path_of(info, 0, 256)["launches_per_step"] == 4
+    assert bench.path_of(info, 256, 256)["launches_per_step"] == 3
 
 
 def test_algorithmic_bytes():

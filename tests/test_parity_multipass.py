@@ -27,7 +27,9 @@ def _need_gpu():
     (262144, "bf16", True, 1, 2),
     (524288, "fp16", False, 1, 1),
     (1048576, "bf16", False, 1, 1),
+    (1048576, "fp16", True, 2, 3),    # two-level RA = 4, gated, six rows
     (2097152, "bf16", False, 1, 1),
+    (2097152, "fp16", True, 1, 2),    # two-level RA = 8, gated
 ])
 def test_multipass_matches_oracle(N, dtype, gated, B, H):
     w = W.Workload("t", B, H, N, dtype, gated, "normal", "decay", "")
