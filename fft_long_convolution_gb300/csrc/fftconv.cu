@@ -404,7 +404,10 @@ std::vector<uint16_t> build_otc_fmat(int dtype) {
 // factor) and, for two levels, the in-place 64-point stages.
 struct OtcTables {
     std::vector<uint16_t> fa, fc, fa2, fc2;
-    std::vector<float> tw2;  // two levels: W_(64 RA)^(n_b k_a) / sqrt(RA) as (re, im), [k_a][n_b]
+    // two levels: W_(64 RA)^(n_b k_a) / sqrt(RA) as packed pairs (re, re', im,
+    // im'): pass A's [k_a < RA/2][n_b] (pairs k_a, k_a + RA/2), then pass C's
+    // [k_a][n_b / 2] (pairs n_b, n_b + 1)
+    std::vector<float> tw2;
 };
 
 template <int R>
@@ -444,13 +447,20 @@ OtcTables build_otc_tables(int R, bool two_level, int dtype, bool full = false) 
         t.fa2 = build_otc_fmat<64, 1>(dtype);
         t.fc2 = build_otc_fmat<64, 2>(dtype);
         const double sc = 1.0 / std::sqrt(double(R));
-        t.tw2.resize(size_t(R) * 64 * 2);
+        auto tw = [&](int ka, int nb) {
+            const cd w = W(64 * R, int64_t(nb) * ka);
+            return cd{w.r * sc, w.i * sc};
+        };
+        auto put = [&](cd a, cd b) {
+            t.tw2.push_back(float(a.r));
+            t.tw2.push_back(float(b.r));
+            t.tw2.push_back(float(a.i));
+            t.tw2.push_back(float(b.i));
+        };
+        for (int kp = 0; kp < R / 2; ++kp)
+            for (int nb = 0; nb < 64; ++nb) put(tw(kp, nb), tw(kp + R / 2, nb));
         for (int ka = 0; ka < R; ++ka)
-            for (int nb = 0; nb < 64; ++nb) {
-                const cd w = W(64 * R, int64_t(nb) * ka);
-                t.tw2[(size_t(ka) * 64 + nb) * 2] = float(w.r * sc);
-                t.tw2[(size_t(ka) * 64 + nb) * 2 + 1] = float(w.i * sc);
-            }
+            for (int nb = 0; nb < 64; nb += 2) put(tw(ka, nb), tw(ka, nb + 1));
     }
     return t;
 }
@@ -764,7 +774,7 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
         if (p->mp2) {
             p->otc_fa2 = d + o_tfa2;
             p->otc_fc2 = d + o_tfc2;
-            p->otc_tw2 = reinterpret_cast<const float2*>(d + o_ttw2);
+            p->otc_tw2 = reinterpret_cast<const float4*>(d + o_ttw2);
         }
     }
     p->tb.lf = reinterpret_cast<const uint4*>(d + o_lf);

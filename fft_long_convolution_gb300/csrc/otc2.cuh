@@ -58,7 +58,10 @@ struct Otc2 {
     // element (row, k) at (row/8) SBO + (k/8) LBO + (row%8) 16 + (k%8) 2 bytes
     static constexpr uint32_t LBO = 128, SBO = 16 * 128;
     static constexpr uint32_t ABYTES = 16 * SBO, BBYTES = 16 * SBO;
-    static constexpr uint32_t TABB = uint32_t(RA) * 64 * 8;  // W_(64 RA)^(n_b k_a) / sqrt(RA), [k_a][n_b]
+    // W_(64 RA)^(n_b k_a) / sqrt(RA) as pairs (re, re', im, im') for packed
+    // f32x2 products: pass A pairs k_a with k_a + RA/2, [k_a < RA/2][n_b];
+    // pass C pairs n_b with n_b + 1, [k_a][n_b / 2]
+    static constexpr uint32_t TABB = uint32_t(RA) * 64 * 8;
     static constexpr int TMEM_COLS = 128;                    // one accumulator of 128 float32 columns
 };
 
@@ -139,12 +142,25 @@ __device__ __forceinline__ void otc2_half_radix(const cpx (&v)[RA], cpx (&out)[R
     }
 }
 
-// fmat: the 64-point DFT matrix / 8 as the B operand; tab: W_(64 RA)^(n_b
-// k_a) / sqrt(RA), [k_a][n_b]; tin: pass A u as 32-bit words [rows][RA/2
+// Word index of the parked value (k_a, n_b, column c) of pass C in the A
+// space (RA x 64 x TC words).  RA = 8 (TC = 16): rows of 32 words hold k_a
+// pairs, the half of a row swapped by bit 2 of n_b, so that the epilogue's
+// warps (two k_a, 16 columns, one n_b) and the last phase's (one k_a, 16
+// columns, n_b four apart) each touch 32 distinct banks.
+template <int RA>
+__device__ __forceinline__ int otc2_park(int ka, int nb, int c) {
+    if constexpr (RA == 8)
+        return (((ka >> 1) * 64 + nb) << 5) + ((((ka & 1) ^ (nb >> 2)) & 1) << 4) + c;
+    else
+        return ((ka * 64 + nb) << 5) + c;
+}
+
+// fmat: the 64-point DFT matrix / 8 as the B operand; tab: this pass's
+// W_(64 RA)^(n_b k_a) / sqrt(RA) pairs (Otc2::TABB bytes); tin: pass A u as 32-bit words [rows][RA/2
 // x 64][4096], pass C T [rows][RA x 64][4096]; tgate: w_in in u's shape.
 template <int DT, int RA, bool FWD, bool GATED>
 __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_t* __restrict__ fmat,
-                                                 const float2* __restrict__ tab,
+                                                 const float4* __restrict__ tab,
                                                  const __grid_constant__ CUtensorMap tin,
                                                  const __grid_constant__ CUtensorMap tgate) {
     using O = Op<DT>;
@@ -157,7 +173,7 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
     uint8_t* sf = smem + P::OFF_B;                                       // DFT matrix
     uint32_t* st = reinterpret_cast<uint32_t*>(smem + P::OFF_ST);        // [NST][NIN][TC]
     uint32_t* sw = st + P::NST * P::STAGE_WORDS;                         // pass A gated: w_in
-    const float2* s_tab = reinterpret_cast<const float2*>(smem + P::OFF_TAB);
+    const float4* s_tab = reinterpret_cast<const float4*>(smem + P::OFF_TAB);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::OFF_BAR);     // [NST]
     uint64_t* mbar = full + P::NST;                                      // contraction done
     uint64_t* fbar = mbar + 1;                                           // matrix and table arrived
@@ -240,10 +256,11 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
                     cpx X[RA];
                     otc2_fwd_radix<RA>(x, X);
                     #pragma unroll
-                    for (int ka = 0; ka < RA; ++ka) {
-                        const float2 tw = s_tab[ka * 64 + nb];
-                        const cpx v = cmul(X[ka], {tw.x, tw.y});
-                        w[ka][i] = O::pack(v.r, v.i);
+                    for (int kp = 0; kp < C::NA; ++kp) {  // k_a = kp and kp + RA/2, packed
+                        const float4 v = cmul2_split(X[kp].r, X[kp + C::NA].r, X[kp].i, X[kp + C::NA].i,
+                                                     s_tab[kp * 64 + nb]);
+                        w[kp][i] = O::pack(v.x, v.z);
+                        w[kp + C::NA][i] = O::pack(v.y, v.w);
                     }
                 }
                 #pragma unroll
@@ -256,27 +273,38 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
                             make_uint4(w[ka][4 * q], w[ka][4 * q + 1], w[ka][4 * q + 2], w[ka][4 * q + 3]);
                 }
             } else {
-                // W_M^(n_c k0), k0 = k_a + RA k_b: steps along k_a and along k_b
+                // W_M^(n_c k0), k0 = k_a + RA k_b, for k_a = 2 kp and 2 kp + 1 as a
+                // packed pair: steps W_M^(RA n_c) along k_b, W_M^(2 n_c) along kp
                 const cpx a1 = twiddle_pow2(n_c, M);
                 const cpx stp = twiddle_pow2((uint32_t(RA) * n_c) & (M - 1), M);
-                cpx tka = twiddle_pow2((n_c * uint32_t(RA * nb0)) & (M - 1), M);
-                #pragma unroll 2
-                for (int ka = 0; ka < RA; ++ka) {
-                    uint32_t w[NBT];
-                    cpx tw = tka;
+                const cpx t0 = twiddle_pow2((n_c * uint32_t(RA * nb0)) & (M - 1), M);
+                const cpx t1 = cmul(t0, a1), a2 = cmul(a1, a1);
+                float4 tp = make_float4(t0.r, t1.r, t0.i, t1.i);
+                const float4 s4 = make_float4(stp.r, stp.r, stp.i, stp.i), a24 = make_float4(a2.r, a2.r, a2.i, a2.i);
+                #pragma unroll 1
+                for (int kp = 0; kp < RA / 2; ++kp) {
+                    uint32_t w0[NBT], w1[NBT];
+                    float4 tw = tp;
                     #pragma unroll
                     for (int i = 0; i < NBT; ++i) {
-                        const cpx v = cmul(O::unpack(sts[(64 * ka + nb0 + i) * TC]), tw);
-                        w[i] = O::pack(v.r, v.i);
-                        tw = cmul(tw, stp);
+                        const cpx x0 = O::unpack(sts[(64 * (2 * kp) + nb0 + i) * TC]);
+                        const cpx x1 = O::unpack(sts[(64 * (2 * kp + 1) + nb0 + i) * TC]);
+                        const float4 v = cmul2_split(x0.r, x1.r, x0.i, x1.i, tw);
+                        w0[i] = O::pack(v.x, v.z);
+                        w1[i] = O::pack(v.y, v.w);
+                        if (i + 1 < NBT) tw = cmul2_split(tw.x, tw.y, tw.z, tw.w, s4);
                     }
-                    tka = cmul(tka, a1);
-                    const int m = ka * TC + c;
-                    uint8_t* arow = sa + (m >> 3) * C::SBO + (m & 7) * 16;
+                    tp = cmul2_split(tp.x, tp.y, tp.z, tp.w, a24);
                     #pragma unroll
-                    for (int q = 0; q < NBT / 4; ++q)
-                        *reinterpret_cast<uint4*>(arow + (nb0 / 4 + q) * C::LBO) =
-                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int m = (2 * kp + h) * TC + c;
+                        uint8_t* arow = sa + (m >> 3) * C::SBO + (m & 7) * 16;
+                        const uint32_t* wv = h ? w1 : w0;
+                        #pragma unroll
+                        for (int q = 0; q < NBT / 4; ++q)
+                            *reinterpret_cast<uint4*>(arow + (nb0 / 4 + q) * C::LBO) =
+                                make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+                    }
                 }
             }
         }
@@ -313,10 +341,17 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
         // ---------------- epilogue: outputs [EOUT eh, EOUT eh + EOUT) of row (eka, ec)
         const uint32_t n_ce = uint32_t(o_base + ec);
         if constexpr (FWD) {
-            // W_M^(n_c (k_a + RA k_b)) along k_b
+            // W_M^(n_c (k_a + RA k_b)) along k_b: in each chunk of 16 outputs,
+            // outputs j and j + 8 as a packed pair of product chains
             const uint32_t k00 = uint32_t(eka + RA * EOUT * eh);
-            cpx tw = twiddle_pow2((n_ce * k00) & (M - 1), M);
-            const cpx stp = twiddle_pow2((uint32_t(RA) * n_ce) & (M - 1), M);
+            const cpx ta = twiddle_pow2((n_ce * k00) & (M - 1), M);
+            const cpx sp = twiddle_pow2((uint32_t(RA) * n_ce) & (M - 1), M);
+            cpx s8 = cmul(sp, sp);
+            s8 = cmul(s8, s8);
+            s8 = cmul(s8, s8);  // W_M^(8 RA n_c)
+            const cpx tb = cmul(ta, s8);
+            float4 tw = make_float4(ta.r, tb.r, ta.i, tb.i);
+            const float4 st4 = make_float4(sp.r, sp.r, sp.i, sp.i), s84 = make_float4(s8.r, s8.r, s8.i, s8.i);
             uint32_t* trow = a.T + row * long(M) + long(64 * eka + EOUT * eh) * C::L + n_ce;
             #pragma unroll
             for (int c0 = 0; c0 < EOUT; c0 += 16) {
@@ -324,14 +359,18 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
                 tc::ld32x32b_x32(tmem + (uint32_t(32 * eq) << 16) + uint32_t(2 * (EOUT * eh + c0)), vv);
                 tc::wait_ld();
                 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const cpx x = cmul({__uint_as_float(vv[2 * j]), __uint_as_float(vv[2 * j + 1])}, tw);
-                    tw = cmul(tw, stp);
-                    trow[long(c0 + j) * C::L] = O::pack(x.r, x.i);
+                for (int j = 0; j < 8; ++j) {
+                    const float4 x = cmul2_split(__uint_as_float(vv[2 * j]), __uint_as_float(vv[2 * j + 16]),
+                                                 __uint_as_float(vv[2 * j + 1]), __uint_as_float(vv[2 * j + 17]), tw);
+                    tw = cmul2_split(tw.x, tw.y, tw.z, tw.w, st4);
+                    trow[long(c0 + j) * C::L] = O::pack(x.x, x.z);
+                    trow[long(c0 + j + 8) * C::L] = O::pack(x.y, x.w);
                 }
+                // (outputs c0 + 8, c0 + 16) -> (c0 + 16, c0 + 24)
+                if (c0 + 16 < EOUT) tw = cmul2_split(tw.x, tw.y, tw.z, tw.w, s84);
             }
         } else {
-            // W_(64 RA)^(n_b k_a) / sqrt(RA), parked as [k_a][n_b][c] in the A space
+            // W_(64 RA)^(n_b k_a) / sqrt(RA) on pairs (n_b, n_b + 1), parked in the A space
             uint32_t* park = reinterpret_cast<uint32_t*>(sa);
             #pragma unroll
             for (int c0 = 0; c0 < EOUT; c0 += 16) {
@@ -339,11 +378,13 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
                 tc::ld32x32b_x32(tmem + (uint32_t(32 * eq) << 16) + uint32_t(2 * (EOUT * eh + c0)), vv);
                 tc::wait_ld();
                 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < 16; j += 2) {
                     const int nb = EOUT * eh + c0 + j;
-                    const float2 tw = s_tab[eka * 64 + nb];
-                    const cpx x = cmul({__uint_as_float(vv[2 * j]), __uint_as_float(vv[2 * j + 1])}, {tw.x, tw.y});
-                    park[(64 * eka + nb) * TC + ec] = O::pack(x.r, x.i);
+                    const float4 x = cmul2_split(__uint_as_float(vv[2 * j]), __uint_as_float(vv[2 * j + 2]),
+                                                 __uint_as_float(vv[2 * j + 1]), __uint_as_float(vv[2 * j + 3]),
+                                                 s_tab[eka * 32 + nb / 2]);
+                    park[otc2_park<RA>(eka, nb, ec)] = O::pack(x.x, x.z);
+                    park[otc2_park<RA>(eka, nb + 1, ec)] = O::pack(x.y, x.w);
                 }
             }
         }
@@ -358,7 +399,7 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
                 const int nb = nb0 + i;
                 cpx v[RA];
                 #pragma unroll
-                for (int ka = 0; ka < RA; ++ka) v[ka] = O::unpack(park[(64 * ka + nb) * TC]);
+                for (int ka = 0; ka < RA; ++ka) v[ka] = O::unpack(park[otc2_park<RA>(ka, nb, 0)]);
                 cpx out[C::NA];
                 otc2_half_radix<RA>(v, out);
                 #pragma unroll

@@ -33,7 +33,9 @@ struct fftconv_plan_s {
     const uint8_t* otc_fc = nullptr;
     const uint8_t* otc_fa2 = nullptr;
     const uint8_t* otc_fc2 = nullptr;
-    const float2* otc_tw2 = nullptr;  // two levels: W_(64 RA)^(n_b k_a) / sqrt(RA), [RA][64]
+    // two levels: W_(64 RA)^(n_b k_a) / sqrt(RA) as packed pairs, pass A's
+    // table then pass C's (Otc2::TABB bytes each)
+    const float4* otc_tw2 = nullptr;
     const uint32_t* fmat = nullptr;  // the 64 x 64 DFT matrix rows (device), N = 4096 and mpL = 4096
     // frequency-sparse plan: a band per factor (every band >= M_j/2 + 1 on a
     // dense plan); on the multi-pass path the pass-B pairs that run and the
@@ -227,7 +229,8 @@ cudaError_t launch_otc2(const fftconv_plan_s* p, const MPArgs& args, int64_t row
     if (G && FWD &&
         !encode_rows_map(&tgate, args.w_in, C::L, P::NIN, uint64_t(rows), uint64_t(2) * C::M, P::BOXR, C::TC))
         return cudaErrorInvalidValue;
-    fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, FWD ? p->otc_fa2 : p->otc_fc2, p->otc_tw2, tin, tgate);
+    const float4* tab = p->otc_tw2 + (FWD ? 0 : C::TABB / 16);
+    fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, FWD ? p->otc_fa2 : p->otc_fc2, tab, tin, tgate);
     return cudaGetLastError();
 }
 
