@@ -41,17 +41,15 @@ cudaError_t launch_r(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, 
     return cudaErrorInvalidValue;
 }
 
-// Two-level outer factor R0 = RA * 64 (N = RA * 64 * 64 * 64): pass B on
-// sub-rows of 4096 (sub-row k0 = a + RA k at position 64 a + k).  Dense
-// plans run each outer direction as one tensor-core pass (otc2.cuh: the
-// RA-point level in registers, the 64-point level as the contraction).
-// Frequency-sparse plans keep four warp-level passes: pass A over RA
-// sub-blocks of L1 = N / RA, the inner 64-point stage in place (all inputs,
-// dead sub-rows not stored), the inner inverse stage in place (dead sub-rows
-// read as zeros), the last pass over RA.
+// Two-level outer factor R0 = RA * 64 (N = RA * 64 * 64 * 64): each outer
+// direction is one tensor-core pass (otc2.cuh: the RA-point level in
+// registers, the 64-point level as the contraction), pass B on sub-rows of
+// 4096 (sub-row k0 = a + RA k at position 64 a + k).  Frequency-sparse plans
+// (SP) skip the dead sub-rows in the outer passes and run only the live
+// pairs in pass B.
 template <int DT, int RA, bool G, bool SP>
 cudaError_t launch_2l_t(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
-    constexpr int L = kMpLtc, L1 = 64 * L, R0 = RA * 64;  // N = RA * L1
+    constexpr int R0 = RA * 64;
     static PerDevice cb;
     int nb = 0;
     cudaError_t e;
@@ -59,45 +57,11 @@ cudaError_t launch_2l_t(const fftconv_plan_s* p, const MPArgs& args, int64_t row
     const int64_t items_b = rows * p->pairs_run, need_b = (items_b + 1) / 2;
     if (items_b >= (int64_t(1) << 30) || rows * RA >= (int64_t(1) << 30)) return cudaErrorInvalidValue;
     const unsigned grid_b = unsigned(need_b < p->num_sms ? need_b : p->num_sms);
-    MPArgs outer = args;  // the RA-point levels see no dead sub-rows
-    outer.zbits = nullptr;
     TcBArgs b{args.T, args.kf, p->fmat, args.B, args.H, R0, args.err, RA, p->pairs_run, p->plist};
-    if constexpr (!SP) {
-        if ((e = launch_otc2<DT, RA, true, G>(p, outer, rows, st)) != cudaSuccess) return e;
-        if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        return launch_otc2<DT, RA, false, G>(p, outer, rows, st);
-    } else {
-        const size_t smem_a1 = mp_pass_a_smem<RA, G>(), smem_c1 = mp_pass_c_smem<RA, G>();
-        const size_t smem_a2 = mp_pass_a_smem<64, false, true>(), smem_c2 = mp_pass_c_smem<64, false>();
-        static PerDevice ca1, ca2, cc2, cc1;
-        int na1 = 0, na2 = 0, nc2 = 0, nc1 = 0;
-        if ((e = prep_kernel(mp_pass_a<DT, RA, G, L1>, smem_a1, 256, ca1, &na1)) != cudaSuccess) return e;
-        if ((e = prep_kernel(mp_pass_a<DT, 64, false, L, true, SP>, smem_a2, 256, ca2, &na2)) != cudaSuccess)
-            return e;
-        if ((e = prep_kernel(mp_pass_c<DT, 64, false, L, true, true, SP>, smem_c2, 32 * mp_pass_c_warps<64>(), cc2,
-                             &nc2)) != cudaSuccess)
-            return e;
-        if ((e = prep_kernel(mp_pass_c<DT, RA, G, L1, true>, smem_c1, 32 * mp_pass_c_warps<RA>(), cc1, &nc1)) !=
-            cudaSuccess)
-            return e;
-        auto grid = [&](int64_t items, int per_sm) {
-            int64_t gsz = int64_t(p->num_sms) * per_sm;
-            return unsigned(gsz < items ? gsz : items);
-        };
-        const int64_t items1 = rows * (L1 / mp_tile<RA>()), items2 = rows * RA * (L / mp_tile<64>());
-        MPArgs inner = args;  // the RA sub-blocks of every row as rows of length 64 * 4096
-        inner.B = args.B * RA;
-        inner.w_in = inner.w_out = nullptr;
-        inner.zmod = RA;  // inner row r holds sub-rows k0 = (r mod RA) + RA j, j < 64
-        mp_pass_a<DT, RA, G, L1><<<grid(items1, na1), 256, smem_a1, st>>>(outer);
-        mp_pass_a<DT, 64, false, L, true, SP><<<grid(items2, na2), 256, smem_a2, st>>>(inner);
-        if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
-        mp_pass_c<DT, 64, false, L, true, true, SP>
-            <<<grid(items2, nc2), 32 * mp_pass_c_warps<64>(), smem_c2, st>>>(inner);
-        mp_pass_c<DT, RA, G, L1, true><<<grid(items1, nc1), 32 * mp_pass_c_warps<RA>(), smem_c1, st>>>(outer);
-        return cudaGetLastError();
-    }
+    if ((e = launch_otc2<DT, RA, true, G, SP>(p, args, rows, st)) != cudaSuccess) return e;
+    if (items_b > 0) mp_pass_b_tc<DT, SP><<<grid_b, TcB::THREADS, TcB::SMEM, st>>>(b);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return launch_otc2<DT, RA, false, G, SP>(p, args, rows, st);
 }
 
 template <int DT, bool G, bool SP>

@@ -40,6 +40,7 @@
 #include <cuda.h>
 
 #include "multipass.cuh"
+#include "otc.cuh"
 #include "tc.cuh"
 
 namespace fftconv {
@@ -155,14 +156,38 @@ __device__ __forceinline__ int otc2_park(int ka, int nb, int c) {
         return ((ka * 64 + nb) << 5) + c;
 }
 
+// Frequency-sparse plans (SP): the sub-rows whose pass-B pair is skipped
+// (bit k_b of zbits[2 k_a], never written by pass B) are not stored by pass
+// A and read as zeros by pass C, which copies, per k_a, only the one or two
+// runs of live rows as boxes of `box` rows (a box may cover dead rows).
+// Returns the boxes of k_a with dead bits z (0, 1 or 2) and their first
+// rows; the host takes `box` as the largest run any k_a needs (64 where a
+// k_a has more than two runs).
+__host__ __device__ inline int otc2_boxes(unsigned long long z, int box, int (&start)[2]) {
+    const OtcRuns r = otc_live_runs(z, 0ull, 64);
+    start[0] = start[1] = 0;
+    if (r.n == 0) return r.box > 0 ? 1 : 0;
+    for (int i = 0; i < r.n; ++i) start[i] = r.start[i] < 64 - box ? r.start[i] : 64 - box;
+    return r.n;
+}
+inline int otc2_box_rows(const unsigned long long* zbits, int RA) {
+    int box = 0;
+    for (int ka = 0; ka < RA; ++ka) {
+        const OtcRuns r = otc_live_runs(zbits[2 * ka], 0ull, 64);
+        const int need = r.n ? r.box : (r.box > 0 ? 64 : 0);
+        box = need > box ? need : box;
+    }
+    return box;
+}
+
 // fmat: the 64-point DFT matrix / 8 as the B operand; tab: this pass's
 // W_(64 RA)^(n_b k_a) / sqrt(RA) pairs (Otc2::TABB bytes); tin: pass A u as 32-bit words [rows][RA/2
 // x 64][4096], pass C T [rows][RA x 64][4096]; tgate: w_in in u's shape.
-template <int DT, int RA, bool FWD, bool GATED>
+template <int DT, int RA, bool FWD, bool GATED, bool SP = false>
 __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_t* __restrict__ fmat,
                                                  const float4* __restrict__ tab,
                                                  const __grid_constant__ CUtensorMap tin,
-                                                 const __grid_constant__ CUtensorMap tgate) {
+                                                 const __grid_constant__ CUtensorMap tgate, int box) {
     using O = Op<DT>;
     using C = Otc2<RA>;
     using P = Otc2Pass<RA, FWD, GATED>;
@@ -184,14 +209,37 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
     const long items = rows * C::TILES;
     const long first_item = blockIdx.x, stride = gridDim.x;
 
+    // SP pass C: the boxes of live rows per k_a (thread 0 issues the copies)
+    constexpr bool SPC = SP && !FWD;
+    int nbx[SPC ? RA : 1] = {}, bst[SPC ? RA : 1][2] = {};
+    uint32_t sp_bytes = 0;
+    if constexpr (SPC) {
+        if (t == 0) {
+            #pragma unroll
+            for (int ka = 0; ka < RA; ++ka) {
+                nbx[ka] = otc2_boxes(a.zbits[2 * ka], box, bst[ka]);
+                sp_bytes += uint32_t(nbx[ka] * box * TC) * 4u;
+            }
+        }
+    }
     auto stage = [&](long item, int s) {
         const int row = int(item / C::TILES);
         const int o_base = int(item % C::TILES) * TC;
-        mbar_expect_tx(&full[s], P::STAGE_WORDS * 4u * (P::NGATE ? 2u : 1u));
-        #pragma unroll
-        for (int bx = 0; bx < P::NBOX; ++bx)
-            tma_load_3d(st + s * P::STAGE_WORDS + bx * P::BOXR * TC, &tin, o_base, bx * P::BOXR, row, &full[s]);
-        if constexpr (P::NGATE > 0) tma_load_3d(sw + s * P::STAGE_WORDS, &tgate, o_base, 0, row, &full[s]);
+        if constexpr (SPC) {
+            mbar_expect_tx(&full[s], sp_bytes);
+            #pragma unroll
+            for (int ka = 0; ka < RA; ++ka)
+                for (int i = 0; i < nbx[ka]; ++i) {
+                    const int r0 = 64 * ka + bst[ka][i];
+                    tma_load_3d(st + s * P::STAGE_WORDS + r0 * TC, &tin, o_base, r0, row, &full[s]);
+                }
+        } else {
+            mbar_expect_tx(&full[s], P::STAGE_WORDS * 4u * (P::NGATE ? 2u : 1u));
+            #pragma unroll
+            for (int bx = 0; bx < P::NBOX; ++bx)
+                tma_load_3d(st + s * P::STAGE_WORDS + bx * P::BOXR * TC, &tin, o_base, bx * P::BOXR, row, &full[s]);
+            if constexpr (P::NGATE > 0) tma_load_3d(sw + s * P::STAGE_WORDS, &tgate, o_base, 0, row, &full[s]);
+        }
     };
 
     uint32_t issued = 0;
@@ -285,10 +333,14 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
                 for (int kp = 0; kp < RA / 2; ++kp) {
                     uint32_t w0[NBT], w1[NBT];
                     float4 tw = tp;
+                    // SP: the dead sub-rows of this pair of k_a (never written by pass B) read as zero
+                    const unsigned long long za = SP ? __ldg(a.zbits + 4 * kp) >> nb0 : 0ull;
+                    const unsigned long long zc = SP ? __ldg(a.zbits + 4 * kp + 2) >> nb0 : 0ull;
                     #pragma unroll
                     for (int i = 0; i < NBT; ++i) {
-                        const cpx x0 = O::unpack(sts[(64 * (2 * kp) + nb0 + i) * TC]);
-                        const cpx x1 = O::unpack(sts[(64 * (2 * kp + 1) + nb0 + i) * TC]);
+                        const uint32_t r0 = ((za >> i) & 1ull) ? 0u : sts[(64 * (2 * kp) + nb0 + i) * TC];
+                        const uint32_t r1 = ((zc >> i) & 1ull) ? 0u : sts[(64 * (2 * kp + 1) + nb0 + i) * TC];
+                        const cpx x0 = O::unpack(r0), x1 = O::unpack(r1);
                         const float4 v = cmul2_split(x0.r, x1.r, x0.i, x1.i, tw);
                         w0[i] = O::pack(v.x, v.z);
                         w1[i] = O::pack(v.y, v.w);
@@ -353,6 +405,8 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
             float4 tw = make_float4(ta.r, tb.r, ta.i, tb.i);
             const float4 st4 = make_float4(sp.r, sp.r, sp.i, sp.i), s84 = make_float4(s8.r, s8.r, s8.i, s8.i);
             uint32_t* trow = a.T + row * long(M) + long(64 * eka + EOUT * eh) * C::L + n_ce;
+            // SP: sub-rows of skipped pass-B pairs are not stored
+            const uint32_t md = SP ? uint32_t(__ldg(a.zbits + 2 * eka) >> (EOUT * eh)) : 0u;
             #pragma unroll
             for (int c0 = 0; c0 < EOUT; c0 += 16) {
                 uint32_t vv[32];
@@ -363,8 +417,8 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
                     const float4 x = cmul2_split(__uint_as_float(vv[2 * j]), __uint_as_float(vv[2 * j + 16]),
                                                  __uint_as_float(vv[2 * j + 1]), __uint_as_float(vv[2 * j + 17]), tw);
                     tw = cmul2_split(tw.x, tw.y, tw.z, tw.w, st4);
-                    trow[long(c0 + j) * C::L] = O::pack(x.x, x.z);
-                    trow[long(c0 + j + 8) * C::L] = O::pack(x.y, x.w);
+                    if (!((md >> (c0 + j)) & 1u)) trow[long(c0 + j) * C::L] = O::pack(x.x, x.z);
+                    if (!((md >> (c0 + j + 8)) & 1u)) trow[long(c0 + j + 8) * C::L] = O::pack(x.y, x.w);
                 }
                 // (outputs c0 + 8, c0 + 16) -> (c0 + 16, c0 + 24)
                 if (c0 + 16 < EOUT) tw = cmul2_split(tw.x, tw.y, tw.z, tw.w, s84);

@@ -83,13 +83,18 @@ def test_multipass_sparse_skips_pairs(N, dtype, gated, B, H, band):
     assert 0 < bd["pairs_run"] < bd["pairs_total"]
 
 
-@pytest.mark.parametrize("N,dtype,band", [
-    (1048576, "bf16", [2, 16, 33, 33]),   # two HBM levels: first-level digits 0, +-1 of 4
-    (2097152, "bf16", [5, 9, 33, 20]),
-    (2097152, "fp16", [1, 33, 33, 33]),   # first-level digit 0 only: 32 of 256 pairs run
+@pytest.mark.parametrize("N,dtype,gated,B,H,band", [
+    (1048576, "bf16", False, 1, 1, [2, 16, 33, 33]),   # two HBM levels: first-level digits 0, +-1 of 4
+    (2097152, "bf16", False, 1, 1, [5, 9, 33, 20]),
+    (2097152, "fp16", False, 1, 1, [1, 33, 33, 33]),   # first-level digit 0 only: 32 of 256 pairs run
+    (1048576, "fp16", True, 2, 3, [2, 9, 33, 33]),     # gated, six rows; live runs of 9 and 8 rows per k_a
+    (2097152, "bf16", True, 1, 2, [8, 5, 33, 33]),     # every k_a live, runs of 5 and 4 rows
 ])
-def test_two_level_sparse(N, dtype, band):
-    bd = _check(N, dtype, False, 1, 1, band)
+def test_two_level_sparse(N, dtype, gated, B, H, band):
+    """The fused outer passes of a two-level plan skip dead sub-rows: pass A
+    does not store them, pass C copies only the runs of live rows of every
+    k_a and reads the rest as zeros."""
+    bd = _check(N, dtype, gated, B, H, band)
     assert 0 < bd["pairs_run"] < bd["pairs_total"]
 
 
