@@ -737,8 +737,6 @@ fftconv_status_t plan_create_impl(fftconv_plan_t* out, int64_t N, fftconv_dtype_
                 p->zhost[0] = sp.zero[0];
                 p->zhost[1] = sp.zero[1];
                 o_zc = append(blob, std::vector<unsigned long long>{sp.zero[0], sp.zero[1]});
-            } else {  // the fused last pass copies the live runs of every k_a
-                p->otc2_box = otc2_box_rows(sp.zbits.data(), info.factors[0]);
             }
         }
     }

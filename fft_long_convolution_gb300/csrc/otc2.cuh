@@ -40,7 +40,6 @@
 #include <cuda.h>
 
 #include "multipass.cuh"
-#include "otc.cuh"
 #include "tc.cuh"
 
 namespace fftconv {
@@ -158,27 +157,10 @@ __device__ __forceinline__ int otc2_park(int ka, int nb, int c) {
 
 // Frequency-sparse plans (SP): the sub-rows whose pass-B pair is skipped
 // (bit k_b of zbits[2 k_a], never written by pass B) are not stored by pass
-// A and read as zeros by pass C, which copies, per k_a, only the one or two
-// runs of live rows as boxes of `box` rows (a box may cover dead rows).
-// Returns the boxes of k_a with dead bits z (0, 1 or 2) and their first
-// rows; the host takes `box` as the largest run any k_a needs (64 where a
-// k_a has more than two runs).
-__host__ __device__ inline int otc2_boxes(unsigned long long z, int box, int (&start)[2]) {
-    const OtcRuns r = otc_live_runs(z, 0ull, 64);
-    start[0] = start[1] = 0;
-    if (r.n == 0) return r.box > 0 ? 1 : 0;
-    for (int i = 0; i < r.n; ++i) start[i] = r.start[i] < 64 - box ? r.start[i] : 64 - box;
-    return r.n;
-}
-inline int otc2_box_rows(const unsigned long long* zbits, int RA) {
-    int box = 0;
-    for (int ka = 0; ka < RA; ++ka) {
-        const OtcRuns r = otc_live_runs(zbits[2 * ka], 0ull, 64);
-        const int need = r.n ? r.box : (r.box > 0 ? 64 : 0);
-        box = need > box ? need : box;
-    }
-    return box;
-}
+// A and read as zeros by pass C.  Pass C still copies every row of a tile:
+// per-k_a boxes of only the live runs (a few rows of 64 bytes each) made the
+// copies latency-bound (275 us against 102 us for all rows on gene-2m with
+// band 5, 8, 33, 33).
 
 // fmat: the 64-point DFT matrix / 8 as the B operand; tab: this pass's
 // W_(64 RA)^(n_b k_a) / sqrt(RA) pairs (Otc2::TABB bytes); tin: pass A u as 32-bit words [rows][RA/2
@@ -187,7 +169,7 @@ template <int DT, int RA, bool FWD, bool GATED, bool SP = false>
 __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_t* __restrict__ fmat,
                                                  const float4* __restrict__ tab,
                                                  const __grid_constant__ CUtensorMap tin,
-                                                 const __grid_constant__ CUtensorMap tgate, int box) {
+                                                 const __grid_constant__ CUtensorMap tgate) {
     using O = Op<DT>;
     using C = Otc2<RA>;
     using P = Otc2Pass<RA, FWD, GATED>;
@@ -209,37 +191,14 @@ __global__ void __launch_bounds__(256, 2) otc2_pass(const MPArgs a, const uint8_
     const long items = rows * C::TILES;
     const long first_item = blockIdx.x, stride = gridDim.x;
 
-    // SP pass C: the boxes of live rows per k_a (thread 0 issues the copies)
-    constexpr bool SPC = SP && !FWD;
-    int nbx[SPC ? RA : 1] = {}, bst[SPC ? RA : 1][2] = {};
-    uint32_t sp_bytes = 0;
-    if constexpr (SPC) {
-        if (t == 0) {
-            #pragma unroll
-            for (int ka = 0; ka < RA; ++ka) {
-                nbx[ka] = otc2_boxes(a.zbits[2 * ka], box, bst[ka]);
-                sp_bytes += uint32_t(nbx[ka] * box * TC) * 4u;
-            }
-        }
-    }
     auto stage = [&](long item, int s) {
         const int row = int(item / C::TILES);
         const int o_base = int(item % C::TILES) * TC;
-        if constexpr (SPC) {
-            mbar_expect_tx(&full[s], sp_bytes);
-            #pragma unroll
-            for (int ka = 0; ka < RA; ++ka)
-                for (int i = 0; i < nbx[ka]; ++i) {
-                    const int r0 = 64 * ka + bst[ka][i];
-                    tma_load_3d(st + s * P::STAGE_WORDS + r0 * TC, &tin, o_base, r0, row, &full[s]);
-                }
-        } else {
-            mbar_expect_tx(&full[s], P::STAGE_WORDS * 4u * (P::NGATE ? 2u : 1u));
-            #pragma unroll
-            for (int bx = 0; bx < P::NBOX; ++bx)
-                tma_load_3d(st + s * P::STAGE_WORDS + bx * P::BOXR * TC, &tin, o_base, bx * P::BOXR, row, &full[s]);
-            if constexpr (P::NGATE > 0) tma_load_3d(sw + s * P::STAGE_WORDS, &tgate, o_base, 0, row, &full[s]);
-        }
+        mbar_expect_tx(&full[s], P::STAGE_WORDS * 4u * (P::NGATE ? 2u : 1u));
+        #pragma unroll
+        for (int bx = 0; bx < P::NBOX; ++bx)
+            tma_load_3d(st + s * P::STAGE_WORDS + bx * P::BOXR * TC, &tin, o_base, bx * P::BOXR, row, &full[s]);
+        if constexpr (P::NGATE > 0) tma_load_3d(sw + s * P::STAGE_WORDS, &tgate, o_base, 0, row, &full[s]);
     };
 
     uint32_t issued = 0;

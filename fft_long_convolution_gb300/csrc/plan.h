@@ -50,7 +50,6 @@ struct fftconv_plan_s {
     // as zeros by the last pass: device copy and host copy
     const unsigned long long* zcbits = nullptr;
     unsigned long long zhost[2] = {0ull, 0ull};
-    int otc2_box = 0;  // two-level sparse plans: rows per copy of the last pass's live runs
     int num_sms = 0;
     bool circular = false;  // circular convolution of length 2 M (every input and output row of the outer passes)
     int device = 0;  // the device the plan's tables live on (current at creation)
@@ -201,8 +200,8 @@ cudaError_t launch_otc(const fftconv_plan_s* p, const MPArgs& args, int64_t rows
 // The fused two-level outer pass (otc2.cuh): pass A (FWD, from u) or pass C
 // (to y) over rows x (4096 / TC) column tiles, as many CTAs per SM as shared
 // and tensor memory hold.  SP: a frequency-sparse plan's dead sub-rows
-// (args.zbits, [RA][2] words) are not stored by pass A and not copied by
-// pass C (boxes of p->otc2_box rows).
+// (args.zbits, [RA][2] words) are not stored by pass A and read as zeros by
+// pass C.
 template <int DT, int RA, bool FWD, bool G, bool SP = false>
 cudaError_t launch_otc2(const fftconv_plan_s* p, const MPArgs& args, int64_t rows, cudaStream_t st) {
     using C = Otc2<RA>;
@@ -222,21 +221,19 @@ cudaError_t launch_otc2(const fftconv_plan_s* p, const MPArgs& args, int64_t row
     if (grid > items) grid = items;
     if (grid < 1) return cudaSuccess;
     if (!p->otc_fa2 || !p->otc_fc2 || !p->otc_tw2 || (SP && !args.zbits)) return cudaErrorInvalidValue;
-    // SP pass C: boxes of the longest run of live rows (at least one row, so
-    // that the map is valid when nothing is live and nothing is copied)
-    const int box = (SP && !FWD) ? (p->otc2_box > 0 ? p->otc2_box : 1) : P::BOXR;
     CUtensorMap tin, tgate;
     std::memset(&tgate, 0, sizeof(tgate));
     // pass A: u as RA/2 x 64 sub-rows of 4096 words per row (2 M bytes);
     // pass C: T as RA x 64 sub-rows per row (4 M bytes)
-    const bool ok = FWD ? encode_rows_map(&tin, args.u, C::L, P::NIN, uint64_t(rows), uint64_t(2) * C::M, box, C::TC)
-                        : encode_rows_map(&tin, args.T, C::L, P::NIN, uint64_t(rows), uint64_t(4) * C::M, box, C::TC);
+    const bool ok =
+        FWD ? encode_rows_map(&tin, args.u, C::L, P::NIN, uint64_t(rows), uint64_t(2) * C::M, P::BOXR, C::TC)
+            : encode_rows_map(&tin, args.T, C::L, P::NIN, uint64_t(rows), uint64_t(4) * C::M, P::BOXR, C::TC);
     if (!ok) return cudaErrorInvalidValue;
     if (G && FWD &&
         !encode_rows_map(&tgate, args.w_in, C::L, P::NIN, uint64_t(rows), uint64_t(2) * C::M, P::BOXR, C::TC))
         return cudaErrorInvalidValue;
     const float4* tab = p->otc_tw2 + (FWD ? 0 : C::TABB / 16);
-    fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, FWD ? p->otc_fa2 : p->otc_fc2, tab, tin, tgate, box);
+    fn<<<unsigned(grid), C::THREADS, smem, st>>>(args, FWD ? p->otc_fa2 : p->otc_fc2, tab, tin, tgate);
     return cudaGetLastError();
 }
 

@@ -92,8 +92,8 @@ def test_multipass_sparse_skips_pairs(N, dtype, gated, B, H, band):
 ])
 def test_two_level_sparse(N, dtype, gated, B, H, band):
     """The fused outer passes of a two-level plan skip dead sub-rows: pass A
-    does not store them, pass C copies only the runs of live rows of every
-    k_a and reads the rest as zeros."""
+    does not store them and pass C reads them as zeros (pass B never writes
+    them)."""
     bd = _check(N, dtype, gated, B, H, band)
     assert 0 < bd["pairs_run"] < bd["pairs_total"]
 
