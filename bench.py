@@ -287,13 +287,10 @@ def path_of(plan_info: dict, pairs_run: Optional[int] = None, pairs_total: Optio
     if plan_info["path"] == 1:
         nb = 0 if pairs_run == 0 else 1
         skips = pairs_run is not None and pairs_total is not None and pairs_run < pairs_total
-        if plan_info["order"] == 4 and plan_info["factors"][3] == 64:  # outer factor in two HBM levels
-            if skips:
-                return {"kernel": "mp_pass_a (RA) + mp_pass_a (64, in place) + mp_pass_b_tc + mp_pass_c (64, in "
-                                  "place) + mp_pass_c (RA) (the whole step, frequency-sparse)",
-                        "launches_per_step": 4 + nb}
+        if plan_info["order"] == 4 and plan_info["factors"][3] == 64:  # outer factor RA x 64, one pass per side
+            sparse = " (dead sub-rows skipped)" if skips else ""
             return {"kernel": "otc2_pass (A: RA in registers, 64 on tcgen05) + mp_pass_b_tc + otc2_pass (C) "
-                              "(the whole step)",
+                              "(the whole step)" + sparse,
                     "launches_per_step": 2 + nb}
         if plan_info["order"] == 3:
             return {"kernel": "otc_pass (A) + mp_pass_b_tc + otc_pass (C) (the whole step)",

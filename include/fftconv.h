@@ -86,12 +86,17 @@ typedef struct {
  * the GPU.  N must be a power of two with 2^10 <= N <= 2^21.  order = 0 picks
  * the factorization; a nonzero order is honoured or rejected.  Factorizations
  * (outer factor first; "Higher-order decompositions" of section 3.4):
- *   N = 4096:             order 2, 64 x 64 (fused, tensor-memory kernel)
- *   N <= 16384 otherwise: order 3, N/256 x 16 x 16 (fused)
- *   32768 <= N <= 2^19:   order 3, N/4096 x 64 x 64 (multi-pass; the default),
+ *   N = 4096, and 1024 / 2048 by default:
+ *                         order 2, 64 x 64 (fused on the tensor cores; rows
+ *                         of 1024 / 2048 zero-padded to 4096)
+ *   N = 1024 / 2048 with order 3: N/256 x 16 x 16 (fused, warp-level MMAs)
+ *   N = 8192, 16384, 32768: order 3, N/4096 x 64 x 64 (fused on the tensor
+ *                         cores, the outer radix in registers); N = 32768
+ *                         with order 4 runs multi-pass as below
+ *   65536 <= N <= 2^19:   order 3, N/4096 x 64 x 64 (multi-pass; the default),
  *                         or order 4, N/16384 x 64 x 16 x 16, on request
- *   N >= 2^20:            order 4, N/2^18 x 64 x 64 x 64 (multi-pass, the outer
- *                         factor in two HBM levels)
+ *   N >= 2^20:            order 4, N/2^18 x 64 x 64 x 64 (multi-pass; the
+ *                         outer factor N/2^18 x 64 in one pass per direction)
  * Returns OK, INVALID (info NULL) or UNSUPPORTED.
  */
 fftconv_status_t fftconv_plan_query(int64_t N, fftconv_dtype_t dtype, int order,

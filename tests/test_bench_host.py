@@ -31,11 +31,13 @@ def test_launches_per_step(N, order, launches):
 
 
 def test_launches_per_step_two_level_sparse():
-    """A frequency-sparse two-level plan that skips pairs keeps the four
-    warp-level outer passes: A, A (in place), B, C (in place), C."""
+    """A frequency-sparse two-level plan runs the same fused outer passes as
+    the dense one (skipping dead sub-rows inside them): A, B, C, and no
+    pass B when every pair is skipped."""
     info = F.query(2097152, F.BF16, 0)
-    assert bench.path_of(info, 40, 256)["launches_per_step"] == 5
-    assert bench.path_of(info, 0, 256)["launches_per_step"] == 4
+    assert bench.path_of(info, 40, 256)["launches_per_step"] == 3
+    assert "skipped" in bench.path_of(info, 40, 256)["kernel"]
+    assert bench.path_of(info, 0, 256)["launches_per_step"] == 2
     assert bench.path_of(info, 256, 256)["launches_per_step"] == 3
 
 
